@@ -1,0 +1,28 @@
+"""CPU oracle for the Kimi Delta Attention (KDA) recurrence.
+
+TEST INFRASTRUCTURE ONLY. Only ``tests/``, ``__graft_entry__.smoke()`` and the
+``cpu_baseline`` / reference legs of ``bench.py`` may import this package. The
+CUDA library never calls it and shares no code with it; the two meet only in
+the seeded input generators, which hold none of the method's arithmetic.
+
+Three independent restatements of the same definition (Kimi K3 -- Architecture
+Notes, section 1.1 "Kimi Delta Attention"):
+
+* ``recurrent`` -- the defining token-by-token recurrence in plain C, fp64
+  (``kda_oracle.c``), threaded over (sequence, head) pairs. This is the oracle
+  the GPU path is compared with.
+* ``chunked``  -- the chunkwise form (section 1.2: "recurrent across chunks and
+  parallel within each chunk") in numpy fp64, with the chunk's triangular
+  system solved by a library inverse. Pinned to ``recurrent`` by agreement.
+* ``exact``    -- the recurrence with explicit dense transition matrices in
+  exact rational arithmetic (``fractions.Fraction``), for tiny inputs.
+
+Parity status: every function here is pinned by the ``-m "not gpu"`` tests
+(exact brute force, closed forms, invariants, recurrent/chunked agreement and
+planted-mistake checks). No worked numeric example exists on the pages, so no
+pin is a printed value.
+"""
+
+from .recurrent import kda_recurrent, kda_recurrent_mutant, MUTATIONS, oracle_library_path  # noqa: F401
+from .chunked import kda_chunked, chunk_quantities  # noqa: F401
+from .exact import kda_exact  # noqa: F401
