@@ -1,0 +1,347 @@
+"""Benchmark: KDA prefill tokens/s on the K3-shaped layer (B=1, T=4096, H=96,
+d_k=d_v=128, bf16 q/k/v, fp32 log_alpha/beta/state, chunk 64), with the
+roofline of the prefill kernel, plus the decode step (B=256, H=96, 64 in-place
+steps) in GB/s against HBM, the fp64 CPU oracle timed on this host, and an
+end-to-end number through host buffers. Prints ONE JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torch.distributed (one process per GPU): every rank runs its
+own independent copy of the workload (weak scaling, no collective on the data
+path); the timed region is bracketed by barriers and the max over ranks is kept.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+PREFILL = dict(workload="prefill_k3_T4096_H96", T=4096, H=96, d_k=128, d_v=128, chunk=64)
+DECODE = dict(B=256, H=96, d_k=128, d_v=128, steps=64)
+METRIC = "KDA prefill tokens/s (H=96,d=128) & % tensor roofline; decode GB/s vs HBM"
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p["bf16_tflops_sustained"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# Algorithmic work of the chunked prefill (chunk C = 64, d_k = d_v = 128), per token-head:
+#   bytes: q, k, v bf16 (3 x 256) + log_alpha fp32 (512) + beta (4) + out fp32 (512) = 1796
+#   flops: 6 d_k d_v + C (3 d_k + 2 d_v) = 139,264 (triangular intra-chunk work counted once)
+# plus the fp32 state read once and written once per (sequence, head): 2 x 64 KiB.
+PREFILL_BYTES_PER_TOKEN_HEAD = 1796
+PREFILL_STATE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4
+PREFILL_FLOPS_PER_TOKEN_HEAD = 6 * 128 * 128 + 64 * (3 * 128 + 2 * 128)
+# decode, per (sequence, head): state read + write (131,072) + q,k,v bf16 (768) + log_alpha (512)
+# + beta (4) + out fp32 (512) = 132,868 bytes
+DECODE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4 + 3 * 256 + 512 + 4 + 512
+
+
+class ClockSampler:
+    """Samples nvidia-smi SM clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def time_prefill(case, steps, warmup, world):
+    from kimi_delta_attention_02_gb300 import binding
+    args = (case.q, case.k, case.v, case.log_alpha, case.beta, case.cu_seqlens, case.init_state)
+    out = torch.empty(case.v.shape, dtype=torch.float32, device=case.v.device)
+    fin = torch.empty_like(case.init_state)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        binding.prefill(*args, out=out, final_state=fin, stream=stream)
+    binding.check_device_error(stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for i in range(steps):
+        starts[i].record(stream)
+        binding.prefill(*args, out=out, final_state=fin, stream=stream)
+        ends[i].record(stream)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    binding.check_device_error(stream)
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return total_ms, launch_ms
+
+
+def time_decode(steps_per_rep, reps, warmup, world, seed=0):
+    from kimi_delta_attention_02_gb300 import binding, workloads
+    B, H = DECODE["B"], DECODE["H"]
+    state = workloads.make_decode_state(B, H, device="cuda", seed=seed)
+    inputs = [workloads.make_decode_step(s, B, H, dtype=torch.bfloat16, device="cuda", seed=seed)
+              for s in range(steps_per_rep)]
+    out = torch.empty((B, H, 128), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        for st in inputs:
+            binding.decode(st.q, st.k, st.v, st.log_alpha, st.beta, state, out=out, stream=stream)
+    binding.check_device_error(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(reps * steps_per_rep)]
+    barrier(world)
+    torch.cuda.synchronize()
+    i = 0
+    for _ in range(reps):
+        for st in inputs:
+            ev[i][0].record(stream)
+            binding.decode(st.q, st.k, st.v, st.log_alpha, st.beta, state, out=out, stream=stream)
+            ev[i][1].record(stream)
+            i += 1
+    torch.cuda.synchronize()
+    barrier(world)
+    binding.check_device_error(stream)
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def time_e2e(case_cpu, steps, warmup):
+    """Prefill through pinned host buffers: H2D inputs, kda_prefill, D2H out + final state."""
+    from kimi_delta_attention_02_gb300 import binding
+    hp = binding.HostPrefill(case_cpu.q, case_cpu.k, case_cpu.v, case_cpu.log_alpha, case_cpu.beta,
+                             case_cpu.cu_seqlens, case_cpu.init_state)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        hp(stream)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    t0.record(stream)
+    for _ in range(steps):
+        hp(stream, sync=False)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    return t0.elapsed_time(t1) / steps, hp.h2d_bytes, hp.d2h_bytes
+
+
+def cpu_oracle_sample(case_cpu, heads: int):
+    """fp64 oracle on the first `heads` heads of the workload; returns (seconds, threads, token-heads)."""
+    from oracle import kda_recurrent
+    threads = os.cpu_count() or 1
+    sl = lambda t: t[:, :heads].contiguous()
+    init = case_cpu.init_state[:, :heads].contiguous()
+    cu = case_cpu.cu_seqlens.long().numpy()
+    t0 = time.perf_counter()
+    kda_recurrent(sl(case_cpu.q), sl(case_cpu.k), sl(case_cpu.v), sl(case_cpu.log_alpha), sl(case_cpu.beta), cu,
+                  init_state=init, num_threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, min(threads, heads * (cu.shape[0] - 1)), case_cpu.total_tokens * heads
+
+
+def run_reference(args, world, rank):
+    """The reference arm: the fp64 CPU oracle as it stands, on host cores, rank 0 only."""
+    if rank != 0:
+        return
+    from kimi_delta_attention_02_gb300 import workloads
+    case = workloads.prefill_workload(PREFILL["workload"], device="cpu", seed=0)
+    heads = 16  # bounded sample per step: 16 of the 96 heads
+    for _ in range(args.warmup):
+        cpu_oracle_sample(case, heads)
+    times = []
+    cores = 0
+    for _ in range(args.steps):
+        dt, cores, th = cpu_oracle_sample(case, heads)
+        times.append(dt)
+    step_s = sum(times) / len(times)
+    tok_s = PREFILL["T"] * heads / PREFILL["H"] / step_s  # full-workload tokens/s equivalent
+    line = {"impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": PREFILL["workload"], "global_batch": 1, "seq_len": PREFILL["T"],
+                       "heads": PREFILL["H"], "d_k": 128, "d_v": 128, "parallelism": "cpu threads"},
+            "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                             "sample": f"{heads} of {PREFILL['H']} heads x {PREFILL['T']} tokens per step, "
+                                       "fp64 token-recurrent C oracle, scaled to the full workload"},
+            "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    if args.impl == "reference":
+        # rank 0 alone times the CPU oracle; other ranks exit without work
+        run_reference(args, int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("RANK", "0")))
+        return
+    world, rank, local = dist_setup(args)
+
+    from kimi_delta_attention_02_gb300 import binding, workloads
+    binding.lib()
+    hbm_gbs, tf_burst, tf_sust, peak_src = peaks()
+
+    case = workloads.prefill_workload(PREFILL["workload"], device="cuda", seed=rank)
+    T, H = case.total_tokens, case.num_heads
+    with ClockSampler(local) as clocks:
+        total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world)
+        dec_ms = time_decode(DECODE["steps"], 1, 1, world, seed=rank)
+    total_ms = max_over_ranks(total_ms, world)
+    ms_per_step = total_ms / args.steps
+    value = world * T / (ms_per_step / 1e3)
+
+    # roofline of the prefill kernel (one launch per step)
+    launch_avg_ms = sum(launch_ms) / len(launch_ms)
+    alg_bytes = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + case.num_seqs * H * PREFILL_STATE_BYTES_PER_SEQ_HEAD
+    alg_flops = T * H * PREFILL_FLOPS_PER_TOKEN_HEAD
+    achieved_gbs = alg_bytes / (launch_avg_ms / 1e3) / 1e9
+    achieved_tf = alg_flops / (launch_avg_ms / 1e3) / 1e12
+    traffic = None
+    tpath = os.path.join(ROOT, "profiles", "prefill_traffic.json")
+    if os.path.exists(tpath):
+        with open(tpath) as fh:
+            traffic = json.load(fh).get("bytes_per_launch")
+
+    dec_avg_ms = sum(dec_ms) / len(dec_ms)
+    dec_bytes = DECODE["B"] * DECODE["H"] * DECODE_BYTES_PER_SEQ_HEAD
+    dec_gbs = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+
+    e2e = None
+    cpu_base = None
+    if rank == 0:
+        case_cpu = workloads.prefill_workload(PREFILL["workload"], device="cpu", seed=0)
+        e2e_ms, h2d, d2h = time_e2e(case_cpu, max(3, args.steps // 4), 2)
+        e2e = {"value": T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+        if not args.no_cpu_baseline:
+            heads = H  # the whole workload: a few seconds on the host's cores
+            dt, cores, th = cpu_oracle_sample(case_cpu, heads)
+            cpu_base = {"value": T * heads / H / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                        "sample": f"{heads} of {H} heads x {T} tokens (fp64 token-recurrent C oracle, "
+                                  f"{dt:.1f} s), scaled to the full workload"}
+
+    if rank == 0:
+        clk = clocks.summary()
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": PREFILL["workload"], "global_batch": world, "out_dtype": "f32", "seq_len": T, "heads": H,
+                       "d_k": 128, "d_v": 128, "chunk": PREFILL["chunk"], "parallelism": f"replicas x{world}",
+                       "l2": f"inputs {alg_bytes / 1e6:.0f} MB > 129 MB L2 per step, no flush"},
+            "roofline": {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm_gbs, "unit": "GB/s",
+                         "frac": achieved_gbs / hbm_gbs, "traffic": traffic,
+                         "peak_source": peak_src, "kernel": "prefill",
+                         "tensor": {"achieved": achieved_tf, "peak": tf_burst, "unit": "TFLOP/s",
+                                    "frac": achieved_tf / tf_burst},
+                         "launch_ms": launch_avg_ms, "alg_bytes": alg_bytes, "alg_flops": alg_flops},
+            "decode": {"workload": "decode_B256_H96", "ms_per_step": dec_avg_ms, "GB/s": dec_gbs,
+                       "peak": hbm_gbs, "frac": dec_gbs / hbm_gbs,
+                       "tokens_per_s": DECODE["B"] / (dec_avg_ms / 1e3), "alg_bytes": dec_bytes},
+            "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk,
+            "gpu_launches": args.steps + DECODE["steps"],
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,145 @@
+/*
+ * kda.h -- C ABI of libkda: Kimi Delta Attention (KDA) prefill and decode on
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation (Kimi K3 -- Architecture Notes, section 1.1 "Kimi Delta
+ * Attention", the two displayed equations), per sequence and per head:
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * S is the d_k x d_v fp32 recurrent state (same section: S in R^{d_k x d_v},
+ * fixed size). alpha_t = exp(g_t) is channel-wise over the d_k key channels,
+ * with g_t = max(log_alpha_t, lower_bound) (section 1.2 "The lower-bounded
+ * decay": g >= g_min = -5); a NaN log_alpha is not clamped and propagates.
+ * beta_t is one scalar per (token, head). q and k are expected L2-normalised
+ * by the caller (section 1.1); the library does not normalise them. `scale`
+ * multiplies the read-out (the pages print none: pass 1).
+ *
+ * Conventions shared by every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, contiguous,
+ *    16-byte aligned. The library never allocates device memory and keeps no
+ *    per-call state; it only enqueues kernels on `stream` (a cudaStream_t,
+ *    passed as void*; NULL = the legacy default stream).
+ *  - Argument errors are detected on the host before anything is enqueued and
+ *    return KDA_ERR_INVALID_ARG or KDA_ERR_UNSUPPORTED; nothing is written.
+ *    Launch failures return KDA_ERR_CUDA. Errors found by a kernel while it
+ *    runs (a bounded wait that gave up) are recorded in a device error word
+ *    that kda_check_device_error() reads.
+ *  - in_dtype is the element type of q, k and v; out_dtype that of out (each
+ *    KDA_BF16 = bfloat16 or KDA_F32 = float). log_alpha, beta and the states
+ *    are always float (fp32). Results are accumulated in fp32; bf16 outputs are
+ *    rounded to nearest-even. A bf16 output carries a relative rounding error
+ *    of up to 2^-9 per element on top of the computation's own error.
+ *  - Outputs must not alias inputs, except that final_state may equal
+ *    init_state (in-place continuation of a prefill).
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  KDA_OK = 0,
+  KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad enum          */
+  KDA_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement        */
+  KDA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed          */
+  KDA_ERR_TIMEOUT = 4      /* a kernel's bounded wait gave up (device error word)  */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/*
+ * kda_prefill -- the chunkwise-parallel prefill form over packed
+ * variable-length sequences (Kimi K3 -- Architecture Notes, section 1.2: the
+ * kernel is recurrent across chunks and parallel within each chunk).
+ *
+ *   q, k        [total_tokens, H, d_k]   in_dtype
+ *   v           [total_tokens, H, d_v]   in_dtype
+ *   log_alpha   [total_tokens, H, d_k]   fp32, clamped below at lower_bound
+ *   beta        [total_tokens, H]        fp32
+ *   cu_seqlens  [num_seqs + 1]           int32, device; cu_seqlens[0] = 0,
+ *               non-decreasing, cu_seqlens[num_seqs] = total_tokens. Sequence
+ *               n is tokens cu_seqlens[n] .. cu_seqlens[n+1]-1; empty
+ *               sequences are allowed (their final state equals their initial
+ *               state). The library trusts these values (it cannot read device
+ *               memory before enqueueing): malformed offsets are undefined.
+ *   init_state  [num_seqs, H, d_k, d_v]  fp32, or NULL for zeros
+ *   out         [total_tokens, H, d_v]   out_dtype, written
+ *   final_state [num_seqs, H, d_k, d_v]  fp32, written, or NULL to skip
+ *
+ * Sizes: 1 <= d_k, d_v <= 128, H >= 1, num_seqs >= 0, total_tokens >= 0.
+ * bf16 inputs with d_k = d_v = 128 and lower_bound >= -5 run the tensor-core
+ * chunked kernel; every other supported case (fp32 inputs, other head sizes, a
+ * lower bound below -5) runs the fp32 token-recurrent kernel. The chunked
+ * kernel rescales keys within 16-token tiles, which is exact in range only when
+ * 16 * |log-decay| stays below 80 (Kimi K3 -- Architecture Notes, section 1.2):
+ * hence the lower-bound condition and the expectation that log_alpha <= 0
+ * (alpha is a retention factor in (0, 1], section 1.1).
+ * Enqueues work on `stream` and returns without synchronising.
+ */
+kda_status kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha,
+                       const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                       int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                       kda_dtype in_dtype, kda_dtype out_dtype, float lower_bound, float scale,
+                       const float *init_state, void *out, float *final_state, void *stream);
+
+/*
+ * kda_prefill_recurrent -- same contract and results as kda_prefill, always on
+ * the fp32 token-recurrent kernel (one token at a time, state kept on chip).
+ * Exposed for cross-checking the chunked kernels and as the reference-accuracy
+ * path for fp32 inputs.
+ */
+kda_status kda_prefill_recurrent(const void *q, const void *k, const void *v,
+                                 const float *log_alpha, const float *beta,
+                                 const int32_t *cu_seqlens, int32_t num_seqs,
+                                 int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                 kda_dtype in_dtype, kda_dtype out_dtype, float lower_bound,
+                                 float scale,
+                                 const float *init_state, void *out, float *final_state,
+                                 void *stream);
+
+/*
+ * kda_decode -- one decode step: B independent sequences each take one new
+ * token, and their states are updated IN PLACE (Kimi K3 -- Architecture Notes,
+ * section 1.1: the fixed-size state replaces a growing KV cache; the update is
+ * the same recurrence with T = 1).
+ *
+ *   q, k        [B, H, d_k]   in_dtype
+ *   v           [B, H, d_v]   in_dtype
+ *   log_alpha   [B, H, d_k]   fp32
+ *   beta        [B, H]        fp32
+ *   state       [B, H, d_k, d_v] fp32, read and overwritten with S_t
+ *   out         [B, H, d_v]   out_dtype, written with scale * S_t^T q_t
+ *
+ * Sizes: 1 <= d_k, d_v <= 128 and d_v a multiple of 4; B, H >= 1.
+ */
+kda_status kda_decode(const void *q, const void *k, const void *v, const float *log_alpha,
+                      const float *beta, float *state, void *out, int32_t B, int32_t H,
+                      int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype,
+                      float lower_bound, float scale, void *stream);
+
+/*
+ * kda_check_device_error -- synchronises `stream`, then reads and clears the
+ * library's device error word. Returns KDA_OK, KDA_ERR_TIMEOUT if a kernel's
+ * bounded wait gave up since the last check, or KDA_ERR_CUDA if the
+ * synchronisation itself failed.
+ */
+kda_status kda_check_device_error(void *stream);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *kda_status_string(kda_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int32_t kda_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,45 @@
+/*
+ * kda_selftest.h -- test-only entry point of libkda.
+ *
+ * The chunked prefill kernels feed tcgen05.mma from shared-memory tiles in a
+ * 128-byte-swizzled layout through hand-built descriptors. The pages describe
+ * the intra-chunk products only as dense tensor-core matmuls (Kimi K3 --
+ * Architecture Notes, section 1.2, "K3's answer"); this entry point runs ONE
+ * such product in isolation so a test can compare it with a host matrix
+ * product and pin every descriptor setting the kernels use.
+ */
+#ifndef KDA_SELFTEST_H
+#define KDA_SELFTEST_H
+
+#include <stdint.h>
+
+#include "kda.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/*
+ * kda_selftest_umma -- D = (negate_a ? -A : A) . B^T on the tensor cores.
+ *
+ *   A  [M, K] bf16 bits, row-major, device      (M = 64 or 128)
+ *   B  [N, K] bf16 bits, row-major, device      (16 <= N <= 256, N % 16 == 0)
+ *   D  [128, N] fp32, device: the raw accumulator, one row per tensor-memory
+ *      lane (for M = 128 row m is lane m; for M = 64 the test learns the lanes)
+ *   K  16 .. 128, a multiple of 16
+ *   a_mn_major / b_mn_major: stage the operand with M (or N) contiguous
+ *      (requires M or N a multiple of 64) instead of K contiguous
+ *   *_lbo, *_sbo: the leading / stride byte offsets put in each descriptor
+ *   status: device int, set to 1 if the MMA completion wait gave up
+ *
+ * One CTA, 128 threads, about 129 KB of shared memory. Enqueued on `stream`.
+ */
+kda_status kda_selftest_umma(const uint16_t *A, const uint16_t *B, float *D, int32_t M, int32_t N, int32_t K,
+                             int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a, uint32_t a_lbo,
+                             uint32_t a_sbo, uint32_t b_lbo, uint32_t b_sbo, int32_t *status, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_SELFTEST_H */

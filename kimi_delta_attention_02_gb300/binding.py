@@ -1,0 +1,219 @@
+"""Thin Python binding of libkda (include/kda.h) over ctypes.
+
+Argument marshalling only: every step of prefill and decode runs in the CUDA
+kernels of ``libkda.so``. Tensors are torch CUDA tensors (PyTorch provides the
+device memory and the stream); the functions check shapes and dtypes, pass raw
+pointers, and raise ``KdaError`` on any non-OK status. There is no CPU
+fallback: if ``libkda.so`` has not been built, importing the library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkda.so")
+ROOT = os.path.dirname(_HERE)
+HEADERS = [os.path.join(ROOT, "include", "kda.h"), os.path.join(ROOT, "include", "kda_selftest.h")]
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+KDA_F32, KDA_BF16 = 0, 1
+
+_lock = threading.Lock()
+_lib = None
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what} failed: {status_string(status)}")
+
+
+def _declare(lib):
+    vp, i32, i64, f32, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_uint32
+    prefill_args = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, f32, f32, vp, vp, vp, vp]
+    lib.kda_prefill.argtypes = prefill_args
+    lib.kda_prefill.restype = i32
+    lib.kda_prefill_recurrent.argtypes = prefill_args
+    lib.kda_prefill_recurrent.restype = i32
+    lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, vp]
+    lib.kda_decode.restype = i32
+    lib.kda_check_device_error.argtypes = [vp]
+    lib.kda_check_device_error.restype = i32
+    lib.kda_status_string.argtypes = [i32]
+    lib.kda_status_string.restype = ctypes.c_char_p
+    lib.kda_version.argtypes = []
+    lib.kda_version.restype = i32
+    lib.kda_selftest_umma.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, u32, u32, u32, u32, vp, vp]
+    lib.kda_selftest_umma.restype = i32
+
+
+def lib():
+    """The loaded libkda (loaded once). Raises if the library was not built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"{LIB_PATH} is missing: build it with __graft_entry__.build() "
+                                   "(the KDA kernels have no fallback)")
+            handle = ctypes.CDLL(LIB_PATH)
+            _declare(handle)
+            _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream_handle(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _io_dtype(dtype) -> int:
+    if dtype == torch.bfloat16:
+        return KDA_BF16
+    if dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"q/k/v and out must be bfloat16 or float32, got {dtype}")
+
+
+def _check_cuda(*tensors):
+    for t in tensors:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("KDA tensors must be contiguous CUDA tensors")
+
+
+def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, out=None, final_state=None,
+            out_dtype=torch.float32, lower_bound: float = -5.0, scale: float = 1.0, stream=None,
+            recurrent: bool = False, want_final: bool = True):
+    """KDA prefill over packed variable-length sequences (``kda_prefill``).
+
+    q, k [T, H, d_k], v [T, H, d_v] (bf16 or fp32, one dtype); log_alpha [T, H, d_k] fp32;
+    beta [T, H] fp32; cu_seqlens [N+1] int32 (device); init_state [N, H, d_k, d_v] fp32 or None.
+    Returns (out [T, H, d_v] in ``out_dtype`` (or out's dtype), final_state [N, H, d_k, d_v] or
+    None). ``recurrent=True`` forces the fp32 token-recurrent kernel (``kda_prefill_recurrent``).
+    """
+    T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    N = cu_seqlens.shape[0] - 1
+    dt = _io_dtype(q.dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if log_alpha.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("log_alpha and beta must be float32")
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=out_dtype, device=q.device)
+    odt = _io_dtype(out.dtype)
+    if final_state is None and want_final:
+        final_state = torch.empty((N, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    _check_cuda(q, k, v, log_alpha, beta, cu_seqlens, init_state, out, final_state)
+    fn = lib().kda_prefill_recurrent if recurrent else lib().kda_prefill
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(cu_seqlens), N, T, H, d_k, d_v, dt,
+            odt, float(lower_bound), float(scale), _ptr(init_state), _ptr(out), _ptr(final_state),
+            _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_recurrent" if recurrent else "kda_prefill")
+    return out, final_state
+
+
+def decode(q, k, v, log_alpha, beta, state, *, out=None, out_dtype=torch.float32, lower_bound: float = -5.0,
+           scale: float = 1.0, stream=None):
+    """One KDA decode step (``kda_decode``); ``state`` [B, H, d_k, d_v] fp32 is updated in place.
+    q, k [B, H, d_k], v [B, H, d_v]; log_alpha [B, H, d_k]; beta [B, H]. Returns out [B, H, d_v]."""
+    B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = _io_dtype(q.dtype)
+    if out is None:
+        out = torch.empty((B, H, d_v), dtype=out_dtype, device=q.device)
+    odt = _io_dtype(out.dtype)
+    _check_cuda(q, k, v, log_alpha, beta, state, out)
+    st = lib().kda_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(state), _ptr(out), B, H,
+                          d_k, d_v, dt, odt, float(lower_bound), float(scale), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode")
+    return out
+
+
+def check_device_error(stream=None):
+    """Synchronise and raise if a kernel recorded a bounded-wait timeout."""
+    st = lib().kda_check_device_error(_stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_check_device_error")
+
+
+def selftest_umma(A, B, M, N, K, *, a_mn_major=False, b_mn_major=False, negate_a=False, a_lbo=16, a_sbo=1024,
+                  b_lbo=16, b_sbo=1024, stream=None):
+    """One tcgen05 MMA on the GPU (``kda_selftest_umma``); returns the raw [128, N] accumulator."""
+    A16 = A.to(torch.bfloat16).contiguous().view(torch.int16)
+    B16 = B.to(torch.bfloat16).contiguous().view(torch.int16)
+    D = torch.full((128, N), float("nan"), dtype=torch.float32, device=A.device)
+    status = torch.zeros(1, dtype=torch.int32, device=A.device)
+    st = lib().kda_selftest_umma(_ptr(A16), _ptr(B16), _ptr(D), M, N, K, int(a_mn_major), int(b_mn_major),
+                                 int(negate_a), a_lbo, a_sbo, b_lbo, b_sbo, _ptr(status), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_selftest_umma")
+    torch.cuda.synchronize()
+    if int(status.item()) != 0:
+        raise KdaError(KDA_ERR_TIMEOUT, "kda_selftest_umma")
+    return D
+
+
+class HostPrefill:
+    """End-to-end prefill from pinned HOST buffers, as an application calls it.
+
+    Each ``__call__`` copies the inputs host -> device, runs ``kda_prefill`` and
+    copies ``out`` and ``final_state`` back to pinned host memory, all on one
+    stream, and waits for the result. Device staging buffers are allocated once.
+    """
+
+    def __init__(self, q, k, v, log_alpha, beta, cu_seqlens, init_state=None, device="cuda",
+                 out_dtype=torch.float32):
+        self.host_in = [t.pin_memory() if not t.is_pinned() else t
+                        for t in (q, k, v, log_alpha, beta, cu_seqlens)]
+        self.host_init = None if init_state is None else init_state.pin_memory()
+        self.dev_in = [torch.empty_like(t, device=device) for t in self.host_in]
+        self.dev_init = None if init_state is None else torch.empty_like(self.host_init, device=device)
+        T, H, _ = q.shape
+        N = cu_seqlens.shape[0] - 1
+        self.dev_out = torch.empty((T, H, v.shape[-1]), dtype=out_dtype, device=device)
+        self.dev_final = torch.empty((N, H, q.shape[-1], v.shape[-1]), dtype=torch.float32, device=device)
+        self.host_out = torch.empty_like(self.dev_out, device="cpu").pin_memory()
+        self.host_final = torch.empty_like(self.dev_final, device="cpu").pin_memory()
+
+    @property
+    def h2d_bytes(self) -> int:
+        n = sum(t.numel() * t.element_size() for t in self.host_in)
+        return n + (0 if self.host_init is None else self.host_init.numel() * 4)
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.host_out.numel() * self.host_out.element_size() + self.host_final.numel() * 4
+
+    def __call__(self, stream=None, sync: bool = True):
+        stream = stream or torch.cuda.current_stream()
+        with torch.cuda.stream(stream):
+            for d, h in zip(self.dev_in, self.host_in):
+                d.copy_(h, non_blocking=True)
+            if self.dev_init is not None:
+                self.dev_init.copy_(self.host_init, non_blocking=True)
+            q, k, v, la, b, cu = self.dev_in
+            prefill(q, k, v, la, b, cu, self.dev_init, out=self.dev_out, final_state=self.dev_final,
+                    stream=stream)
+            self.host_out.copy_(self.dev_out, non_blocking=True)
+            self.host_final.copy_(self.dev_final, non_blocking=True)
+        if sync:
+            stream.synchronize()
+        return self.host_out, self.host_final

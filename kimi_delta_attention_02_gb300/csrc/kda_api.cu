@@ -1,0 +1,172 @@
+// kda_api.cu -- the C ABI of libkda (declared in include/kda.h): argument
+// validation on the host, dispatch to the kernels, the device error word.
+#include <cstdint>
+
+#include "kda_common.cuh"
+
+#include <atomic>
+#include <mutex>
+
+namespace kda {
+
+namespace {
+__device__ uint32_t g_device_error = 0;
+constexpr int kMaxDevices = 64;
+std::atomic<uint32_t *> g_error_word[kMaxDevices];
+std::mutex g_error_word_mu;
+}  // namespace
+
+uint32_t *device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  uint32_t *p = g_error_word[dev].load(std::memory_order_acquire);
+  if (p != nullptr) return p;
+  std::lock_guard<std::mutex> lock(g_error_word_mu);
+  p = g_error_word[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_device_error) != cudaSuccess) return nullptr;
+    p = static_cast<uint32_t *>(addr);
+    g_error_word[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
+                          float *state, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
+                          float lb, float scale, cudaStream_t stream);
+cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const float *log_alpha,
+                             const float *beta, const int32_t *cu_seqlens, int num_seqs, int H, int d_k, int d_v,
+                             bool in_bf16, bool out_bf16, float lb, float scale, const float *init_state,
+                             void *out, float *final_state, cudaStream_t stream);
+bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb);
+kda_status launch_chunked(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
+                          const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H, bool out_bf16,
+                          float lb, float scale, const float *init_state, void *out, float *final_state,
+                          cudaStream_t stream);
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+kda_status check_prefill_args(const void *q, const void *k, const void *v, const float *log_alpha,
+                              const float *beta, const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                              int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype,
+                              const float *init_state, const void *out, const float *final_state) {
+  if (in_dtype != KDA_F32 && in_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (out_dtype != KDA_F32 && out_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
+  if (d_k > 128 || d_v > 128) return KDA_ERR_UNSUPPORTED;
+  if (total_tokens > INT32_MAX) return KDA_ERR_UNSUPPORTED;  // cu_seqlens are int32
+  if (int64_t(num_seqs) * H > INT32_MAX / 4) return KDA_ERR_UNSUPPORTED;
+  if (cu_seqlens == nullptr || !aligned4(cu_seqlens)) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0) {
+    if (!q || !k || !v || !log_alpha || !beta || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || !aligned16(out) ||
+        !aligned4(beta))
+      return KDA_ERR_INVALID_ARG;
+  }
+  if (init_state && !aligned16(init_state)) return KDA_ERR_INVALID_ARG;
+  if (final_state && !aligned16(final_state)) return KDA_ERR_INVALID_ARG;
+  // outputs must not overlap the inputs (final_state == init_state is allowed)
+  const size_t es = in_dtype == KDA_BF16 ? 2 : 4, eo = out_dtype == KDA_BF16 ? 2 : 4;
+  auto overlaps = [](const void *a, size_t na, const void *b, size_t nb) {
+    if (!a || !b || !na || !nb) return false;
+    const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+    return pa < pb + nb && pb < pa + na;
+  };
+  const size_t nk = size_t(total_tokens) * H * d_k, nv = size_t(total_tokens) * H * d_v;
+  const size_t ns = size_t(num_seqs) * H * d_k * d_v * 4;
+  const void *ins[5] = {q, k, v, log_alpha, beta};
+  const size_t in_bytes[5] = {nk * es, nk * es, nv * es, nk * 4, size_t(total_tokens) * H * 4};
+  for (int i = 0; i < 5; ++i) {
+    if (overlaps(out, nv * eo, ins[i], in_bytes[i])) return KDA_ERR_INVALID_ARG;
+    if (overlaps(final_state, ns, ins[i], in_bytes[i])) return KDA_ERR_INVALID_ARG;
+  }
+  if (overlaps(out, nv * eo, init_state, ns) || overlaps(out, nv * eo, final_state, ns))
+    return KDA_ERR_INVALID_ARG;
+  if (final_state != init_state && overlaps(final_state, ns, init_state, ns)) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" {
+
+kda_status kda_prefill_recurrent(const void *q, const void *k, const void *v, const float *log_alpha,
+                                 const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                 int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
+                                 kda_dtype out_dtype, float lower_bound, float scale, const float *init_state,
+                                 void *out, float *final_state, void *stream) {
+  const kda_status st = check_prefill_args(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, H, d_k,
+                                           d_v, in_dtype, out_dtype, init_state, out, final_state);
+  if (st != KDA_OK) return st;
+  if (num_seqs == 0) return KDA_OK;
+  const cudaError_t err = launch_recurrent(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, H, d_k, d_v,
+                                           in_dtype == KDA_BF16, out_dtype == KDA_BF16, lower_bound, scale,
+                                           init_state, out, final_state, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
+                       const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                       int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype, float lower_bound, float scale,
+                       const float *init_state, void *out, float *final_state, void *stream) {
+  const kda_status st = check_prefill_args(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, H, d_k,
+                                           d_v, in_dtype, out_dtype, init_state, out, final_state);
+  if (st != KDA_OK) return st;
+  if (num_seqs == 0) return KDA_OK;
+  if (total_tokens > 0 && chunked_supported(d_k, d_v, in_dtype == KDA_BF16, lower_bound))
+    return launch_chunked(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, H, out_dtype == KDA_BF16,
+                          lower_bound, scale, init_state, out, final_state, static_cast<cudaStream_t>(stream));
+  const cudaError_t err = launch_recurrent(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, H, d_k, d_v,
+                                           in_dtype == KDA_BF16, out_dtype == KDA_BF16, lower_bound, scale,
+                                           init_state, out, final_state, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_decode(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
+                      float *state, void *out, int32_t B, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
+                      kda_dtype out_dtype, float lower_bound, float scale, void *stream) {
+  if (in_dtype != KDA_F32 && in_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (out_dtype != KDA_F32 && out_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
+  if (d_k > 128 || d_v > 128 || (d_v & 3) != 0) return KDA_ERR_UNSUPPORTED;
+  if (int64_t(B) * H > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !log_alpha || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || !aligned16(state) ||
+      !aligned16(out) || !aligned4(beta))
+    return KDA_ERR_INVALID_ARG;
+  const cudaError_t err = launch_decode(q, k, v, log_alpha, beta, state, out, B, H, d_k, d_v, in_dtype == KDA_BF16,
+                                        out_dtype == KDA_BF16, lower_bound, scale, static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status kda_check_device_error(void *stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
+  uint32_t word = 0;
+  if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof word) != cudaSuccess) return KDA_ERR_CUDA;
+  if (word == 0) return KDA_OK;
+  const uint32_t zero = 0;
+  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return KDA_ERR_CUDA;
+  return KDA_ERR_TIMEOUT;
+}
+
+const char *kda_status_string(kda_status status) {
+  switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+  }
+  return "KDA_ERR_UNKNOWN";
+}
+
+int32_t kda_version(void) { return 100; }
+
+}  // extern "C"

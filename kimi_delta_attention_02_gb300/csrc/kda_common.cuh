@@ -1,0 +1,224 @@
+// kda_common.cuh -- device helpers shared by the libkda kernels (sm_103a only).
+//
+// bf16 conversion, the library's device error word, mbarrier / TMA / tcgen05
+// inline-PTX wrappers and the shared-memory operand layout used by the
+// tensor-core kernels. Everything here is written for Blackwell (sm_100 family,
+// compiled as sm_103a); nothing has a fallback for older architectures.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+// ---------------------------------------------------------------------------
+// Device error word. Kernels OR a code into it when a bounded wait gives up;
+// kda_check_device_error() reads and clears it. It lives in kda_api.cu; kernels
+// receive its device address (device_error_word()) as an argument.
+// ---------------------------------------------------------------------------
+enum : uint32_t {
+  DEVERR_NONE = 0,
+  DEVERR_TMA_TIMEOUT = 1u << 0,
+  DEVERR_MMA_TIMEOUT = 1u << 1,
+};
+
+// Device address of the error word on the current device (nullptr if the
+// lookup failed). Host only; defined in kda_api.cu.
+uint32_t *device_error_word();
+
+__device__ __forceinline__ void raise_device_error(uint32_t *word, uint32_t code) {
+  if (word != nullptr) atomicOr(word, code);
+}
+
+// A spin of this many polls (each a try_wait that itself suspends for a
+// hardware-chosen time) is far beyond any legitimate wait in these kernels.
+constexpr uint32_t kSpinLimit = 1u << 24;
+
+// ---------------------------------------------------------------------------
+// bf16 <-> fp32 without the cuda_bf16 header: bf16 is the top half of binary32.
+// Conversion to bf16 rounds to nearest-even (NaN stays NaN).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) { return __uint_as_float(uint32_t(h) << 16); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint16_t f32_to_bf16(float x) { return uint16_t(pack_bf16x2(x, 0.f) & 0xffffu); }
+
+__device__ __forceinline__ float2 unpack_bf16x2(uint32_t p) {
+  return make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xffff0000u));
+}
+
+// Element load/store for the two I/O dtypes (fp32 or bf16 bits).
+template <bool kBF16>
+__device__ __forceinline__ float load_elem(const void *base, int64_t idx) {
+  if constexpr (kBF16) return bf16_to_f32(static_cast<const uint16_t *>(base)[idx]);
+  else return static_cast<const float *>(base)[idx];
+}
+template <bool kBF16>
+__device__ __forceinline__ void store_elem(void *base, int64_t idx, float x) {
+  if constexpr (kBF16) static_cast<uint16_t *>(base)[idx] = f32_to_bf16(x);
+  else static_cast<float *>(base)[idx] = x;
+}
+
+// log-decay clamp: g < lb ? lb : g (a NaN compares false and passes through)
+__device__ __forceinline__ float clamp_log_decay(float g, float lb) { return g < lb ? lb : g; }
+
+// ---------------------------------------------------------------------------
+// Shared-memory addresses and fences
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// Make generic-proxy shared-memory writes visible to the async proxy (TMA, tcgen05.mma).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------------------
+// mbarrier
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbarrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity to complete. Returns false
+// (and records `code` in the device error word) when the limit is reached.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err_word, uint32_t code) {
+  for (uint32_t i = 0; i < kSpinLimit; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  raise_device_error(err_word, code);
+  return false;
+}
+
+// ---------------------------------------------------------------------------
+// TMA (tensor map loads into shared memory, completion on an mbarrier)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, uint64_t *bar, int32_t x,
+                                            int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, "
+      "%5}], [%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
+}
+
+// ---------------------------------------------------------------------------
+// tcgen05: tensor memory allocation, MMA, commit, loads, fences
+// ---------------------------------------------------------------------------
+// Allocate `ncols` TMEM columns (power of two >= 32); whole warp; address -> *dst (smem).
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// D[tmem] (+)= A[smem desc] x B[smem desc], kind::f16 (bf16 inputs, fp32 accumulate).
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Arrive on `bar` once all previously issued tcgen05.mma of this thread complete.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+                   smem_u32(bar))
+               : "memory");
+}
+
+// 32 lanes x 32-bit, 16 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// ---------------------------------------------------------------------------
+// Operand layouts in shared memory (128-byte swizzle, bf16).
+//
+// A tile is stored as "blocks" of 64 contiguous elements (128 bytes) along its
+// contiguous dimension; within a block, row r occupies 128 bytes at r*128 and
+// its 16-byte chunk j sits at chunk (j XOR (r mod 8)). Blocks follow each other
+// at `rows * 128` bytes. Block bases are 1024-byte aligned. This is the layout
+// TMA writes with CU_TENSOR_MAP_SWIZZLE_128B and a 64-element inner box.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col, uint32_t rows) {
+  // byte offset of bf16 element (row, col) in a tile with `rows` rows
+  const uint32_t blk = col >> 6, c = col & 63u;
+  return blk * rows * 128u + row * 128u + ((((c >> 3) ^ row) & 7u) << 4) + ((c & 7u) << 1);
+}
+// byte offset of the 16-byte chunk holding elements (row, 8*j .. 8*j+7) of block `blk`
+__device__ __forceinline__ uint32_t sw128_chunk(uint32_t row, uint32_t j, uint32_t blk, uint32_t rows) {
+  return blk * rows * 128u + row * 128u + (((j ^ row) & 7u) << 4);
+}
+
+// Shared-memory matrix descriptor (tcgen05): start address, leading and stride
+// byte offsets (all >> 4), fixed version bits 0b001 at [46,49), swizzle mode at [61,64).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
+                                              uint32_t swizzle_mode) {
+  uint64_t d = 0;
+  d |= uint64_t((saddr >> 4) & 0x3FFFu);
+  d |= uint64_t((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= uint64_t((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t(1) << 46;
+  d |= uint64_t(swizzle_mode & 7u) << 61;
+  return d;
+}
+constexpr uint32_t kSwizzle128B = 2;
+
+// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(uint32_t M, uint32_t N, bool a_mn_major, bool b_mn_major,
+                                                       bool negate_a) {
+  return (1u << 4)                      // D format: f32
+         | (1u << 7)                    // A format: bf16
+         | (1u << 10)                   // B format: bf16
+         | (uint32_t(negate_a) << 13)   // negate A
+         | (uint32_t(a_mn_major) << 15) // A major: 0 = K-major, 1 = MN-major
+         | (uint32_t(b_mn_major) << 16) // B major
+         | ((N >> 3) << 17)             // N / 8
+         | ((M >> 4) << 24);            // M / 16
+}
+
+}  // namespace kda

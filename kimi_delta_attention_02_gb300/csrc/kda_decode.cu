@@ -1,0 +1,123 @@
+// kda_decode.cu -- one-token KDA decode step, state updated in place.
+//
+// Kimi K3 -- Architecture Notes, section 1.1: S_t = (I - b k k^T) Diag(a) S_{t-1}
+// + b k v^T, o_t = S_t^T q. With D = Diag(a) and S' = D S_{t-1} this is
+//     y = S'^T k,   z = S'^T q,   u = b (v - y),
+//     S_t = S' + k u^T,           o = scale (z + u (k . q)),
+// one read and one write of the d_k x d_v fp32 state per (sequence, head): the
+// step is bound by HBM bandwidth (about 0.86 flop per byte).
+//
+// One CTA of 256 threads per (sequence, head). Thread (ty, tx) owns value
+// columns 4tx..4tx+3 of key rows ty, ty+8, ..., ty+120: every state access is a
+// 128-bit load or store and each warp touches whole 512-byte rows, so the state
+// streams through HBM fully coalesced. The 16 state loads of a thread are issued
+// before anything waits on them.
+#include "kda_common.cuh"
+
+namespace kda {
+
+constexpr int kDecodeThreads = 256;
+constexpr int kDecodeRowsPerThread = 16;  // 128 key rows / 8 row groups
+
+template <bool kInBF16, bool kOutBF16>
+__global__ void __launch_bounds__(kDecodeThreads, 2)
+    kda_decode_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
+                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                      float *__restrict__ state, void *__restrict__ out, int d_k, int d_v, float lb,
+                      float scale) {
+  __shared__ float s_k[128], s_q[128], s_a[128], s_v[128];
+  __shared__ float s_red_y[8][128], s_red_z[8][128];
+  __shared__ float s_kq[8];
+
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  const int64_t bh = blockIdx.x;  // (sequence, head) pair, head fastest
+  const int64_t vec_base = bh * d_k;
+  float *S = state + bh * int64_t(d_k) * d_v;
+  const int col = 4 * tx;
+  const bool col_ok = col < d_v;
+
+  // 1. issue all state loads of this thread (rows ty + 8 j)
+  float4 s4[kDecodeRowsPerThread];
+#pragma unroll
+  for (int j = 0; j < kDecodeRowsPerThread; ++j) {
+    const int c = ty + 8 * j;
+    s4[j] = (col_ok && c < d_k) ? __ldcs(reinterpret_cast<const float4 *>(S + int64_t(c) * d_v + col))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  // 2. token vectors: decay, key, query, value; k.q by warp reduction
+  float kq = 0.f;
+  if (tid < 128) {
+    float kk = 0.f, qq = 0.f, a = 0.f;
+    if (tid < d_k) {
+      kk = load_elem<kInBF16>(k, vec_base + tid);
+      qq = load_elem<kInBF16>(q, vec_base + tid);
+      a = __expf(clamp_log_decay(log_alpha[vec_base + tid], lb));
+    }
+    s_k[tid] = kk;
+    s_q[tid] = qq;
+    s_a[tid] = a;
+    s_v[tid] = tid < d_v ? load_elem<kInBF16>(v, bh * d_v + tid) : 0.f;
+    kq = kk * qq;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+    if (tx == 0) s_kq[ty] = kq;
+  }
+  const float b = beta[bh];
+  __syncthreads();
+
+  // 3. decay rows, partial predictions y = S'^T k and readouts z = S'^T q
+  float y[4] = {0.f, 0.f, 0.f, 0.f}, z[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < kDecodeRowsPerThread; ++j) {
+    const int c = ty + 8 * j;
+    const float a = s_a[c & 127], kc = s_k[c & 127], qc = s_q[c & 127];
+    s4[j].x *= a; s4[j].y *= a; s4[j].z *= a; s4[j].w *= a;
+    y[0] += kc * s4[j].x; y[1] += kc * s4[j].y; y[2] += kc * s4[j].z; y[3] += kc * s4[j].w;
+    z[0] += qc * s4[j].x; z[1] += qc * s4[j].y; z[2] += qc * s4[j].z; z[3] += qc * s4[j].w;
+  }
+  *reinterpret_cast<float4 *>(&s_red_y[ty][col]) = make_float4(y[0], y[1], y[2], y[3]);
+  *reinterpret_cast<float4 *>(&s_red_z[ty][col]) = make_float4(z[0], z[1], z[2], z[3]);
+  __syncthreads();
+
+  float yt[4] = {0.f, 0.f, 0.f, 0.f}, zt[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    const float4 ya = *reinterpret_cast<const float4 *>(&s_red_y[r][col]);
+    const float4 za = *reinterpret_cast<const float4 *>(&s_red_z[r][col]);
+    yt[0] += ya.x; yt[1] += ya.y; yt[2] += ya.z; yt[3] += ya.w;
+    zt[0] += za.x; zt[1] += za.y; zt[2] += za.z; zt[3] += za.w;
+  }
+  kq = s_kq[0] + s_kq[1] + s_kq[2] + s_kq[3];
+
+  // 4. delta-rule write u = b (v - y), S_t = S' + k u^T, o = scale (z + u (k.q))
+  float u[4];
+#pragma unroll
+  for (int e = 0; e < 4; ++e) u[e] = b * (s_v[(col + e) & 127] - yt[e]);
+#pragma unroll
+  for (int j = 0; j < kDecodeRowsPerThread; ++j) {
+    const int c = ty + 8 * j;
+    if (col_ok && c < d_k) {
+      const float kc = s_k[c];
+      const float4 w = make_float4(s4[j].x + kc * u[0], s4[j].y + kc * u[1], s4[j].z + kc * u[2],
+                                   s4[j].w + kc * u[3]);
+      __stcs(reinterpret_cast<float4 *>(S + int64_t(c) * d_v + col), w);
+    }
+  }
+  if (ty == 0 && col_ok) {
+#pragma unroll
+    for (int e = 0; e < 4; ++e) store_elem<kOutBF16>(out, bh * d_v + col + e, scale * (zt[e] + u[e] * kq));
+  }
+}
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
+                          float *state, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
+                          float lb, float scale, cudaStream_t stream) {
+  const dim3 grid(unsigned(int64_t(B) * H)), block(kDecodeThreads);
+  auto kern = in_bf16 ? (out_bf16 ? kda_decode_kernel<true, true> : kda_decode_kernel<true, false>)
+                      : (out_bf16 ? kda_decode_kernel<false, true> : kda_decode_kernel<false, false>);
+  kern<<<grid, block, 0, stream>>>(q, k, v, log_alpha, beta, state, out, d_k, d_v, lb, scale);
+  return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,100 @@
+// kda_selftest.cu -- a single tcgen05.mma on operands staged in the same
+// 128-byte-swizzled shared-memory layouts the chunked prefill kernel uses, with
+// the whole 128-lane accumulator copied back. Tests compare it with a host
+// matrix product to pin the descriptor encodings (K-major and MN-major
+// operands, the M = 64 accumulator lanes, the negate bit) that the chunked
+// kernel depends on.
+#include "../../include/kda_selftest.h"
+#include "kda_common.cuh"
+
+namespace kda {
+
+constexpr int kSelftestTileBytes = 64 * 1024;  // per operand; twice the largest tile
+
+__global__ void __launch_bounds__(128, 1)
+    selftest_umma_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B, float *__restrict__ D,
+                         int M, int N, int K, int a_mn, int b_mn, int neg_a, uint32_t a_lbo, uint32_t a_sbo,
+                         uint32_t b_lbo, uint32_t b_sbo, int *__restrict__ status, uint32_t *err_word) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t *sA = smem, *sB = smem + kSelftestTileBytes;
+  __shared__ uint64_t bar;
+  __shared__ uint32_t tmem_base;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  for (int i = tid; i < 2 * kSelftestTileBytes / 16; i += 128) reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
+  __syncthreads();
+  // stage A[m][k] and B[n][k]; K-major tiles have rows m (or n) and 64-wide K blocks,
+  // MN-major tiles have rows k and 64-wide M (or N) blocks.
+  for (int i = tid; i < M * K; i += 128) {
+    const int m = i / K, kk = i % K;
+    const uint32_t off = a_mn ? sw128_offset(kk, m, K) : sw128_offset(m, kk, M);
+    *reinterpret_cast<uint16_t *>(sA + off) = A[i];
+  }
+  for (int i = tid; i < N * K; i += 128) {
+    const int n = i / K, kk = i % K;
+    const uint32_t off = b_mn ? sw128_offset(kk, n, K) : sw128_offset(n, kk, N);
+    *reinterpret_cast<uint16_t *>(sB + off) = B[i];
+  }
+  fence_proxy_async_smem();
+  if (tid == 0) {
+    mbar_init(&bar, 1);
+    fence_mbarrier_init();
+  }
+  if (warp == 0) tmem_alloc(&tmem_base, 256);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+
+  if (tid == 0) {
+    const uint32_t idesc = umma_idesc_bf16(M, N, a_mn, b_mn, neg_a);
+    const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
+    for (int ks = 0; ks < K / 16; ++ks) {
+      const int k0 = ks * 16;
+      // K-major: next K block every 64 elements, 32 bytes per 16-element step inside a block
+      // MN-major: 16 rows of K are 16 * 128 bytes further on
+      const uint32_t a_addr = a_mn ? a0 + k0 * 128 : a0 + (k0 / 64) * M * 128 + (k0 % 64) * 2;
+      const uint32_t b_addr = b_mn ? b0 + k0 * 128 : b0 + (k0 / 64) * N * 128 + (k0 % 64) * 2;
+      umma_f16(tmem, umma_desc(a_addr, a_lbo, a_sbo, kSwizzle128B), umma_desc(b_addr, b_lbo, b_sbo, kSwizzle128B),
+               idesc, ks > 0);
+    }
+    umma_commit(&bar);
+  }
+  const bool ok = mbar_wait(&bar, 0, err_word, DEVERR_MMA_TIMEOUT);
+  if (!ok && tid == 0) *status = 1;
+  tc_fence_after();
+  // copy the accumulator: warp w reads lanes 32w..32w+31, all N columns
+  if (ok) {
+    for (int c0 = 0; c0 < N; c0 += 16) {
+      float vals[16];
+      tmem_ld16(tmem + (uint32_t(32 * warp) << 16) + c0, vals);
+      tmem_ld_wait();
+      for (int j = 0; j < 16; ++j) D[(32 * warp + lane) * N + c0 + j] = vals[j];
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, 256);
+}
+
+}  // namespace kda
+
+extern "C" kda_status kda_selftest_umma(const uint16_t *A, const uint16_t *B, float *D, int32_t M, int32_t N,
+                                        int32_t K, int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a,
+                                        uint32_t a_lbo, uint32_t a_sbo, uint32_t b_lbo, uint32_t b_sbo,
+                                        int32_t *status, void *stream) {
+  using namespace kda;
+  if (!A || !B || !D || !status) return KDA_ERR_INVALID_ARG;
+  if (!(M == 64 || M == 128) || N < 16 || N > 256 || N % 16 || K < 16 || K > 128 || K % 16)
+    return KDA_ERR_UNSUPPORTED;
+  if (a_mn_major && M % 64) return KDA_ERR_UNSUPPORTED;
+  if (b_mn_major && N % 64) return KDA_ERR_UNSUPPORTED;
+  if (a_lbo > 32768 || a_sbo > 32768 || b_lbo > 32768 || b_sbo > 32768) return KDA_ERR_UNSUPPORTED;
+  const int smem = 2 * kSelftestTileBytes + 1024;
+  if (cudaFuncSetAttribute(selftest_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  selftest_umma_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
+      A, B, D, M, N, K, a_mn_major, b_mn_major, negate_a, a_lbo, a_sbo, b_lbo, b_sbo, status, device_error_word());
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}

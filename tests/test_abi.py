@@ -1,0 +1,106 @@
+"""The C-ABI library: it loads, exports every declared entry point, and its
+host-side argument validation rejects bad calls before touching a GPU."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import __graft_entry__
+from kimi_delta_attention_02_gb300 import binding as B
+
+NULL = None
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(B.LIB_PATH):
+        __graft_entry__.build()
+    return B.lib()
+
+
+def declared_functions():
+    names = []
+    for path in B.HEADERS:
+        with open(path) as fh:
+            text = fh.read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(kda_[a-z_0-9]+)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert {"kda_prefill", "kda_decode", "kda_prefill_recurrent", "kda_check_device_error",
+            "kda_status_string", "kda_version", "kda_selftest_umma"} <= set(names)
+    for name in names:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings_and_version(lib):
+    assert B.status_string(0) == "KDA_OK"
+    assert B.status_string(4) == "KDA_ERR_TIMEOUT"
+    assert B.status_string(99) == "KDA_ERR_UNKNOWN"
+    assert lib.kda_version() >= 100
+
+
+def _prefill(lib, fn="kda_prefill", **over):
+    """Call with host-side fake addresses: validation must reject before any CUDA call."""
+    a = dict(q=0x10000, k=0x20000, v=0x30000, la=0x40000, beta=0x50000, cu=0x60000, N=1, T=4, H=2, dk=128,
+             dv=128, dtype=1, odtype=0, lb=-5.0, scale=1.0, init=NULL, out=0x70000, fin=0x80000, stream=NULL)
+    a.update(over)
+    return getattr(lib, fn)(a["q"], a["k"], a["v"], a["la"], a["beta"], a["cu"], a["N"], a["T"], a["H"], a["dk"],
+                            a["dv"], a["dtype"], a["odtype"], a["lb"], a["scale"], a["init"], a["out"], a["fin"],
+                            a["stream"])
+
+
+@pytest.mark.parametrize("fn", ["kda_prefill", "kda_prefill_recurrent"])
+@pytest.mark.parametrize("over,expect", [
+    (dict(q=NULL), B.KDA_ERR_INVALID_ARG),
+    (dict(cu=NULL), B.KDA_ERR_INVALID_ARG),
+    (dict(out=NULL), B.KDA_ERR_INVALID_ARG),
+    (dict(q=0x10008), B.KDA_ERR_INVALID_ARG),          # misaligned
+    (dict(cu=0x60002), B.KDA_ERR_INVALID_ARG),
+    (dict(dtype=7), B.KDA_ERR_INVALID_ARG),
+    (dict(odtype=3), B.KDA_ERR_INVALID_ARG),
+    (dict(H=0), B.KDA_ERR_INVALID_ARG),
+    (dict(N=-1), B.KDA_ERR_INVALID_ARG),
+    (dict(T=-1), B.KDA_ERR_INVALID_ARG),
+    (dict(dk=129), B.KDA_ERR_UNSUPPORTED),
+    (dict(dv=0), B.KDA_ERR_INVALID_ARG),
+    (dict(T=1 << 31), B.KDA_ERR_UNSUPPORTED),
+    (dict(out=0x10000), B.KDA_ERR_INVALID_ARG),       # output aliases an input
+    (dict(fin=0x40000), B.KDA_ERR_INVALID_ARG),
+    (dict(init=0x90000, fin=0x90000 + 4096), B.KDA_ERR_INVALID_ARG),  # partial overlap
+])
+def test_prefill_rejects(lib, fn, over, expect):
+    assert _prefill(lib, fn, **over) == expect
+
+
+def test_prefill_accepts_empty_work(lib):
+    # zero sequences and zero tokens: nothing to enqueue, no CUDA call is made
+    assert _prefill(lib, N=0, T=0, q=NULL, k=NULL, v=NULL, la=NULL, beta=NULL, out=NULL, fin=NULL) == B.KDA_OK
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(state=NULL), B.KDA_ERR_INVALID_ARG),
+    (dict(B=0), B.KDA_ERR_INVALID_ARG),
+    (dict(dv=6), B.KDA_ERR_UNSUPPORTED),
+    (dict(dk=256), B.KDA_ERR_UNSUPPORTED),
+    (dict(state=0x90004), B.KDA_ERR_INVALID_ARG),
+    (dict(dtype=2), B.KDA_ERR_INVALID_ARG),
+    (dict(odtype=-1), B.KDA_ERR_INVALID_ARG),
+])
+def test_decode_rejects(lib, over, expect):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, la=0x40000, beta=0x50000, state=0x90000, out=0x70000, B=2, H=2,
+             dk=128, dv=128, dtype=1, odtype=0)
+    a.update(over)
+    st = lib.kda_decode(a["q"], a["k"], a["v"], a["la"], a["beta"], a["state"], a["out"], a["B"], a["H"], a["dk"],
+                        a["dv"], a["dtype"], a["odtype"], -5.0, 1.0, NULL)
+    assert st == expect
+
+
+def test_selftest_rejects_bad_shapes(lib):
+    st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, 96, 64, 64, 0, 0, 0, 16, 1024, 16, 1024, 0x4000, NULL)
+    assert st == B.KDA_ERR_UNSUPPORTED
