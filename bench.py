@@ -28,7 +28,7 @@ sys.path.insert(0, ROOT)
 import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
-PREFILL = dict(workload="prefill_k3_T4096_H96", T=4096, H=96, d_k=128, d_v=128, chunk=64)
+PREFILL = dict(workload="prefill_k3_T4096_H96", T=4096, H=96, d_k=128, d_v=128, chunk=32)
 DECODE = dict(B=256, H=96, d_k=128, d_v=128, steps=64)
 METRIC = "KDA prefill tokens/s (H=96,d=128) & % tensor roofline; decode GB/s vs HBM"
 
@@ -45,7 +45,7 @@ def peaks():
 
 # Algorithmic work of the chunked prefill (chunk C = 64, d_k = d_v = 128), per token-head:
 #   bytes: q, k, v bf16 (3 x 256) + log_alpha fp32 (512) + beta (4) + out fp32 (512) = 1796
-#   flops: 6 d_k d_v + C (3 d_k + 2 d_v) = 139,264 (triangular intra-chunk work counted once)
+#   flops: 6 d_k d_v + C (3 d_k + 2 d_v) with C = 64 = 139,264 (the pages' chunk; triangular work once)
 # plus the fp32 state read once and written once per (sequence, head): 2 x 64 KiB.
 PREFILL_BYTES_PER_TOKEN_HEAD = 1796
 PREFILL_STATE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4

@@ -22,20 +22,22 @@ extern "C" {
 /*
  * kda_selftest_umma -- D = (negate_a ? -A : A) . B^T on the tensor cores.
  *
- *   A  [M, K] bf16 bits, row-major, device      (M = 64 or 128)
- *   B  [N, K] bf16 bits, row-major, device      (16 <= N <= 256, N % 16 == 0)
+ *   A  [M, K] fp32, row-major, device           (M = 64 or 128)
+ *   B  [N, K] fp32, row-major, device           (16 <= N <= 256, N % 16 == 0)
+ *   fmt operand format the inputs are rounded to before the product:
+ *      0 = fp16, 1 = bf16 (kind::f16), 2 = tf32 (kind::tf32, round to nearest)
  *   D  [128, N] fp32, device: the raw accumulator, one row per tensor-memory
  *      lane (for M = 128 row m is lane m; for M = 64 the test learns the lanes)
  *   K  16 .. 128, a multiple of 16
  *   a_mn_major / b_mn_major: stage the operand with M (or N) contiguous
- *      (requires M or N a multiple of 64) instead of K contiguous
+ *      (16-bit formats; M or N a multiple of 64) instead of K contiguous
  *   *_lbo, *_sbo: the leading / stride byte offsets put in each descriptor
  *   status: device int, set to 1 if the MMA completion wait gave up
  *
  * One CTA, 128 threads, about 129 KB of shared memory. Enqueued on `stream`.
  */
-kda_status kda_selftest_umma(const uint16_t *A, const uint16_t *B, float *D, int32_t M, int32_t N, int32_t K,
-                             int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a, uint32_t a_lbo,
+kda_status kda_selftest_umma(const float *A, const float *B, float *D, int32_t M, int32_t N, int32_t K,
+                             int32_t fmt, int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a, uint32_t a_lbo,
                              uint32_t a_sbo, uint32_t b_lbo, uint32_t b_sbo, int32_t *status, void *stream);
 
 #ifdef __cplusplus

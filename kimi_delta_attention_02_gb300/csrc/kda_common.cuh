@@ -53,6 +53,22 @@ __device__ __forceinline__ float2 unpack_bf16x2(uint32_t p) {
   return make_float2(__uint_as_float(p << 16), __uint_as_float(p & 0xffff0000u));
 }
 
+// fp16 pack (round to nearest-even); used for tensor-core operands whose range fits binary16
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+__device__ __forceinline__ uint16_t f32_to_f16(float x) { return uint16_t(pack_f16x2(x, 0.f) & 0xffffu); }
+
+// fp32 -> tf32 (10-bit mantissa), round to nearest with ties away from zero; the
+// tensor core would otherwise drop the low mantissa bits
+__device__ __forceinline__ float round_tf32(float x) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+  return __uint_as_float(r);
+}
+
 // Element load/store for the two I/O dtypes (fp32 or bf16 bits).
 template <bool kBF16>
 __device__ __forceinline__ float load_elem(const void *base, int64_t idx) {
@@ -146,12 +162,22 @@ __device__ __forceinline__ void tc_fence_before() {
 }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 
-// D[tmem] (+)= A[smem desc] x B[smem desc], kind::f16 (bf16 inputs, fp32 accumulate).
+// D[tmem] (+)= A[smem desc] x B[smem desc], kind::f16 (bf16 or fp16 inputs per the
+// instruction descriptor, fp32 accumulate).
 __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                          uint32_t accumulate) {
   asm volatile(
       "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D[tmem] (+)= A x B, kind::tf32 (fp32 operands read as tf32, fp32 accumulate).
+__device__ __forceinline__ void umma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
@@ -185,9 +211,14 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 // TMA writes with CU_TENSOR_MAP_SWIZZLE_128B and a 64-element inner box.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t sw128_offset(uint32_t row, uint32_t col, uint32_t rows) {
-  // byte offset of bf16 element (row, col) in a tile with `rows` rows
+  // byte offset of 16-bit element (row, col) in a tile with `rows` rows
   const uint32_t blk = col >> 6, c = col & 63u;
   return blk * rows * 128u + row * 128u + ((((c >> 3) ^ row) & 7u) << 4) + ((c & 7u) << 1);
+}
+__device__ __forceinline__ uint32_t sw128_offset32(uint32_t row, uint32_t col, uint32_t rows) {
+  // byte offset of 32-bit element (row, col): blocks of 32 elements per 128-byte row
+  const uint32_t blk = col >> 5, c = col & 31u;
+  return blk * rows * 128u + row * 128u + ((((c >> 2) ^ row) & 7u) << 4) + ((c & 3u) << 2);
 }
 // byte offset of the 16-byte chunk holding elements (row, 8*j .. 8*j+7) of block `blk`
 __device__ __forceinline__ uint32_t sw128_chunk(uint32_t row, uint32_t j, uint32_t blk, uint32_t rows) {
@@ -208,17 +239,23 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo_bytes
 }
 constexpr uint32_t kSwizzle128B = 2;
 
-// Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.
-__host__ __device__ constexpr uint32_t umma_idesc_bf16(uint32_t M, uint32_t N, bool a_mn_major, bool b_mn_major,
-                                                       bool negate_a) {
+// Instruction descriptor with fp32 D. Operand format codes: kind::f16 takes
+// 0 = f16 or 1 = bf16 (A and B the same), kind::tf32 takes 2 = tf32.
+enum : uint32_t { UMMA_F16 = 0, UMMA_BF16 = 1, UMMA_TF32 = 2 };
+__host__ __device__ constexpr uint32_t umma_idesc(uint32_t fmt, uint32_t M, uint32_t N, bool a_mn_major,
+                                                  bool b_mn_major, bool negate_a) {
   return (1u << 4)                      // D format: f32
-         | (1u << 7)                    // A format: bf16
-         | (1u << 10)                   // B format: bf16
+         | (fmt << 7)                   // A format
+         | (fmt << 10)                  // B format
          | (uint32_t(negate_a) << 13)   // negate A
          | (uint32_t(a_mn_major) << 15) // A major: 0 = K-major, 1 = MN-major
          | (uint32_t(b_mn_major) << 16) // B major
          | ((N >> 3) << 17)             // N / 8
          | ((M >> 4) << 24);            // M / 16
+}
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(uint32_t M, uint32_t N, bool a_mn_major, bool b_mn_major,
+                                                       bool negate_a) {
+  return umma_idesc(UMMA_BF16, M, N, a_mn_major, b_mn_major, negate_a);
 }
 
 }  // namespace kda

@@ -12,8 +12,8 @@ namespace kda {
 constexpr int kSelftestTileBytes = 64 * 1024;  // per operand; twice the largest tile
 
 __global__ void __launch_bounds__(128, 1)
-    selftest_umma_kernel(const uint16_t *__restrict__ A, const uint16_t *__restrict__ B, float *__restrict__ D,
-                         int M, int N, int K, int a_mn, int b_mn, int neg_a, uint32_t a_lbo, uint32_t a_sbo,
+    selftest_umma_kernel(const float *__restrict__ A, const float *__restrict__ B, float *__restrict__ D, int M,
+                         int N, int K, int fmt, int a_mn, int b_mn, int neg_a, uint32_t a_lbo, uint32_t a_sbo,
                          uint32_t b_lbo, uint32_t b_sbo, int *__restrict__ status, uint32_t *err_word) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -24,17 +24,26 @@ __global__ void __launch_bounds__(128, 1)
 
   for (int i = tid; i < 2 * kSelftestTileBytes / 16; i += 128) reinterpret_cast<uint4 *>(smem)[i] = make_uint4(0, 0, 0, 0);
   __syncthreads();
-  // stage A[m][k] and B[n][k]; K-major tiles have rows m (or n) and 64-wide K blocks,
-  // MN-major tiles have rows k and 64-wide M (or N) blocks.
+  // stage A[m][k] and B[n][k] in the operand format. K-major tiles have rows m (or n)
+  // and 128-byte K blocks (64 16-bit or 32 tf32 elements); MN-major tiles (16-bit
+  // only) have rows k and 64-wide M (or N) blocks.
+  auto put = [&](uint8_t *tile, uint32_t row, uint32_t col, uint32_t rows, float x) {
+    if (fmt == UMMA_TF32) {
+      *reinterpret_cast<float *>(tile + sw128_offset32(row, col, rows)) = round_tf32(x);
+    } else {
+      const uint16_t h = fmt == UMMA_BF16 ? f32_to_bf16(x) : f32_to_f16(x);
+      *reinterpret_cast<uint16_t *>(tile + sw128_offset(row, col, rows)) = h;
+    }
+  };
   for (int i = tid; i < M * K; i += 128) {
     const int m = i / K, kk = i % K;
-    const uint32_t off = a_mn ? sw128_offset(kk, m, K) : sw128_offset(m, kk, M);
-    *reinterpret_cast<uint16_t *>(sA + off) = A[i];
+    if (a_mn) put(sA, kk, m, K, A[i]);
+    else put(sA, m, kk, M, A[i]);
   }
   for (int i = tid; i < N * K; i += 128) {
     const int n = i / K, kk = i % K;
-    const uint32_t off = b_mn ? sw128_offset(kk, n, K) : sw128_offset(n, kk, N);
-    *reinterpret_cast<uint16_t *>(sB + off) = B[i];
+    if (b_mn) put(sB, kk, n, K, B[i]);
+    else put(sB, n, kk, N, B[i]);
   }
   fence_proxy_async_smem();
   if (tid == 0) {
@@ -48,16 +57,18 @@ __global__ void __launch_bounds__(128, 1)
   const uint32_t tmem = tmem_base;
 
   if (tid == 0) {
-    const uint32_t idesc = umma_idesc_bf16(M, N, a_mn, b_mn, neg_a);
+    const uint32_t idesc = umma_idesc(uint32_t(fmt), M, N, a_mn, b_mn, neg_a);
     const uint32_t a0 = smem_u32(sA), b0 = smem_u32(sB);
-    for (int ks = 0; ks < K / 16; ++ks) {
-      const int k0 = ks * 16;
-      // K-major: next K block every 64 elements, 32 bytes per 16-element step inside a block
-      // MN-major: 16 rows of K are 16 * 128 bytes further on
-      const uint32_t a_addr = a_mn ? a0 + k0 * 128 : a0 + (k0 / 64) * M * 128 + (k0 % 64) * 2;
-      const uint32_t b_addr = b_mn ? b0 + k0 * 128 : b0 + (k0 / 64) * N * 128 + (k0 % 64) * 2;
-      umma_f16(tmem, umma_desc(a_addr, a_lbo, a_sbo, kSwizzle128B), umma_desc(b_addr, b_lbo, b_sbo, kSwizzle128B),
-               idesc, ks > 0);
+    const int kstep = fmt == UMMA_TF32 ? 8 : 16;  // K per instruction: 32 bytes of either type
+    for (int ks = 0; ks < K / kstep; ++ks) {
+      // K-major: 4 instruction steps of 32 bytes per 128-byte block, then the next block
+      // MN-major: the next 16 rows of K are 16 * 128 bytes further on
+      const uint32_t a_addr = a_mn ? a0 + ks * 2048 : a0 + (ks / 4) * M * 128 + (ks % 4) * 32;
+      const uint32_t b_addr = b_mn ? b0 + ks * 2048 : b0 + (ks / 4) * N * 128 + (ks % 4) * 32;
+      const uint64_t ad = umma_desc(a_addr, a_lbo, a_sbo, kSwizzle128B);
+      const uint64_t bd = umma_desc(b_addr, b_lbo, b_sbo, kSwizzle128B);
+      if (fmt == UMMA_TF32) umma_tf32(tmem, ad, bd, idesc, ks > 0);
+      else umma_f16(tmem, ad, bd, idesc, ks > 0);
     }
     umma_commit(&bar);
   }
@@ -80,21 +91,24 @@ __global__ void __launch_bounds__(128, 1)
 
 }  // namespace kda
 
-extern "C" kda_status kda_selftest_umma(const uint16_t *A, const uint16_t *B, float *D, int32_t M, int32_t N,
-                                        int32_t K, int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a,
+extern "C" kda_status kda_selftest_umma(const float *A, const float *B, float *D, int32_t M, int32_t N, int32_t K,
+                                        int32_t fmt, int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a,
                                         uint32_t a_lbo, uint32_t a_sbo, uint32_t b_lbo, uint32_t b_sbo,
                                         int32_t *status, void *stream) {
   using namespace kda;
   if (!A || !B || !D || !status) return KDA_ERR_INVALID_ARG;
+  if (fmt < 0 || fmt > 2) return KDA_ERR_INVALID_ARG;
   if (!(M == 64 || M == 128) || N < 16 || N > 256 || N % 16 || K < 16 || K > 128 || K % 16)
     return KDA_ERR_UNSUPPORTED;
-  if (a_mn_major && M % 64) return KDA_ERR_UNSUPPORTED;
-  if (b_mn_major && N % 64) return KDA_ERR_UNSUPPORTED;
+  if (a_mn_major && (M % 64 || fmt == UMMA_TF32)) return KDA_ERR_UNSUPPORTED;
+  if (b_mn_major && (N % 64 || fmt == UMMA_TF32)) return KDA_ERR_UNSUPPORTED;
+  if (fmt == UMMA_TF32 && negate_a) return KDA_ERR_UNSUPPORTED;
   if (a_lbo > 32768 || a_sbo > 32768 || b_lbo > 32768 || b_sbo > 32768) return KDA_ERR_UNSUPPORTED;
   const int smem = 2 * kSelftestTileBytes + 1024;
   if (cudaFuncSetAttribute(selftest_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return KDA_ERR_CUDA;
   selftest_umma_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
-      A, B, D, M, N, K, a_mn_major, b_mn_major, negate_a, a_lbo, a_sbo, b_lbo, b_sbo, status, device_error_word());
+      A, B, D, M, N, K, fmt, a_mn_major, b_mn_major, negate_a, a_lbo, a_sbo, b_lbo, b_sbo, status,
+      device_error_word());
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
