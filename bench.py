@@ -132,13 +132,19 @@ def barrier(world):
         dist.barrier()
 
 
-def max_over_ranks(x: float, world: int) -> float:
+def max_over_ranks(x: float, world: int, device="cuda") -> float:
+    """The slowest rank's time: every rank's timed region ends at the same barrier."""
     if world == 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    t = torch.tensor([x], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def weak_scaling_value(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
+    """Whole-job tokens/s: every rank processes its own copy of the workload."""
+    return world * tokens_per_rank / (ms_per_step / 1e3)
 
 
 def time_prefill(case, steps, warmup, world):
@@ -233,7 +239,7 @@ def cpu_oracle_sample(case_cpu, heads: int):
 def run_reference(args, world, rank):
     """The reference arm: the fp64 CPU oracle as it stands, on host cores, rank 0 only."""
     if rank != 0:
-        return
+        return None
     from kimi_delta_attention_02_gb300 import workloads
     case = workloads.prefill_workload(PREFILL["workload"], device="cpu", seed=0)
     heads = 16  # bounded sample per step: 16 of the 96 heads
@@ -265,6 +271,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--heads", type=int, default=PREFILL["H"],
+                    help="prefill heads (a smaller value is for profiler captures; the headline uses 96)")
+    ap.add_argument("--prefill-only", action="store_true",
+                    help="time the prefill kernel only (no decode, e2e or CPU baseline): for profiler captures")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -278,14 +288,22 @@ def main():
     binding.lib()
     hbm_gbs, tf_burst, tf_sust, peak_src = peaks()
 
-    case = workloads.prefill_workload(PREFILL["workload"], device="cuda", seed=rank)
+    if args.heads == PREFILL["H"]:
+        case = workloads.prefill_workload(PREFILL["workload"], device="cuda", seed=rank)
+    else:
+        case = workloads.make_prefill([PREFILL["T"]], H=args.heads, device="cuda", seed=rank)
     T, H = case.total_tokens, case.num_heads
     with ClockSampler(local) as clocks:
         total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world)
-        dec_ms = time_decode(DECODE["steps"], 1, 1, world, seed=rank)
+        dec_ms = None if args.prefill_only else time_decode(DECODE["steps"], 1, 1, world, seed=rank)
+    if args.prefill_only:
+        if rank == 0:
+            print(json.dumps({"prefill_only": True, "heads": H, "ms_per_step": total_ms / args.steps,
+                              "launch_ms": sum(launch_ms) / len(launch_ms)}), flush=True)
+        return
     total_ms = max_over_ranks(total_ms, world)
     ms_per_step = total_ms / args.steps
-    value = world * T / (ms_per_step / 1e3)
+    value = weak_scaling_value(world, T, ms_per_step)
 
     # roofline of the prefill kernel (one launch per step)
     launch_avg_ms = sum(launch_ms) / len(launch_ms)

@@ -31,14 +31,16 @@ def _lanes_m64():
 
 
 CASES = [
-    # fmt,  M,   N,   K, a_mn, b_mn, neg    use in the kernel
-    ("tf32", 64, 32, 128, False, False, False),  # Gram tiles per subtile
-    ("f16", 64, 128, 32, False, True, False),    # W = T' Kg, Kg token-major
-    ("f16", 128, 32, 32, True, False, False),    # U~^T = V^T T'^T, V token-major
-    ("f16", 128, 32, 128, False, False, True),   # U^T -= S^T W^T
-    ("f16", 128, 32, 128, False, False, False),  # O^T = S^T Q~^T
-    ("f16", 128, 32, 32, False, False, False),   # O^T += U^T P^T
-    ("f16", 128, 128, 32, False, True, False),   # dS^T = U^T K^, K^ token-major
+    # fmt,  M,   N,   K, a_mn, b_mn, neg    use in the chunked kernel
+    ("tf32", 64, 48, 128, False, False, False),  # Gram: all query/key rows x keys under two references
+    ("f16", 128, 32, 32, True, False, False),    # W^T = Kg^T T'^T, Kg token-major
+    ("f16", 128, 64, 32, True, False, False),    # [U~^T | 0] = V^T [T'; 0]^T, V token-major
+    ("f16", 128, 64, 128, False, True, False),   # [U^T | O^T] += S^T [-W^T | Q~^T] (128-row MN-major B)
+    ("f16", 128, 160, 32, False, False, False),  # [O^T | S^T] += U^T [P ; K^^T]^T
+    ("tf32", 64, 32, 128, False, False, False),
+    ("f16", 64, 128, 32, False, True, False),
+    ("f16", 128, 32, 128, False, False, True),   # negate-A bit
+    ("f16", 128, 128, 32, False, True, False),
     ("bf16", 128, 64, 128, False, False, False),
     ("bf16", 128, 128, 64, False, True, False),
     ("bf16", 64, 32, 128, False, False, False),
