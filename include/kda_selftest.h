@@ -26,6 +26,8 @@ extern "C" {
  *   B  [N, K] fp32, row-major, device           (16 <= N <= 256, N % 16 == 0)
  *   fmt operand format the inputs are rounded to before the product:
  *      0 = fp16, 1 = bf16 (kind::f16), 2 = tf32 (kind::tf32, round to nearest)
+ *   sw64: K-major 16-bit operands use the 64-byte swizzle (rows of 32 elements)
+ *      instead of the 128-byte one
  *   D  [128, N] fp32, device: the raw accumulator, one row per tensor-memory
  *      lane (for M = 128 row m is lane m; for M = 64 the test learns the lanes)
  *   K  16 .. 128, a multiple of 16
@@ -37,7 +39,8 @@ extern "C" {
  * One CTA, 128 threads, about 129 KB of shared memory. Enqueued on `stream`.
  */
 kda_status kda_selftest_umma(const float *A, const float *B, float *D, int32_t M, int32_t N, int32_t K,
-                             int32_t fmt, int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a, uint32_t a_lbo,
+                             int32_t fmt, int32_t sw64, int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a,
+                             uint32_t a_lbo,
                              uint32_t a_sbo, uint32_t b_lbo, uint32_t b_sbo, int32_t *status, void *stream);
 
 #ifdef __cplusplus

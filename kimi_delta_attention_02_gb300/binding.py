@@ -48,7 +48,7 @@ def _declare(lib):
     lib.kda_status_string.restype = ctypes.c_char_p
     lib.kda_version.argtypes = []
     lib.kda_version.restype = i32
-    lib.kda_selftest_umma.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, u32, u32, u32, u32, vp, vp]
+    lib.kda_selftest_umma.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, u32, u32, u32, u32, vp, vp]
     lib.kda_selftest_umma.restype = i32
 
 
@@ -157,15 +157,15 @@ def check_device_error(stream=None):
 UMMA_FORMATS = {"f16": 0, "bf16": 1, "tf32": 2}
 
 
-def selftest_umma(A, B, M, N, K, *, fmt="bf16", a_mn_major=False, b_mn_major=False, negate_a=False, a_lbo=16,
-                  a_sbo=1024, b_lbo=16, b_sbo=1024, stream=None):
+def selftest_umma(A, B, M, N, K, *, fmt="bf16", sw64=False, a_mn_major=False, b_mn_major=False, negate_a=False,
+                  a_lbo=16, a_sbo=1024, b_lbo=16, b_sbo=1024, stream=None):
     """One tcgen05 MMA on the GPU (``kda_selftest_umma``); returns the raw [128, N] accumulator.
     A [M, K] and B [N, K] are rounded on the device to ``fmt`` (f16, bf16 or tf32)."""
     A32 = A.to(torch.float32).contiguous()
     B32 = B.to(torch.float32).contiguous()
     D = torch.full((128, N), float("nan"), dtype=torch.float32, device=A.device)
     status = torch.zeros(1, dtype=torch.int32, device=A.device)
-    st = lib().kda_selftest_umma(_ptr(A32), _ptr(B32), _ptr(D), M, N, K, UMMA_FORMATS[fmt], int(a_mn_major),
+    st = lib().kda_selftest_umma(_ptr(A32), _ptr(B32), _ptr(D), M, N, K, UMMA_FORMATS[fmt], int(sw64), int(a_mn_major),
                                  int(b_mn_major), int(negate_a), a_lbo, a_sbo, b_lbo, b_sbo, _ptr(status),
                                  _stream_handle(stream))
     if st != KDA_OK:

@@ -118,11 +118,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// try_wait that lets the thread sleep until the phase completes or `ns` nanoseconds pass
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait for the phase with the given parity to complete. Returns false
 // (and records `code` in the device error word) when the limit is reached.
 __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32_t *err_word, uint32_t code) {
   for (uint32_t i = 0; i < kSpinLimit; ++i)
     if (mbar_try_wait(bar, parity)) return true;
+  raise_device_error(err_word, code);
+  return false;
+}
+// The same bound, waiting in sleeps of up to 10 microseconds (about 2 s in total):
+// a waiting thread issues a handful of instructions instead of spinning.
+constexpr uint32_t kSleepNs = 10000, kSleepLimit = 200000;
+__device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t *err_word, uint32_t code) {
+  for (uint32_t i = 0; i < kSleepLimit; ++i)
+    if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
   raise_device_error(err_word, code);
   return false;
 }
@@ -199,6 +218,15 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {  // v: 16 
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// 32 lanes x 32-bit, 8 consecutive columns per thread.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
 // 32 lanes x 32-bit, 16 consecutive columns per thread, registers -> tensor memory.
@@ -239,6 +267,16 @@ __device__ __forceinline__ uint32_t sw128_chunk(uint32_t row, uint32_t j, uint32
   return blk * rows * 128u + row * 128u + (((j ^ row) & 7u) << 4);
 }
 
+// The 64-byte swizzle (K-major tiles whose rows hold 32 16-bit elements): row r
+// occupies 64 bytes at r*64 and its 16-byte chunk j sits at chunk (j XOR ((r/2) mod 4));
+// atoms of 8 rows (512 bytes) are 512-byte aligned.
+__device__ __forceinline__ uint32_t sw64_chunk(uint32_t row, uint32_t j) {
+  return row * 64u + (((j ^ (row >> 1)) & 3u) << 4);
+}
+__device__ __forceinline__ uint32_t sw64_offset(uint32_t row, uint32_t col) {
+  return sw64_chunk(row, col >> 3) + ((col & 7u) << 1);
+}
+
 // Shared-memory matrix descriptor (tcgen05): start address, leading and stride
 // byte offsets (all >> 4), fixed version bits 0b001 at [46,49), swizzle mode at [61,64).
 __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes,
@@ -251,7 +289,7 @@ __device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo_bytes
   d |= uint64_t(swizzle_mode & 7u) << 61;
   return d;
 }
-constexpr uint32_t kSwizzle128B = 2;
+constexpr uint32_t kSwizzle128B = 2, kSwizzle64B = 4;
 
 // Instruction descriptor with fp32 D. Operand format codes: kind::f16 takes
 // 0 = f16 or 1 = bf16 (A and B the same), kind::tf32 takes 2 = tf32.

@@ -13,7 +13,8 @@ constexpr int kSelftestTileBytes = 64 * 1024;  // per operand; twice the largest
 
 __global__ void __launch_bounds__(128, 1)
     selftest_umma_kernel(const float *__restrict__ A, const float *__restrict__ B, float *__restrict__ D, int M,
-                         int N, int K, int fmt, int a_mn, int b_mn, int neg_a, uint32_t a_lbo, uint32_t a_sbo,
+                         int N, int K, int fmt, int sw64, int a_mn, int b_mn, int neg_a, uint32_t a_lbo,
+                         uint32_t a_sbo,
                          uint32_t b_lbo, uint32_t b_sbo, int *__restrict__ status, uint32_t *err_word) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -27,8 +28,13 @@ __global__ void __launch_bounds__(128, 1)
   // stage A[m][k] and B[n][k] in the operand format. K-major tiles have rows m (or n)
   // and 128-byte K blocks (64 16-bit or 32 tf32 elements); MN-major tiles (16-bit
   // only) have rows k and 64-wide M (or N) blocks.
-  auto put = [&](uint8_t *tile, uint32_t row, uint32_t col, uint32_t rows, float x) {
-    if (fmt == UMMA_TF32) {
+  // with sw64, K-major 16-bit tiles use 64-byte rows: blocks of 32 K elements, `rows` * 64 bytes apart
+  // (MN-major tiles keep the 128-byte swizzle)
+  auto put = [&](uint8_t *tile, uint32_t row, uint32_t col, uint32_t rows, float x, bool k_major) {
+    if (sw64 && k_major) {
+      const uint16_t h = fmt == UMMA_BF16 ? f32_to_bf16(x) : f32_to_f16(x);
+      *reinterpret_cast<uint16_t *>(tile + (col >> 5) * rows * 64 + sw64_offset(row, col & 31)) = h;
+    } else if (fmt == UMMA_TF32) {
       *reinterpret_cast<float *>(tile + sw128_offset32(row, col, rows)) = round_tf32(x);
     } else {
       const uint16_t h = fmt == UMMA_BF16 ? f32_to_bf16(x) : f32_to_f16(x);
@@ -37,13 +43,13 @@ __global__ void __launch_bounds__(128, 1)
   };
   for (int i = tid; i < M * K; i += 128) {
     const int m = i / K, kk = i % K;
-    if (a_mn) put(sA, kk, m, K, A[i]);
-    else put(sA, m, kk, M, A[i]);
+    if (a_mn) put(sA, kk, m, K, A[i], false);
+    else put(sA, m, kk, M, A[i], true);
   }
   for (int i = tid; i < N * K; i += 128) {
     const int n = i / K, kk = i % K;
-    if (b_mn) put(sB, kk, n, K, B[i]);
-    else put(sB, n, kk, N, B[i]);
+    if (b_mn) put(sB, kk, n, K, B[i], false);
+    else put(sB, n, kk, N, B[i], true);
   }
   fence_proxy_async_smem();
   if (tid == 0) {
@@ -63,10 +69,11 @@ __global__ void __launch_bounds__(128, 1)
     for (int ks = 0; ks < K / kstep; ++ks) {
       // K-major: 4 instruction steps of 32 bytes per 128-byte block, then the next block
       // MN-major: the next 16 rows of K are 16 * 128 bytes further on
-      const uint32_t a_addr = a_mn ? a0 + ks * 2048 : a0 + (ks / 4) * M * 128 + (ks % 4) * 32;
-      const uint32_t b_addr = b_mn ? b0 + ks * 2048 : b0 + (ks / 4) * N * 128 + (ks % 4) * 32;
-      const uint64_t ad = umma_desc(a_addr, a_lbo, a_sbo, kSwizzle128B);
-      const uint64_t bd = umma_desc(b_addr, b_lbo, b_sbo, kSwizzle128B);
+      const uint32_t per_blk = sw64 ? 2 : 4, row_bytes = sw64 ? 64 : 128;
+      const uint32_t a_addr = a_mn ? a0 + ks * 2048 : a0 + (ks / per_blk) * M * row_bytes + (ks % per_blk) * 32;
+      const uint32_t b_addr = b_mn ? b0 + ks * 2048 : b0 + (ks / per_blk) * N * row_bytes + (ks % per_blk) * 32;
+      const uint64_t ad = umma_desc(a_addr, a_lbo, a_sbo, (sw64 && !a_mn) ? kSwizzle64B : kSwizzle128B);
+      const uint64_t bd = umma_desc(b_addr, b_lbo, b_sbo, (sw64 && !b_mn) ? kSwizzle64B : kSwizzle128B);
       if (fmt == UMMA_TF32) umma_tf32(tmem, ad, bd, idesc, ks > 0);
       else umma_f16(tmem, ad, bd, idesc, ks > 0);
     }
@@ -92,7 +99,8 @@ __global__ void __launch_bounds__(128, 1)
 }  // namespace kda
 
 extern "C" kda_status kda_selftest_umma(const float *A, const float *B, float *D, int32_t M, int32_t N, int32_t K,
-                                        int32_t fmt, int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a,
+                                        int32_t fmt, int32_t sw64, int32_t a_mn_major, int32_t b_mn_major,
+                                        int32_t negate_a,
                                         uint32_t a_lbo, uint32_t a_sbo, uint32_t b_lbo, uint32_t b_sbo,
                                         int32_t *status, void *stream) {
   using namespace kda;
@@ -103,12 +111,13 @@ extern "C" kda_status kda_selftest_umma(const float *A, const float *B, float *D
   if (a_mn_major && (M % 64 || fmt == UMMA_TF32)) return KDA_ERR_UNSUPPORTED;
   if (b_mn_major && (N % 64 || fmt == UMMA_TF32)) return KDA_ERR_UNSUPPORTED;
   if (fmt == UMMA_TF32 && negate_a) return KDA_ERR_UNSUPPORTED;
+  if (sw64 && fmt == UMMA_TF32) return KDA_ERR_UNSUPPORTED;
   if (a_lbo > 32768 || a_sbo > 32768 || b_lbo > 32768 || b_sbo > 32768) return KDA_ERR_UNSUPPORTED;
   const int smem = 2 * kSelftestTileBytes + 1024;
   if (cudaFuncSetAttribute(selftest_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return KDA_ERR_CUDA;
   selftest_umma_kernel<<<1, 128, smem, static_cast<cudaStream_t>(stream)>>>(
-      A, B, D, M, N, K, fmt, a_mn_major, b_mn_major, negate_a, a_lbo, a_sbo, b_lbo, b_sbo, status,
+      A, B, D, M, N, K, fmt, sw64 != 0, a_mn_major, b_mn_major, negate_a, a_lbo, a_sbo, b_lbo, b_sbo, status,
       device_error_word());
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

@@ -102,9 +102,9 @@ def test_decode_rejects(lib, over, expect):
 
 
 def test_selftest_rejects_bad_shapes(lib):
-    st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, 96, 64, 64, 1, 0, 0, 0, 16, 1024, 16, 1024, 0x4000, NULL)
+    st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, 96, 64, 64, 1, 0, 0, 0, 0, 16, 1024, 16, 1024, 0x4000, NULL)
     assert st == B.KDA_ERR_UNSUPPORTED
-    st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, 128, 64, 64, 2, 1, 0, 0, 16, 1024, 16, 1024, 0x4000, NULL)
+    st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, 128, 64, 64, 2, 0, 1, 0, 0, 16, 1024, 16, 1024, 0x4000, NULL)
     assert st == B.KDA_ERR_UNSUPPORTED  # tf32 operands are K-major only
-    st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, 128, 64, 64, 5, 0, 0, 0, 16, 1024, 16, 1024, 0x4000, NULL)
+    st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, 128, 64, 64, 5, 0, 0, 0, 0, 16, 1024, 16, 1024, 0x4000, NULL)
     assert st == B.KDA_ERR_INVALID_ARG

@@ -31,7 +31,7 @@ def _lanes_m64():
 
 
 CASES = [
-    # fmt,  M,   N,   K, a_mn, b_mn, neg    use in the chunked kernel
+    # fmt,  M,   N,   K, a_mn, b_mn, neg    use in the chunked kernel (sw64 cases: see SW64_CASES)
     ("tf32", 64, 48, 128, False, False, False),  # Gram: all query/key rows x keys under two references
     ("f16", 128, 32, 32, True, False, False),    # W^T = Kg^T T'^T, Kg token-major
     ("f16", 128, 64, 32, True, False, False),    # [U~^T | 0] = V^T [T'; 0]^T, V token-major
@@ -47,13 +47,35 @@ CASES = [
 ]
 
 
+# 64-byte-swizzled K-major operands (rows of 32 fp16): the half-width tiles of the pipelined kernel
+SW64_CASES = [
+    ("f16", 128, 32, 32, True, False, False),    # W^T = Kg^T T'^T with T' 64-byte swizzled
+    ("f16", 128, 64, 32, True, False, False),    # [U~^T | 0] = V^T [T'; 0]^T
+    ("f16", 128, 32, 32, False, False, False),   # O^T += U^T P^T (U^T, P both 64-byte swizzled)
+    ("f16", 128, 128, 32, False, False, False),  # S^T += U^T K^ (K^^T rows 64-byte swizzled)
+    ("f16", 128, 128, 64, False, False, False),  # two 32-wide K blocks
+    ("bf16", 64, 32, 32, False, False, False),
+]
+
+
+@pytest.mark.parametrize("fmt,M,N,K,a_mn,b_mn,neg", SW64_CASES)
+def test_umma_layouts_sw64(fmt, M, N, K, a_mn, b_mn, neg):
+    _check(fmt, M, N, K, a_mn, b_mn, neg, sw64=True)
+
+
 @pytest.mark.parametrize("fmt,M,N,K,a_mn,b_mn,neg", CASES)
 def test_umma_layouts(fmt, M, N, K, a_mn, b_mn, neg):
+    _check(fmt, M, N, K, a_mn, b_mn, neg, sw64=False)
+
+
+def _check(fmt, M, N, K, a_mn, b_mn, neg, sw64):
     g = torch.Generator(device="cpu").manual_seed(M * 7 + N * 3 + K + 11 * a_mn + 5 * b_mn)
     A = torch.randn(M, K, generator=g)
     Bm = torch.randn(N, K, generator=g)
     E = _round(A, fmt).double() @ _round(Bm, fmt).double().T
-    kw = dict(fmt=fmt, a_mn_major=a_mn, b_mn_major=b_mn, negate_a=neg, a_lbo=16, a_sbo=1024, b_lbo=16, b_sbo=1024)
+    sbo = 512 if sw64 else 1024  # one 8-row swizzle atom
+    kw = dict(fmt=fmt, sw64=sw64, a_mn_major=a_mn, b_mn_major=b_mn, negate_a=neg, a_lbo=16,
+              a_sbo=1024 if a_mn else sbo, b_lbo=16, b_sbo=1024 if b_mn else sbo)
     if a_mn:
         kw["a_lbo"] = K * 128  # block of 64 M-elements holds K rows of 128 bytes
     if b_mn:
