@@ -27,7 +27,9 @@
 // (e = 2^-11), which needs no more shared memory than bf16. Accumulation is
 // fp32 throughout and the state is kept in fp32 (tensor memory).
 //
-// Layout of the work. One CTA (16 warps) per (sequence, head) chain. The fp32
+// Layout of the work. One CTA per (sequence, head) chain: 16 compute warps and one
+// issuing warp (one thread of it issues every TMA load and tensor-core MMA, so the
+// ~90 cycles each MMA issue takes never holds up the compute warps). The fp32
 // state S^T (rows v = value channels, columns c = key channels) stays in tensor
 // memory for the whole sequence. Each iteration j runs the state chain of chunk
 // j interleaved with the state-independent work of chunk j+1, so that each
@@ -55,7 +57,8 @@ namespace {
 
 constexpr int kC = 32;      // chunk length (two 16-token subtiles)
 constexpr int kD = 128;     // d_k = d_v
-constexpr int kThreads = 512;
+constexpr int kWorkers = 512;               // 16 compute warps
+constexpr int kThreads = kWorkers + 32;     // + one warp that issues TMA loads and MMAs
 constexpr int kALd = 36;    // fp32 row stride of the A / T scratch
 
 // shared-memory map (bytes from a 1024-aligned base)
@@ -129,7 +132,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3, grp = warp >> 2;  // TMEM lane quarter, column group
+  const int quarter = warp & 3, grp = warp >> 2;  // TMEM lane quarter, column group (compute warps)
+  const bool issuer = tid == kWorkers;             // lane 0 of warp 16
+  const bool worker = tid < kWorkers;
   const int h = int(blockIdx.x % H);
   const int64_t n = blockIdx.x / H;
   const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
@@ -167,22 +172,24 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = uint32_t(32 * quarter) << 16;
   const uint32_t s_cols = tmem + lane_base + TM_S + 32 * grp;  // this thread's 32 state columns
+  if (worker) {
 #pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    float x[16];
+    for (int u = 0; u < 2; ++u) {
+      float x[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-      x[j] = init_state != nullptr ? init_state[st_base + int64_t(32 * grp + 16 * u + j) * kD + v_own] : 0.f;
-    tmem_st16(s_cols + 16 * u, x);
+      for (int j = 0; j < 16; ++j)
+        x[j] = init_state != nullptr ? init_state[st_base + int64_t(32 * grp + 16 * u + j) * kD + v_own] : 0.f;
+      tmem_st16(s_cols + 16 * u, x);
+    }
+    tmem_st_wait();
   }
-  tmem_st_wait();
 
   auto chunk_t0 = [&](int c) { return bos + int64_t(c) * kC; };
   auto chunk_len = [&](int c) {
     const int64_t r = eos - chunk_t0(c);
     return int(r < kC ? r : kC);
   };
-  auto issue_qkg = [&](int c) {  // thread 0
+  auto issue_qkg = [&](int c) {  // issuer
     const int32_t t0 = int32_t(chunk_t0(c));
     mbar_arrive_expect_tx(&bars->qkg, 2 * 8192 + 16384);
     tma_load_3d(sm + OFF_QKG + SQ, &tm_q, &bars->qkg, 0, h, t0);
@@ -191,7 +198,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_3d(sm + OFF_QKG + SK + 4096, &tm_k, &bars->qkg, 64, h, t0);
     tma_load_3d(sm + OFF_QKG + SG, &tm_g, &bars->qkg, 0, h, t0);
   };
-  auto issue_v = [&](int c) {  // thread 0
+  auto issue_v = [&](int c) {  // issuer
     const int32_t t0 = int32_t(chunk_t0(c));
     uint8_t *dst = sm + OFF_V + (c & 1) * 8192;
     mbar_arrive_expect_tx(&bars->v[c & 1], 8192);
@@ -203,11 +210,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   // chunk index of a TMA load issued and not yet waited for (-1: none); tracked by every thread
   int qkg_inflight = -1, v_inflight[2] = {-1, -1};
   if (n_chunks > 0) {
-    if (tid == 0) issue_qkg(0);
+    if (issuer) issue_qkg(0);
     qkg_inflight = 0;
   }
   for (int c = 0; c < 2 && c < n_chunks; ++c) {
-    if (tid == 0) issue_v(c);
+    if (issuer) issue_v(c);
     v_inflight[c] = c;
   }
   float b_next = (tid < kC && tid < eos - bos) ? beta[(bos + tid) * H + h] : 0.f;  // beta of chunk 0
@@ -221,14 +228,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     bad |= !mbar_wait_sleep(&bars->qkg, uint32_t(c & 1), err_word, DEVERR_TMA_TIMEOUT);
     qkg_inflight = -1;
     // warp: subtile s = warp / 8, channels 16 (warp % 8) .. +15; lane: token pair tp = lane % 8
-    // (tokens 16 s + 2 tp, +1), channel quad cg = lane / 8 (channels c0 .. c0 + 3)
-    const int s = warp >> 3, tp = lane & 7, cg = lane >> 3;
+    // (tokens 16 s + 2 tp, +1), channel quad cg = lane / 8 (channels c0 .. c0 + 3); compute warps only
+    const int s = (warp >> 3) & 1, tp = lane & 7, cg = lane >> 3;
     const int c0 = 16 * (warp & 7) + 4 * cg, tb = 16 * s + 2 * tp;
     const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG);
     float a[2][4];
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
-      const float4 g = *reinterpret_cast<const float4 *>(gin + (tb + r) * kD + c0);
+      const float4 g = worker ? *reinterpret_cast<const float4 *>(gin + (tb + r) * kD + c0)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
       const bool ok = tb + r < L;
       a[r][0] = ok ? __expf(clamp_log_decay(g.x, lb)) : 1.f;
       a[r][1] = ok ? __expf(clamp_log_decay(g.y, lb)) : 1.f;
@@ -263,9 +271,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       e2[0][e] = sex * a[1][e];
       e2[1][e] = sex;
     }
-    if (tp == 0) *reinterpret_cast<float4 *>(s_tau + s * kD + c0) = make_float4(tau[0], tau[1], tau[2], tau[3]);
+    if (worker && tp == 0)
+      *reinterpret_cast<float4 *>(s_tau + s * kD + c0) = make_float4(tau[0], tau[1], tau[2], tau[3]);
     if (tid < kC) s_beta[tid] = b_pref;
     __syncthreads();
+    if (!worker) return;
     const float4 t0v = *reinterpret_cast<const float4 *>(s_tau + c0);
     const float4 t1v = *reinterpret_cast<const float4 *>(s_tau + kD + c0);
     const float tau0[4] = {t0v.x, t0v.y, t0v.z, t0v.w}, tau1[4] = {t1v.x, t1v.y, t1v.z, t1v.w};
@@ -332,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  auto issue_gram = [&]() {  // thread 0
+  auto issue_gram = [&]() {  // issuer
     const uint64_t qk = kdesc128(sbase + OFF_QK), bb = kdesc128(sbase + OFF_B);
 #pragma unroll
     for (int ks = 0; ks < 16; ++ks) {
@@ -397,11 +407,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) Ts[(lane >> 1) * kALd + 16 + 8 * (lane & 1) + e] = 0.f;  // block above
-    } else {
+    } else if (worker) {
       // v tile of this chunk: bf16 -> fp16 in place, rows past the sequence end zeroed
       bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
       uint8_t *vt = sm + OFF_V + b * 8192;
-      for (int e = tid - 32; e < kC * 16; e += kThreads - 32) {
+      for (int e = tid - 32; e < kC * 16; e += kWorkers - 32) {
         const int t = e >> 4, cj = e & 15;
         uint4 *p = reinterpret_cast<uint4 *>(vt + sw128_chunk(t, cj & 7, cj >> 3, kC));
         uint4 w = make_uint4(0, 0, 0, 0);
@@ -445,7 +455,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   };
 
-  auto issue_wu = [&](int c) {  // thread 0: W^T and [U~^T | 0]
+  auto issue_wu = [&](int c) {  // issuer: W^T and [U~^T | 0]
     const int b = c & 1;
     const uint64_t tp = kdesc64(sbase + OFF_TP), kg = mndesc(sbase + OFF_KG, kC * 128),
                    vin = mndesc(sbase + OFF_V + b * 8192, kC * 128);
@@ -463,9 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     bad |= !mbar_wait_sleep(&bars->wu, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
     if (c + 2 < n_chunks) {  // the v stage of chunk c is consumed: load chunk c + 2 into it
-      if (tid == 0) issue_v(c + 2);
+      if (issuer) issue_v(c + 2);
       v_inflight[b] = c + 2;
     }
+    if (!worker) return;
     float x[8];
     tmem_ld8(tmem + lane_base + TM_W + 8 * grp, x);  // W^T row c = v_own, columns t = 8 grp ..
     tmem_ld_wait();
@@ -483,16 +494,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (__syncthreads_or(bad)) goto abort;
     tc_fence_after();
     if (n_chunks > 1) {
-      if (tid == 0) issue_qkg(1);
+      if (issuer) issue_qkg(1);
       qkg_inflight = 1;
     }
-    if (tid == 0) issue_gram();
+    if (issuer) issue_gram();
     extract_inverse(0);
     fence_proxy_async_smem();
     tc_fence_before();
     if (__syncthreads_or(bad)) goto abort;
     tc_fence_after();
-    if (tid == 0) issue_wu(0);
+    if (issuer) issue_wu(0);
     wt_extract(0);
     fence_proxy_async_smem();
     tc_fence_before();
@@ -504,7 +515,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = j & 1;
     const bool more = j + 1 < n_chunks;
     // ---------------- P1: chain j, fp16 copy of S^T and decay in place; MMA1
-    {
+    if (worker) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         float x[16];
@@ -523,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     if (__syncthreads_or(bad)) goto abort;
     tc_fence_after();
-    if (tid == 0) {
+    if (issuer) {
       const uint64_t st = kdesc128(sbase + OFF_ST), wq = mndesc(sbase + OFF_WQ + b * kWQBytes, 128 * 128);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {  // [U^T | O^T] += S^T [-W^T | Q~^T]
@@ -540,15 +551,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (__syncthreads_or(bad)) goto abort;
       tc_fence_after();
       if (j + 2 < n_chunks) {
-        if (tid == 0) issue_qkg(j + 2);
+        if (issuer) issue_qkg(j + 2);
         qkg_inflight = j + 2;
       }
-      if (tid == 0) issue_gram();
+      if (issuer) issue_gram();
     }
     // ---------------- P3: chain j, U^T to fp16; MMA2
     bad |= !mbar_wait_sleep(&bars->mma1, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
-    {
+    if (worker) {
       float x[8];
       tmem_ld8(tmem + lane_base + tm_uo(b) + 8 * grp, x);  // U^T row v, columns t = 8 grp ..
       tmem_ld_wait();
@@ -558,7 +569,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     if (__syncthreads_or(bad)) goto abort;
     tc_fence_after();
-    if (tid == 0) {
+    if (issuer) {
       const uint64_t ut = kdesc64(sbase + OFF_UT), pk = kdesc64(sbase + OFF_PK + b * kPKBytes);
 #pragma unroll
       for (int ks = 0; ks < 2; ++ks) {  // O^T += U^T P^T ; S^T += U^T K^
@@ -574,12 +585,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       if (__syncthreads_or(bad)) goto abort;
       tc_fence_after();
-      if (tid == 0) issue_wu(j + 1);
+      if (issuer) issue_wu(j + 1);
     }
     // ---------------- P5: chain j, outputs
     bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
-    {
+    if (worker) {
       const int L = chunk_len(j);
       const int64_t t0 = chunk_t0(j);
       float x[8];
@@ -599,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
   }
 
-  if (final_state != nullptr) {
+  if (final_state != nullptr && worker) {
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       float x[16];
@@ -616,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 abort:
   // a bounded wait gave up: let this CTA's own copies in flight land (bounded), release TMEM
-  if (tid == 0) {
+  if (issuer) {
     if (qkg_inflight >= 0) mbar_wait_sleep(&bars->qkg, uint32_t(qkg_inflight & 1), err_word, DEVERR_TMA_TIMEOUT);
     for (int s = 0; s < 2; ++s)
       if (v_inflight[s] >= 0)
