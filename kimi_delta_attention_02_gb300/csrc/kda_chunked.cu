@@ -12,11 +12,14 @@
 //   P[t,i] =     sum_c q_tc k_ic e^{G_tc - G_ic}   (i <= t)     T' = T Diag(b)
 //   W = T' (K * Gamma),  U~ = T' V,  U = U~ - W S
 //   O = (Q * Gamma) S + P U,   S <- Diag(Gamma_last) S + (K * e^{G_last - G})^T U
-// e^{G_t - G_i} is split per 16-token subtile s with reference r_s = G at the
-// end of subtile s-1: the query/key side q_t e^{G_t - r_s} <= 1 is built once,
-// the other side k_i e^{r_s - G_i} once per row subtile (<= 1 below the
-// diagonal, < e^80 on it). Every factor is a running product of alpha = exp(g)
-// inside a subtile times per-channel subtile totals.
+// e^{G_t - G_i} is split at one reference per chunk, r = G at the end of its first
+// 16-token subtile: e^{G_t - G_i} = f_t g_i with f = e^{G - r}, g = 1 / f. Both
+// lie in [e^-80, e^80] (at most 16 clamped steps on either side of r), inside the
+// fp32 / tf32 range. The Gram products [Q * f ; K * f] (K * g)^T are exact on
+// and below the diagonal, where the two factors meet as e^{G_t - G_i} <= 1; the
+// entries above it may overflow and are never read. Every other operand is the
+// same rescaled by a per-channel constant: Q * Gamma = (Q * f) e^r,
+// K * Gamma = (K * f) e^r, K * e^{G_last - G} = (K * g) e^{G_last - r}.
 //
 // Precision. Outputs and states are heavy-tailed (their largest entries are
 // about ten times their rms), so a per-element relative error e shows up as
@@ -31,14 +34,16 @@
 // issuing warp (one thread of it issues every TMA load and tensor-core MMA, so the
 // ~90 cycles each MMA issue takes never holds up the compute warps). The fp32
 // state S^T (rows v = value channels, columns c = key channels) stays in tensor
-// memory for the whole sequence. Each iteration j runs the state chain of chunk
-// j interleaved with the state-independent work of chunk j+1, so that each
-// tensor-core group runs while the threads work on the other stream:
-//   P1  chain j : fp16 copy of S^T, S^T <- S^T Diag(Gamma_j) in place;
+// memory for the whole sequence, in two copies used alternately. Each iteration
+// j runs the state chain of chunk j interleaved with the state-independent work
+// of chunk j+1, so that each tensor-core group runs while the threads work on
+// the other stream:
+//   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy;
 //                 MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]              (N = 64)
-//   P2  next j+1: decay scan (shuffles), operand tiles; Gram (kind::tf32,
-//                 M = 64 query/key rows x N = 48 keys under the two references)
-//   P3  chain j : U^T to fp16; MMA2: O^T += U^T P^T, S^T += U^T K^     (N = 32, 128)
+//   P2  next j+1: decay prefix sums and the operand tiles (a thread owns one key
+//                 channel and 8 tokens); Gram (kind::tf32, M = 64 rows
+//                 [Q f ; K f] x N = 32 keys K g)
+//   P3  chain j : U^T to fp16; MMA2: [O^T | S^T] += U^T [P ; K^^T]^T   (N = 160)
 //   P4  next j+1: P and A out of TMEM, fp32 inverse of I + A (one warp), T',
 //                 v -> fp16; W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
 //   P5  chain j : O^T out of TMEM to global memory
@@ -60,35 +65,37 @@ constexpr int kD = 128;     // d_k = d_v
 constexpr int kWorkers = 512;               // 16 compute warps
 constexpr int kThreads = kWorkers + 32;     // + one warp that issues TMA loads and MMAs
 constexpr int kALd = 36;    // fp32 row stride of the A / T scratch
+constexpr float kLog2e = 1.4426950408889634f;
 
 // shared-memory map (bytes from a 1024-aligned base)
 constexpr uint32_t OFF_QKG = 0;              // q [32][128] bf16 | k | log-decay [32][128] fp32
 constexpr uint32_t SQ = 0, SK = 8 * 1024, SG = 16 * 1024;
 constexpr uint32_t OFF_V = 32 * 1024;        // two v stages [32][128] bf16, converted to fp16 in place
-constexpr uint32_t OFF_QK = 48 * 1024;       // Gram A side: tf32 [64 rows][128] (rows 32 s..: 16 query, 16 key)
-constexpr uint32_t OFF_B = 80 * 1024;        // Gram B side: tf32 [48 rows][128] (0..15: r_0, 16..47: r_1)
-constexpr uint32_t OFF_ST = 104 * 1024;      // S^T fp16 [128][128]; the inverse's fp32 A, T, X alias it
+constexpr uint32_t OFF_QK = 48 * 1024;       // Gram A side, tf32 [64 rows][128 c]: Q f (rows t), K f (rows 32 + t)
+constexpr uint32_t OFF_B = 80 * 1024;        // Gram B side, tf32 [32 rows i][128 c]: K g
+constexpr uint32_t OFF_ST = 96 * 1024;       // S^T fp16 [128][128]; the inverse's fp32 A, T, X alias it
 constexpr uint32_t G_A = 0, G_T = 5 * 1024, G_X = 10 * 1024;
-constexpr uint32_t OFF_UT = 136 * 1024;      // U^T fp16 [128][32], 64-byte swizzle
-constexpr uint32_t OFF_TP = 144 * 1024;      // T' fp16 [64][32], 64-byte swizzle; rows 32..63 stay zero
-constexpr uint32_t OFF_KG = 148 * 1024;      // K * Gamma fp16 [32 i][128 c] (MN-major A of W^T)
-constexpr uint32_t OFF_WQ = 156 * 1024;      // 2 x [-W^T | Q~^T] fp16 [128 c][64] (MN-major B of MMA1)
+constexpr uint32_t OFF_UT = 128 * 1024;      // U^T fp16 [128][32], 64-byte swizzle
+constexpr uint32_t OFF_TP = 136 * 1024;      // T' fp16 [64][32], 64-byte swizzle; rows 32..63 stay zero
+constexpr uint32_t OFF_KG = 140 * 1024;      // Kg^T = (K * Gamma)^T fp16 [128 c][32 i], 64-byte swizzle
+constexpr uint32_t OFF_WQ = 148 * 1024;      // 2 x [-W^T | Q~^T] fp16 [128 c][64] (MN-major B of MMA1)
 constexpr uint32_t kWQBytes = 16 * 1024;
-constexpr uint32_t OFF_PK = 188 * 1024;      // 2 x [P ; K^^T] fp16 [160 rows][32], 64-byte swizzle
+constexpr uint32_t OFF_PK = 180 * 1024;      // 2 x [P ; K^^T] fp16 [160 rows][32], 64-byte swizzle
 constexpr uint32_t kPKBytes = 10 * 1024;
-constexpr uint32_t OFF_MISC = 208 * 1024;    // beta, Gamma_last x2, subtile totals, barriers
-constexpr uint32_t kSmemBytes = 212 * 1024 + 1024;
+constexpr uint32_t OFF_MISC = 200 * 1024;    // beta, Gamma_last x2, group decay totals, barriers
+constexpr uint32_t kSmemBytes = 204 * 1024 + 1024;
 
-// TMEM columns: Gram | W^T | [U^T | O^T] x 2 | S^T
-constexpr uint32_t TM_GRAM = 0, TM_W = 64, TM_UO = 128, TM_S = 256, TM_COLS = 512;
-__device__ __forceinline__ uint32_t tm_uo(int b) { return TM_UO + 64u * uint32_t(b); }
+// TMEM columns: two groups [U^T | O^T | S^T] (32 + 32 + 128) used by chunk parity, then
+// Gram and W^T. Chunk j's MMA1 and MMA2 write group j % 2; its MMA2 leaves the state for
+// chunk j + 1 there, which P1 of chunk j + 1 reads and rewrites, decayed, into the other.
+constexpr uint32_t TM_GROUP = 192, TM_O = 32, TM_SS = 64, TM_GRAM = 384, TM_W = 416, TM_COLS = 512;
+__device__ __forceinline__ uint32_t tm_grp(int b) { return TM_GROUP * uint32_t(b); }
 
-constexpr uint32_t IDESC_GRAM = umma_idesc(UMMA_TF32, 64, 48, false, false, false);
-constexpr uint32_t IDESC_WT = umma_idesc(UMMA_F16, 128, 32, true, false, false);   // W^T = Kg^T T'^T
+constexpr uint32_t IDESC_GRAM = umma_idesc(UMMA_TF32, 64, 32, false, false, false);
+constexpr uint32_t IDESC_WT = umma_idesc(UMMA_F16, 128, 32, false, false, false);  // W^T = Kg^T T'^T
 constexpr uint32_t IDESC_UT = umma_idesc(UMMA_F16, 128, 64, true, false, false);   // [U~^T | 0] = V^T [T'; 0]^T
 constexpr uint32_t IDESC_UO = umma_idesc(UMMA_F16, 128, 64, false, true, false);   // += S^T [-W^T | Q~^T]
-constexpr uint32_t IDESC_O2 = umma_idesc(UMMA_F16, 128, 32, false, false, false);  // O^T += U^T P^T
-constexpr uint32_t IDESC_S2 = umma_idesc(UMMA_F16, 128, 128, false, false, false); // S^T += U^T K^
+constexpr uint32_t IDESC_OS = umma_idesc(UMMA_F16, 128, 160, false, false, false); // [O^T | S^T] += U^T [P ; K^^T]^T
 
 __device__ __forceinline__ uint64_t kdesc128(uint32_t addr) { return umma_desc(addr, 16, 1024, kSwizzle128B); }
 __device__ __forceinline__ uint64_t kdesc64(uint32_t addr) { return umma_desc(addr, 16, 512, kSwizzle64B); }
@@ -106,10 +113,11 @@ __device__ __forceinline__ void st_at(uint8_t *base, uint32_t off, T v) {
 __device__ __forceinline__ uint4 pack8_f16(const float *x) {
   return make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]), pack_f16x2(x[6], x[7]));
 }
-// byte offset of the 16-byte group holding fp32 elements (row, c0..c0+3) in a 128-byte
-// swizzled tf32 tile of `rows` rows (32 elements per 128-byte row)
-__device__ __forceinline__ uint32_t tf32_quad(uint32_t row, uint32_t c0, uint32_t rows) {
-  return (c0 >> 5) * rows * 128u + row * 128u + (((((c0 & 31u) >> 2) ^ row) & 7u) << 4);
+// 2^x on the SFU (ex2.approx, subnormal results flushed to zero)
+__device__ __forceinline__ float exp2_sfu(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
 }
 
 struct Bars {
@@ -127,8 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   float *s_beta = reinterpret_cast<float *>(sm + OFF_MISC);  // [32] of the chunk being prepared
   float *s_gamma = s_beta + 32;                               // [2][128] Gamma_last by chunk parity
-  float *s_tau = s_gamma + 2 * 128;                           // [2][128] subtile totals
-  Bars *bars = reinterpret_cast<Bars *>(s_tau + 2 * 128);
+  float *s_tot = s_gamma + 2 * 128;                           // [4][128] log2 decay of each 8-token group
+  Bars *bars = reinterpret_cast<Bars *>(s_tot + 4 * 128);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -163,7 +171,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int e = tid; e < 32 * 4; e += kThreads)
     st_at(sm, OFF_TP + sw64_chunk(32 + (e >> 2), e & 3), make_uint4(0, 0, 0, 0));
 
-  const int v_own = 32 * quarter + lane;  // state row (TMEM lane) of this thread
+  const int v_own = 32 * quarter + lane;  // state row (TMEM lane) of this thread; key channel in P2
   const int64_t st_base = (n * H + h) * int64_t(kD) * kD;
 
   tc_fence_before();
@@ -171,15 +179,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
   const uint32_t lane_base = uint32_t(32 * quarter) << 16;
-  const uint32_t s_cols = tmem + lane_base + TM_S + 32 * grp;  // this thread's 32 state columns
-  if (worker) {
+  // this thread's 32 state columns in group b
+  auto s_cols = [&](int b) { return tmem + lane_base + tm_grp(b) + TM_SS + 32 * grp; };
+  if (worker) {  // the state entering chunk 0 sits where chunk -1 would have left it: group 1
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       float x[16];
 #pragma unroll
       for (int j = 0; j < 16; ++j)
         x[j] = init_state != nullptr ? init_state[st_base + int64_t(32 * grp + 16 * u + j) * kD + v_own] : 0.f;
-      tmem_st16(s_cols + 16 * u, x);
+      tmem_st16(s_cols(1) + 16 * u, x);
     }
     tmem_st_wait();
   }
@@ -220,6 +229,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   float b_next = (tid < kC && tid < eos - bos) ? beta[(bos + tid) * H + h] : 0.f;  // beta of chunk 0
 
   // ------------------------------------------------------------------ P2: operand tiles
+  // Thread (channel ch = v_own, tokens 8 grp .. 8 grp + 7): the decay prefix sums run
+  // along its own 8 tokens; the 4 group totals of a channel meet in shared memory.
+  // Everything is kept in log2 units (x log2 e), so each factor is one ex2.
   auto prep = [&](int c) {
     const int b = c & 1, L = chunk_len(c);
     const int64_t t0 = chunk_t0(c);
@@ -227,127 +239,80 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (tid < kC) b_next = (tid < eos - t0 - kC) ? beta[(t0 + kC + tid) * H + h] : 0.f;  // next chunk's
     bad |= !mbar_wait_sleep(&bars->qkg, uint32_t(c & 1), err_word, DEVERR_TMA_TIMEOUT);
     qkg_inflight = -1;
-    // warp: subtile s = warp / 8, channels 16 (warp % 8) .. +15; lane: token pair tp = lane % 8
-    // (tokens 16 s + 2 tp, +1), channel quad cg = lane / 8 (channels c0 .. c0 + 3); compute warps only
-    const int s = (warp >> 3) & 1, tp = lane & 7, cg = lane >> 3;
-    const int c0 = 16 * (warp & 7) + 4 * cg, tb = 16 * s + 2 * tp;
-    const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG);
-    float a[2][4];
+    const int ch = v_own, tb = 8 * grp;
+    float lg[8];  // log2 of Gamma within the group: sum of the group's decays up to each token
+    if (worker) {
+      const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG) + tb * kD + ch;
+      float run = 0.f;
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const float4 g = worker ? *reinterpret_cast<const float4 *>(gin + (tb + r) * kD + c0)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-      const bool ok = tb + r < L;
-      a[r][0] = ok ? __expf(clamp_log_decay(g.x, lb)) : 1.f;
-      a[r][1] = ok ? __expf(clamp_log_decay(g.y, lb)) : 1.f;
-      a[r][2] = ok ? __expf(clamp_log_decay(g.z, lb)) : 1.f;
-      a[r][3] = ok ? __expf(clamp_log_decay(g.w, lb)) : 1.f;
-    }
-    // e1 = product of alpha over the subtile up to and including the token, e2 = product over
-    // the tokens after it; scans over the 8 lanes of a token-pair group
-    float e1[2][4], e2[2][4], tau[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float tot = a[0][e] * a[1][e];
-      float inc = tot;
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        const float up = __shfl_up_sync(0xffffffffu, inc, o, 8);
-        if (tp >= o) inc *= up;
+      for (int r = 0; r < 8; ++r) {
+        const float g = tb + r < L ? clamp_log_decay(gin[r * kD], lb) : 0.f;  // alpha = 1 past the end
+        run = fmaf(g, kLog2e, run);
+        lg[r] = run;
       }
-      float ex = __shfl_up_sync(0xffffffffu, inc, 1, 8);
-      if (tp == 0) ex = 1.f;
-      float sinc = tot;
-#pragma unroll
-      for (int o = 1; o < 8; o <<= 1) {
-        const float dn = __shfl_down_sync(0xffffffffu, sinc, o, 8);
-        if (tp + o < 8) sinc *= dn;
-      }
-      float sex = __shfl_down_sync(0xffffffffu, sinc, 1, 8);
-      if (tp == 7) sex = 1.f;
-      tau[e] = __shfl_sync(0xffffffffu, inc, (lane & ~7) | 7, 32);
-      e1[0][e] = ex * a[0][e];
-      e1[1][e] = ex * tot;
-      e2[0][e] = sex * a[1][e];
-      e2[1][e] = sex;
+      s_tot[grp * kD + ch] = run;
     }
-    if (worker && tp == 0)
-      *reinterpret_cast<float4 *>(s_tau + s * kD + c0) = make_float4(tau[0], tau[1], tau[2], tau[3]);
     if (tid < kC) s_beta[tid] = b_pref;
     __syncthreads();
     if (!worker) return;
-    const float4 t0v = *reinterpret_cast<const float4 *>(s_tau + c0);
-    const float4 t1v = *reinterpret_cast<const float4 *>(s_tau + kD + c0);
-    const float tau0[4] = {t0v.x, t0v.y, t0v.z, t0v.w}, tau1[4] = {t1v.x, t1v.y, t1v.z, t1v.w};
-    float pre[4], post[4], inv_tau[4];
+    const float T0 = s_tot[ch], T1 = s_tot[kD + ch], T2 = s_tot[2 * kD + ch], T3 = s_tot[3 * kD + ch];
+    const float r2 = T0 + T1;                                                // log2 e^r
+    const float last2 = r2 + (T2 + T3);                                      // log2 Gamma_last
+    const float start = grp == 0 ? -r2 : grp == 1 ? -T1 : grp == 2 ? 0.f : T2;  // log2 e^{G_start - r}
+    const float tau0 = exp2_sfu(r2), tau1 = exp2_sfu(last2 - r2);
+    if (grp == 0) s_gamma[b * kD + ch] = exp2_sfu(last2);
+    // q and k of the 8 tokens: bf16 element (t, ch) of the 128-byte-swizzled TMA tiles
+    const uint32_t cc = uint32_t(ch & 63);
+    const uint8_t *qk0 = sm + OFF_QKG + (ch >> 6) * 4096 + tb * 128 + (cc & 7u) * 2;
+    const uint32_t xj = (cc >> 3) << 4;
+    // Gram operands, K-major tf32 (blocks of 32 channels, one 128-byte row per token): the 32
+    // lanes of a warp hold one whole row, so each 4-byte store is conflict-free. fp16 operands,
+    // one 16-byte chunk each: Q~^T (columns 32 + t of [-W^T | Q~^T]), K^^T (row 32 + ch of
+    // [P ; K^^T]) and Kg^T (row ch). Two halves of 4 tokens keep few values live.
+    const uint32_t cb = uint32_t(ch >> 5), cq = uint32_t(ch & 31) >> 2;
+    float *gq = reinterpret_cast<float *>(sm + OFF_QK + cb * 64 * 128 + tb * 128 + (ch & 3) * 4);
+    float *gk = reinterpret_cast<float *>(sm + OFF_QK + cb * 64 * 128 + (32 + tb) * 128 + (ch & 3) * 4);
+    float *gb = reinterpret_cast<float *>(sm + OFF_B + cb * 32 * 128 + tb * 128 + (ch & 3) * 4);
+    const uint32_t row = uint32_t(ch) * 128u, sw = uint32_t(ch) & 7u;
+    uint32_t hq[4], hk[4], hg[4];  // fp16 pairs
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      pre[e] = s == 1 ? tau0[e] : 1.f;   // Gamma at the start of the subtile
-      post[e] = s == 0 ? tau1[e] : 1.f;  // decay from the end of the subtile to the chunk end
-      inv_tau[e] = __fdividef(1.f, s == 0 ? tau0[e] : tau1[e]);
-    }
-    if (s == 0 && tp == 0)
-      *reinterpret_cast<float4 *>(s_gamma + b * kD + c0) =
-          make_float4(tau0[0] * tau1[0], tau0[1] * tau1[1], tau0[2] * tau1[2], tau0[3] * tau1[3]);
-    const uint32_t j16 = uint32_t((c0 & 63) >> 3), sub16 = uint32_t(c0 & 4) * 2, blk16 = uint32_t(c0 >> 6);
-    float qt_col[4][2], kh_col[4][2];  // [channel][token] for the transposed tiles
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-      const int t = tb + r;
-      float q[4] = {0.f, 0.f, 0.f, 0.f}, k[4] = {0.f, 0.f, 0.f, 0.f};
-      const uint32_t off16 = blk16 * (kC * 128) + t * 128 + (((j16 ^ t) & 7u) << 4) + sub16;
-      if (t < L) {
-        const uint2 qb = *reinterpret_cast<const uint2 *>(sm + OFF_QKG + SQ + off16);
-        const uint2 kb2 = *reinterpret_cast<const uint2 *>(sm + OFF_QKG + SK + off16);
-        const float2 q01 = unpack_bf16x2(qb.x), q23 = unpack_bf16x2(qb.y);
-        const float2 k01 = unpack_bf16x2(kb2.x), k23 = unpack_bf16x2(kb2.y);
-        q[0] = q01.x; q[1] = q01.y; q[2] = q23.x; q[3] = q23.y;
-        k[0] = k01.x; k[1] = k01.y; k[2] = k23.x; k[3] = k23.y;
-      }
-      float qs[4], ks[4], kb[4];
+    for (int half = 0; half < 2; ++half) {
+      float qf[4], kf[4], kg[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        qs[e] = q[e] * e1[r][e];
-        ks[e] = k[e] * e1[r][e];
-        kb[e] = k[e] * e2[r][e];
-        qt_col[e][r] = qs[e] * pre[e];
-        kh_col[e][r] = kb[e] * post[e];
+        const int r = 4 * half + e;
+        const uint32_t off = r * 128 + (xj ^ uint32_t(r << 4));
+        const bool ok = tb + r < L;
+        const float q = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SQ + off)) : 0.f;
+        const float k = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SK + off)) : 0.f;
+        const float d = start + lg[r];  // log2 e^{G_t - r}
+        const float f = exp2_sfu(d), g = exp2_sfu(-d);
+        qf[e] = q * f;
+        kf[e] = k * f;
+        kg[e] = k * g;
+        const uint32_t o4 = (r * 128 + ((cq ^ uint32_t(r)) << 4)) >> 2;  // token tb + r: row tb + r, t & 7 = r
+        gq[o4] = round_tf32(qf[e]);
+        gk[o4] = round_tf32(kf[e]);
+        gb[o4] = round_tf32(kg[e]);
       }
-      auto f4 = [](float x0, float x1, float x2, float x3) {
-        return make_float4(round_tf32(x0), round_tf32(x1), round_tf32(x2), round_tf32(x3));
-      };
-      st_at(sm, OFF_QK + tf32_quad(32 * s + 2 * tp + r, c0, 64), f4(qs[0], qs[1], qs[2], qs[3]));
-      st_at(sm, OFF_QK + tf32_quad(32 * s + 16 + 2 * tp + r, c0, 64), f4(ks[0], ks[1], ks[2], ks[3]));
-      if (s == 0) {
-        st_at(sm, OFF_B + tf32_quad(t, c0, 48),
-              f4(kb[0] * inv_tau[0], kb[1] * inv_tau[1], kb[2] * inv_tau[2], kb[3] * inv_tau[3]));
-        st_at(sm, OFF_B + tf32_quad(16 + t, c0, 48), f4(kb[0], kb[1], kb[2], kb[3]));
-      } else {
-        st_at(sm, OFF_B + tf32_quad(16 + t, c0, 48),
-              f4(kb[0] * inv_tau[0], kb[1] * inv_tau[1], kb[2] * inv_tau[2], kb[3] * inv_tau[3]));
-      }
-      st_at(sm, OFF_KG + off16,
-            make_uint2(pack_f16x2(ks[0] * pre[0], ks[1] * pre[1]), pack_f16x2(ks[2] * pre[2], ks[3] * pre[3])));
+      hq[2 * half] = pack_f16x2(qf[0] * tau0, qf[1] * tau0);
+      hq[2 * half + 1] = pack_f16x2(qf[2] * tau0, qf[3] * tau0);
+      hk[2 * half] = pack_f16x2(kf[0] * tau0, kf[1] * tau0);
+      hk[2 * half + 1] = pack_f16x2(kf[2] * tau0, kf[3] * tau0);
+      hg[2 * half] = pack_f16x2(kg[0] * tau1, kg[1] * tau1);
+      hg[2 * half + 1] = pack_f16x2(kg[2] * tau1, kg[3] * tau1);
     }
-    // transposed tiles, per channel the 2 tokens of this thread: Q~^T into columns 32 + t of
-    // [-W^T | Q~^T], K^^T into row 32 + c of [P ; K^^T]
-    uint8_t *wq = sm + OFF_WQ + b * kWQBytes;
-    uint8_t *pk = sm + OFF_PK + b * kPKBytes;
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const uint32_t c = uint32_t(c0 + e);
-      const uint32_t col = 32u + uint32_t(tb);
-      st_at(wq, c * 128 + ((((col >> 3) ^ c) & 7u) << 4) + (col & 7u) * 2, pack_f16x2(qt_col[e][0], qt_col[e][1]));
-      st_at(pk, sw64_offset(32 + c, uint32_t(tb)), pack_f16x2(kh_col[e][0], kh_col[e][1]));
-    }
+    st_at(sm, OFF_WQ + b * kWQBytes + row + (((4u + grp) ^ sw) << 4), make_uint4(hq[0], hq[1], hq[2], hq[3]));
+    st_at(sm, OFF_PK + b * kPKBytes + sw64_chunk(32u + ch, grp), make_uint4(hg[0], hg[1], hg[2], hg[3]));
+    st_at(sm, OFF_KG + sw64_chunk(ch, grp), make_uint4(hk[0], hk[1], hk[2], hk[3]));
   };
 
-  auto issue_gram = [&]() {  // issuer
+  auto issue_gram = [&]() {  // issuer: 16 steps of 8 channels (32 bytes; 4 per 32-channel block)
     const uint64_t qk = kdesc128(sbase + OFF_QK), bb = kdesc128(sbase + OFF_B);
 #pragma unroll
     for (int ks = 0; ks < 16; ++ks) {
       const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-      umma_tf32(tmem + TM_GRAM, dadv(qk, kb * 64 * 128 + ko), dadv(bb, kb * 48 * 128 + ko), IDESC_GRAM, ks > 0);
+      umma_tf32(tmem + TM_GRAM, dadv(qk, kb * 64 * 128 + ko), dadv(bb, kb * 32 * 128 + ko), IDESC_GRAM, ks > 0);
     }
     umma_commit(&bars->gram);
   };
@@ -357,16 +322,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = c & 1, L = chunk_len(c);
     bad |= !mbar_wait_sleep(&bars->gram, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
-    // Gram row t' = 16 quarter + lane (M = 64 layout, lanes 0..15 of each quarter): quarters
-    // 0 / 2 hold the query rows of subtile 0 / 1 (P), quarters 1 / 3 the key rows (A)
+    // Gram row m = 16 quarter + lane (M = 64 layout, lanes 0..15 of each quarter): quarters
+    // 0 / 1 hold query rows t = 0..15 / 16..31 (P), quarters 2 / 3 the key rows (A);
+    // column i = key i
     uint8_t *pk = sm + OFF_PK + b * kPKBytes;
     float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
     if (grp < 2) {
-      const int s = quarter >> 1, part = grp, t = 16 * s + (lane & 15);
-      const bool is_p = (quarter & 1) == 0, have = part <= s;
+      const int s = quarter & 1, part = grp, t = 16 * s + (lane & 15);
+      const bool is_p = quarter < 2, have = part <= s;
       float vals[16];
       if (have) {
-        tmem_ld16(tmem + lane_base + TM_GRAM + (s == 0 ? 0 : 16) + 16 * part, vals);
+        tmem_ld16(tmem + lane_base + TM_GRAM + 16 * part, vals);
         tmem_ld_wait();
       }
       if (lane < 16) {
@@ -457,12 +423,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto issue_wu = [&](int c) {  // issuer: W^T and [U~^T | 0]
     const int b = c & 1;
-    const uint64_t tp = kdesc64(sbase + OFF_TP), kg = mndesc(sbase + OFF_KG, kC * 128),
+    const uint64_t tp = kdesc64(sbase + OFF_TP), kg = kdesc64(sbase + OFF_KG),
                    vin = mndesc(sbase + OFF_V + b * 8192, kC * 128);
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-      umma_f16(tmem + TM_W, dadv(kg, ks * 2048), dadv(tp, ks * 32), IDESC_WT, ks > 0);
-      umma_f16(tmem + tm_uo(b), dadv(vin, ks * 2048), dadv(tp, ks * 32), IDESC_UT, ks > 0);
+      umma_f16(tmem + TM_W, dadv(kg, ks * 32), dadv(tp, ks * 32), IDESC_WT, ks > 0);
+      umma_f16(tmem + tm_grp(b), dadv(vin, ks * 2048), dadv(tp, ks * 32), IDESC_UT, ks > 0);
     }
     umma_commit(&bars->wu);
   };
@@ -514,19 +480,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   for (int j = 0; j < n_chunks; ++j) {
     const int b = j & 1;
     const bool more = j + 1 < n_chunks;
-    // ---------------- P1: chain j, fp16 copy of S^T and decay in place; MMA1
+    // ---------------- P1: chain j, fp16 copy of S^T; decayed S^T into group j % 2; MMA1
     if (worker) {
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         float x[16];
-        tmem_ld16(s_cols + 16 * u, x);
+        tmem_ld16(s_cols(b ^ 1) + 16 * u, x);
         tmem_ld_wait();
         const uint32_t col = uint32_t(32 * grp + 16 * u);  // state column c of x[0]
         st_at(sm + OFF_ST, sw128_chunk(v_own, (col & 63u) >> 3, col >> 6, 128), pack8_f16(x));
         st_at(sm + OFF_ST, sw128_chunk(v_own, ((col & 63u) >> 3) + 1, col >> 6, 128), pack8_f16(x + 8));
+        const float4 *gam = reinterpret_cast<const float4 *>(s_gamma + b * kD + col);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) x[e] *= s_gamma[b * kD + col + e];
-        tmem_st16(s_cols + 16 * u, x);
+        for (int e = 0; e < 4; ++e) {
+          const float4 gv = gam[e];
+          x[4 * e] *= gv.x;
+          x[4 * e + 1] *= gv.y;
+          x[4 * e + 2] *= gv.z;
+          x[4 * e + 3] *= gv.w;
+        }
+        tmem_st16(s_cols(b) + 16 * u, x);
       }
       tmem_st_wait();
     }
@@ -539,7 +512,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {  // [U^T | O^T] += S^T [-W^T | Q~^T]
         const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-        umma_f16(tmem + tm_uo(b), dadv(st, kb * 16384 + ko), dadv(wq, ks * 2048), IDESC_UO, 1);
+        umma_f16(tmem + tm_grp(b), dadv(st, kb * 16384 + ko), dadv(wq, ks * 2048), IDESC_UO, 1);
       }
       umma_commit(&bars->mma1);
     }
@@ -561,7 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     if (worker) {
       float x[8];
-      tmem_ld8(tmem + lane_base + tm_uo(b) + 8 * grp, x);  // U^T row v, columns t = 8 grp ..
+      tmem_ld8(tmem + lane_base + tm_grp(b) + 8 * grp, x);  // U^T row v, columns t = 8 grp ..
       tmem_ld_wait();
       st_at(sm + OFF_UT, sw64_chunk(uint32_t(v_own), uint32_t(grp)), pack8_f16(x));
     }
@@ -572,10 +545,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (issuer) {
       const uint64_t ut = kdesc64(sbase + OFF_UT), pk = kdesc64(sbase + OFF_PK + b * kPKBytes);
 #pragma unroll
-      for (int ks = 0; ks < 2; ++ks) {  // O^T += U^T P^T ; S^T += U^T K^
-        umma_f16(tmem + tm_uo(b) + 32, dadv(ut, ks * 32), dadv(pk, ks * 32), IDESC_O2, 1);
-        umma_f16(tmem + TM_S, dadv(ut, ks * 32), dadv(pk, 32 * 64 + ks * 32), IDESC_S2, 1);
-      }
+      for (int ks = 0; ks < 2; ++ks)  // [O^T | S^T] += U^T [P ; K^^T]^T
+        umma_f16(tmem + tm_grp(b) + TM_O, dadv(ut, ks * 32), dadv(pk, ks * 32), IDESC_OS, 1);
       umma_commit(&bars->mma2);
     }
     // ---------------- P4: P, A, inverse, T', v of chunk j + 1; W^T and U~^T
@@ -594,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int L = chunk_len(j);
       const int64_t t0 = chunk_t0(j);
       float x[8];
-      tmem_ld8(tmem + lane_base + tm_uo(b) + 32 + 8 * grp, x);  // O^T row v, tokens 8 grp ..
+      tmem_ld8(tmem + lane_base + tm_grp(b) + TM_O + 8 * grp, x);  // O^T row v, tokens 8 grp ..
       tmem_ld_wait();
       int64_t idx = ((t0 + 8 * grp) * H + h) * int64_t(kD) + v_own;
       const int64_t step = int64_t(H) * kD;
@@ -610,11 +581,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
   }
 
-  if (final_state != nullptr && worker) {
+  if (final_state != nullptr && worker) {  // the last chunk's MMA2 left the state in its group
 #pragma unroll
     for (int u = 0; u < 2; ++u) {
       float x[16];
-      tmem_ld16(s_cols + 16 * u, x);
+      tmem_ld16(s_cols((n_chunks + 1) & 1) + 16 * u, x);
       tmem_ld_wait();
 #pragma unroll
       for (int e = 0; e < 16; ++e) final_state[st_base + int64_t(32 * grp + 16 * u + e) * kD + v_own] = x[e];

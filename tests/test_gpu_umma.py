@@ -4,7 +4,8 @@ on the GPU against host matrix products (kda_selftest_umma).
 Settings pinned here: 128-byte-swizzled K-major operands (leading byte offset
 16, stride byte offset 1024 = one 8-row swizzle atom) for bf16, fp16 and tf32;
 MN-major 16-bit operands with leading byte offset = the 64-element block
-stride (rows x 128 bytes) and stride byte offset 1024; the negate-A bit; and,
+stride (rows x 128 bytes) and stride byte offset 1024; 64-byte-swizzled K-major
+16-bit operands; the negate-A bit; and,
 for M = 64, accumulator row m in tensor-memory lane (m mod 16) + 32 (m div 16).
 The shapes are the ones the chunk-32 kernel issues."""
 
@@ -32,12 +33,12 @@ def _lanes_m64():
 
 CASES = [
     # fmt,  M,   N,   K, a_mn, b_mn, neg    use in the chunked kernel (sw64 cases: see SW64_CASES)
-    ("tf32", 64, 48, 128, False, False, False),  # Gram: all query/key rows x keys under two references
+    ("tf32", 64, 48, 128, False, False, False),
     ("f16", 128, 32, 32, True, False, False),    # W^T = Kg^T T'^T, Kg token-major
     ("f16", 128, 64, 32, True, False, False),    # [U~^T | 0] = V^T [T'; 0]^T, V token-major
     ("f16", 128, 64, 128, False, True, False),   # [U^T | O^T] += S^T [-W^T | Q~^T] (128-row MN-major B)
     ("f16", 128, 160, 32, False, False, False),  # [O^T | S^T] += U^T [P ; K^^T]^T
-    ("tf32", 64, 32, 128, False, False, False),
+    ("tf32", 64, 32, 128, False, False, False),  # Gram: [Q f ; K f] (K g)^T, one reference per chunk
     ("f16", 64, 128, 32, False, True, False),
     ("f16", 128, 32, 128, False, False, True),   # negate-A bit
     ("f16", 128, 128, 32, False, True, False),
@@ -54,6 +55,7 @@ SW64_CASES = [
     ("f16", 128, 32, 32, False, False, False),   # O^T += U^T P^T (U^T, P both 64-byte swizzled)
     ("f16", 128, 128, 32, False, False, False),  # S^T += U^T K^ (K^^T rows 64-byte swizzled)
     ("f16", 128, 128, 64, False, False, False),  # two 32-wide K blocks
+    ("f16", 128, 160, 32, False, False, False),  # [O^T | S^T] += U^T [P ; K^^T]^T in one product
     ("bf16", 64, 32, 32, False, False, False),
 ]
 
