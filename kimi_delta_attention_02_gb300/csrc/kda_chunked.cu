@@ -141,8 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, grp = warp >> 2;  // TMEM lane quarter, column group (compute warps)
-  const bool issuer = tid == kWorkers;             // lane 0 of warp 16
-  const bool worker = tid < kWorkers;
+  const bool worker = tid < kWorkers;              // warps 0..15; warp 16 issues TMA loads and MMAs
   const int h = int(blockIdx.x % H);
   const int64_t n = blockIdx.x / H;
   const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
@@ -162,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->mma2, 1);
     mbar_init(&bars->wu, 1);
     fence_mbarrier_init();
+    s_tmem[1] = 0u;  // abort flag
   }
   if (warp == 0) {
     tmem_alloc(s_tmem, TM_COLS);
@@ -215,33 +215,45 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_3d(dst + 4096, &tm_v, &bars->v[c & 1], 64, h, t0);
   };
 
-  bool bad = false;
-  // chunk index of a TMA load issued and not yet waited for (-1: none); tracked by every thread
-  int qkg_inflight = -1, v_inflight[2] = {-1, -1};
-  if (n_chunks > 0) {
-    if (issuer) issue_qkg(0);
-    qkg_inflight = 0;
-  }
-  for (int c = 0; c < 2 && c < n_chunks; ++c) {
-    if (issuer) issue_v(c);
-    v_inflight[c] = c;
-  }
+  bool bad = false;  // a bounded wait of this thread gave up
+  volatile uint32_t *s_abort = s_tmem + 1;
+  // chunks whose q/k/g and v loads were issued last (the issuer's abort path waits for them)
+  int qkg_last = -1, v_last[2] = {-1, -1};
   float b_next = (tid < kC && tid < eos - bos) ? beta[(bos + tid) * H + h] : 0.f;  // beta of chunk 0
+
+  // Synchronisation. The 16 compute warps meet on barrier BAR_WORK where they share
+  // data. They hand each finished group of operands to the issuing warp through one
+  // barrier per event (compute warps arrive, the issuer syncs), so MMA issue never
+  // holds them up. An event of chunk j + 1 always comes after a wait on an MMA or a
+  // load the issuer starts only past the same event of chunk j, so the compute warps
+  // never arrive twice at a barrier the issuer has not yet passed. If a compute
+  // thread's wait gave up, the compute warps raise s_abort before the hand-off the
+  // issuer waits for next, and both sides leave for the teardown.
+  constexpr uint32_t BAR_WORK = 1, H_COPY = 2, H_PREP = 3, H_U = 4, H_INV = 5;
+  auto handoff = [&](uint32_t id) {  // compute warps: operands of this event written
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_arrive(id, kThreads);
+  };
+  auto give_up = [&](uint32_t id) {
+    if (tid == 0) *s_abort = 1u;
+    handoff(id);
+  };
 
   // ------------------------------------------------------------------ P2: operand tiles
   // Thread (channel ch = v_own, tokens 8 grp .. 8 grp + 7): the decay prefix sums run
   // along its own 8 tokens; the 4 group totals of a channel meet in shared memory.
   // Everything is kept in log2 units (x log2 e), so each factor is one ex2.
-  auto prep = [&](int c) {
+  // Returns false when the compute warps give up.
+  auto prep = [&](int c) -> bool {
     const int b = c & 1, L = chunk_len(c);
     const int64_t t0 = chunk_t0(c);
     const float b_pref = b_next;
     if (tid < kC) b_next = (tid < eos - t0 - kC) ? beta[(t0 + kC + tid) * H + h] : 0.f;  // next chunk's
     bad |= !mbar_wait_sleep(&bars->qkg, uint32_t(c & 1), err_word, DEVERR_TMA_TIMEOUT);
-    qkg_inflight = -1;
     const int ch = v_own, tb = 8 * grp;
     float lg[8];  // log2 of Gamma within the group: sum of the group's decays up to each token
-    if (worker) {
+    {
       const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG) + tb * kD + ch;
       float run = 0.f;
 #pragma unroll
@@ -253,8 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       s_tot[grp * kD + ch] = run;
     }
     if (tid < kC) s_beta[tid] = b_pref;
-    __syncthreads();
-    if (!worker) return;
+    if (named_bar_or(BAR_WORK, kWorkers, bad)) {
+      give_up(H_PREP);
+      return false;
+    }
     const float T0 = s_tot[ch], T1 = s_tot[kD + ch], T2 = s_tot[2 * kD + ch], T3 = s_tot[3 * kD + ch];
     const float r2 = T0 + T1;                                                // log2 e^r
     const float last2 = r2 + (T2 + T3);                                      // log2 Gamma_last
@@ -291,9 +305,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         kf[e] = k * f;
         kg[e] = k * g;
         const uint32_t o4 = (r * 128 + ((cq ^ uint32_t(r)) << 4)) >> 2;  // token tb + r: row tb + r, t & 7 = r
-        gq[o4] = round_tf32(qf[e]);
-        gk[o4] = round_tf32(kf[e]);
-        gb[o4] = round_tf32(kg[e]);
+        gq[o4] = round_tf32_alu(qf[e]);
+        gk[o4] = round_tf32_alu(kf[e]);
+        gb[o4] = round_tf32_alu(kg[e]);
       }
       hq[2 * half] = pack_f16x2(qf[0] * tau0, qf[1] * tau0);
       hq[2 * half + 1] = pack_f16x2(qf[2] * tau0, qf[3] * tau0);
@@ -302,9 +316,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       hg[2 * half] = pack_f16x2(kg[0] * tau1, kg[1] * tau1);
       hg[2 * half + 1] = pack_f16x2(kg[2] * tau1, kg[3] * tau1);
     }
+    handoff(H_PREP);  // the Gram operands are complete; the fp16 tiles are needed later
     st_at(sm, OFF_WQ + b * kWQBytes + row + (((4u + grp) ^ sw) << 4), make_uint4(hq[0], hq[1], hq[2], hq[3]));
     st_at(sm, OFF_PK + b * kPKBytes + sw64_chunk(32u + ch, grp), make_uint4(hg[0], hg[1], hg[2], hg[3]));
     st_at(sm, OFF_KG + sw64_chunk(ch, grp), make_uint4(hk[0], hk[1], hk[2], hk[3]));
+    return true;
   };
 
   auto issue_gram = [&]() {  // issuer: 16 steps of 8 channels (32 bytes; 4 per 32-channel block)
@@ -318,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // ------------------------------------------------------------------ P4: P, A, inverse, T', v
-  auto extract_inverse = [&](int c) {
+  // Returns false when the compute warps give up.
+  auto extract_inverse = [&](int c) -> bool {
     const int b = c & 1, L = chunk_len(c);
     bad |= !mbar_wait_sleep(&bars->gram, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
@@ -355,7 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
     tc_fence_before();
-    __syncthreads();
+    named_bar_sync(BAR_WORK, kWorkers);
     float *Ts = reinterpret_cast<float *>(sm + OFF_ST + G_T);
     float *Xs = reinterpret_cast<float *>(sm + OFF_ST + G_X);
     if (warp == 0) {
@@ -373,7 +390,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) Ts[(lane >> 1) * kALd + 16 + 8 * (lane & 1) + e] = 0.f;  // block above
-    } else if (worker) {
+    } else {
       // v tile of this chunk: bf16 -> fp16 in place, rows past the sequence end zeroed
       bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
       uint8_t *vt = sm + OFF_V + b * 8192;
@@ -391,8 +408,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         *p = w;
       }
     }
-    v_inflight[b] = -1;
-    __syncthreads();
+    named_bar_sync(BAR_WORK, kWorkers);
     {
       // T_10 = -T_11 (A_10 T_00): thread (r, col) of the 16 x 16 block on warps 0..7
       const int r = (tid >> 4) & 15, col = tid & 15;
@@ -402,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int kk = 0; kk < 16; ++kk) xv = fmaf(As[(16 + r) * kALd + kk], Ts[kk * kALd + col], xv);
         Xs[r * 16 + col] = xv;
       }
-      __syncthreads();
+      named_bar_sync(BAR_WORK, kWorkers);
       if (tid < 256) {
         xv = 0.f;
 #pragma unroll
@@ -410,7 +426,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (kk <= r) xv = fmaf(Ts[(16 + r) * kALd + 16 + kk], Xs[kk * 16 + col], xv);
         Ts[(16 + r) * kALd + col] = -xv;
       }
-      __syncthreads();
+      named_bar_sync(BAR_WORK, kWorkers);
     }
     if (tid < 128) {  // T' = T Diag(beta) -> fp16 [t][i]
       const int t = tid >> 2, cj = tid & 3;
@@ -419,6 +435,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 8; ++e) x[e] = Ts[t * kALd + 8 * cj + e] * s_beta[8 * cj + e];
       st_at(sm, OFF_TP + sw64_chunk(t, cj), pack8_f16(x));
     }
+    // the inverse's scratch aliases the S^T tile that the next chain step rewrites: all
+    // compute threads are past it before any goes on
+    fence_proxy_async_smem();
+    const bool ab = named_bar_or(BAR_WORK, kWorkers, bad);
+    if (ab) give_up(H_INV);
+    else handoff(H_INV);
+    return !ab;
   };
 
   auto issue_wu = [&](int c) {  // issuer: W^T and [U~^T | 0]
@@ -438,11 +461,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int b = c & 1;
     bad |= !mbar_wait_sleep(&bars->wu, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
-    if (c + 2 < n_chunks) {  // the v stage of chunk c is consumed: load chunk c + 2 into it
-      if (issuer) issue_v(c + 2);
-      v_inflight[b] = c + 2;
-    }
-    if (!worker) return;
     float x[8];
     tmem_ld8(tmem + lane_base + TM_W + 8 * grp, x);  // W^T row c = v_own, columns t = 8 grp ..
     tmem_ld_wait();
@@ -452,36 +470,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     st_at(sm + OFF_WQ + b * kWQBytes, cr * 128 + (((uint32_t(grp) ^ cr) & 7u) << 4), pack8_f16(x));
   };
 
-  // ------------------------------------------------------------------ prologue: chunk 0's operands
-  if (n_chunks > 0) {
-    prep(0);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(bad)) goto abort;
-    tc_fence_after();
-    if (n_chunks > 1) {
-      if (issuer) issue_qkg(1);
-      qkg_inflight = 1;
+  if (worker) {
+    // ---------------------------------------------------------------- compute warps
+    if (n_chunks > 0) {  // chunk 0's operands
+      if (!prep(0)) goto teardown;
+      if (!extract_inverse(0)) goto teardown;
+      wt_extract(0);
     }
-    if (issuer) issue_gram();
-    extract_inverse(0);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(bad)) goto abort;
-    tc_fence_after();
-    if (issuer) issue_wu(0);
-    wt_extract(0);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(bad)) goto abort;
-    tc_fence_after();
-  }
-
-  for (int j = 0; j < n_chunks; ++j) {
-    const int b = j & 1;
-    const bool more = j + 1 < n_chunks;
-    // ---------------- P1: chain j, fp16 copy of S^T; decayed S^T into group j % 2; MMA1
-    if (worker) {
+    for (int j = 0; j < n_chunks; ++j) {
+      const int b = j & 1;
+      const bool more = j + 1 < n_chunks;
+      // ---------------- P1: chain j, fp16 copy of S^T; decayed S^T into group j % 2 -> MMA1
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         float x[16];
@@ -502,108 +501,130 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(s_cols(b) + 16 * u, x);
       }
       tmem_st_wait();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(bad)) goto abort;
-    tc_fence_after();
-    if (issuer) {
-      const uint64_t st = kdesc128(sbase + OFF_ST), wq = mndesc(sbase + OFF_WQ + b * kWQBytes, 128 * 128);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {  // [U^T | O^T] += S^T [-W^T | Q~^T]
-        const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-        umma_f16(tmem + tm_grp(b), dadv(st, kb * 16384 + ko), dadv(wq, ks * 2048), IDESC_UO, 1);
-      }
-      umma_commit(&bars->mma1);
-    }
-    // ---------------- P2: operand tiles of chunk j + 1; Gram
-    if (more) {
-      prep(j + 1);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      if (__syncthreads_or(bad)) goto abort;
+      handoff(H_COPY);
+      // ---------------- P2: operand tiles of chunk j + 1 -> Gram
+      if (more && !prep(j + 1)) goto teardown;
+      // ---------------- P3: chain j, U^T to fp16 -> MMA2
+      bad |= !mbar_wait_sleep(&bars->mma1, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
       tc_fence_after();
-      if (j + 2 < n_chunks) {
-        if (issuer) issue_qkg(j + 2);
-        qkg_inflight = j + 2;
+      {
+        float x[8];
+        tmem_ld8(tmem + lane_base + tm_grp(b) + 8 * grp, x);  // U^T row v, columns t = 8 grp ..
+        tmem_ld_wait();
+        st_at(sm + OFF_UT, sw64_chunk(uint32_t(v_own), uint32_t(grp)), pack8_f16(x));
       }
-      if (issuer) issue_gram();
-    }
-    // ---------------- P3: chain j, U^T to fp16; MMA2
-    bad |= !mbar_wait_sleep(&bars->mma1, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
-    tc_fence_after();
-    if (worker) {
-      float x[8];
-      tmem_ld8(tmem + lane_base + tm_grp(b) + 8 * grp, x);  // U^T row v, columns t = 8 grp ..
-      tmem_ld_wait();
-      st_at(sm + OFF_UT, sw64_chunk(uint32_t(v_own), uint32_t(grp)), pack8_f16(x));
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(bad)) goto abort;
-    tc_fence_after();
-    if (issuer) {
-      const uint64_t ut = kdesc64(sbase + OFF_UT), pk = kdesc64(sbase + OFF_PK + b * kPKBytes);
-#pragma unroll
-      for (int ks = 0; ks < 2; ++ks)  // [O^T | S^T] += U^T [P ; K^^T]^T
-        umma_f16(tmem + tm_grp(b) + TM_O, dadv(ut, ks * 32), dadv(pk, ks * 32), IDESC_OS, 1);
-      umma_commit(&bars->mma2);
-    }
-    // ---------------- P4: P, A, inverse, T', v of chunk j + 1; W^T and U~^T
-    if (more) {
-      extract_inverse(j + 1);
-      fence_proxy_async_smem();
-      tc_fence_before();
-      if (__syncthreads_or(bad)) goto abort;
+      handoff(H_U);
+      // ---------------- P4: P, A, inverse, T', v of chunk j + 1 -> W^T and U~^T
+      if (more && !extract_inverse(j + 1)) goto teardown;
+      // ---------------- P5: chain j, outputs
+      bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
       tc_fence_after();
-      if (issuer) issue_wu(j + 1);
-    }
-    // ---------------- P5: chain j, outputs
-    bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
-    tc_fence_after();
-    if (worker) {
-      const int L = chunk_len(j);
-      const int64_t t0 = chunk_t0(j);
-      float x[8];
-      tmem_ld8(tmem + lane_base + tm_grp(b) + TM_O + 8 * grp, x);  // O^T row v, tokens 8 grp ..
-      tmem_ld_wait();
-      int64_t idx = ((t0 + 8 * grp) * H + h) * int64_t(kD) + v_own;
-      const int64_t step = int64_t(H) * kD;
+      {
+        const int L = chunk_len(j);
+        const int64_t t0 = chunk_t0(j);
+        float x[8];
+        tmem_ld8(tmem + lane_base + tm_grp(b) + TM_O + 8 * grp, x);  // O^T row v, tokens 8 grp ..
+        tmem_ld_wait();
+        int64_t idx = ((t0 + 8 * grp) * H + h) * int64_t(kD) + v_own;
+        const int64_t step = int64_t(H) * kD;
 #pragma unroll
-      for (int e = 0; e < 8; ++e, idx += step)
-        if (8 * grp + e < L) store_elem<kOutBF16>(out, idx, scale * x[e]);
+        for (int e = 0; e < 8; ++e, idx += step)
+          if (8 * grp + e < L) store_elem<kOutBF16>(out, idx, scale * x[e]);
+      }
+      // ---------------- P6: -W^T of chunk j + 1
+      if (more) wt_extract(j + 1);
     }
-    // ---------------- P6: -W^T of chunk j + 1
-    if (more) wt_extract(j + 1);
-    fence_proxy_async_smem();
-    tc_fence_before();
-    if (__syncthreads_or(bad)) goto abort;
-    tc_fence_after();
+    if (final_state != nullptr) {  // the last chunk's MMA2 left the state in its group
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float x[16];
+        tmem_ld16(s_cols((n_chunks + 1) & 1) + 16 * u, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) final_state[st_base + int64_t(32 * grp + 16 * u + e) * kD + v_own] = x[e];
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- issuing warp
+    // The whole warp follows the hand-offs; lane 0 issues.
+    const bool leader = lane == 0;
+    auto sync_on = [&](uint32_t id) {
+      named_bar_sync(id, kThreads);
+      tc_fence_after();
+      return *s_abort == 0u;
+    };
+    if (n_chunks > 0) {
+      if (leader) {
+        issue_qkg(0);
+        issue_v(0);
+        if (n_chunks > 1) issue_v(1);
+      }
+      qkg_last = 0;
+      v_last[0] = 0;
+      if (n_chunks > 1) v_last[1] = 1;
+      if (!sync_on(H_PREP)) goto issuer_abort;
+      if (leader) {
+        if (n_chunks > 1) issue_qkg(1);
+        issue_gram();
+      }
+      if (n_chunks > 1) qkg_last = 1;
+      if (!sync_on(H_INV)) goto issuer_abort;
+      if (leader) issue_wu(0);
+      if (n_chunks > 2) {  // v stage 0 is free once W^T / U~^T of chunk 0 are done
+        mbar_wait_sleep(&bars->wu, 0u, err_word, DEVERR_MMA_TIMEOUT);
+        if (leader) issue_v(2);
+        v_last[0] = 2;
+      }
+    }
+    for (int j = 0; j < n_chunks; ++j) {
+      const int b = j & 1;
+      const bool more = j + 1 < n_chunks;
+      if (!sync_on(H_COPY)) goto issuer_abort;
+      if (leader) {  // MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]
+        const uint64_t st = kdesc128(sbase + OFF_ST), wq = mndesc(sbase + OFF_WQ + b * kWQBytes, 128 * 128);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
+          umma_f16(tmem + tm_grp(b), dadv(st, kb * 16384 + ko), dadv(wq, ks * 2048), IDESC_UO, 1);
+        }
+        umma_commit(&bars->mma1);
+      }
+      if (more) {
+        if (!sync_on(H_PREP)) goto issuer_abort;
+        if (leader) {
+          if (j + 2 < n_chunks) issue_qkg(j + 2);
+          issue_gram();
+        }
+        if (j + 2 < n_chunks) qkg_last = j + 2;
+      }
+      if (!sync_on(H_U)) goto issuer_abort;
+      if (leader) {  // MMA2: [O^T | S^T] += U^T [P ; K^^T]^T
+        const uint64_t ut = kdesc64(sbase + OFF_UT), pk = kdesc64(sbase + OFF_PK + b * kPKBytes);
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          umma_f16(tmem + tm_grp(b) + TM_O, dadv(ut, ks * 32), dadv(pk, ks * 32), IDESC_OS, 1);
+        umma_commit(&bars->mma2);
+      }
+      if (more) {
+        if (!sync_on(H_INV)) goto issuer_abort;
+        if (leader) issue_wu(j + 1);
+        if (j + 3 < n_chunks) {  // v stage (j + 1) % 2 is free once W^T / U~^T of chunk j + 1 are done
+          mbar_wait_sleep(&bars->wu, uint32_t((j + 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+          if (leader) issue_v(j + 3);
+          v_last[(j + 3) & 1] = j + 3;
+        }
+      }
+    }
   }
+  goto teardown;
 
-  if (final_state != nullptr && worker) {  // the last chunk's MMA2 left the state in its group
-#pragma unroll
-    for (int u = 0; u < 2; ++u) {
-      float x[16];
-      tmem_ld16(s_cols((n_chunks + 1) & 1) + 16 * u, x);
-      tmem_ld_wait();
-#pragma unroll
-      for (int e = 0; e < 16; ++e) final_state[st_base + int64_t(32 * grp + 16 * u + e) * kD + v_own] = x[e];
-    }
-  }
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, TM_COLS);
-  return;
+issuer_abort:
+  // the compute warps gave up: let this CTA's own loads in flight land (bounded) before exit
+  if (qkg_last >= 0) mbar_wait_sleep(&bars->qkg, uint32_t(qkg_last & 1), err_word, DEVERR_TMA_TIMEOUT);
+  for (int s = 0; s < 2; ++s)
+    if (v_last[s] >= 0) mbar_wait_sleep(&bars->v[s], uint32_t((v_last[s] >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
 
-abort:
-  // a bounded wait gave up: let this CTA's own copies in flight land (bounded), release TMEM
-  if (issuer) {
-    if (qkg_inflight >= 0) mbar_wait_sleep(&bars->qkg, uint32_t(qkg_inflight & 1), err_word, DEVERR_TMA_TIMEOUT);
-    for (int s = 0; s < 2; ++s)
-      if (v_inflight[s] >= 0)
-        mbar_wait_sleep(&bars->v[s], uint32_t((v_inflight[s] >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
-  }
+teardown:
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);

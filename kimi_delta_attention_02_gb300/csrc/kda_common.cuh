@@ -68,6 +68,13 @@ __device__ __forceinline__ float round_tf32(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return __uint_as_float(r);
 }
+// The same rounding on the integer ALU: adding half a tf32 unit in the last place to
+// the magnitude bits and clearing the 13 dropped bits rounds half away from zero (a
+// carry into the exponent is the correct round-up). Finite inputs only: a NaN whose
+// payload sits in the dropped bits may come out as infinity.
+__device__ __forceinline__ float round_tf32_alu(float x) {
+  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
+}
 
 // Element load/store for the two I/O dtypes (fp32 or bf16 bits).
 template <bool kBF16>
@@ -144,6 +151,29 @@ __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, 
     if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
   raise_device_error(err_word, code);
   return false;
+}
+
+// ---------------------------------------------------------------------------
+// Named CTA barriers (ids 1..15; id 0 is the one __syncthreads uses). `n` counts
+// threads, a multiple of 32; each taking part warp executes the call as a whole.
+// An arrive does not wait; it releases the arriving threads' earlier writes to
+// the threads that sync on the same barrier.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t n) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+// barrier among `n` threads that also returns the OR of `pred` over them
+__device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(uint32_t(pred)), "r"(id), "r"(n)
+      : "memory");
+  return r != 0;
 }
 
 // ---------------------------------------------------------------------------
