@@ -36,20 +36,23 @@
 // state S^T (rows v = value channels, columns c = key channels) stays in tensor
 // memory for the whole sequence, in two copies used alternately. Each iteration
 // j runs the state chain of chunk j interleaved with the state-independent work
-// of chunk j+1, so that each tensor-core group runs while the threads work on
-// the other stream:
+// of chunks j+1 and j+2, so that each tensor-core group runs while the threads
+// work on the other streams:
 //   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy;
 //                 MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]              (N = 64)
-//   P2  next j+1: decay prefix sums and the operand tiles (a thread owns one key
+//   P2  next j+2: decay prefix sums and the operand tiles (a thread owns one key
 //                 channel and 8 tokens); Gram (kind::tf32, M = 64 rows
 //                 [Q f ; K f] x N = 32 keys K g)
 //   P3  chain j : U^T to fp16; MMA2: [O^T | S^T] += U^T [P ; K^^T]^T   (N = 160)
-//   P4  next j+1: P and A out of TMEM, fp32 inverse of I + A (one warp), T',
-//                 v -> fp16; W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
+//   P4  next j+1: P and A out of TMEM (their Gram ran during the previous
+//                 iteration), fp32 inverse of I + A, T', v -> fp16;
+//                 W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
 //   P5  chain j : O^T out of TMEM to global memory
 //   P6  next j+1: -W^T into the [-W^T | Q~^T] tile
-// Per-chunk operand tiles are double-buffered by chunk parity. TMA brings q, k
-// and log-decay one chunk ahead and v two chunks ahead (128-byte swizzle).
+// Per-chunk operand tiles are double-buffered by chunk parity ([P ; K^^T] three
+// times, since it lives from P2 of chunk j to MMA2 of chunk j + 2), and so are the
+// Gram accumulators. TMA brings q, k and log-decay one chunk ahead of P2 and v two
+// chunks ahead of P4 (128-byte swizzle).
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -77,19 +80,22 @@ constexpr uint32_t OFF_ST = 96 * 1024;       // S^T fp16 [128][128]; the inverse
 constexpr uint32_t G_A = 0, G_T = 5 * 1024, G_X = 10 * 1024;
 constexpr uint32_t OFF_UT = 128 * 1024;      // U^T fp16 [128][32], 64-byte swizzle
 constexpr uint32_t OFF_TP = 136 * 1024;      // T' fp16 [64][32], 64-byte swizzle; rows 32..63 stay zero
-constexpr uint32_t OFF_KG = 140 * 1024;      // Kg^T = (K * Gamma)^T fp16 [128 c][32 i], 64-byte swizzle
-constexpr uint32_t OFF_WQ = 148 * 1024;      // 2 x [-W^T | Q~^T] fp16 [128 c][64] (MN-major B of MMA1)
+constexpr uint32_t OFF_KG = 140 * 1024;      // 2 x Kg^T = (K * Gamma)^T fp16 [128 c][32 i], 64-byte swizzle
+constexpr uint32_t kKGBytes = 8 * 1024;
+constexpr uint32_t OFF_WQ = 156 * 1024;      // 2 x [-W^T | Q~^T] fp16 [128 c][64] (MN-major B of MMA1)
 constexpr uint32_t kWQBytes = 16 * 1024;
-constexpr uint32_t OFF_PK = 180 * 1024;      // 2 x [P ; K^^T] fp16 [160 rows][32], 64-byte swizzle
+constexpr uint32_t OFF_PK = 188 * 1024;      // 3 x [P ; K^^T] fp16 [160 rows][32], 64-byte swizzle
 constexpr uint32_t kPKBytes = 10 * 1024;
-constexpr uint32_t OFF_MISC = 200 * 1024;    // beta, Gamma_last x2, group decay totals, barriers
-constexpr uint32_t kSmemBytes = 204 * 1024 + 1024;
+constexpr uint32_t OFF_MISC = 218 * 1024;    // beta x2, Gamma_last x2, group decay totals, barriers
+constexpr uint32_t kSmemBytes = 222 * 1024 + 1024;
 
 // TMEM columns: two groups [U^T | O^T | S^T] (32 + 32 + 128) used by chunk parity, then
-// Gram and W^T. Chunk j's MMA1 and MMA2 write group j % 2; its MMA2 leaves the state for
-// chunk j + 1 there, which P1 of chunk j + 1 reads and rewrites, decayed, into the other.
+// Gram (chunk parity 0), W^T, Gram (parity 1). Chunk j's MMA1 and MMA2 write group j % 2;
+// its MMA2 leaves the state for chunk j + 1 there, which P1 of chunk j + 1 reads and
+// rewrites, decayed, into the other.
 constexpr uint32_t TM_GROUP = 192, TM_O = 32, TM_SS = 64, TM_GRAM = 384, TM_W = 416, TM_COLS = 512;
 __device__ __forceinline__ uint32_t tm_grp(int b) { return TM_GROUP * uint32_t(b); }
+__device__ __forceinline__ uint32_t tm_gram(int c) { return TM_GRAM + 64u * uint32_t(c & 1); }
 
 constexpr uint32_t IDESC_GRAM = umma_idesc(UMMA_TF32, 64, 32, false, false, false);
 constexpr uint32_t IDESC_WT = umma_idesc(UMMA_F16, 128, 32, false, false, false);  // W^T = Kg^T T'^T
@@ -121,7 +127,7 @@ __device__ __forceinline__ float exp2_sfu(float x) {
 }
 
 struct Bars {
-  uint64_t qkg, v[2], mma1, gram, mma2, wu;
+  uint64_t qkg, v[2], mma1, gram[2], mma2, wu;
 };
 
 template <bool kOutBF16>
@@ -133,8 +139,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                        float *__restrict__ final_state, int H, float lb, float scale, uint32_t *err_word) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  float *s_beta = reinterpret_cast<float *>(sm + OFF_MISC);  // [32] of the chunk being prepared
-  float *s_gamma = s_beta + 32;                               // [2][128] Gamma_last by chunk parity
+  float *s_beta = reinterpret_cast<float *>(sm + OFF_MISC);  // [2][32] beta by chunk parity
+  float *s_gamma = s_beta + 2 * 32;                           // [2][128] Gamma_last by chunk parity
   float *s_tot = s_gamma + 2 * 128;                           // [4][128] log2 decay of each 8-token group
   Bars *bars = reinterpret_cast<Bars *>(s_tot + 4 * 128);
   uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 1);
@@ -157,7 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->v[0], 1);
     mbar_init(&bars->v[1], 1);
     mbar_init(&bars->mma1, 1);
-    mbar_init(&bars->gram, 1);
+    mbar_init(&bars->gram[0], 1);
+    mbar_init(&bars->gram[1], 1);
     mbar_init(&bars->mma2, 1);
     mbar_init(&bars->wu, 1);
     fence_mbarrier_init();
@@ -244,13 +251,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Thread (channel ch = v_own, tokens 8 grp .. 8 grp + 7): the decay prefix sums run
   // along its own 8 tokens; the 4 group totals of a channel meet in shared memory.
   // Everything is kept in log2 units (x log2 e), so each factor is one ex2.
-  // Returns false when the compute warps give up.
+  // Runs two chunks ahead of the state chain. Returns false when the compute warps give up.
   auto prep = [&](int c) -> bool {
     const int b = c & 1, L = chunk_len(c);
     const int64_t t0 = chunk_t0(c);
     const float b_pref = b_next;
     if (tid < kC) b_next = (tid < eos - t0 - kC) ? beta[(t0 + kC + tid) * H + h] : 0.f;  // next chunk's
     bad |= !mbar_wait_sleep(&bars->qkg, uint32_t(c & 1), err_word, DEVERR_TMA_TIMEOUT);
+    if (c >= 1)  // the Gram of chunk c - 1 has read the Gram tiles
+      bad |= !mbar_wait_sleep(&bars->gram[(c - 1) & 1], uint32_t(((c - 1) >> 1) & 1), err_word,
+                              DEVERR_MMA_TIMEOUT);
     const int ch = v_own, tb = 8 * grp;
     float lg[8];  // log2 of Gamma within the group: sum of the group's decays up to each token
     {
@@ -264,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       s_tot[grp * kD + ch] = run;
     }
-    if (tid < kC) s_beta[tid] = b_pref;
+    if (tid < kC) s_beta[b * kC + tid] = b_pref;
     if (named_bar_or(BAR_WORK, kWorkers, bad)) {
       give_up(H_PREP);
       return false;
@@ -317,43 +327,46 @@ __global__ void __launch_bounds__(kThreads, 1)
       hg[2 * half + 1] = pack_f16x2(kg[2] * tau1, kg[3] * tau1);
     }
     handoff(H_PREP);  // the Gram operands are complete; the fp16 tiles are needed later
+    st_at(sm, OFF_PK + (c % 3) * kPKBytes + sw64_chunk(32u + ch, grp), make_uint4(hg[0], hg[1], hg[2], hg[3]));
+    st_at(sm, OFF_KG + b * kKGBytes + sw64_chunk(ch, grp), make_uint4(hk[0], hk[1], hk[2], hk[3]));
+    if (c >= 2)  // MMA1 of chunk c - 2 has read its [-W^T | Q~^T] buffer, which chunk c reuses
+      bad |= !mbar_wait_sleep(&bars->mma1, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
     st_at(sm, OFF_WQ + b * kWQBytes + row + (((4u + grp) ^ sw) << 4), make_uint4(hq[0], hq[1], hq[2], hq[3]));
-    st_at(sm, OFF_PK + b * kPKBytes + sw64_chunk(32u + ch, grp), make_uint4(hg[0], hg[1], hg[2], hg[3]));
-    st_at(sm, OFF_KG + sw64_chunk(ch, grp), make_uint4(hk[0], hk[1], hk[2], hk[3]));
     return true;
   };
 
-  auto issue_gram = [&]() {  // issuer: 16 steps of 8 channels (32 bytes; 4 per 32-channel block)
+  auto issue_gram = [&](int c) {  // issuer: 16 steps of 8 channels (32 bytes; 4 per 32-channel block)
     const uint64_t qk = kdesc128(sbase + OFF_QK), bb = kdesc128(sbase + OFF_B);
 #pragma unroll
     for (int ks = 0; ks < 16; ++ks) {
       const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
-      umma_tf32(tmem + TM_GRAM, dadv(qk, kb * 64 * 128 + ko), dadv(bb, kb * 32 * 128 + ko), IDESC_GRAM, ks > 0);
+      umma_tf32(tmem + tm_gram(c), dadv(qk, kb * 64 * 128 + ko), dadv(bb, kb * 32 * 128 + ko), IDESC_GRAM,
+                ks > 0);
     }
-    umma_commit(&bars->gram);
+    umma_commit(&bars->gram[c & 1]);
   };
 
   // ------------------------------------------------------------------ P4: P, A, inverse, T', v
   // Returns false when the compute warps give up.
   auto extract_inverse = [&](int c) -> bool {
     const int b = c & 1, L = chunk_len(c);
-    bad |= !mbar_wait_sleep(&bars->gram, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
+    bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
     // Gram row m = 16 quarter + lane (M = 64 layout, lanes 0..15 of each quarter): quarters
     // 0 / 1 hold query rows t = 0..15 / 16..31 (P), quarters 2 / 3 the key rows (A);
     // column i = key i
-    uint8_t *pk = sm + OFF_PK + b * kPKBytes;
+    uint8_t *pk = sm + OFF_PK + (c % 3) * kPKBytes;
     float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
     if (grp < 2) {
       const int s = quarter & 1, part = grp, t = 16 * s + (lane & 15);
       const bool is_p = quarter < 2, have = part <= s;
       float vals[16];
       if (have) {
-        tmem_ld16(tmem + lane_base + TM_GRAM + 16 * part, vals);
+        tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * part, vals);
         tmem_ld_wait();
       }
       if (lane < 16) {
-        const float bt = s_beta[t];
+        const float bt = s_beta[b * kC + t];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
           const int i = 16 * part + e;
@@ -432,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t = tid >> 2, cj = tid & 3;
       float x[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = Ts[t * kALd + 8 * cj + e] * s_beta[8 * cj + e];
+      for (int e = 0; e < 8; ++e) x[e] = Ts[t * kALd + 8 * cj + e] * s_beta[b * kC + 8 * cj + e];
       st_at(sm, OFF_TP + sw64_chunk(t, cj), pack8_f16(x));
     }
     // the inverse's scratch aliases the S^T tile that the next chain step rewrites: all
@@ -446,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   auto issue_wu = [&](int c) {  // issuer: W^T and [U~^T | 0]
     const int b = c & 1;
-    const uint64_t tp = kdesc64(sbase + OFF_TP), kg = kdesc64(sbase + OFF_KG),
+    const uint64_t tp = kdesc64(sbase + OFF_TP), kg = kdesc64(sbase + OFF_KG + b * kKGBytes),
                    vin = mndesc(sbase + OFF_V + b * 8192, kC * 128);
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
@@ -472,8 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (worker) {
     // ---------------------------------------------------------------- compute warps
-    if (n_chunks > 0) {  // chunk 0's operands
+    if (n_chunks > 0) {  // operands of chunks 0 and 1
       if (!prep(0)) goto teardown;
+      if (n_chunks > 1 && !prep(1)) goto teardown;
       if (!extract_inverse(0)) goto teardown;
       wt_extract(0);
     }
@@ -502,8 +516,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       handoff(H_COPY);
-      // ---------------- P2: operand tiles of chunk j + 1 -> Gram
-      if (more && !prep(j + 1)) goto teardown;
+      // ---------------- P2: operand tiles of chunk j + 2 -> Gram
+      if (j + 2 < n_chunks && !prep(j + 2)) goto teardown;
       // ---------------- P3: chain j, U^T to fp16 -> MMA2
       bad |= !mbar_wait_sleep(&bars->mma1, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
       tc_fence_after();
@@ -562,12 +576,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       qkg_last = 0;
       v_last[0] = 0;
       if (n_chunks > 1) v_last[1] = 1;
-      if (!sync_on(H_PREP)) goto issuer_abort;
-      if (leader) {
-        if (n_chunks > 1) issue_qkg(1);
-        issue_gram();
+      for (int c = 0; c < 2 && c < n_chunks; ++c) {
+        if (!sync_on(H_PREP)) goto issuer_abort;
+        if (leader) {
+          if (c + 1 < n_chunks) issue_qkg(c + 1);
+          issue_gram(c);
+        }
+        if (c + 1 < n_chunks) qkg_last = c + 1;
       }
-      if (n_chunks > 1) qkg_last = 1;
       if (!sync_on(H_INV)) goto issuer_abort;
       if (leader) issue_wu(0);
       if (n_chunks > 2) {  // v stage 0 is free once W^T / U~^T of chunk 0 are done
@@ -589,17 +605,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(&bars->mma1);
       }
-      if (more) {
+      if (j + 2 < n_chunks) {
         if (!sync_on(H_PREP)) goto issuer_abort;
         if (leader) {
-          if (j + 2 < n_chunks) issue_qkg(j + 2);
-          issue_gram();
+          if (j + 3 < n_chunks) issue_qkg(j + 3);
+          issue_gram(j + 2);
         }
-        if (j + 2 < n_chunks) qkg_last = j + 2;
+        if (j + 3 < n_chunks) qkg_last = j + 3;
       }
       if (!sync_on(H_U)) goto issuer_abort;
       if (leader) {  // MMA2: [O^T | S^T] += U^T [P ; K^^T]^T
-        const uint64_t ut = kdesc64(sbase + OFF_UT), pk = kdesc64(sbase + OFF_PK + b * kPKBytes);
+        const uint64_t ut = kdesc64(sbase + OFF_UT), pk = kdesc64(sbase + OFF_PK + (j % 3) * kPKBytes);
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks)
           umma_f16(tmem + tm_grp(b) + TM_O, dadv(ut, ks * 32), dadv(pk, ks * 32), IDESC_OS, 1);
