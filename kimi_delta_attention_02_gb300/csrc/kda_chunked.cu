@@ -45,7 +45,7 @@
 //                 [Q f ; K f] x N = 32 keys K g)
 //   P3  chain j : U^T to fp16; MMA2: [O^T | S^T] += U^T [P ; K^^T]^T   (N = 160)
 //   P4  next j+1: P and A out of TMEM (their Gram ran during the previous
-//                 iteration), fp32 inverse of I + A, T', v -> fp16;
+//                 iteration), fp32 inverse of I + A (one warp), T', v -> fp16;
 //                 W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
 //   P5  chain j : O^T out of TMEM to global memory
 //   P6  next j+1: -W^T into the [-W^T | Q~^T] tile
@@ -350,37 +350,47 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Returns false when the compute warps give up.
   auto extract_inverse = [&](int c) -> bool {
     const int b = c & 1, L = chunk_len(c);
+    {  // v tile of this chunk: bf16 -> fp16 in place, rows past the sequence end zeroed (one chunk each)
+      bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
+      const int t = tid >> 4, cj = tid & 15;
+      uint4 *p = reinterpret_cast<uint4 *>(sm + OFF_V + b * 8192 + sw128_chunk(t, cj & 7, cj >> 3, kC));
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (t < L) {
+        const uint4 bv = *p;
+        const float2 a0 = unpack_bf16x2(bv.x), a1 = unpack_bf16x2(bv.y), a2 = unpack_bf16x2(bv.z),
+                     a3 = unpack_bf16x2(bv.w);
+        const float x[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
+        w = pack8_f16(x);
+      }
+      *p = w;
+    }
     bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
     // Gram row m = 16 quarter + lane (M = 64 layout, lanes 0..15 of each quarter): quarters
     // 0 / 1 hold query rows t = 0..15 / 16..31 (P), quarters 2 / 3 the key rows (A);
-    // column i = key i
-    uint8_t *pk = sm + OFF_PK + (c % 3) * kPKBytes;
+    // column i = key i. Warp (quarter, grp) takes columns 8 grp .. 8 grp + 7.
     float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
-    if (grp < 2) {
-      const int s = quarter & 1, part = grp, t = 16 * s + (lane & 15);
-      const bool is_p = quarter < 2, have = part <= s;
-      float vals[16];
+    {
+      const int s = quarter & 1, t = 16 * s + (lane & 15);
+      const bool is_p = quarter < 2, have = grp < 2 * (s + 1);  // columns up to the row block's end
+      float vals[8];
       if (have) {
-        tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * part, vals);
+        tmem_ld8(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
         tmem_ld_wait();
       }
       if (lane < 16) {
         const float bt = s_beta[b * kC + t];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int i = 16 * part + e;
+        for (int e = 0; e < 8; ++e) {
+          const int i = 8 * grp + e;
           const bool keep = have && t < L && (is_p ? i <= t : i < t);
           vals[e] = keep ? (is_p ? vals[e] : bt * vals[e]) : 0.f;
         }
         if (is_p) {
-          st_at(pk, sw64_chunk(t, 2 * part), pack8_f16(vals));
-          st_at(pk, sw64_chunk(t, 2 * part + 1), pack8_f16(vals + 8));
-        } else {
-#pragma unroll
-          for (int i4 = 0; i4 < 4; ++i4)
-            *reinterpret_cast<float4 *>(As + t * kALd + 16 * part + 4 * i4) =
-                make_float4(vals[4 * i4], vals[4 * i4 + 1], vals[4 * i4 + 2], vals[4 * i4 + 3]);
+          st_at(sm + OFF_PK + (c % 3) * kPKBytes, sw64_chunk(t, grp), pack8_f16(vals));
+        } else if (have) {
+          *reinterpret_cast<float4 *>(As + t * kALd + 8 * grp) = make_float4(vals[0], vals[1], vals[2], vals[3]);
+          *reinterpret_cast<float4 *>(As + t * kALd + 8 * grp + 4) = make_float4(vals[4], vals[5], vals[6], vals[7]);
         }
       }
     }
@@ -403,23 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
 #pragma unroll
       for (int e = 0; e < 8; ++e) Ts[(lane >> 1) * kALd + 16 + 8 * (lane & 1) + e] = 0.f;  // block above
-    } else {
-      // v tile of this chunk: bf16 -> fp16 in place, rows past the sequence end zeroed
-      bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
-      uint8_t *vt = sm + OFF_V + b * 8192;
-      for (int e = tid - 32; e < kC * 16; e += kWorkers - 32) {
-        const int t = e >> 4, cj = e & 15;
-        uint4 *p = reinterpret_cast<uint4 *>(vt + sw128_chunk(t, cj & 7, cj >> 3, kC));
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (t < L) {
-          const uint4 bv = *p;
-          const float2 a0 = unpack_bf16x2(bv.x), a1 = unpack_bf16x2(bv.y), a2 = unpack_bf16x2(bv.z),
-                       a3 = unpack_bf16x2(bv.w);
-          const float x[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
-          w = pack8_f16(x);
-        }
-        *p = w;
-      }
     }
     named_bar_sync(BAR_WORK, kWorkers);
     {
