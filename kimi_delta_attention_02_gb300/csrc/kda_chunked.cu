@@ -38,17 +38,17 @@
 // j runs the state chain of chunk j interleaved with the state-independent work
 // of chunks j+1 and j+2, so that each tensor-core group runs while the threads
 // work on the other streams:
-//   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy;
-//                 MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]              (N = 64)
+//   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy
+//   P6  chain j : -W^T of chunk j into the [-W^T | Q~^T] tile (its MMA ran during
+//                 P1); MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]           (N = 64)
 //   P2  next j+2: decay prefix sums and the operand tiles (a thread owns one key
 //                 channel and 8 tokens); Gram (kind::tf32, M = 64 rows
 //                 [Q f ; K f] x N = 32 keys K g)
 //   P3  chain j : U^T to fp16; MMA2: [O^T | S^T] += U^T [P ; K^^T]^T   (N = 160)
 //   P4  next j+1: P and A out of TMEM (their Gram ran during the previous
-//                 iteration), fp32 inverse of I + A (one warp), T', v -> fp16;
+//                 iteration), v -> fp16; then warps 0..3 invert I + A and form T'
+//                 while warps 4..15 write O^T of chunk j (P5) to global memory;
 //                 W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
-//   P5  chain j : O^T out of TMEM to global memory
-//   P6  next j+1: -W^T into the [-W^T | Q~^T] tile
 // Per-chunk operand tiles are double-buffered by chunk parity ([P ; K^^T] three
 // times, since it lives from P2 of chunk j to MMA2 of chunk j + 2), and so are the
 // Gram accumulators. TMA brings q, k and log-decay one chunk ahead of P2 and v two
@@ -236,7 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // never arrive twice at a barrier the issuer has not yet passed. If a compute
   // thread's wait gave up, the compute warps raise s_abort before the hand-off the
   // issuer waits for next, and both sides leave for the teardown.
-  constexpr uint32_t BAR_WORK = 1, H_COPY = 2, H_PREP = 3, H_U = 4, H_INV = 5;
+  constexpr uint32_t BAR_WORK = 1, H_COPY = 2, H_PREP = 3, H_U = 4, H_INV = 5, BAR_INV = 6;
   auto handoff = [&](uint32_t id) {  // compute warps: operands of this event written
     fence_proxy_async_smem();
     tc_fence_before();
@@ -346,9 +346,31 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma_commit(&bars->gram[c & 1]);
   };
 
+  // ------------------------------------------------------------------ P5: outputs
+  // O^T of chunk j out of TMEM to global memory, on warps 4..15 (column groups 1..3 of each
+  // lane quarter): group g takes 11, 11 and 10 of the 32 tokens.
+  auto out_chunk = [&](int j) {
+    bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
+    tc_fence_after();
+    const int L = chunk_len(j), g1 = grp - 1;
+    const int col0 = g1 == 0 ? 0 : g1 == 1 ? 11 : 16;           // first TMEM column loaded
+    const int lo = g1 == 0 ? 0 : g1 == 1 ? 11 : 22, hi = g1 == 0 ? 11 : g1 == 1 ? 22 : 32;
+    float x[16];
+    tmem_ld16(tmem + lane_base + tm_grp(j & 1) + TM_O + col0, x);  // O^T row v, tokens col0 ..
+    tmem_ld_wait();
+    int64_t idx = ((chunk_t0(j) + col0) * H + h) * int64_t(kD) + v_own;
+    const int64_t step = int64_t(H) * kD;
+#pragma unroll
+    for (int e = 0; e < 16; ++e, idx += step) {
+      const int tok = col0 + e;
+      if (tok >= lo && tok < hi && tok < L) store_elem<kOutBF16>(out, idx, scale * x[e]);
+    }
+  };
+
   // ------------------------------------------------------------------ P4: P, A, inverse, T', v
-  // Returns false when the compute warps give up.
-  auto extract_inverse = [&](int c) -> bool {
+  // Inverse-side work of chunk c on warps 0..3 while warps 4..15 write the outputs of chunk
+  // j_out (if >= 0). Returns false when the compute warps give up.
+  auto extract_inverse = [&](int c, int j_out) -> bool {
     const int b = c & 1, L = chunk_len(c);
     {  // v tile of this chunk: bf16 -> fp16 in place, rows past the sequence end zeroed (one chunk each)
       bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
@@ -396,50 +418,71 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_before();
     named_bar_sync(BAR_WORK, kWorkers);
-    float *Ts = reinterpret_cast<float *>(sm + OFF_ST + G_T);
-    float *Xs = reinterpret_cast<float *>(sm + OFF_ST + G_X);
-    if (warp == 0) {
-      // T = (I + A)^{-1}: lanes 0..15 column `lane` of diagonal block 0, lanes 16..31 of block 1
-      // (right-looking forward substitution); the block below the diagonal follows
-      const int s = lane >> 4, j = lane & 15;
-      float x[16];
+    if (grp == 0) {
+      // warps 0..3: T = (I + A)^{-1}, then T' = T Diag(beta)
+      float *Ts = reinterpret_cast<float *>(sm + OFF_ST + G_T);
+      float *Xs = reinterpret_cast<float *>(sm + OFF_ST + G_X);
+      if (warp == 0) {
+        // diagonal blocks: lanes 0..15 column `lane` of block 0, lanes 16..31 of block 1
+        // (right-looking forward substitution), and the zero block above the diagonal
+        const int s = lane >> 4, j = lane & 15;
+        float x[16];
 #pragma unroll
-      for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+        for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
 #pragma unroll
-      for (int m = 0; m < 16; ++m) {
-        Ts[(16 * s + m) * kALd + 16 * s + j] = x[m];
+        for (int m = 0; m < 16; ++m) {
+          Ts[(16 * s + m) * kALd + 16 * s + j] = x[m];
 #pragma unroll
-        for (int r = m + 1; r < 16; ++r) x[r] = fmaf(-As[(16 * s + r) * kALd + 16 * s + m], x[m], x[r]);
+          for (int r = m + 1; r < 16; ++r) x[r] = fmaf(-As[(16 * s + r) * kALd + 16 * s + m], x[m], x[r]);
+        }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) Ts[(lane >> 1) * kALd + 16 + 8 * (lane & 1) + e] = 0.f;
       }
+      named_bar_sync(BAR_INV, 128);
+      // block below the diagonal, T_10 = -T_11 (A_10 T_00): thread (row r, columns 2 c2, 2 c2 + 1)
+      const int r = tid >> 3, c2 = tid & 7;
+      float rowv[16];
+      auto load_row = [&](const float *src) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) Ts[(lane >> 1) * kALd + 16 + 8 * (lane & 1) + e] = 0.f;  // block above
-    }
-    named_bar_sync(BAR_WORK, kWorkers);
-    {
-      // T_10 = -T_11 (A_10 T_00): thread (r, col) of the 16 x 16 block on warps 0..7
-      const int r = (tid >> 4) & 15, col = tid & 15;
-      float xv = 0.f;
-      if (tid < 256) {
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 v4 = reinterpret_cast<const float4 *>(src)[q4];
+          rowv[4 * q4] = v4.x;
+          rowv[4 * q4 + 1] = v4.y;
+          rowv[4 * q4 + 2] = v4.z;
+          rowv[4 * q4 + 3] = v4.w;
+        }
+      };
+      load_row(As + (16 + r) * kALd);  // A_10 row r
+      float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk) xv = fmaf(As[(16 + r) * kALd + kk], Ts[kk * kALd + col], xv);
-        Xs[r * 16 + col] = xv;
+      for (int k = 0; k < 16; ++k) {
+        const float2 t2 = *reinterpret_cast<const float2 *>(Ts + k * kALd + 2 * c2);  // T_00 row k
+        acc.x = fmaf(rowv[k], t2.x, acc.x);
+        acc.y = fmaf(rowv[k], t2.y, acc.y);
       }
-      named_bar_sync(BAR_WORK, kWorkers);
-      if (tid < 256) {
-        xv = 0.f;
+      *reinterpret_cast<float2 *>(Xs + r * 16 + 2 * c2) = acc;
+      named_bar_sync(BAR_INV, 128);
+      load_row(Ts + (16 + r) * kALd + 16);  // T_11 row r (zero above its diagonal)
+      acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int kk = 0; kk < 16; ++kk)
-          if (kk <= r) xv = fmaf(Ts[(16 + r) * kALd + 16 + kk], Xs[kk * 16 + col], xv);
-        Ts[(16 + r) * kALd + col] = -xv;
+      for (int k = 0; k < 16; ++k) {
+        const float2 x2 = *reinterpret_cast<const float2 *>(Xs + k * 16 + 2 * c2);
+        acc.x = fmaf(-rowv[k], x2.x, acc.x);
+        acc.y = fmaf(-rowv[k], x2.y, acc.y);
       }
-      named_bar_sync(BAR_WORK, kWorkers);
-    }
-    if (tid < 128) {  // T' = T Diag(beta) -> fp16 [t][i]
-      const int t = tid >> 2, cj = tid & 3;
-      float x[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) x[e] = Ts[t * kALd + 8 * cj + e] * s_beta[b * kC + 8 * cj + e];
-      st_at(sm, OFF_TP + sw64_chunk(t, cj), pack8_f16(x));
+      *reinterpret_cast<float2 *>(Ts + (16 + r) * kALd + 2 * c2) = acc;
+      named_bar_sync(BAR_INV, 128);
+      {  // T' = T Diag(beta) -> fp16 [t][i]
+        const int t = tid >> 2, cj = tid & 3;
+        const float4 *trow = reinterpret_cast<const float4 *>(Ts + t * kALd + 8 * cj);
+        const float4 *brow = reinterpret_cast<const float4 *>(s_beta + b * kC + 8 * cj);
+        const float4 t0v = trow[0], t1v = trow[1], b0v = brow[0], b1v = brow[1];
+        const float x[8] = {t0v.x * b0v.x, t0v.y * b0v.y, t0v.z * b0v.z, t0v.w * b0v.w,
+                            t1v.x * b1v.x, t1v.y * b1v.y, t1v.z * b1v.z, t1v.w * b1v.w};
+        st_at(sm, OFF_TP + sw64_chunk(t, cj), pack8_f16(x));
+      }
+    } else if (j_out >= 0) {
+      out_chunk(j_out);  // warps 4..15 meanwhile write the outputs of the chain's chunk
     }
     // the inverse's scratch aliases the S^T tile that the next chain step rewrites: all
     // compute threads are past it before any goes on
@@ -481,13 +524,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n_chunks > 0) {  // operands of chunks 0 and 1
       if (!prep(0)) goto teardown;
       if (n_chunks > 1 && !prep(1)) goto teardown;
-      if (!extract_inverse(0)) goto teardown;
-      wt_extract(0);
+      if (!extract_inverse(0, -1)) goto teardown;
     }
     for (int j = 0; j < n_chunks; ++j) {
       const int b = j & 1;
       const bool more = j + 1 < n_chunks;
-      // ---------------- P1: chain j, fp16 copy of S^T; decayed S^T into group j % 2 -> MMA1
+      // ---------------- P1: chain j, fp16 copy of S^T; decayed S^T into group j % 2
+      if (j > 0) {  // the state MMA2 of chunk j - 1 left (warps 4..15 have waited for it already)
+        bad |= !mbar_wait_sleep(&bars->mma2, uint32_t((j - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+        tc_fence_after();
+      }
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         float x[16];
@@ -508,6 +554,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(s_cols(b) + 16 * u, x);
       }
       tmem_st_wait();
+      // ---------------- P6: -W^T of chunk j (its W^T / U~^T MMA ran during P1) -> MMA1
+      wt_extract(j);
       handoff(H_COPY);
       // ---------------- P2: operand tiles of chunk j + 2 -> Gram
       if (j + 2 < n_chunks && !prep(j + 2)) goto teardown;
@@ -521,25 +569,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_at(sm + OFF_UT, sw64_chunk(uint32_t(v_own), uint32_t(grp)), pack8_f16(x));
       }
       handoff(H_U);
-      // ---------------- P4: P, A, inverse, T', v of chunk j + 1 -> W^T and U~^T
-      if (more && !extract_inverse(j + 1)) goto teardown;
-      // ---------------- P5: chain j, outputs
-      bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
-      tc_fence_after();
-      {
-        const int L = chunk_len(j);
-        const int64_t t0 = chunk_t0(j);
-        float x[8];
-        tmem_ld8(tmem + lane_base + tm_grp(b) + TM_O + 8 * grp, x);  // O^T row v, tokens 8 grp ..
-        tmem_ld_wait();
-        int64_t idx = ((t0 + 8 * grp) * H + h) * int64_t(kD) + v_own;
-        const int64_t step = int64_t(H) * kD;
-#pragma unroll
-        for (int e = 0; e < 8; ++e, idx += step)
-          if (8 * grp + e < L) store_elem<kOutBF16>(out, idx, scale * x[e]);
+      // ---------------- P4 / P5: inverse side of chunk j + 1 -> W^T and U~^T, and outputs of chunk j
+      if (more) {
+        if (!extract_inverse(j + 1, j)) goto teardown;
+      } else if (grp >= 1) {
+        out_chunk(j);
       }
-      // ---------------- P6: -W^T of chunk j + 1
-      if (more) wt_extract(j + 1);
+    }
+    if (n_chunks > 0) {  // the last chunk's MMA2 (warps 4..15 have waited for it already)
+      bad |= !mbar_wait_sleep(&bars->mma2, uint32_t((n_chunks - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+      tc_fence_after();
     }
     if (final_state != nullptr) {  // the last chunk's MMA2 left the state in its group
 #pragma unroll
