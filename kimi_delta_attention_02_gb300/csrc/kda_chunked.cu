@@ -46,7 +46,8 @@
 //                 [Q f ; K f] x N = 32 keys K g)
 //   P3  chain j : U^T to fp16; MMA2: [O^T | S^T] += U^T [P ; K^^T]^T   (N = 160)
 //   P4  next j+1: P and A out of TMEM (their Gram ran during the previous
-//                 iteration), v -> fp16; then warps 0..3 invert I + A and form T'
+//                 iteration), v -> fp16; then warps 0..3 invert I + A (8 x 8 and
+//                 16 x 16 blocks) and form T'
 //                 while warps 4..15 write O^T of chunk j (P5) to global memory;
 //                 W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
 // Per-chunk operand tiles are double-buffered by chunk parity ([P ; K^^T] three
@@ -422,21 +423,60 @@ __global__ void __launch_bounds__(kThreads, 1)
       // warps 0..3: T = (I + A)^{-1}, then T' = T Diag(beta)
       float *Ts = reinterpret_cast<float *>(sm + OFF_ST + G_T);
       float *Xs = reinterpret_cast<float *>(sm + OFF_ST + G_X);
-      if (warp == 0) {
-        // diagonal blocks: lanes 0..15 column `lane` of block 0, lanes 16..31 of block 1
-        // (right-looking forward substitution), and the zero block above the diagonal
-        const int s = lane >> 4, j = lane & 15;
-        float x[16];
+      if (warp < 2) {
+        // diagonal block s = warp (16 x 16) in 8 x 8 pieces, warp-synchronous
+        const int base = 16 * warp;
+        if (lane < 16) {  // the two 8 x 8 diagonal pieces: lane = column of its piece
+          const int o = base + 8 * (lane >> 3), cc = lane & 7;
+          float x[8];
 #pragma unroll
-        for (int r = 0; r < 16; ++r) x[r] = (r == j) ? 1.f : 0.f;
+          for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-        for (int m = 0; m < 16; ++m) {
-          Ts[(16 * s + m) * kALd + 16 * s + j] = x[m];
+          for (int m = 0; m < 8; ++m) {
+            Ts[(o + m) * kALd + o + cc] = x[m];
 #pragma unroll
-          for (int r = m + 1; r < 16; ++r) x[r] = fmaf(-As[(16 * s + r) * kALd + 16 * s + m], x[m], x[r]);
+            for (int r = m + 1; r < 8; ++r) x[r] = fmaf(-As[(o + r) * kALd + o + m], x[m], x[r]);
+          }
+        } else {  // the zero 8 x 8 piece above the diagonal
+          const int l = lane - 16;
+          *reinterpret_cast<float4 *>(Ts + (base + (l >> 1)) * kALd + base + 8 + 4 * (l & 1)) =
+              make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        __syncwarp();
+        // piece below the diagonal: -T_11 (A_10 T_00); lane (row r8, columns 2 c8, 2 c8 + 1)
+        float *Xw = Xs + 64 * warp;
+        const int r8 = lane >> 2, c8 = lane & 3;
+        float a8[8];
+        {
+          const float4 *ar = reinterpret_cast<const float4 *>(As + (base + 8 + r8) * kALd + base);
+          const float4 p0 = ar[0], p1 = ar[1];
+          a8[0] = p0.x; a8[1] = p0.y; a8[2] = p0.z; a8[3] = p0.w; a8[4] = p1.x; a8[5] = p1.y; a8[6] = p1.z; a8[7] = p1.w;
+        }
+        float2 acc8 = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) Ts[(lane >> 1) * kALd + 16 + 8 * (lane & 1) + e] = 0.f;
+        for (int k = 0; k < 8; ++k) {
+          const float2 t2 = *reinterpret_cast<const float2 *>(Ts + (base + k) * kALd + base + 2 * c8);
+          acc8.x = fmaf(a8[k], t2.x, acc8.x);
+          acc8.y = fmaf(a8[k], t2.y, acc8.y);
+        }
+        *reinterpret_cast<float2 *>(Xw + r8 * 8 + 2 * c8) = acc8;
+        __syncwarp();
+        {
+          const float4 *tr = reinterpret_cast<const float4 *>(Ts + (base + 8 + r8) * kALd + base + 8);
+          const float4 p0 = tr[0], p1 = tr[1];
+          a8[0] = p0.x; a8[1] = p0.y; a8[2] = p0.z; a8[3] = p0.w; a8[4] = p1.x; a8[5] = p1.y; a8[6] = p1.z; a8[7] = p1.w;
+        }
+        acc8 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float2 x2 = *reinterpret_cast<const float2 *>(Xw + k * 8 + 2 * c8);
+          acc8.x = fmaf(-a8[k], x2.x, acc8.x);
+          acc8.y = fmaf(-a8[k], x2.y, acc8.y);
+        }
+        *reinterpret_cast<float2 *>(Ts + (base + 8 + r8) * kALd + base + 2 * c8) = acc8;
+      } else {  // warps 2, 3: the zero 16 x 16 block above the diagonal
+        const int l = tid - 64;
+        *reinterpret_cast<float4 *>(Ts + (l >> 2) * kALd + 16 + 4 * (l & 3)) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       named_bar_sync(BAR_INV, 128);
       // block below the diagonal, T_10 = -T_11 (A_10 T_00): thread (row r, columns 2 c2, 2 c2 + 1)

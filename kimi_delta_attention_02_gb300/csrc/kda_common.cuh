@@ -144,9 +144,12 @@ __device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity, uint32
   return false;
 }
 // The same bound, waiting in sleeps of up to 10 microseconds (about 2 s in total):
-// a waiting thread issues a handful of instructions instead of spinning.
+// a waiting thread issues a handful of instructions instead of spinning. A phase that
+// has already completed is seen by one plain probe, which is much cheaper than a
+// probe with a suspend-time hint.
 constexpr uint32_t kSleepNs = 10000, kSleepLimit = 200000;
 __device__ __forceinline__ bool mbar_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t *err_word, uint32_t code) {
+  if (mbar_try_wait(bar, parity)) return true;
   for (uint32_t i = 0; i < kSleepLimit; ++i)
     if (mbar_try_wait_sleep(bar, parity, kSleepNs)) return true;
   raise_device_error(err_word, code);
