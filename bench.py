@@ -1,5 +1,6 @@
 """Benchmark: KDA prefill tokens/s on the K3-shaped layer (B=1, T=4096, H=96,
-d_k=d_v=128, bf16 q/k/v, fp32 log_alpha/beta/state, chunk 64), with the
+d_k=d_v=128, bf16 q/k/v, fp32 log_alpha/beta/state; the kernel walks 32-token
+chunks, which gives the same result as any other chunk length), with the
 roofline of the prefill kernel, plus the decode step (B=256, H=96, 64 in-place
 steps) in GB/s against HBM, the fp64 CPU oracle timed on this host, and an
 end-to-end number through host buffers. Prints ONE JSON line (rank 0).
@@ -14,6 +15,7 @@ path); the timed region is bracketed by barriers and the max over ranks is kept.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import os
 import statistics
@@ -145,6 +147,23 @@ def max_over_ranks(x: float, world: int, device="cuda") -> float:
 def weak_scaling_value(world: int, tokens_per_rank: int, ms_per_step: float) -> float:
     """Whole-job tokens/s: every rank processes its own copy of the workload."""
     return world * tokens_per_rank / (ms_per_step / 1e3)
+
+
+def prefill_traffic():
+    """DRAM bytes (read + write) of one prefill launch on the headline workload, from the ncu
+    capture recorded in profiles/prefill_traffic.json, or None when the kernel sources have
+    changed since that capture (the record carries a hash of them)."""
+    path = os.path.join(ROOT, "profiles", "prefill_traffic.json")
+    try:
+        with open(path) as fh:
+            rec = json.load(fh)
+        h = hashlib.sha256()
+        for rel in rec["sources"]:
+            with open(os.path.join(ROOT, rel), "rb") as fh:
+                h.update(fh.read())
+    except (OSError, KeyError, ValueError):
+        return None
+    return rec.get("bytes_per_launch") if h.hexdigest() == rec.get("sources_sha256") else None
 
 
 def time_prefill(case, steps, warmup, world):
@@ -311,11 +330,7 @@ def main():
     alg_flops = T * H * PREFILL_FLOPS_PER_TOKEN_HEAD
     achieved_gbs = alg_bytes / (launch_avg_ms / 1e3) / 1e9
     achieved_tf = alg_flops / (launch_avg_ms / 1e3) / 1e12
-    traffic = None
-    tpath = os.path.join(ROOT, "profiles", "prefill_traffic.json")
-    if os.path.exists(tpath):
-        with open(tpath) as fh:
-            traffic = json.load(fh).get("bytes_per_launch")
+    traffic = prefill_traffic() if H == PREFILL["H"] else None
 
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     dec_bytes = DECODE["B"] * DECODE["H"] * DECODE_BYTES_PER_SEQ_HEAD
@@ -351,9 +366,10 @@ def main():
                          "launch_ms": launch_avg_ms, "alg_bytes": alg_bytes, "alg_flops": alg_flops},
             "decode": {"workload": "decode_B256_H96", "ms_per_step": dec_avg_ms, "GB/s": dec_gbs,
                        "peak": hbm_gbs, "frac": dec_gbs / hbm_gbs,
-                       "tokens_per_s": DECODE["B"] / (dec_avg_ms / 1e3), "alg_bytes": dec_bytes},
+                       "tokens_per_s": DECODE["B"] / (dec_avg_ms / 1e3), "alg_bytes": dec_bytes,
+                       "launches": len(dec_ms)},
             "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk,
-            "gpu_launches": args.steps + DECODE["steps"],
+            "gpu_launches": args.steps,  # one prefill launch per timed step (decode: its own region)
         }
         print(json.dumps(line), flush=True)
     if world > 1:
