@@ -58,6 +58,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "kda_common.cuh"
 
@@ -263,70 +264,80 @@ __global__ void __launch_bounds__(kThreads, 1)
       bad |= !mbar_wait_sleep(&bars->gram[(c - 1) & 1], uint32_t(((c - 1) >> 1) & 1), err_word,
                               DEVERR_MMA_TIMEOUT);
     const int ch = v_own, tb = 8 * grp;
+    // Every chunk but the last of a sequence is full: it takes code without the masks.
+    const bool full = L == kC;
     float lg[8];  // log2 of Gamma within the group: sum of the group's decays up to each token
-    {
+    auto decay_sums = [&](auto full_tag) {
+      constexpr bool kFull = decltype(full_tag)::value;
       const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG) + tb * kD + ch;
       float run = 0.f;
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        const float g = tb + r < L ? clamp_log_decay(gin[r * kD], lb) : 0.f;  // alpha = 1 past the end
+      for (int r = 0; r < 8; ++r) {  // alpha = 1 past the end of the sequence
+        const float g = (kFull || tb + r < L) ? clamp_log_decay(gin[r * kD], lb) : 0.f;
         run = fmaf(g, kLog2e, run);
         lg[r] = run;
       }
       s_tot[grp * kD + ch] = run;
-    }
+    };
+    if (full) decay_sums(std::true_type{});
+    else decay_sums(std::false_type{});
     if (tid < kC) s_beta[b * kC + tid] = b_pref;
     if (named_bar_or(BAR_WORK, kWorkers, bad)) {
       give_up(H_PREP);
       return false;
     }
-    const float T0 = s_tot[ch], T1 = s_tot[kD + ch], T2 = s_tot[2 * kD + ch], T3 = s_tot[3 * kD + ch];
-    const float r2 = T0 + T1;                                                // log2 e^r
-    const float last2 = r2 + (T2 + T3);                                      // log2 Gamma_last
-    const float start = grp == 0 ? -r2 : grp == 1 ? -T1 : grp == 2 ? 0.f : T2;  // log2 e^{G_start - r}
-    const float tau0 = exp2_sfu(r2), tau1 = exp2_sfu(last2 - r2);
-    if (grp == 0) s_gamma[b * kD + ch] = exp2_sfu(last2);
-    // q and k of the 8 tokens: bf16 element (t, ch) of the 128-byte-swizzled TMA tiles
-    const uint32_t cc = uint32_t(ch & 63);
-    const uint8_t *qk0 = sm + OFF_QKG + (ch >> 6) * 4096 + tb * 128 + (cc & 7u) * 2;
-    const uint32_t xj = (cc >> 3) << 4;
-    // Gram operands, K-major tf32 (blocks of 32 channels, one 128-byte row per token): the 32
-    // lanes of a warp hold one whole row, so each 4-byte store is conflict-free. fp16 operands,
-    // one 16-byte chunk each: Q~^T (columns 32 + t of [-W^T | Q~^T]), K^^T (row 32 + ch of
-    // [P ; K^^T]) and Kg^T (row ch). Two halves of 4 tokens keep few values live.
-    const uint32_t cb = uint32_t(ch >> 5), cq = uint32_t(ch & 31) >> 2;
-    float *gq = reinterpret_cast<float *>(sm + OFF_QK + cb * 64 * 128 + tb * 128 + (ch & 3) * 4);
-    float *gk = reinterpret_cast<float *>(sm + OFF_QK + cb * 64 * 128 + (32 + tb) * 128 + (ch & 3) * 4);
-    float *gb = reinterpret_cast<float *>(sm + OFF_B + cb * 32 * 128 + tb * 128 + (ch & 3) * 4);
     const uint32_t row = uint32_t(ch) * 128u, sw = uint32_t(ch) & 7u;
     uint32_t hq[4], hk[4], hg[4];  // fp16 pairs
+    auto operands = [&](auto full_tag) {
+      constexpr bool kFull = decltype(full_tag)::value;
+      const float T0 = s_tot[ch], T1 = s_tot[kD + ch], T2 = s_tot[2 * kD + ch], T3 = s_tot[3 * kD + ch];
+      const float r2 = T0 + T1;                                                // log2 e^r
+      const float last2 = r2 + (T2 + T3);                                      // log2 Gamma_last
+      const float start = grp == 0 ? -r2 : grp == 1 ? -T1 : grp == 2 ? 0.f : T2;  // log2 e^{G_start - r}
+      const float tau0 = exp2_sfu(r2), tau1 = exp2_sfu(last2 - r2);
+      if (grp == 0) s_gamma[b * kD + ch] = exp2_sfu(last2);
+      // q and k of the 8 tokens: bf16 element (t, ch) of the 128-byte-swizzled TMA tiles
+      const uint32_t cc = uint32_t(ch & 63);
+      const uint8_t *qk0 = sm + OFF_QKG + (ch >> 6) * 4096 + tb * 128 + (cc & 7u) * 2;
+      const uint32_t xj = (cc >> 3) << 4;
+      // Gram operands, K-major tf32 (blocks of 32 channels, one 128-byte row per token): the 32
+      // lanes of a warp hold one whole row, so each 4-byte store is conflict-free. fp16 operands,
+      // one 16-byte chunk each: Q~^T (columns 32 + t of [-W^T | Q~^T]), K^^T (row 32 + ch of
+      // [P ; K^^T]) and Kg^T (row ch). Two halves of 4 tokens keep few values live.
+      const uint32_t cb = uint32_t(ch >> 5), cq = uint32_t(ch & 31) >> 2;
+      float *gq = reinterpret_cast<float *>(sm + OFF_QK + cb * 64 * 128 + tb * 128 + (ch & 3) * 4);
+      float *gk = reinterpret_cast<float *>(sm + OFF_QK + cb * 64 * 128 + (32 + tb) * 128 + (ch & 3) * 4);
+      float *gb = reinterpret_cast<float *>(sm + OFF_B + cb * 32 * 128 + tb * 128 + (ch & 3) * 4);
 #pragma unroll
-    for (int half = 0; half < 2; ++half) {
-      float qf[4], kf[4], kg[4];
+      for (int half = 0; half < 2; ++half) {
+        float qf[4], kf[4], kg[4];
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int r = 4 * half + e;
-        const uint32_t off = r * 128 + (xj ^ uint32_t(r << 4));
-        const bool ok = tb + r < L;
-        const float q = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SQ + off)) : 0.f;
-        const float k = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SK + off)) : 0.f;
-        const float d = start + lg[r];  // log2 e^{G_t - r}
-        const float f = exp2_sfu(d), g = exp2_sfu(-d);
-        qf[e] = q * f;
-        kf[e] = k * f;
-        kg[e] = k * g;
-        const uint32_t o4 = (r * 128 + ((cq ^ uint32_t(r)) << 4)) >> 2;  // token tb + r: row tb + r, t & 7 = r
-        gq[o4] = round_tf32_alu(qf[e]);
-        gk[o4] = round_tf32_alu(kf[e]);
-        gb[o4] = round_tf32_alu(kg[e]);
+        for (int e = 0; e < 4; ++e) {
+          const int r = 4 * half + e;
+          const uint32_t off = r * 128 + (xj ^ uint32_t(r << 4));
+          const bool ok = kFull || tb + r < L;
+          const float q = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SQ + off)) : 0.f;
+          const float k = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SK + off)) : 0.f;
+          const float d = start + lg[r];  // log2 e^{G_t - r}
+          const float f = exp2_sfu(d), g = exp2_sfu(-d);
+          qf[e] = q * f;
+          kf[e] = k * f;
+          kg[e] = k * g;
+          const uint32_t o4 = (r * 128 + ((cq ^ uint32_t(r)) << 4)) >> 2;  // row tb + r, whose t & 7 = r
+          gq[o4] = round_tf32_alu(qf[e]);
+          gk[o4] = round_tf32_alu(kf[e]);
+          gb[o4] = round_tf32_alu(kg[e]);
+        }
+        hq[2 * half] = pack_f16x2(qf[0] * tau0, qf[1] * tau0);
+        hq[2 * half + 1] = pack_f16x2(qf[2] * tau0, qf[3] * tau0);
+        hk[2 * half] = pack_f16x2(kf[0] * tau0, kf[1] * tau0);
+        hk[2 * half + 1] = pack_f16x2(kf[2] * tau0, kf[3] * tau0);
+        hg[2 * half] = pack_f16x2(kg[0] * tau1, kg[1] * tau1);
+        hg[2 * half + 1] = pack_f16x2(kg[2] * tau1, kg[3] * tau1);
       }
-      hq[2 * half] = pack_f16x2(qf[0] * tau0, qf[1] * tau0);
-      hq[2 * half + 1] = pack_f16x2(qf[2] * tau0, qf[3] * tau0);
-      hk[2 * half] = pack_f16x2(kf[0] * tau0, kf[1] * tau0);
-      hk[2 * half + 1] = pack_f16x2(kf[2] * tau0, kf[3] * tau0);
-      hg[2 * half] = pack_f16x2(kg[0] * tau1, kg[1] * tau1);
-      hg[2 * half + 1] = pack_f16x2(kg[2] * tau1, kg[3] * tau1);
-    }
+    };
+    if (full) operands(std::true_type{});
+    else operands(std::false_type{});
     handoff(H_PREP);  // the Gram operands are complete; the fp16 tiles are needed later
     st_at(sm, OFF_PK + (c % 3) * kPKBytes + sw64_chunk(32u + ch, grp), make_uint4(hg[0], hg[1], hg[2], hg[3]));
     st_at(sm, OFF_KG + b * kKGBytes + sw64_chunk(ch, grp), make_uint4(hk[0], hk[1], hk[2], hk[3]));
@@ -570,7 +581,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = j & 1;
       const bool more = j + 1 < n_chunks;
       // ---------------- P1: chain j, fp16 copy of S^T; decayed S^T into group j % 2
-      if (j > 0) {  // the state MMA2 of chunk j - 1 left (warps 4..15 have waited for it already)
+      if (j > 0 && grp == 0) {  // the state MMA2 of chunk j - 1 left (warps 4..15 waited for it)
         bad |= !mbar_wait_sleep(&bars->mma2, uint32_t((j - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
         tc_fence_after();
       }
