@@ -45,10 +45,10 @@
 //                 channel and 8 tokens); Gram (kind::tf32, M = 64 rows
 //                 [Q f ; K f] x N = 32 keys K g)
 //   P3  chain j : U^T to fp16; MMA2: [O^T | S^T] += U^T [P ; K^^T]^T   (N = 160)
-//   P4  next j+1: P and A out of TMEM (their Gram ran during the previous
-//                 iteration), v -> fp16; then warps 0..3 invert I + A (8 x 8 and
-//                 16 x 16 blocks) and form T'
-//                 while warps 4..15 write O^T of chunk j (P5) to global memory;
+//   P4  next j+1: warps 2, 3, 6, 7 (whose TMEM lanes hold the key rows of the Gram) take
+//                 A out of TMEM, invert I + A (8 x 8 and 16 x 16 blocks) and form T',
+//                 while the other 12 warps convert v to fp16, take P out of TMEM and
+//                 write O^T of chunk j (P5) to global memory;
 //                 W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
 // Per-chunk operand tiles are double-buffered by chunk parity ([P ; K^^T] three
 // times, since it lives from P2 of chunk j to MMA2 of chunk j + 2), and so are the
@@ -358,85 +358,76 @@ __global__ void __launch_bounds__(kThreads, 1)
     umma_commit(&bars->gram[c & 1]);
   };
 
+  // Warps 2, 3, 6, 7 (TMEM lane quarters 2 and 3, column groups 0 and 1) form the inverse
+  // group: the key rows of the Gram (A) live in their lanes. The other 12 warps write
+  // outputs, convert v and take the query rows (P).
+  const bool inv_group = quarter >= 2 && grp < 2;
+  const int iw = (quarter - 2) + 2 * grp;  // inverse group: warp 0..3 of the group
+  const int itid = 32 * iw + lane;         // inverse group: thread 0..127 of the group
+
   // ------------------------------------------------------------------ P5: outputs
-  // O^T of chunk j out of TMEM to global memory, on warps 4..15 (column groups 1..3 of each
-  // lane quarter): group g takes 11, 11 and 10 of the 32 tokens.
+  // O^T of chunk j out of TMEM to global memory, on the 12 warps outside the inverse group:
+  // lane quarters 0 and 1 have 4 of them (8 tokens each), quarters 2 and 3 have 2 (16 each).
   auto out_chunk = [&](int j) {
     bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
-    const int L = chunk_len(j), g1 = grp - 1;
-    const int col0 = g1 == 0 ? 0 : g1 == 1 ? 11 : 16;           // first TMEM column loaded
-    const int lo = g1 == 0 ? 0 : g1 == 1 ? 11 : 22, hi = g1 == 0 ? 11 : g1 == 1 ? 22 : 32;
-    float x[16];
-    tmem_ld16(tmem + lane_base + tm_grp(j & 1) + TM_O + col0, x);  // O^T row v, tokens col0 ..
-    tmem_ld_wait();
-    int64_t idx = ((chunk_t0(j) + col0) * H + h) * int64_t(kD) + v_own;
+    const int L = chunk_len(j);
     const int64_t step = int64_t(H) * kD;
+    const uint32_t ocols = tmem + lane_base + tm_grp(j & 1) + TM_O;
+    if (quarter < 2) {
+      float x[8];
+      tmem_ld8(ocols + 8 * grp, x);  // O^T row v, tokens 8 grp ..
+      tmem_ld_wait();
+      int64_t idx = ((chunk_t0(j) + 8 * grp) * H + h) * int64_t(kD) + v_own;
 #pragma unroll
-    for (int e = 0; e < 16; ++e, idx += step) {
-      const int tok = col0 + e;
-      if (tok >= lo && tok < hi && tok < L) store_elem<kOutBF16>(out, idx, scale * x[e]);
+      for (int e = 0; e < 8; ++e, idx += step)
+        if (8 * grp + e < L) store_elem<kOutBF16>(out, idx, scale * x[e]);
+    } else {
+      const int t0 = 16 * (grp - 2);
+      float x[16];
+      tmem_ld16(ocols + t0, x);  // O^T row v, tokens t0 ..
+      tmem_ld_wait();
+      int64_t idx = ((chunk_t0(j) + t0) * H + h) * int64_t(kD) + v_own;
+#pragma unroll
+      for (int e = 0; e < 16; ++e, idx += step)
+        if (t0 + e < L) store_elem<kOutBF16>(out, idx, scale * x[e]);
     }
   };
 
   // ------------------------------------------------------------------ P4: P, A, inverse, T', v
-  // Inverse-side work of chunk c on warps 0..3 while warps 4..15 write the outputs of chunk
-  // j_out (if >= 0). Returns false when the compute warps give up.
+  // Inverse-side work of chunk c; the 12 warps outside the inverse group also write the
+  // outputs of chunk j_out (if >= 0). Returns false when the compute warps give up.
   auto extract_inverse = [&](int c, int j_out) -> bool {
     const int b = c & 1, L = chunk_len(c);
-    {  // v tile of this chunk: bf16 -> fp16 in place, rows past the sequence end zeroed (one chunk each)
-      bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
-      const int t = tid >> 4, cj = tid & 15;
-      uint4 *p = reinterpret_cast<uint4 *>(sm + OFF_V + b * 8192 + sw128_chunk(t, cj & 7, cj >> 3, kC));
-      uint4 w = make_uint4(0, 0, 0, 0);
-      if (t < L) {
-        const uint4 bv = *p;
-        const float2 a0 = unpack_bf16x2(bv.x), a1 = unpack_bf16x2(bv.y), a2 = unpack_bf16x2(bv.z),
-                     a3 = unpack_bf16x2(bv.w);
-        const float x[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
-        w = pack8_f16(x);
-      }
-      *p = w;
-    }
-    bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
-    tc_fence_after();
-    // Gram row m = 16 quarter + lane (M = 64 layout, lanes 0..15 of each quarter): quarters
-    // 0 / 1 hold query rows t = 0..15 / 16..31 (P), quarters 2 / 3 the key rows (A);
-    // column i = key i. Warp (quarter, grp) takes columns 8 grp .. 8 grp + 7.
     float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
-    {
-      const int s = quarter & 1, t = 16 * s + (lane & 15);
-      const bool is_p = quarter < 2, have = grp < 2 * (s + 1);  // columns up to the row block's end
-      float vals[8];
-      if (have) {
-        tmem_ld8(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
-        tmem_ld_wait();
-      }
-      if (lane < 16) {
-        const float bt = s_beta[b * kC + t];
+    if (inv_group) {
+      bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+      tc_fence_after();
+      {  // A rows t = 16 (quarter - 2) + lane (lanes 0..15; M = 64 layout), columns 16 grp .. + 15
+        const int s = quarter - 2, t = 16 * s + (lane & 15);
+        if (grp <= s) {  // columns past the row block are all zero and never read
+          float vals[16];
+          tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * grp, vals);
+          tmem_ld_wait();
+          if (lane < 16) {
+            const float bt = s_beta[b * kC + t];
+            const int lim = t < L ? t - 16 * grp : 0;  // keep i < t
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const int i = 8 * grp + e;
-          const bool keep = have && t < L && (is_p ? i <= t : i < t);
-          vals[e] = keep ? (is_p ? vals[e] : bt * vals[e]) : 0.f;
-        }
-        if (is_p) {
-          st_at(sm + OFF_PK + (c % 3) * kPKBytes, sw64_chunk(t, grp), pack8_f16(vals));
-        } else if (have) {
-          *reinterpret_cast<float4 *>(As + t * kALd + 8 * grp) = make_float4(vals[0], vals[1], vals[2], vals[3]);
-          *reinterpret_cast<float4 *>(As + t * kALd + 8 * grp + 4) = make_float4(vals[4], vals[5], vals[6], vals[7]);
+            for (int e = 0; e < 16; ++e) vals[e] = e < lim ? bt * vals[e] : 0.f;
+            float4 *arow = reinterpret_cast<float4 *>(As + t * kALd + 16 * grp);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              arow[q4] = make_float4(vals[4 * q4], vals[4 * q4 + 1], vals[4 * q4 + 2], vals[4 * q4 + 3]);
+          }
         }
       }
-    }
-    tc_fence_before();
-    named_bar_sync(BAR_WORK, kWorkers);
-    if (grp == 0) {
-      // warps 0..3: T = (I + A)^{-1}, then T' = T Diag(beta)
+      named_bar_sync(BAR_INV, 128);
+      // T = (I + A)^{-1}, then T' = T Diag(beta)
       float *Ts = reinterpret_cast<float *>(sm + OFF_ST + G_T);
       float *Xs = reinterpret_cast<float *>(sm + OFF_ST + G_X);
-      if (warp < 2) {
-        // diagonal block s = warp (16 x 16) in 8 x 8 pieces, warp-synchronous
-        const int base = 16 * warp;
+      if (iw < 2) {
+        // diagonal block iw (16 x 16) in 8 x 8 pieces, warp-synchronous
+        const int base = 16 * iw;
         if (lane < 16) {  // the two 8 x 8 diagonal pieces: lane = column of its piece
           const int o = base + 8 * (lane >> 3), cc = lane & 7;
           float x[8];
@@ -455,14 +446,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         __syncwarp();
         // piece below the diagonal: -T_11 (A_10 T_00); lane (row r8, columns 2 c8, 2 c8 + 1)
-        float *Xw = Xs + 64 * warp;
+        float *Xw = Xs + 64 * iw;
         const int r8 = lane >> 2, c8 = lane & 3;
         float a8[8];
-        {
-          const float4 *ar = reinterpret_cast<const float4 *>(As + (base + 8 + r8) * kALd + base);
-          const float4 p0 = ar[0], p1 = ar[1];
-          a8[0] = p0.x; a8[1] = p0.y; a8[2] = p0.z; a8[3] = p0.w; a8[4] = p1.x; a8[5] = p1.y; a8[6] = p1.z; a8[7] = p1.w;
-        }
+        auto load8 = [&](const float *src) {
+          const float4 p0 = reinterpret_cast<const float4 *>(src)[0], p1 = reinterpret_cast<const float4 *>(src)[1];
+          a8[0] = p0.x;
+          a8[1] = p0.y;
+          a8[2] = p0.z;
+          a8[3] = p0.w;
+          a8[4] = p1.x;
+          a8[5] = p1.y;
+          a8[6] = p1.z;
+          a8[7] = p1.w;
+        };
+        load8(As + (base + 8 + r8) * kALd + base);
         float2 acc8 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -472,11 +470,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         *reinterpret_cast<float2 *>(Xw + r8 * 8 + 2 * c8) = acc8;
         __syncwarp();
-        {
-          const float4 *tr = reinterpret_cast<const float4 *>(Ts + (base + 8 + r8) * kALd + base + 8);
-          const float4 p0 = tr[0], p1 = tr[1];
-          a8[0] = p0.x; a8[1] = p0.y; a8[2] = p0.z; a8[3] = p0.w; a8[4] = p1.x; a8[5] = p1.y; a8[6] = p1.z; a8[7] = p1.w;
-        }
+        load8(Ts + (base + 8 + r8) * kALd + base + 8);
         acc8 = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -485,13 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           acc8.y = fmaf(-a8[k], x2.y, acc8.y);
         }
         *reinterpret_cast<float2 *>(Ts + (base + 8 + r8) * kALd + base + 2 * c8) = acc8;
-      } else {  // warps 2, 3: the zero 16 x 16 block above the diagonal
-        const int l = tid - 64;
+      } else {  // the zero 16 x 16 block above the diagonal
+        const int l = itid - 64;
         *reinterpret_cast<float4 *>(Ts + (l >> 2) * kALd + 16 + 4 * (l & 3)) = make_float4(0.f, 0.f, 0.f, 0.f);
       }
       named_bar_sync(BAR_INV, 128);
       // block below the diagonal, T_10 = -T_11 (A_10 T_00): thread (row r, columns 2 c2, 2 c2 + 1)
-      const int r = tid >> 3, c2 = tid & 7;
+      const int r = itid >> 3, c2 = itid & 7;
       float rowv[16];
       auto load_row = [&](const float *src) {
 #pragma unroll
@@ -524,7 +518,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<float2 *>(Ts + (16 + r) * kALd + 2 * c2) = acc;
       named_bar_sync(BAR_INV, 128);
       {  // T' = T Diag(beta) -> fp16 [t][i]
-        const int t = tid >> 2, cj = tid & 3;
+        const int t = itid >> 2, cj = itid & 3;
         const float4 *trow = reinterpret_cast<const float4 *>(Ts + t * kALd + 8 * cj);
         const float4 *brow = reinterpret_cast<const float4 *>(s_beta + b * kC + 8 * cj);
         const float4 t0v = trow[0], t1v = trow[1], b0v = brow[0], b1v = brow[1];
@@ -532,12 +526,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                             t1v.x * b1v.x, t1v.y * b1v.y, t1v.z * b1v.z, t1v.w * b1v.w};
         st_at(sm, OFF_TP + sw64_chunk(t, cj), pack8_f16(x));
       }
-    } else if (j_out >= 0) {
-      out_chunk(j_out);  // warps 4..15 meanwhile write the outputs of the chain's chunk
+    } else {
+      // the 12 other warps: v tile of this chunk bf16 -> fp16 in place (rows past the end
+      // zeroed), the query rows P of the Gram, then the outputs of chunk j_out
+      const int ot = (quarter < 2 ? 64 * grp + 32 * quarter : 256 + 64 * (grp - 2) + 32 * (quarter - 2)) + lane;
+      bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
+      for (int e = ot; e < kC * 16; e += 384) {
+        const int t = e >> 4, cj = e & 15;
+        uint4 *p = reinterpret_cast<uint4 *>(sm + OFF_V + b * 8192 + sw128_chunk(t, cj & 7, cj >> 3, kC));
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (t < L) {
+          const uint4 bv = *p;
+          const float2 a0 = unpack_bf16x2(bv.x), a1 = unpack_bf16x2(bv.y), a2 = unpack_bf16x2(bv.z),
+                       a3 = unpack_bf16x2(bv.w);
+          const float x[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
+          w = pack8_f16(x);
+        }
+        *p = w;
+      }
+      if (quarter < 2) {  // P rows t = 16 quarter + lane (lanes 0..15), columns 8 grp .. + 7
+        bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+        tc_fence_after();
+        const int t = 16 * quarter + (lane & 15);
+        const bool have = grp < 2 * (quarter + 1);  // columns up to the row block's end
+        float vals[8];
+        if (have) {
+          tmem_ld8(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
+          tmem_ld_wait();
+        }
+        if (lane < 16) {
+          const int lim = (have && t < L) ? t + 1 - 8 * grp : 0;  // keep i <= t
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vals[e] = e < lim ? vals[e] : 0.f;
+          st_at(sm + OFF_PK + (c % 3) * kPKBytes, sw64_chunk(t, grp), pack8_f16(vals));
+        }
+      }
+      if (j_out >= 0) out_chunk(j_out);
     }
     // the inverse's scratch aliases the S^T tile that the next chain step rewrites: all
     // compute threads are past it before any goes on
     fence_proxy_async_smem();
+    tc_fence_before();
     const bool ab = named_bar_or(BAR_WORK, kWorkers, bad);
     if (ab) give_up(H_INV);
     else handoff(H_INV);
@@ -581,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int b = j & 1;
       const bool more = j + 1 < n_chunks;
       // ---------------- P1: chain j, fp16 copy of S^T; decayed S^T into group j % 2
-      if (j > 0 && grp == 0) {  // the state MMA2 of chunk j - 1 left (warps 4..15 waited for it)
+      if (j > 0 && inv_group) {  // the state MMA2 of chunk j - 1 left (the other warps waited for it)
         bad |= !mbar_wait_sleep(&bars->mma2, uint32_t((j - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
         tc_fence_after();
       }
@@ -623,11 +652,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---------------- P4 / P5: inverse side of chunk j + 1 -> W^T and U~^T, and outputs of chunk j
       if (more) {
         if (!extract_inverse(j + 1, j)) goto teardown;
-      } else if (grp >= 1) {
+      } else if (!inv_group) {
         out_chunk(j);
       }
     }
-    if (n_chunks > 0) {  // the last chunk's MMA2 (warps 4..15 have waited for it already)
+    if (n_chunks > 0) {  // the last chunk's MMA2 (the warps outside the inverse group waited already)
       bad |= !mbar_wait_sleep(&bars->mma2, uint32_t((n_chunks - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
       tc_fence_after();
     }
