@@ -10,7 +10,9 @@ Notes, section 1.1 "Kimi Delta Attention"):
 
 * ``recurrent`` -- the defining token-by-token recurrence in plain C, fp64
   (``kda_oracle.c``), threaded over (sequence, head) pairs. This is the oracle
-  the GPU path is compared with.
+  the GPU path is compared with. ``kda_recurrent_gated`` is the same recurrence
+  with the log-decay of the gated form, ``g = g_min * Sigmoid(e^{A_h} z)``
+  (section 1.2, the K3 row of the mapping table).
 * ``chunked``  -- the chunkwise form (section 1.2: "recurrent across chunks and
   parallel within each chunk") in numpy fp64, with the chunk's triangular
   system solved by a library inverse. Pinned to ``recurrent`` by agreement.
@@ -23,6 +25,7 @@ planted-mistake checks). No worked numeric example exists on the pages, so no
 pin is a printed value.
 """
 
-from .recurrent import kda_recurrent, kda_recurrent_mutant, MUTATIONS, oracle_library_path  # noqa: F401
+from .recurrent import (kda_recurrent, kda_recurrent_mutant, kda_recurrent_gated, MUTATIONS,  # noqa: F401
+                        GATE_MUTATIONS, oracle_library_path)
 from .chunked import kda_chunked, chunk_quantities  # noqa: F401
 from .exact import kda_exact  # noqa: F401

@@ -17,6 +17,11 @@
  * (same page, section 1.2 "The lower-bounded decay": g >= g_min = -5), taken
  * here as a clamp g = max(log_alpha, lower_bound). A NaN log_alpha stays NaN.
  *
+ * Gated form (section 1.2, the K3 row of the mapping table): the log-decay is
+ * computed from decay logits z and a per-head log-scale A_h as
+ *     g = g_min * Sigmoid(e^{A_h} z),   Sigmoid(x) = 1 / (1 + e^{-x}),
+ * which lies in (g_min, 0) by construction, so no clamp is applied.
+ *
  * Expanding the product, (I - b k k^T) D S + b k v^T = D S + k (b (v - (D S)^T k))^T,
  * so each token is: decay the key rows of S, predict (D S)^T k, write the
  * rank-1 correction, read out S_t^T q_t. That is the order of the loop below;
@@ -46,6 +51,9 @@ enum {
   MUT_DECAY_VALUE_AXIS = 5,  /* decay columns (value axis) instead of key rows */
   MUT_NO_CLAMP = 6,          /* lower bound ignored                            */
   MUT_NO_BETA = 7,           /* beta dropped from the write                    */
+  MUT_GATE_NO_EXP = 8,       /* gated form: A_h used where e^{A_h} belongs     */
+  MUT_GATE_SOFTPLUS = 9,     /* gated form: the unbounded g = -e^{A_h} Softplus(z) */
+  MUT_GATE_SIGN = 10,        /* gated form: Sigmoid(-e^{A_h} z)                */
 };
 
 static double load(const void *base, int dtype, int64_t idx) {
@@ -61,6 +69,7 @@ static double load(const void *base, int dtype, int64_t idx) {
 typedef struct {
   const void *q, *k, *v, *log_alpha, *beta, *init;
   int dt_qk, dt_v, dt_la, dt_beta, dt_init;
+  const double *A_log; /* gated form: per-head log-scale (log_alpha then holds z); NULL: clamp */
   const int64_t *cu;
   int64_t num_seqs, H, dk, dv;
   double lb, scale;
@@ -86,7 +95,15 @@ static void run_unit(job_t *J, int64_t unit, double *S, double *a, double *kk,
     const double b = load(J->beta, J->dt_beta, t * H + h);
     for (int64_t c = 0; c < dk; ++c) {
       double g = load(J->log_alpha, J->dt_la, row_k + c);
-      if (mut != MUT_NO_CLAMP && g < J->lb) g = J->lb; /* NaN fails the test and stays NaN */
+      if (J->A_log) {
+        /* g = g_min Sigmoid(e^{A_h} z); lb holds g_min */
+        const double x = (mut == MUT_GATE_NO_EXP) ? J->A_log[h] * g : exp(J->A_log[h]) * g;
+        if (mut == MUT_GATE_SOFTPLUS) g = -exp(J->A_log[h]) * log1p(exp(g));
+        else if (mut == MUT_GATE_SIGN) g = J->lb / (1.0 + exp(x));
+        else g = J->lb / (1.0 + exp(-x));
+      } else if (mut != MUT_NO_CLAMP && g < J->lb) {
+        g = J->lb; /* NaN fails the test and stays NaN */
+      }
       a[c] = (mut == MUT_NO_DECAY) ? 1.0 : exp(g);
       kk[c] = load(J->k, J->dt_qk, row_k + c);
       qq[c] = load(J->q, J->dt_qk, row_k + c);
@@ -164,13 +181,14 @@ static void *worker(void *arg) {
   return NULL;
 }
 
-/* Returns 0 on success, 1 on a bad argument, 2 when memory or threads fail. */
-int kda_oracle_recurrent_mutant(const void *q, const void *k, int dt_qk, const void *v, int dt_v,
-                                const void *log_alpha, int dt_la, const void *beta, int dt_beta,
-                                const int64_t *cu_seqlens, int64_t num_seqs, int64_t H,
-                                int64_t dk, int64_t dv, double lower_bound, double scale,
-                                const void *init_state, int dt_init, double *out,
-                                double *final_state, int num_threads, int mutation) {
+/* Returns 0 on success, 1 on a bad argument, 2 when memory or threads fail.
+ * With A_log non-NULL (one double per head) log_alpha holds the decay logits z
+ * and lower_bound is g_min of the gated form. */
+static int oracle_run(const void *q, const void *k, int dt_qk, const void *v, int dt_v,
+                      const void *log_alpha, int dt_la, const double *A_log, const void *beta,
+                      int dt_beta, const int64_t *cu_seqlens, int64_t num_seqs, int64_t H, int64_t dk,
+                      int64_t dv, double lower_bound, double scale, const void *init_state,
+                      int dt_init, double *out, double *final_state, int num_threads, int mutation) {
   if (!cu_seqlens || num_seqs < 0 || H <= 0 || dk <= 0 || dv <= 0) return 1;
   if (mutation == MUT_DECAY_VALUE_AXIS && dk != dv) return 1;
   for (int64_t n = 0; n < num_seqs; ++n)
@@ -180,6 +198,7 @@ int kda_oracle_recurrent_mutant(const void *q, const void *k, int dt_qk, const v
   job_t J;
   memset(&J, 0, sizeof J);
   J.q = q; J.k = k; J.v = v; J.log_alpha = log_alpha; J.beta = beta; J.init = init_state;
+  J.A_log = A_log;
   J.dt_qk = dt_qk; J.dt_v = dt_v; J.dt_la = dt_la; J.dt_beta = dt_beta; J.dt_init = dt_init;
   J.cu = cu_seqlens; J.num_seqs = num_seqs; J.H = H; J.dk = dk; J.dv = dv;
   J.lb = lower_bound; J.scale = scale; J.out = out; J.final_state = final_state;
@@ -205,6 +224,18 @@ int kda_oracle_recurrent_mutant(const void *q, const void *k, int dt_qk, const v
   return rc;
 }
 
+int kda_oracle_recurrent_mutant(const void *q, const void *k, int dt_qk, const void *v, int dt_v,
+                                const void *log_alpha, int dt_la, const void *beta, int dt_beta,
+                                const int64_t *cu_seqlens, int64_t num_seqs, int64_t H,
+                                int64_t dk, int64_t dv, double lower_bound, double scale,
+                                const void *init_state, int dt_init, double *out,
+                                double *final_state, int num_threads, int mutation) {
+  if (mutation >= MUT_GATE_NO_EXP) return 1;
+  return oracle_run(q, k, dt_qk, v, dt_v, log_alpha, dt_la, NULL, beta, dt_beta, cu_seqlens,
+                    num_seqs, H, dk, dv, lower_bound, scale, init_state, dt_init, out, final_state,
+                    num_threads, mutation);
+}
+
 int kda_oracle_recurrent(const void *q, const void *k, int dt_qk, const void *v, int dt_v,
                          const void *log_alpha, int dt_la, const void *beta, int dt_beta,
                          const int64_t *cu_seqlens, int64_t num_seqs, int64_t H, int64_t dk,
@@ -213,4 +244,18 @@ int kda_oracle_recurrent(const void *q, const void *k, int dt_qk, const void *v,
   return kda_oracle_recurrent_mutant(q, k, dt_qk, v, dt_v, log_alpha, dt_la, beta, dt_beta,
                                      cu_seqlens, num_seqs, H, dk, dv, lower_bound, scale,
                                      init_state, dt_init, out, final_state, num_threads, MUT_NONE);
+}
+
+/* The gated form: z [T_tot, H, d_k] decay logits, A_log [H] per-head log-scales. */
+int kda_oracle_recurrent_gated(const void *q, const void *k, int dt_qk, const void *v, int dt_v,
+                               const void *z, int dt_z, const double *A_log, const void *beta,
+                               int dt_beta, const int64_t *cu_seqlens, int64_t num_seqs, int64_t H,
+                               int64_t dk, int64_t dv, double g_min, double scale,
+                               const void *init_state, int dt_init, double *out,
+                               double *final_state, int num_threads, int mutation) {
+  if (!A_log) return 1;
+  if (mutation != MUT_NONE && mutation < MUT_GATE_NO_EXP && mutation != MUT_NO_DECAY) return 1;
+  return oracle_run(q, k, dt_qk, v, dt_v, z, dt_z, A_log, beta, dt_beta, cu_seqlens, num_seqs, H,
+                    dk, dv, g_min, scale, init_state, dt_init, out, final_state, num_threads,
+                    mutation);
 }

@@ -5,7 +5,9 @@ here with the host ``gcc`` on first use (or by ``__graft_entry__.build()``),
 into ``oracle/_build/``. Definition followed: Kimi K3 -- Architecture Notes,
 section 1.1, ``S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T``,
 ``o_t = S_t^T q_t``, with ``log a_t`` clamped below at ``lower_bound``
-(section 1.2).
+(section 1.2), or, in the gated form of section 1.2 (the K3 row of its mapping
+table), computed from decay logits ``z`` and per-head log-scales ``A_h`` as
+``g = g_min * Sigmoid(e^{A_h} z)``.
 """
 
 from __future__ import annotations
@@ -33,6 +35,13 @@ MUTATIONS = {
     "decay_value_axis": 5,
     "no_clamp": 6,
     "no_beta": 7,
+}
+
+# planted mistakes of the gated form, understood by kda_recurrent_gated(mutation=...)
+GATE_MUTATIONS = {
+    "gate_no_exp": 8,
+    "gate_softplus": 9,
+    "gate_sign": 10,
 }
 
 _lock = threading.Lock()
@@ -67,6 +76,10 @@ def _load():
             fn.argtypes = [vp, vp, i32, vp, i32, vp, i32, vp, i32, vp, i64, i64, i64, i64,
                            f64, f64, vp, i32, vp, vp, i32, i32]
             fn.restype = i32
+            fg = lib.kda_oracle_recurrent_gated
+            fg.argtypes = [vp, vp, i32, vp, i32, vp, i32, vp, vp, i32, vp, i64, i64, i64, i64,
+                           f64, f64, vp, i32, vp, vp, i32, i32]
+            fg.restype = i32
             _lib = lib
     return _lib
 
@@ -147,3 +160,56 @@ def kda_recurrent(q, k, v, log_alpha, beta, cu_seqlens, *, lower_bound: float = 
     return kda_recurrent_mutant(q, k, v, log_alpha, beta, cu_seqlens, mutation=0,
                                 lower_bound=lower_bound, scale=scale, init_state=init_state,
                                 num_threads=num_threads)
+
+
+def kda_recurrent_gated(q, k, v, z, A_log, beta, cu_seqlens, *, g_min: float = -5.0, scale: float = 1.0,
+                        init_state=None, num_threads: int | None = None, mutation: int = 0):
+    """fp64 KDA recurrence with the gated log-decay ``g = g_min * Sigmoid(e^{A_h} z)``.
+
+    z [T_tot, H, d_k] (float or bf16 bits, like q/k); A_log [H]; other arguments as in
+    ``kda_recurrent_mutant``. ``mutation`` may be one of ``GATE_MUTATIONS`` (or 1, no decay).
+    Returns (out [T_tot, H, d_v], final_state [N, H, d_k, d_v]) as float64.
+    """
+    lib = _load()
+    qa, dt_qk = _as_array(q)
+    ka, dt_k = _as_array(k)
+    if dt_k != dt_qk:
+        raise ValueError("q and k must share one element type")
+    va, dt_v = _as_array(v)
+    za, dt_z = _as_array(z)
+    ba, dt_b = _as_array(beta)
+    ia, dt_i = _as_array(init_state)
+    try:
+        import torch
+        if isinstance(A_log, torch.Tensor):
+            A_log = A_log.detach().cpu().double().numpy()
+    except ImportError:
+        pass
+    aa = np.ascontiguousarray(np.asarray(A_log, dtype=np.float64))
+    cu = np.ascontiguousarray(np.asarray(cu_seqlens, dtype=np.int64))
+    T_tot, H, dk = qa.shape
+    dv = va.shape[-1]
+    N = cu.shape[0] - 1
+    if ka.shape != (T_tot, H, dk) or za.shape != (T_tot, H, dk) or va.shape[:2] != (T_tot, H):
+        raise ValueError("q/k/z/v shapes disagree")
+    if aa.shape != (H,):
+        raise ValueError("A_log must be [H]")
+    if ba.shape != (T_tot, H):
+        raise ValueError("beta must be [T_tot, H]")
+    if ia is not None and ia.shape != (N, H, dk, dv):
+        raise ValueError("init_state must be [N, H, d_k, d_v]")
+    if N < 0 or cu[0] != 0 or cu[-1] != T_tot:
+        raise ValueError("cu_seqlens must start at 0 and end at T_tot")
+    out = np.zeros((T_tot, H, dv), dtype=np.float64)
+    final = np.zeros((N, H, dk, dv), dtype=np.float64)
+    nt = num_threads or os.cpu_count() or 1
+
+    def ptr(a):
+        return None if a is None else a.ctypes.data
+
+    rc = lib.kda_oracle_recurrent_gated(
+        ptr(qa), ptr(ka), dt_qk, ptr(va), dt_v, ptr(za), dt_z, ptr(aa), ptr(ba), dt_b, ptr(cu), N, H, dk, dv,
+        float(g_min), float(scale), ptr(ia), dt_i, ptr(out), ptr(final), int(nt), int(mutation))
+    if rc != 0:
+        raise RuntimeError(f"kda_oracle_recurrent_gated failed with code {rc}")
+    return out, final

@@ -1,0 +1,133 @@
+"""CPU pins of the oracle's gated log-decay, g = g_min * Sigmoid(e^{A_h} z)
+(Kimi K3 -- Architecture Notes, section 1.2, the K3 row of the mapping table).
+
+Each pin compares the gated oracle with the clamped one on inputs where the
+gate's value is fixed by mathematics alone: Sigmoid(0) = 1/2 for every A_h, the
+saturated limits of very large |e^{A_h} z|, the strict bounds g in (g_min, 0),
+and the monotonicity in z. Planted mistakes in the gate (A_h where e^{A_h}
+belongs, the unbounded Softplus map of the earlier models, a flipped sign) must
+each fail one of them.
+"""
+
+import numpy as np
+import pytest
+
+from oracle import GATE_MUTATIONS, kda_recurrent, kda_recurrent_gated
+
+G_MIN = -5.0
+
+
+def _problem(rng, T, H, dk, dv):
+    q = rng.standard_normal((T, H, dk)); q /= np.linalg.norm(q, axis=-1, keepdims=True)
+    k = rng.standard_normal((T, H, dk)); k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, dv))
+    b = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    S0 = 0.02 * rng.standard_normal((2, H, dk, dv))
+    cu = np.array([0, T // 3, T])
+    return q, k, v, b, cu, S0
+
+
+def _gated(mutation):
+    def run(q, k, v, z, A, b, cu, S0):
+        return kda_recurrent_gated(q, k, v, z, A, b, cu, g_min=G_MIN, init_state=S0, num_threads=2,
+                                   mutation=mutation)
+    return run
+
+
+def _clamped(q, k, v, g, b, cu, S0):
+    return kda_recurrent(q, k, v, g, b, cu, lower_bound=G_MIN, init_state=S0, num_threads=2)
+
+
+def _close(a, b, tol):
+    for x, y in zip(a, b):
+        scale = max(float(np.abs(y).max()), 1e-300)
+        assert float(np.abs(x - y).max()) <= tol * scale, float(np.abs(x - y).max()) / scale
+
+
+def pin_zero_logit(run):
+    """z = 0: Sigmoid(e^{A_h} 0) = 1/2 for any A_h, so g = g_min / 2 exactly."""
+    rng = np.random.default_rng(20)
+    q, k, v, b, cu, S0 = _problem(rng, 23, 3, 8, 5)
+    z = np.zeros_like(q)
+    A = np.array([-3.0, 0.0, 4.0])
+    _close(run(q, k, v, z, A, b, cu, S0), _clamped(q, k, v, np.full_like(q, G_MIN / 2), b, cu, S0), 1e-15)
+
+
+def pin_saturated_limits(run):
+    """e^{A_h} z -> +inf gives g = g_min, -> -inf gives g = 0 (alpha = 1), both exactly in fp64."""
+    rng = np.random.default_rng(21)
+    q, k, v, b, cu, S0 = _problem(rng, 19, 2, 6, 7)
+    z = np.where(rng.standard_normal(q.shape) > 0, 1.0e3, -1.0e3)
+    A = np.array([0.0, 1.0])
+    g = np.where(z > 0, G_MIN, 0.0)
+    _close(run(q, k, v, z, A, b, cu, S0), _clamped(q, k, v, g, b, cu, S0), 1e-15)
+
+
+def pin_per_head_scale(run):
+    """Head 0 with e^{A_0} ~ 2e-22 sits at the midpoint g_min/2; head 1 with e^{A_1} ~ 2.2e4
+    and |z| = 0.1 saturates to g_min or 0 by the sign of z: A_h belongs to its own head and
+    enters through e^{A_h}."""
+    rng = np.random.default_rng(22)
+    q, k, v, b, cu, S0 = _problem(rng, 21, 2, 6, 6)
+    z = 0.1 * np.sign(rng.standard_normal(q.shape))
+    A = np.array([-50.0, 10.0])
+    g = np.empty_like(q)
+    g[:, 0] = G_MIN / 2
+    g[:, 1] = np.where(z[:, 1] > 0, G_MIN, 0.0)
+    _close(run(q, k, v, z, A, b, cu, S0), _clamped(q, k, v, g, b, cu, S0), 1e-12)
+
+
+def pin_bounds_and_monotone(run):
+    """With beta = 0 and d_k = d_v = 1 one step gives S_1 = alpha S_0: every alpha lies in
+    (e^{g_min}, 1) and decreases as z grows (fixed A_h)."""
+    T, H = 1, 64
+    z = np.linspace(-4.0, 4.0, H).reshape(1, H, 1)
+    A = np.full(H, 0.3)
+    q = np.ones((T, H, 1)); k = np.ones((T, H, 1)); v = np.zeros((T, H, 1))
+    b = np.zeros((T, H))
+    S0 = np.ones((1, H, 1, 1))
+    _, fin = run(q, k, v, z, A, b, np.array([0, T]), S0)
+    alpha = fin[0, :, 0, 0]
+    assert np.all(alpha > np.exp(G_MIN)) and np.all(alpha < 1.0)
+    assert np.all(np.diff(alpha) < 0)
+
+
+GATE_PINS = [pin_zero_logit, pin_saturated_limits, pin_per_head_scale, pin_bounds_and_monotone]
+
+
+@pytest.mark.parametrize("pin", GATE_PINS, ids=lambda p: p.__name__)
+def test_gated_oracle_pins(pin):
+    pin(_gated(0))
+
+
+@pytest.mark.parametrize("name,mut", sorted(GATE_MUTATIONS.items()))
+def test_gate_planted_mistakes_are_caught(name, mut):
+    failures = []
+    for pin in GATE_PINS:
+        try:
+            pin(_gated(mut))
+        except AssertionError:
+            failures.append(pin.__name__)
+    assert failures, f"gate mutation {name} passed every pin"
+
+
+def test_gated_oracle_reads_bf16_logits():
+    """z given as bf16 bits is read exactly: the same values as float32 inputs."""
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(23)
+    q, k, v, b, cu, S0 = _problem(rng, 9, 2, 4, 3)
+    z32 = torch.tensor(rng.standard_normal(q.shape), dtype=torch.float32).bfloat16()
+    A = np.array([0.2, -0.4])
+    a = kda_recurrent_gated(q, k, v, z32, A, b, cu, g_min=G_MIN, init_state=S0)
+    c = kda_recurrent_gated(q, k, v, z32.float().numpy(), A, b, cu, g_min=G_MIN, init_state=S0)
+    for x, y in zip(a, c):
+        assert np.array_equal(x, y)
+
+
+def test_gated_oracle_rejects_bad_arguments():
+    rng = np.random.default_rng(24)
+    q, k, v, b, cu, S0 = _problem(rng, 6, 2, 4, 3)
+    with pytest.raises(ValueError):
+        kda_recurrent_gated(q, k, v, np.zeros_like(q), np.zeros(3), b, cu)  # A_log must be [H]
+    with pytest.raises(RuntimeError):
+        kda_recurrent_gated(q, k, v, np.zeros_like(q), np.zeros(2), b, cu, mutation=3)  # not a gate mutation
