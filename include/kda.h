@@ -125,6 +125,47 @@ kda_status kda_decode(const void *q, const void *k, const void *v, const float *
                       float lower_bound, float scale, void *stream);
 
 /*
+ * The gated log-decay (Kimi K3 -- Architecture Notes, section 1.2, the K3 row of
+ * the mapping table from decay logits to log-decay): instead of log_alpha, the
+ * caller passes the decay logits z and one log-scale A_h per head, and
+ *
+ *     g_t = g_min * Sigmoid(e^{A_h} z_t),   Sigmoid(x) = 1 / (1 + e^{-x}),
+ *
+ * is computed inside the kernels. g lies in (g_min, 0) by construction, so no
+ * clamp is applied; a NaN logit propagates. z has the element type of q, k, v
+ * (so the bf16 path streams 2 bytes per channel instead of the 4 of log_alpha).
+ *
+ *   z      [total_tokens, H, d_k] (prefill) or [B, H, d_k] (decode)   in_dtype
+ *   A_log  [H]   fp32, device; e^{A_h} must be finite in fp32 (A_h < 88)
+ *   g_min  the lower end of the log-decay, <= 0 and finite (the pages fix -5)
+ *
+ * Every other argument, the conventions and the results are those of the
+ * clamped entry point with the same suffix. kda_prefill_gated runs the chunked
+ * tensor-core kernel when in_dtype is KDA_BF16, d_k = d_v = 128 and
+ * g_min >= -5, and the fp32 token-recurrent kernel otherwise;
+ * kda_prefill_gated_recurrent always runs the latter.
+ */
+kda_status kda_prefill_gated(const void *q, const void *k, const void *v, const void *z,
+                             const float *A_log, const float *beta, const int32_t *cu_seqlens,
+                             int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                             int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype, float g_min,
+                             float scale, const float *init_state, void *out, float *final_state,
+                             void *stream);
+
+kda_status kda_prefill_gated_recurrent(const void *q, const void *k, const void *v, const void *z,
+                                       const float *A_log, const float *beta,
+                                       const int32_t *cu_seqlens, int32_t num_seqs,
+                                       int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                       kda_dtype in_dtype, kda_dtype out_dtype, float g_min,
+                                       float scale, const float *init_state, void *out,
+                                       float *final_state, void *stream);
+
+kda_status kda_decode_gated(const void *q, const void *k, const void *v, const void *z,
+                            const float *A_log, const float *beta, float *state, void *out,
+                            int32_t B, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
+                            kda_dtype out_dtype, float g_min, float scale, void *stream);
+
+/*
  * kda_check_device_error -- synchronises `stream`, then reads and clears the
  * library's device error word. Returns KDA_OK, KDA_ERR_TIMEOUT if a kernel's
  * bounded wait gave up since the last check, or KDA_ERR_CUDA if the

@@ -42,6 +42,13 @@ def _declare(lib):
     lib.kda_prefill_recurrent.restype = i32
     lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, vp]
     lib.kda_decode.restype = i32
+    gated_args = [vp, vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, f32, f32, vp, vp, vp, vp]
+    lib.kda_prefill_gated.argtypes = gated_args
+    lib.kda_prefill_gated.restype = i32
+    lib.kda_prefill_gated_recurrent.argtypes = gated_args
+    lib.kda_prefill_gated_recurrent.restype = i32
+    lib.kda_decode_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, vp]
+    lib.kda_decode_gated.restype = i32
     lib.kda_check_device_error.argtypes = [vp]
     lib.kda_check_device_error.restype = i32
     lib.kda_status_string.argtypes = [i32]
@@ -127,6 +134,57 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, out=None, 
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_recurrent" if recurrent else "kda_prefill")
     return out, final_state
+
+
+def prefill_gated(q, k, v, z, A_log, beta, cu_seqlens, init_state=None, *, out=None, final_state=None,
+                  out_dtype=torch.float32, g_min: float = -5.0, scale: float = 1.0, stream=None,
+                  recurrent: bool = False, want_final: bool = True):
+    """KDA prefill with the gated log-decay g = g_min * Sigmoid(e^{A_h} z) (``kda_prefill_gated``).
+
+    z [T, H, d_k] in the dtype of q/k/v; A_log [H] float32; the rest as in ``prefill``.
+    ``recurrent=True`` forces the fp32 token-recurrent kernel (``kda_prefill_gated_recurrent``).
+    """
+    T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    N = cu_seqlens.shape[0] - 1
+    dt = _io_dtype(q.dtype)
+    if k.dtype != q.dtype or v.dtype != q.dtype or z.dtype != q.dtype:
+        raise TypeError("q, k, v and z must share one dtype")
+    if A_log.dtype != torch.float32 or beta.dtype != torch.float32:
+        raise TypeError("A_log and beta must be float32")
+    if cu_seqlens.dtype != torch.int32:
+        raise TypeError("cu_seqlens must be int32")
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=out_dtype, device=q.device)
+    odt = _io_dtype(out.dtype)
+    if final_state is None and want_final:
+        final_state = torch.empty((N, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    _check_cuda(q, k, v, z, A_log, beta, cu_seqlens, init_state, out, final_state)
+    fn = lib().kda_prefill_gated_recurrent if recurrent else lib().kda_prefill_gated
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A_log), _ptr(beta), _ptr(cu_seqlens), N, T, H, d_k, d_v, dt,
+            odt, float(g_min), float(scale), _ptr(init_state), _ptr(out), _ptr(final_state), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_gated_recurrent" if recurrent else "kda_prefill_gated")
+    return out, final_state
+
+
+def decode_gated(q, k, v, z, A_log, beta, state, *, out=None, out_dtype=torch.float32, g_min: float = -5.0,
+                 scale: float = 1.0, stream=None):
+    """One decode step with the gated log-decay (``kda_decode_gated``); ``state`` is updated in place."""
+    B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    dt = _io_dtype(q.dtype)
+    if z.dtype != q.dtype or A_log.dtype != torch.float32:
+        raise TypeError("z must have the dtype of q, A_log must be float32")
+    if out is None:
+        out = torch.empty((B, H, d_v), dtype=out_dtype, device=q.device)
+    odt = _io_dtype(out.dtype)
+    _check_cuda(q, k, v, z, A_log, beta, state, out)
+    st = lib().kda_decode_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(z), _ptr(A_log), _ptr(beta), _ptr(state), _ptr(out),
+                                B, H, d_k, d_v, dt, odt, float(g_min), float(scale), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_gated")
+    return out
 
 
 def decode(q, k, v, log_alpha, beta, state, *, out=None, out_dtype=torch.float32, lower_bound: float = -5.0,

@@ -1,5 +1,6 @@
 // kda_api.cu -- the C ABI of libkda (declared in include/kda.h): argument
 // validation on the host, dispatch to the kernels, the device error word.
+#include <cmath>
 #include <cstdint>
 
 #include "kda_common.cuh"
@@ -32,25 +33,28 @@ uint32_t *device_error_word() {
   return p;
 }
 
-cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
-                          float *state, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
-                          float lb, float scale, cudaStream_t stream);
-cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const float *log_alpha,
+// Each launcher takes the decay input as `decay` + `A_log`: log_alpha (fp32) with A_log null
+// (the clamped form), or the gated form's logits z (input dtype) with A_log [H].
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
+                          const float *beta, float *state, void *out, int B, int H, int d_k, int d_v, bool in_bf16,
+                          bool out_bf16, float lb, float scale, cudaStream_t stream);
+cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                              const float *beta, const int32_t *cu_seqlens, int num_seqs, int H, int d_k, int d_v,
                              bool in_bf16, bool out_bf16, float lb, float scale, const float *init_state,
                              void *out, float *final_state, cudaStream_t stream);
 bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb);
-kda_status launch_chunked(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
-                          const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H, bool out_bf16,
-                          float lb, float scale, const float *init_state, void *out, float *final_state,
-                          cudaStream_t stream);
+kda_status launch_chunked(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
+                          const float *beta, const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H,
+                          bool out_bf16, float lb, float scale, const float *init_state, void *out,
+                          float *final_state, cudaStream_t stream);
 
 namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
 
-kda_status check_prefill_args(const void *q, const void *k, const void *v, const float *log_alpha,
+// decay: log_alpha (fp32) when A_log is null, else the gated form's logits z (in_dtype)
+kda_status check_prefill_args(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                               const float *beta, const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                               int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype,
                               const float *init_state, const void *out, const float *final_state) {
@@ -62,8 +66,8 @@ kda_status check_prefill_args(const void *q, const void *k, const void *v, const
   if (int64_t(num_seqs) * H > INT32_MAX / 4) return KDA_ERR_UNSUPPORTED;
   if (cu_seqlens == nullptr || !aligned4(cu_seqlens)) return KDA_ERR_INVALID_ARG;
   if (total_tokens > 0) {
-    if (!q || !k || !v || !log_alpha || !beta || !out) return KDA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || !aligned16(out) ||
+    if (!q || !k || !v || !decay || !beta || !out) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(decay) || !aligned16(out) ||
         !aligned4(beta))
       return KDA_ERR_INVALID_ARG;
   }
@@ -78,9 +82,10 @@ kda_status check_prefill_args(const void *q, const void *k, const void *v, const
   };
   const size_t nk = size_t(total_tokens) * H * d_k, nv = size_t(total_tokens) * H * d_v;
   const size_t ns = size_t(num_seqs) * H * d_k * d_v * 4;
-  const void *ins[5] = {q, k, v, log_alpha, beta};
-  const size_t in_bytes[5] = {nk * es, nk * es, nv * es, nk * 4, size_t(total_tokens) * H * 4};
-  for (int i = 0; i < 5; ++i) {
+  const void *ins[6] = {q, k, v, decay, beta, A_log};
+  const size_t in_bytes[6] = {nk * es, nk * es, nv * es, nk * (A_log ? es : 4), size_t(total_tokens) * H * 4,
+                              A_log ? size_t(H) * 4 : 0};
+  for (int i = 0; i < 6; ++i) {
     if (overlaps(out, nv * eo, ins[i], in_bytes[i])) return KDA_ERR_INVALID_ARG;
     if (overlaps(final_state, ns, ins[i], in_bytes[i])) return KDA_ERR_INVALID_ARG;
   }
@@ -88,6 +93,50 @@ kda_status check_prefill_args(const void *q, const void *k, const void *v, const
     return KDA_ERR_INVALID_ARG;
   if (final_state != init_state && overlaps(final_state, ns, init_state, ns)) return KDA_ERR_INVALID_ARG;
   return KDA_OK;
+}
+
+// the gated form's parameters: A_log [H] fp32 on the device, g_min finite and <= 0
+kda_status check_gate_args(const float *A_log, float g_min) {
+  if (A_log == nullptr || !aligned4(A_log)) return KDA_ERR_INVALID_ARG;
+  if (!(g_min <= 0.f) || !(g_min > -INFINITY)) return KDA_ERR_INVALID_ARG;  // rejects NaN and -inf
+  return KDA_OK;
+}
+
+kda_status prefill_impl(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
+                        const float *beta, const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                        int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype, float lb,
+                        float scale, const float *init_state, void *out, float *final_state, void *stream,
+                        bool force_recurrent) {
+  const kda_status st = check_prefill_args(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, d_k,
+                                           d_v, in_dtype, out_dtype, init_state, out, final_state);
+  if (st != KDA_OK) return st;
+  if (num_seqs == 0) return KDA_OK;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (!force_recurrent && total_tokens > 0 && chunked_supported(d_k, d_v, in_dtype == KDA_BF16, lb))
+    return launch_chunked(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, out_dtype == KDA_BF16,
+                          lb, scale, init_state, out, final_state, s);
+  const cudaError_t err = launch_recurrent(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, H, d_k, d_v,
+                                           in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale, init_state, out,
+                                           final_state, s);
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status decode_impl(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
+                       const float *beta, float *state, void *out, int32_t B, int32_t H, int32_t d_k, int32_t d_v,
+                       kda_dtype in_dtype, kda_dtype out_dtype, float lb, float scale, void *stream) {
+  if (in_dtype != KDA_F32 && in_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (out_dtype != KDA_F32 && out_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (B < 1 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
+  if (d_k > 128 || d_v > 128 || (d_v & 3) != 0) return KDA_ERR_UNSUPPORTED;
+  if (int64_t(B) * H > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+  if (!q || !k || !v || !decay || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(decay) || !aligned16(state) ||
+      !aligned16(out) || !aligned4(beta))
+    return KDA_ERR_INVALID_ARG;
+  const cudaError_t err = launch_decode(q, k, v, decay, A_log, beta, state, out, B, H, d_k, d_v,
+                                        in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale,
+                                        static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 }  // namespace
@@ -102,48 +151,54 @@ kda_status kda_prefill_recurrent(const void *q, const void *k, const void *v, co
                                  int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
                                  kda_dtype out_dtype, float lower_bound, float scale, const float *init_state,
                                  void *out, float *final_state, void *stream) {
-  const kda_status st = check_prefill_args(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, H, d_k,
-                                           d_v, in_dtype, out_dtype, init_state, out, final_state);
-  if (st != KDA_OK) return st;
-  if (num_seqs == 0) return KDA_OK;
-  const cudaError_t err = launch_recurrent(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, H, d_k, d_v,
-                                           in_dtype == KDA_BF16, out_dtype == KDA_BF16, lower_bound, scale,
-                                           init_state, out, final_state, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  return prefill_impl(q, k, v, log_alpha, nullptr, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype,
+                      out_dtype, lower_bound, scale, init_state, out, final_state, stream, true);
 }
 
 kda_status kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
                        const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                        int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype, float lower_bound, float scale,
                        const float *init_state, void *out, float *final_state, void *stream) {
-  const kda_status st = check_prefill_args(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, H, d_k,
-                                           d_v, in_dtype, out_dtype, init_state, out, final_state);
+  return prefill_impl(q, k, v, log_alpha, nullptr, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype,
+                      out_dtype, lower_bound, scale, init_state, out, final_state, stream, false);
+}
+
+kda_status kda_prefill_gated(const void *q, const void *k, const void *v, const void *z, const float *A_log,
+                             const float *beta, const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                             int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype,
+                             float g_min, float scale, const float *init_state, void *out, float *final_state,
+                             void *stream) {
+  const kda_status st = check_gate_args(A_log, g_min);
   if (st != KDA_OK) return st;
-  if (num_seqs == 0) return KDA_OK;
-  if (total_tokens > 0 && chunked_supported(d_k, d_v, in_dtype == KDA_BF16, lower_bound))
-    return launch_chunked(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, H, out_dtype == KDA_BF16,
-                          lower_bound, scale, init_state, out, final_state, static_cast<cudaStream_t>(stream));
-  const cudaError_t err = launch_recurrent(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, H, d_k, d_v,
-                                           in_dtype == KDA_BF16, out_dtype == KDA_BF16, lower_bound, scale,
-                                           init_state, out, final_state, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  return prefill_impl(q, k, v, z, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype, out_dtype,
+                      g_min, scale, init_state, out, final_state, stream, false);
+}
+
+kda_status kda_prefill_gated_recurrent(const void *q, const void *k, const void *v, const void *z,
+                                       const float *A_log, const float *beta, const int32_t *cu_seqlens,
+                                       int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                                       kda_dtype in_dtype, kda_dtype out_dtype, float g_min, float scale,
+                                       const float *init_state, void *out, float *final_state, void *stream) {
+  const kda_status st = check_gate_args(A_log, g_min);
+  if (st != KDA_OK) return st;
+  return prefill_impl(q, k, v, z, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype, out_dtype,
+                      g_min, scale, init_state, out, final_state, stream, true);
 }
 
 kda_status kda_decode(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
                       float *state, void *out, int32_t B, int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype,
                       kda_dtype out_dtype, float lower_bound, float scale, void *stream) {
-  if (in_dtype != KDA_F32 && in_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
-  if (out_dtype != KDA_F32 && out_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
-  if (B < 1 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
-  if (d_k > 128 || d_v > 128 || (d_v & 3) != 0) return KDA_ERR_UNSUPPORTED;
-  if (int64_t(B) * H > INT32_MAX) return KDA_ERR_UNSUPPORTED;
-  if (!q || !k || !v || !log_alpha || !beta || !state || !out) return KDA_ERR_INVALID_ARG;
-  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || !aligned16(state) ||
-      !aligned16(out) || !aligned4(beta))
-    return KDA_ERR_INVALID_ARG;
-  const cudaError_t err = launch_decode(q, k, v, log_alpha, beta, state, out, B, H, d_k, d_v, in_dtype == KDA_BF16,
-                                        out_dtype == KDA_BF16, lower_bound, scale, static_cast<cudaStream_t>(stream));
-  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+  return decode_impl(q, k, v, log_alpha, nullptr, beta, state, out, B, H, d_k, d_v, in_dtype, out_dtype,
+                     lower_bound, scale, stream);
+}
+
+kda_status kda_decode_gated(const void *q, const void *k, const void *v, const void *z, const float *A_log,
+                            const float *beta, float *state, void *out, int32_t B, int32_t H, int32_t d_k,
+                            int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype, float g_min, float scale,
+                            void *stream) {
+  const kda_status st = check_gate_args(A_log, g_min);
+  if (st != KDA_OK) return st;
+  return decode_impl(q, k, v, z, A_log, beta, state, out, B, H, d_k, d_v, in_dtype, out_dtype, g_min, scale, stream);
 }
 
 kda_status kda_check_device_error(void *stream) {

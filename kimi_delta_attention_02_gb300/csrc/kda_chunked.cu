@@ -73,7 +73,7 @@ constexpr int kALd = 36;    // fp32 row stride of the A / T scratch
 constexpr float kLog2e = 1.4426950408889634f;
 
 // shared-memory map (bytes from a 1024-aligned base)
-constexpr uint32_t OFF_QKG = 0;              // q [32][128] bf16 | k | log-decay [32][128] fp32
+constexpr uint32_t OFF_QKG = 0;              // q [32][128] bf16 | k | log-decay [32][128] fp32 (or bf16 logits)
 constexpr uint32_t SQ = 0, SK = 8 * 1024, SG = 16 * 1024;
 constexpr uint32_t OFF_V = 32 * 1024;        // two v stages [32][128] bf16, converted to fp16 in place
 constexpr uint32_t OFF_QK = 48 * 1024;       // Gram A side, tf32 [64 rows][128 c]: Q f (rows t), K f (rows 32 + t)
@@ -132,11 +132,15 @@ struct Bars {
   uint64_t qkg, v[2], mma1, gram[2], mma2, wu;
 };
 
-template <bool kOutBF16>
+// kGated: the log-decay is the gated form g = g_min Sigmoid(e^{A_h} z) of section 1.2 (tm_g
+// then maps the bf16 logits z; lb holds g_min); otherwise tm_g maps the fp32 log_alpha,
+// clamped below at lb.
+template <bool kOutBF16, bool kGated>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
-                       const float *__restrict__ beta, const int32_t *__restrict__ cu_seqlens,
+                       const float *__restrict__ A_log, const float *__restrict__ beta,
+                       const int32_t *__restrict__ cu_seqlens,
                        const float *__restrict__ init_state, void *__restrict__ out,
                        float *__restrict__ final_state, int H, float lb, float scale, uint32_t *err_word) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -155,6 +159,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
   const int n_chunks = int((eos - bos + kC - 1) / kC);
   const uint32_t sbase = smem_u32(sm);
+  const float a_h = kGated ? __expf(A_log[h]) : 0.f;  // e^{A_h} of the gated form
 
   if (tid == 0) {
     tma_prefetch_desc(&tm_q);
@@ -209,7 +214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
   auto issue_qkg = [&](int c) {  // issuer
     const int32_t t0 = int32_t(chunk_t0(c));
-    mbar_arrive_expect_tx(&bars->qkg, 2 * 8192 + 16384);
+    mbar_arrive_expect_tx(&bars->qkg, 2 * 8192 + (kGated ? 8192 : 16384));
     tma_load_3d(sm + OFF_QKG + SQ, &tm_q, &bars->qkg, 0, h, t0);
     tma_load_3d(sm + OFF_QKG + SQ + 4096, &tm_q, &bars->qkg, 64, h, t0);
     tma_load_3d(sm + OFF_QKG + SK, &tm_k, &bars->qkg, 0, h, t0);
@@ -270,10 +275,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto decay_sums = [&](auto full_tag) {
       constexpr bool kFull = decltype(full_tag)::value;
       const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG) + tb * kD + ch;
+      const uint16_t *zin = reinterpret_cast<const uint16_t *>(sm + OFF_QKG + SG) + tb * kD + ch;
       float run = 0.f;
 #pragma unroll
       for (int r = 0; r < 8; ++r) {  // alpha = 1 past the end of the sequence
-        const float g = (kFull || tb + r < L) ? clamp_log_decay(gin[r * kD], lb) : 0.f;
+        const float g = !(kFull || tb + r < L) ? 0.f
+                        : kGated              ? gated_log_decay(bf16_to_f32(zin[r * kD]), a_h, lb)
+                                              : clamp_log_decay(gin[r * kD], lb);
         run = fmaf(g, kLog2e, run);
         lg[r] = run;
       }
@@ -776,18 +784,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 3-D map over a token-major [T, H, 128] tensor: dims (channel, head, token); boxes of
-// 32 tokens x 64 channels (bf16, 128-byte swizzle) or 32 tokens x 128 channels (fp32).
-bool make_map(CUtensorMap *map, const void *base, bool bf16, int64_t T, int H) {
+// 32 tokens x 64 channels (bf16, 128-byte swizzle: the MMA operands q, k, v) or 32 tokens x
+// 128 channels without swizzle (the decay input: fp32 log_alpha or bf16 logits z).
+bool make_map(CUtensorMap *map, const void *base, bool bf16, bool swizzled, int64_t T, int H) {
   auto fn = encode_fn();
   if (fn == nullptr) return false;
   const uint64_t es = bf16 ? 2 : 4;
   const cuuint64_t dims[3] = {cuuint64_t(kD), cuuint64_t(H), cuuint64_t(T)};
   const cuuint64_t strides[2] = {cuuint64_t(kD * es), cuuint64_t(H) * kD * es};
-  const cuuint32_t box[3] = {bf16 ? 64u : 128u, 1u, cuuint32_t(kC)};
+  const cuuint32_t box[3] = {swizzled ? 64u : 128u, 1u, cuuint32_t(kC)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
                         const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        bf16 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
@@ -798,20 +807,23 @@ bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb) {
   return in_bf16 && d_k == kD && d_v == kD && lb >= -5.0f;
 }
 
-kda_status launch_chunked(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
-                          const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H, bool out_bf16,
-                          float lb, float scale, const float *init_state, void *out, float *final_state,
-                          cudaStream_t stream) {
+// decay: log_alpha (fp32) when A_log is null, else the gated form's bf16 logits z
+kda_status launch_chunked(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
+                          const float *beta, const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H,
+                          bool out_bf16, float lb, float scale, const float *init_state, void *out,
+                          float *final_state, cudaStream_t stream) {
+  const bool gated = A_log != nullptr;
   CUtensorMap mq, mk, mv, mg;
-  if (!make_map(&mq, q, true, total_tokens, H) || !make_map(&mk, k, true, total_tokens, H) ||
-      !make_map(&mv, v, true, total_tokens, H) || !make_map(&mg, log_alpha, false, total_tokens, H))
+  if (!make_map(&mq, q, true, true, total_tokens, H) || !make_map(&mk, k, true, true, total_tokens, H) ||
+      !make_map(&mv, v, true, true, total_tokens, H) || !make_map(&mg, decay, gated, false, total_tokens, H))
     return KDA_ERR_CUDA;
-  auto kern = out_bf16 ? kda_chunked_kernel<true> : kda_chunked_kernel<false>;
+  auto kern = out_bf16 ? (gated ? kda_chunked_kernel<true, true> : kda_chunked_kernel<true, false>)
+                       : (gated ? kda_chunked_kernel<false, true> : kda_chunked_kernel<false, false>);
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes)) != cudaSuccess)
     return KDA_ERR_CUDA;
   const dim3 grid(unsigned(int64_t(num_seqs) * H)), block(kThreads);
-  kern<<<grid, block, kSmemBytes, stream>>>(mq, mk, mv, mg, beta, cu_seqlens, init_state, out, final_state, H, lb,
-                                            scale, device_error_word());
+  kern<<<grid, block, kSmemBytes, stream>>>(mq, mk, mv, mg, A_log, beta, cu_seqlens, init_state, out, final_state,
+                                            H, lb, scale, device_error_word());
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

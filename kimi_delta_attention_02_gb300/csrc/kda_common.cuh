@@ -91,6 +91,18 @@ __device__ __forceinline__ void store_elem(void *base, int64_t idx, float x) {
 // log-decay clamp: g < lb ? lb : g (a NaN compares false and passes through)
 __device__ __forceinline__ float clamp_log_decay(float g, float lb) { return g < lb ? lb : g; }
 
+// The gated log-decay (Kimi K3 -- Architecture Notes, section 1.2, the K3 row of the
+// mapping table from decay logits to log-decay): g = g_min * Sigmoid(e^{A_h} z), with
+// a_h = e^{A_h} taken once per head. The result lies in (g_min, 0]. Where e^{-a_h z} is
+// beyond 2^100 the quotient is below 2^-97 |g_min|, i.e. alpha = 1 in fp32, so the
+// denominator is capped there to keep the fast division in its range; a NaN logit
+// stays NaN.
+__device__ __forceinline__ float gated_log_decay(float z, float a_h, float g_min) {
+  float e = __expf(-a_h * z);
+  e = e > 0x1p100f ? 0x1p100f : e;
+  return __fdividef(g_min, 1.f + e);
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses and fences
 // ---------------------------------------------------------------------------

@@ -11,7 +11,8 @@
 // columns 4tx..4tx+3 of key rows ty, ty+8, ..., ty+120: every state access is a
 // 128-bit load or store and each warp touches whole 512-byte rows, so the state
 // streams through HBM fully coalesced. The 16 state loads of a thread are issued
-// before anything waits on them.
+// before anything waits on them. The log-decay is either the clamped log_alpha
+// input or, in the gated form (section 1.2), g = g_min * Sigmoid(e^{A_h} z).
 #include "kda_common.cuh"
 
 namespace kda {
@@ -19,12 +20,12 @@ namespace kda {
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeRowsPerThread = 16;  // 128 key rows / 8 row groups
 
-template <bool kInBF16, bool kOutBF16>
+template <bool kInBF16, bool kOutBF16, bool kGated>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
     kda_decode_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
-                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
-                      float *__restrict__ state, void *__restrict__ out, int d_k, int d_v, float lb,
-                      float scale) {
+                      const void *__restrict__ decay, const float *__restrict__ A_log,
+                      const float *__restrict__ beta, float *__restrict__ state, void *__restrict__ out, int H,
+                      int d_k, int d_v, float lb, float scale) {
   __shared__ float s_k[128], s_q[128], s_a[128], s_v[128];
   __shared__ float s_red_y[8][128], s_red_z[8][128];
   __shared__ float s_kq[8];
@@ -52,7 +53,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     if (tid < d_k) {
       kk = load_elem<kInBF16>(k, vec_base + tid);
       qq = load_elem<kInBF16>(q, vec_base + tid);
-      a = __expf(clamp_log_decay(log_alpha[vec_base + tid], lb));
+      a = __expf(kGated ? gated_log_decay(load_elem<kInBF16>(decay, vec_base + tid), __expf(A_log[bh % H]), lb)
+                        : clamp_log_decay(static_cast<const float *>(decay)[vec_base + tid], lb));
     }
     s_k[tid] = kk;
     s_q[tid] = qq;
@@ -110,13 +112,19 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   }
 }
 
-cudaError_t launch_decode(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
-                          float *state, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
-                          float lb, float scale, cudaStream_t stream) {
+// decay: log_alpha (fp32) when A_log is null, else the gated form's logits z (input dtype)
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
+                          const float *beta, float *state, void *out, int B, int H, int d_k, int d_v, bool in_bf16,
+                          bool out_bf16, float lb, float scale, cudaStream_t stream) {
   const dim3 grid(unsigned(int64_t(B) * H)), block(kDecodeThreads);
-  auto kern = in_bf16 ? (out_bf16 ? kda_decode_kernel<true, true> : kda_decode_kernel<true, false>)
-                      : (out_bf16 ? kda_decode_kernel<false, true> : kda_decode_kernel<false, false>);
-  kern<<<grid, block, 0, stream>>>(q, k, v, log_alpha, beta, state, out, d_k, d_v, lb, scale);
+  using Kern = decltype(&kda_decode_kernel<false, false, false>);
+  static const Kern table[8] = {
+      kda_decode_kernel<false, false, false>, kda_decode_kernel<false, false, true>,
+      kda_decode_kernel<false, true, false>,  kda_decode_kernel<false, true, true>,
+      kda_decode_kernel<true, false, false>,  kda_decode_kernel<true, false, true>,
+      kda_decode_kernel<true, true, false>,   kda_decode_kernel<true, true, true>};
+  const Kern kern = table[4 * int(in_bf16) + 2 * int(out_bf16) + int(A_log != nullptr)];
+  kern<<<grid, block, 0, stream>>>(q, k, v, decay, A_log, beta, state, out, H, d_k, d_v, lb, scale);
   return cudaGetLastError();
 }
 

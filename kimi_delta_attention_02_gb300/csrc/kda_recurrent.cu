@@ -10,7 +10,9 @@
 // 32w .. 32w+31 and lane l owns value column 32*slice + l; the reductions over
 // key rows go through shared memory. Token t+1's inputs are fetched while
 // token t is computed. It handles every supported shape and both dtypes; the
-// tensor-core chunked kernels are the fast path for bf16, d = 128.
+// tensor-core chunked kernels are the fast path for bf16, d = 128. The log-decay
+// is either the clamped log_alpha input or, in the gated form (section 1.2),
+// g = g_min * Sigmoid(e^{A_h} z) from decay logits z in the input dtype.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -18,10 +20,11 @@ namespace kda {
 constexpr int kRecThreads = 128;  // 4 warps x 32 key rows
 constexpr int kRecCols = 32;      // value columns per CTA
 
-template <bool kInBF16, bool kOutBF16>
+template <bool kInBF16, bool kOutBF16, bool kGated>
 __global__ void __launch_bounds__(kRecThreads)
     kda_recurrent_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
-                         const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                         const void *__restrict__ decay, const float *__restrict__ A_log,
+                         const float *__restrict__ beta,
                          const int32_t *__restrict__ cu_seqlens, const float *__restrict__ init_state,
                          void *__restrict__ out, float *__restrict__ final_state, int H, int d_k, int d_v,
                          int n_slices, float lb, float scale) {
@@ -37,6 +40,7 @@ __global__ void __launch_bounds__(kRecThreads)
   const int col = slice * kRecCols + lane;
   const bool col_ok = col < d_v;
   const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
+  const float a_h = kGated ? __expf(A_log[h]) : 0.f;  // e^{A_h} of the gated form
 
   // state rows 32w + r of column `col`
   float S[32];
@@ -54,7 +58,8 @@ __global__ void __launch_bounds__(kRecThreads)
     if (tid < d_k) {
       pk = load_elem<kInBF16>(k, base * d_k + tid);
       pq = load_elem<kInBF16>(q, base * d_k + tid);
-      pla = log_alpha[base * d_k + tid];
+      pla = kGated ? load_elem<kInBF16>(decay, base * d_k + tid)
+                   : static_cast<const float *>(decay)[base * d_k + tid];
     }
     if (w == 0) pv = col_ok ? load_elem<kInBF16>(v, base * d_v + col) : 0.f;
     if (tid == 0) pb = beta[base];
@@ -68,7 +73,7 @@ __global__ void __launch_bounds__(kRecThreads)
       const bool ch = tid < d_k;
       s_k[buf][tid] = ch ? pk : 0.f;
       s_q[buf][tid] = ch ? pq : 0.f;
-      s_a[buf][tid] = ch ? __expf(clamp_log_decay(pla, lb)) : 0.f;
+      s_a[buf][tid] = ch ? __expf(kGated ? gated_log_decay(pla, a_h, lb) : clamp_log_decay(pla, lb)) : 0.f;
       float kq = ch ? pk * pq : 0.f;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
@@ -124,16 +129,22 @@ __global__ void __launch_bounds__(kRecThreads)
   }
 }
 
-cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const float *log_alpha,
+// decay: log_alpha (fp32) when A_log is null, else the gated form's logits z (input dtype)
+cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                              const float *beta, const int32_t *cu_seqlens, int num_seqs, int H, int d_k, int d_v,
                              bool in_bf16, bool out_bf16, float lb, float scale, const float *init_state,
                              void *out, float *final_state, cudaStream_t stream) {
   const int n_slices = (d_v + kRecCols - 1) / kRecCols;
   const dim3 grid(unsigned(int64_t(num_seqs) * H * n_slices)), block(kRecThreads);
-  auto kern = in_bf16 ? (out_bf16 ? kda_recurrent_kernel<true, true> : kda_recurrent_kernel<true, false>)
-                      : (out_bf16 ? kda_recurrent_kernel<false, true> : kda_recurrent_kernel<false, false>);
-  kern<<<grid, block, 0, stream>>>(q, k, v, log_alpha, beta, cu_seqlens, init_state, out, final_state, H, d_k, d_v,
-                                   n_slices, lb, scale);
+  using Kern = decltype(&kda_recurrent_kernel<false, false, false>);
+  static const Kern table[8] = {
+      kda_recurrent_kernel<false, false, false>, kda_recurrent_kernel<false, false, true>,
+      kda_recurrent_kernel<false, true, false>,  kda_recurrent_kernel<false, true, true>,
+      kda_recurrent_kernel<true, false, false>,  kda_recurrent_kernel<true, false, true>,
+      kda_recurrent_kernel<true, true, false>,   kda_recurrent_kernel<true, true, true>};
+  const Kern kern = table[4 * int(in_bf16) + 2 * int(out_bf16) + int(A_log != nullptr)];
+  kern<<<grid, block, 0, stream>>>(q, k, v, decay, A_log, beta, cu_seqlens, init_state, out, final_state, H, d_k,
+                                   d_v, n_slices, lb, scale);
   return cudaGetLastError();
 }
 

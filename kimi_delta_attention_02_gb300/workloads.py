@@ -17,6 +17,10 @@ Recipe (the pages publish no dataset; every workload is synthetic):
   other half near zero (-0.01 softplus(N(0,1))).
 * beta = sigmoid(N(0, 1)) in fp32, one per (token, head).
 * initial state: zeros, or 0.02 N(0, 1) in fp32 per (sequence, head).
+* gated form (decay logits instead of log_alpha): z = -1 + 2 N(0, 1) per
+  channel, cast to the workload dtype, and one log-scale A_h = 0.5 N(0, 1) per
+  head in fp32. Through g = -5 Sigmoid(e^{A_h} z) this spreads the retention
+  over nearly the whole bounded range (alpha from about e^-5 to 1).
 
 Every (tensor, head[, step]) pair draws from its own ``torch.Generator``
 stream, so any single head can be regenerated without the others and large
@@ -31,7 +35,7 @@ import numpy as np
 import torch
 
 # tensor ids used to derive stream seeds
-_Q, _K, _V, _LA, _BETA, _INIT = 1, 2, 3, 4, 5, 6
+_Q, _K, _V, _LA, _BETA, _INIT, _Z, _A = 1, 2, 3, 4, 5, 6, 7, 8
 
 
 def _stream(seed: int, tensor_id: int, head: int, step: int, device) -> torch.Generator:
@@ -53,7 +57,8 @@ def _unit_rows(x: torch.Tensor) -> torch.Tensor:
 class PrefillCase:
     """One packed varlen prefill problem. Token-major layouts:
     q, k [T_tot, H, d_k]; v [T_tot, H, d_v] (dtype); log_alpha [T_tot, H, d_k] fp32;
-    beta [T_tot, H] fp32; cu_seqlens [N+1] int32; init_state [N, H, d_k, d_v] fp32 or None."""
+    beta [T_tot, H] fp32; cu_seqlens [N+1] int32; init_state [N, H, d_k, d_v] fp32 or None;
+    gated form only: z [T_tot, H, d_k] (dtype) and A_log [H] fp32."""
     name: str
     q: torch.Tensor
     k: torch.Tensor
@@ -63,6 +68,8 @@ class PrefillCase:
     cu_seqlens: torch.Tensor
     init_state: torch.Tensor | None
     lengths: list = field(default_factory=list)
+    z: torch.Tensor | None = None
+    A_log: torch.Tensor | None = None
 
     @property
     def total_tokens(self) -> int:
@@ -79,8 +86,9 @@ class PrefillCase:
 
 def make_prefill(lengths, H: int, d_k: int = 128, d_v: int = 128, *, dtype=torch.bfloat16,
                  device="cpu", seed: int = 0, init_std: float | None = 0.02,
-                 log_alpha_mode: str = "softplus", name: str = "prefill") -> PrefillCase:
-    """Generate a packed prefill problem. ``init_std=None`` means no initial state."""
+                 log_alpha_mode: str = "softplus", name: str = "prefill", gated: bool = False) -> PrefillCase:
+    """Generate a packed prefill problem. ``init_std=None`` means no initial state;
+    ``gated`` adds the gated form's decay logits z and log-scales A_log."""
     lengths = [int(x) for x in lengths]
     T = int(sum(lengths))
     N = len(lengths)
@@ -107,7 +115,14 @@ def make_prefill(lengths, H: int, d_k: int = 128, d_v: int = 128, *, dtype=torch
         for h in range(H):
             init[:, h] = init_std * _randn((N, d_k, d_v), seed, _INIT, h, 0, device)
     cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), device=device)
-    return PrefillCase(name, q, k, v, la, beta, cu, init, lengths)
+    case = PrefillCase(name, q, k, v, la, beta, cu, init, lengths)
+    if gated:
+        case.z = torch.empty((T, H, d_k), dtype=dtype, device=device)
+        case.A_log = torch.empty((H,), dtype=torch.float32, device=device)
+        for h in range(H):
+            case.z[:, h] = (-1.0 + 2.0 * _randn((T, d_k), seed, _Z, h, 0, device)).to(dtype)
+            case.A_log[h] = 0.5 * _randn((1,), seed, _A, h, 0, device)[0]
+    return case
 
 
 def varlen_lengths(num_seqs: int = 8, lo: int = 1024, hi: int = 32768, seed: int = 0):
@@ -127,6 +142,8 @@ PREFILL_WORKLOADS = {
     "prefill_varlen8_H96": dict(lengths=None, H=96, dtype=torch.bfloat16, init_std=0.02,
                                 log_alpha_mode="split"),
     "prefill_long_T1M_H32": dict(lengths=[1 << 20], H=32, dtype=torch.bfloat16, init_std=None),
+    # the gated decay form on the K3-shaped layer
+    "prefill_k3_gated_T4096_H96": dict(lengths=[4096], H=96, dtype=torch.bfloat16, init_std=0.02, gated=True),
 }
 
 
@@ -140,12 +157,16 @@ def prefill_workload(name: str, device="cpu", seed: int = 0) -> PrefillCase:
 @dataclass
 class DecodeStep:
     """Inputs of one decode step for B independent sequences: q, k [B, H, d_k],
-    v [B, H, d_v] (dtype); log_alpha [B, H, d_k] fp32; beta [B, H] fp32."""
+    v [B, H, d_v] (dtype); log_alpha [B, H, d_k] fp32; beta [B, H] fp32; gated form
+    only: z [B, H, d_k] (dtype) and A_log [H] fp32 (a per-head parameter, the same
+    for every step)."""
     q: torch.Tensor
     k: torch.Tensor
     v: torch.Tensor
     log_alpha: torch.Tensor
     beta: torch.Tensor
+    z: torch.Tensor | None = None
+    A_log: torch.Tensor | None = None
 
 
 def make_decode_state(B: int, H: int, d_k: int = 128, d_v: int = 128, *, device="cpu", seed: int = 0,
@@ -157,7 +178,7 @@ def make_decode_state(B: int, H: int, d_k: int = 128, d_v: int = 128, *, device=
 
 
 def make_decode_step(step: int, B: int, H: int, d_k: int = 128, d_v: int = 128, *,
-                     dtype=torch.bfloat16, device="cpu", seed: int = 0) -> DecodeStep:
+                     dtype=torch.bfloat16, device="cpu", seed: int = 0, gated: bool = False) -> DecodeStep:
     """Fresh inputs for decode step ``step`` (streams differ per step)."""
     s = step + 1
     q = _unit_rows(_randn((B, H, d_k), seed, _Q, 0, s, device)).to(dtype)
@@ -165,7 +186,11 @@ def make_decode_step(step: int, B: int, H: int, d_k: int = 128, d_v: int = 128, 
     v = _randn((B, H, d_v), seed, _V, 0, s, device).to(dtype)
     la = -torch.nn.functional.softplus(_randn((B, H, d_k), seed, _LA, 0, s, device))
     beta = torch.sigmoid(_randn((B, H), seed, _BETA, 0, s, device))
-    return DecodeStep(q, k, v, la, beta)
+    st = DecodeStep(q, k, v, la, beta)
+    if gated:
+        st.z = (-1.0 + 2.0 * _randn((B, H, d_k), seed, _Z, 0, s, device)).to(dtype)
+        st.A_log = 0.5 * _randn((H,), seed, _A, 0, 0, device)
+    return st
 
 
 DECODE_WORKLOAD = dict(B=256, H=96, d_k=128, d_v=128, steps=64, dtype=torch.bfloat16)

@@ -33,7 +33,8 @@ def declared_functions():
 def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert {"kda_prefill", "kda_decode", "kda_prefill_recurrent", "kda_check_device_error",
-            "kda_status_string", "kda_version", "kda_selftest_umma"} <= set(names)
+            "kda_status_string", "kda_version", "kda_selftest_umma", "kda_prefill_gated",
+            "kda_prefill_gated_recurrent", "kda_decode_gated"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -108,3 +109,50 @@ def test_selftest_rejects_bad_shapes(lib):
     assert st == B.KDA_ERR_UNSUPPORTED  # tf32 operands are K-major only
     st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, 128, 64, 64, 5, 0, 0, 0, 0, 16, 1024, 16, 1024, 0x4000, NULL)
     assert st == B.KDA_ERR_INVALID_ARG
+
+
+def _prefill_gated(lib, fn="kda_prefill_gated", **over):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, z=0x40000, A=0xa0000, beta=0x50000, cu=0x60000, N=1, T=4, H=2,
+             dk=128, dv=128, dtype=1, odtype=0, gmin=-5.0, scale=1.0, init=NULL, out=0x70000, fin=0x80000,
+             stream=NULL)
+    a.update(over)
+    return getattr(lib, fn)(a["q"], a["k"], a["v"], a["z"], a["A"], a["beta"], a["cu"], a["N"], a["T"], a["H"],
+                            a["dk"], a["dv"], a["dtype"], a["odtype"], a["gmin"], a["scale"], a["init"], a["out"],
+                            a["fin"], a["stream"])
+
+
+@pytest.mark.parametrize("fn", ["kda_prefill_gated", "kda_prefill_gated_recurrent"])
+@pytest.mark.parametrize("over,expect", [
+    (dict(z=NULL), B.KDA_ERR_INVALID_ARG),
+    (dict(A=NULL), B.KDA_ERR_INVALID_ARG),
+    (dict(A=0xa0002), B.KDA_ERR_INVALID_ARG),          # misaligned A_log
+    (dict(z=0x40008), B.KDA_ERR_INVALID_ARG),          # misaligned z
+    (dict(gmin=0.5), B.KDA_ERR_INVALID_ARG),           # g_min must be <= 0
+    (dict(gmin=float("nan")), B.KDA_ERR_INVALID_ARG),
+    (dict(gmin=float("-inf")), B.KDA_ERR_INVALID_ARG),
+    (dict(out=0x40000), B.KDA_ERR_INVALID_ARG),        # output aliases z
+    (dict(fin=0xa0000), B.KDA_ERR_INVALID_ARG),        # final state aliases A_log
+    (dict(dk=129), B.KDA_ERR_UNSUPPORTED),
+])
+def test_prefill_gated_rejects(lib, fn, over, expect):
+    assert _prefill_gated(lib, fn, **over) == expect
+
+
+def test_prefill_gated_accepts_empty_work(lib):
+    assert _prefill_gated(lib, N=0, T=0, q=NULL, k=NULL, v=NULL, z=NULL, beta=NULL, out=NULL, fin=NULL) == B.KDA_OK
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(z=NULL), B.KDA_ERR_INVALID_ARG),
+    (dict(A=NULL), B.KDA_ERR_INVALID_ARG),
+    (dict(gmin=1.0), B.KDA_ERR_INVALID_ARG),
+    (dict(state=NULL), B.KDA_ERR_INVALID_ARG),
+    (dict(dv=6), B.KDA_ERR_UNSUPPORTED),
+])
+def test_decode_gated_rejects(lib, over, expect):
+    a = dict(q=0x10000, k=0x20000, v=0x30000, z=0x40000, A=0xa0000, beta=0x50000, state=0x90000, out=0x70000, B=2,
+             H=2, dk=128, dv=128, dtype=1, odtype=0, gmin=-5.0)
+    a.update(over)
+    st = lib.kda_decode_gated(a["q"], a["k"], a["v"], a["z"], a["A"], a["beta"], a["state"], a["out"], a["B"],
+                              a["H"], a["dk"], a["dv"], a["dtype"], a["odtype"], a["gmin"], 1.0, NULL)
+    assert st == expect
