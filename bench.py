@@ -52,6 +52,8 @@ def peaks():
 PREFILL_BYTES_PER_TOKEN_HEAD = 1796
 PREFILL_STATE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4
 PREFILL_FLOPS_PER_TOKEN_HEAD = 6 * 128 * 128 + 64 * (3 * 128 + 2 * 128)
+# the gated log-decay form reads bf16 logits z instead of fp32 log_alpha: 768 + 256 + 4 + 512 = 1540
+GATED_BYTES_PER_TOKEN_HEAD = 1540
 # decode, per (sequence, head): state read + write (131,072) + q,k,v bf16 (768) + log_alpha (512)
 # + beta (4) + out fp32 (512) = 132,868 bytes
 DECODE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4 + 3 * 256 + 512 + 4 + 512
@@ -166,14 +168,19 @@ def prefill_traffic():
     return rec.get("bytes_per_launch") if h.hexdigest() == rec.get("sources_sha256") else None
 
 
-def time_prefill(case, steps, warmup, world):
+def time_prefill(case, steps, warmup, world, gated=False):
     from kimi_delta_attention_02_gb300 import binding
-    args = (case.q, case.k, case.v, case.log_alpha, case.beta, case.cu_seqlens, case.init_state)
+    if gated:
+        fn = binding.prefill_gated
+        args = (case.q, case.k, case.v, case.z, case.A_log, case.beta, case.cu_seqlens, case.init_state)
+    else:
+        fn = binding.prefill
+        args = (case.q, case.k, case.v, case.log_alpha, case.beta, case.cu_seqlens, case.init_state)
     out = torch.empty(case.v.shape, dtype=torch.float32, device=case.v.device)
     fin = torch.empty_like(case.init_state)
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
-        binding.prefill(*args, out=out, final_state=fin, stream=stream)
+        fn(*args, out=out, final_state=fin, stream=stream)
     binding.check_device_error(stream)
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
@@ -183,7 +190,7 @@ def time_prefill(case, steps, warmup, world):
     t0.record(stream)
     for i in range(steps):
         starts[i].record(stream)
-        binding.prefill(*args, out=out, final_state=fin, stream=stream)
+        fn(*args, out=out, final_state=fin, stream=stream)
         ends[i].record(stream)
     t1.record(stream)
     torch.cuda.synchronize()
@@ -315,6 +322,12 @@ def main():
     with ClockSampler(local) as clocks:
         total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world)
         dec_ms = None if args.prefill_only else time_decode(DECODE["steps"], 1, 1, world, seed=rank)
+        gated_ms = None
+        if not args.prefill_only and args.heads == PREFILL["H"]:
+            gcase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
+            _, g_launch = time_prefill(gcase, args.steps, args.warmup, world, gated=True)
+            gated_ms = sum(g_launch) / len(g_launch)
+            del gcase
     if args.prefill_only:
         if rank == 0:
             print(json.dumps({"prefill_only": True, "heads": H, "ms_per_step": total_ms / args.steps,
@@ -332,6 +345,14 @@ def main():
     achieved_tf = alg_flops / (launch_avg_ms / 1e3) / 1e12
     traffic = prefill_traffic() if H == PREFILL["H"] else None
 
+    gated = None
+    if gated_ms is not None:
+        g_bytes = T * H * GATED_BYTES_PER_TOKEN_HEAD + case.num_seqs * H * (PREFILL_STATE_BYTES_PER_SEQ_HEAD + 4)
+        g_gbs = g_bytes / (gated_ms / 1e3) / 1e9
+        gated = {"workload": "prefill_k3_gated_T4096_H96", "launch_ms": gated_ms,
+                 "tokens_per_s": world * T / (gated_ms / 1e3), "GB/s": g_gbs, "peak": hbm_gbs,
+                 "frac": g_gbs / hbm_gbs, "alg_bytes": g_bytes,
+                 "tensor_frac": alg_flops / (gated_ms / 1e3) / 1e12 / tf_burst}
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     dec_bytes = DECODE["B"] * DECODE["H"] * DECODE_BYTES_PER_SEQ_HEAD
     dec_gbs = dec_bytes / (dec_avg_ms / 1e3) / 1e9
@@ -368,6 +389,7 @@ def main():
                        "peak": hbm_gbs, "frac": dec_gbs / hbm_gbs,
                        "tokens_per_s": DECODE["B"] / (dec_avg_ms / 1e3), "alg_bytes": dec_bytes,
                        "launches": len(dec_ms)},
+            "gated_decay": gated,
             "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk,
             "gpu_launches": args.steps,  # one prefill launch per timed step (decode: its own region)
         }
