@@ -280,3 +280,79 @@ class HostPrefill:
         if sync:
             stream.synchronize()
         return self.host_out, self.host_final
+
+
+class HostPrefillStream:
+    """Prefill from pinned HOST buffers, streamed: step i's host-to-device copies, its kernel and
+    its device-to-host copies run on three CUDA streams, so that step i+1's inputs travel while
+    step i computes and step i-1's results come back.
+
+    Every step still moves all its inputs to the device and all its outputs (``out`` and the
+    final state) back to pinned host memory; two device staging sets and two host result sets
+    alternate between steps. ``run(steps)`` enqueues the steps and waits for the last result.
+    """
+
+    def __init__(self, q, k, v, log_alpha, beta, cu_seqlens, init_state=None, device="cuda",
+                 out_dtype=torch.float32):
+        self.host_in = [t.pin_memory() if not t.is_pinned() else t
+                        for t in (q, k, v, log_alpha, beta, cu_seqlens)]
+        self.host_init = None if init_state is None else init_state.pin_memory()
+        T, H, _ = q.shape
+        N = cu_seqlens.shape[0] - 1
+        self.dev_in = [[torch.empty_like(t, device=device) for t in self.host_in] for _ in range(2)]
+        self.dev_init = [None if init_state is None else torch.empty_like(self.host_init, device=device)
+                         for _ in range(2)]
+        self.dev_out = [torch.empty((T, H, v.shape[-1]), dtype=out_dtype, device=device) for _ in range(2)]
+        self.dev_final = [torch.empty((N, H, q.shape[-1], v.shape[-1]), dtype=torch.float32, device=device)
+                          for _ in range(2)]
+        self.host_out = [torch.empty_like(self.dev_out[0], device="cpu").pin_memory() for _ in range(2)]
+        self.host_final = [torch.empty_like(self.dev_final[0], device="cpu").pin_memory() for _ in range(2)]
+        self.s_in, self.s_run, self.s_back = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+        self.ev_in = [torch.cuda.Event() for _ in range(2)]
+        self.ev_run = [torch.cuda.Event() for _ in range(2)]
+        self.ev_back = [torch.cuda.Event() for _ in range(2)]
+        self.steps_done = 0
+
+    @property
+    def h2d_bytes(self) -> int:
+        n = sum(t.numel() * t.element_size() for t in self.host_in)
+        return n + (0 if self.host_init is None else self.host_init.numel() * 4)
+
+    @property
+    def d2h_bytes(self) -> int:
+        return self.host_out[0].numel() * self.host_out[0].element_size() + self.host_final[0].numel() * 4
+
+    def enqueue(self):
+        """Enqueue one step (copies in, kernel, copies back) without waiting."""
+        i = self.steps_done
+        b = i & 1
+        with torch.cuda.stream(self.s_in):
+            if i >= 2:
+                self.s_in.wait_event(self.ev_run[b])  # step i-2's kernel has read this staging set
+            for d, h in zip(self.dev_in[b], self.host_in):
+                d.copy_(h, non_blocking=True)
+            if self.dev_init[b] is not None:
+                self.dev_init[b].copy_(self.host_init, non_blocking=True)
+            self.ev_in[b].record(self.s_in)
+        with torch.cuda.stream(self.s_run):
+            self.s_run.wait_event(self.ev_in[b])
+            if i >= 2:
+                self.s_run.wait_event(self.ev_back[b])  # step i-2's results have left this set
+            q, k, v, la, bt, cu = self.dev_in[b]
+            prefill(q, k, v, la, bt, cu, self.dev_init[b], out=self.dev_out[b], final_state=self.dev_final[b],
+                    stream=self.s_run)
+            self.ev_run[b].record(self.s_run)
+        with torch.cuda.stream(self.s_back):
+            self.s_back.wait_event(self.ev_run[b])
+            self.host_out[b].copy_(self.dev_out[b], non_blocking=True)
+            self.host_final[b].copy_(self.dev_final[b], non_blocking=True)
+            self.ev_back[b].record(self.s_back)
+        self.steps_done += 1
+
+    def run(self, steps: int):
+        """Run ``steps`` streamed steps and return the last step's (out, final_state) on the host."""
+        for _ in range(steps):
+            self.enqueue()
+        b = (self.steps_done - 1) & 1
+        self.ev_back[b].synchronize()
+        return self.host_out[b], self.host_final[b]

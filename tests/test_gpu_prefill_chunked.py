@@ -138,3 +138,19 @@ def test_long_context_sampled_heads():
     """B=1, T=2^20, H=32, zero initial state; the seeded 4-head sample."""
     case = workloads.prefill_workload("prefill_long_T1M_H32", device="cuda")
     _check(case, heads=workloads.sampled_heads(32, 4, seed=0))
+
+
+@pytest.mark.parametrize("streamed", [False, True])
+def test_host_buffer_prefill_matches_device_call(streamed):
+    """The host-buffer paths (one step at a time, and streamed over two staging sets) return
+    exactly the device call's out and final state, at every step of a run."""
+    case = workloads.make_prefill([40, 0, 97], H=4, device="cpu", seed=23)
+    o_ref, f_ref = binding.prefill(*(t.cuda() for t in (case.q, case.k, case.v, case.log_alpha, case.beta,
+                                                        case.cu_seqlens, case.init_state)))
+    cls = binding.HostPrefillStream if streamed else binding.HostPrefill
+    hp = cls(case.q, case.k, case.v, case.log_alpha, case.beta, case.cu_seqlens, case.init_state)
+    for steps in (1, 1, 3, 2):
+        out, fin = hp.run(steps) if streamed else hp()
+        assert out.device.type == "cpu" and fin.device.type == "cpu"
+        assert torch.equal(out, o_ref.cpu()) and torch.equal(fin, f_ref.cpu())
+    binding.check_device_error()
