@@ -18,6 +18,8 @@ Notes, section 1.1 "Kimi Delta Attention"):
   system solved by a library inverse. Pinned to ``recurrent`` by agreement.
 * ``exact``    -- the recurrence with explicit dense transition matrices in
   exact rational arithmetic (``fractions.Fraction``), for tiny inputs.
+* ``epilogue`` -- the output gate with head-wise RMSNorm of section 1.3
+  ("Full-rank output gate"), applied to a read-out, in numpy fp64.
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (exact brute force, closed forms, invariants, recurrent/chunked agreement and
@@ -29,3 +31,4 @@ from .recurrent import (kda_recurrent, kda_recurrent_mutant, kda_recurrent_gated
                         GATE_MUTATIONS, oracle_library_path)
 from .chunked import kda_chunked, chunk_quantities  # noqa: F401
 from .exact import kda_exact  # noqa: F401
+from .epilogue import output_gate_rmsnorm, EPILOGUE_MUTATIONS  # noqa: F401
