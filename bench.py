@@ -54,6 +54,8 @@ PREFILL_STATE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4
 PREFILL_FLOPS_PER_TOKEN_HEAD = 6 * 128 * 128 + 64 * (3 * 128 + 2 * 128)
 # the gated log-decay form reads bf16 logits z instead of fp32 log_alpha: 768 + 256 + 4 + 512 = 1540
 GATED_BYTES_PER_TOKEN_HEAD = 1540
+# gated decay + output gate (bf16 gate logits in, bf16 output): 768 + 256 + 4 + 256 + 256 = 1540
+OUTGATE_BYTES_PER_TOKEN_HEAD = 1540
 # decode, per (sequence, head): state read + write (131,072) + q,k,v bf16 (768) + log_alpha (512)
 # + beta (4) + out fp32 (512) = 132,868 bytes
 DECODE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4 + 3 * 256 + 512 + 4 + 512
@@ -168,15 +170,24 @@ def prefill_traffic():
     return rec.get("bytes_per_launch") if h.hexdigest() == rec.get("sources_sha256") else None
 
 
-def time_prefill(case, steps, warmup, world, gated=False):
+def time_prefill(case, steps, warmup, world, gated=False, out_gate=False):
     from kimi_delta_attention_02_gb300 import binding
-    if gated:
+    out_dtype = torch.float32
+    if out_gate:  # gated decay, output gate, bf16 output: the parameter-block entry point
+        out_dtype = torch.bfloat16
+        args = ()
+
+        def fn(out, final_state, stream):
+            binding.prefill_ex(case.q, case.k, case.v, case.beta, case.cu_seqlens, z=case.z, A_log=case.A_log,
+                               init_state=case.init_state, out_gate=case.out_gate, norm_weight=case.norm_weight,
+                               out=out, final_state=final_state, stream=stream)
+    elif gated:
         fn = binding.prefill_gated
         args = (case.q, case.k, case.v, case.z, case.A_log, case.beta, case.cu_seqlens, case.init_state)
     else:
         fn = binding.prefill
         args = (case.q, case.k, case.v, case.log_alpha, case.beta, case.cu_seqlens, case.init_state)
-    out = torch.empty(case.v.shape, dtype=torch.float32, device=case.v.device)
+    out = torch.empty(case.v.shape, dtype=out_dtype, device=case.v.device)
     fin = torch.empty_like(case.init_state)
     stream = torch.cuda.current_stream()
     for _ in range(warmup):
@@ -325,12 +336,16 @@ def main():
     with ClockSampler(local) as clocks:
         total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world)
         dec_ms = None if args.prefill_only else time_decode(DECODE["steps"], 1, 1, world, seed=rank)
-        gated_ms = None
+        gated_ms = outgate_ms = None
         if not args.prefill_only and args.heads == PREFILL["H"]:
             gcase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
             _, g_launch = time_prefill(gcase, args.steps, args.warmup, world, gated=True)
             gated_ms = sum(g_launch) / len(g_launch)
             del gcase
+            ocase = workloads.prefill_workload("prefill_k3_outgate_T4096_H96", device="cuda", seed=rank)
+            _, o_launch = time_prefill(ocase, args.steps, args.warmup, world, out_gate=True)
+            outgate_ms = sum(o_launch) / len(o_launch)
+            del ocase
     if args.prefill_only:
         if rank == 0:
             print(json.dumps({"prefill_only": True, "heads": H, "ms_per_step": total_ms / args.steps,
@@ -356,6 +371,14 @@ def main():
                  "tokens_per_s": world * T / (gated_ms / 1e3), "GB/s": g_gbs, "peak": hbm_gbs,
                  "frac": g_gbs / hbm_gbs, "alg_bytes": g_bytes,
                  "tensor_frac": alg_flops / (gated_ms / 1e3) / 1e12 / tf_burst}
+    outgate = None
+    if outgate_ms is not None:
+        o_bytes = T * H * OUTGATE_BYTES_PER_TOKEN_HEAD + case.num_seqs * H * (PREFILL_STATE_BYTES_PER_SEQ_HEAD + 4) + 512
+        o_gbs = o_bytes / (outgate_ms / 1e3) / 1e9
+        outgate = {"workload": "prefill_k3_outgate_T4096_H96", "launch_ms": outgate_ms,
+                   "tokens_per_s": world * T / (outgate_ms / 1e3), "GB/s": o_gbs, "peak": hbm_gbs,
+                   "frac": o_gbs / hbm_gbs, "alg_bytes": o_bytes, "out_dtype": "bf16",
+                   "tensor_frac": alg_flops / (outgate_ms / 1e3) / 1e12 / tf_burst}
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     dec_bytes = DECODE["B"] * DECODE["H"] * DECODE_BYTES_PER_SEQ_HEAD
     dec_gbs = dec_bytes / (dec_avg_ms / 1e3) / 1e9
@@ -395,6 +418,7 @@ def main():
                        "tokens_per_s": DECODE["B"] / (dec_avg_ms / 1e3), "alg_bytes": dec_bytes,
                        "launches": len(dec_ms)},
             "gated_decay": gated,
+            "output_gate": outgate,
             "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk,
             "gpu_launches": args.steps,  # one prefill launch per timed step (decode: its own region)
         }

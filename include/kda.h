@@ -166,6 +166,83 @@ kda_status kda_decode_gated(const void *q, const void *k, const void *v, const v
                             kda_dtype out_dtype, float g_min, float scale, void *stream);
 
 /*
+ * Parameter-block entry points: every option of the calls above in one struct,
+ * plus the output gate of Kimi K3 -- Architecture Notes, section 1.3
+ * ("Full-rank output gate": y = W_o [Sigmoid(W_g x) (.) RMSNorm(o)]). The two
+ * projections W_g and W_o are the caller's matmuls; when `out_gate` is given the
+ * library applies the bracket to each read-out before writing it, per token and
+ * head over the d_v value channels:
+ *
+ *     out_t = Sigmoid(r_t) * w * o_t / sqrt(mean_j o_tj^2 + norm_eps),
+ *     o_t = scale * S_t^T q_t,   r_t = W_g x_t (the gate logits),
+ *
+ * with w the RMSNorm weight. The page gives neither eps nor the shape of the
+ * weight; this library takes the usual RMSNorm: eps inside the square root and
+ * one weight per value channel, shared by the heads. norm_eps = 0 with an
+ * all-zero read-out gives NaN (0 / 0), as the formula does.
+ *
+ * Fields (sizes and layouts as in kda_prefill / kda_decode):
+ *   struct_size   sizeof the struct; any other value returns KDA_ERR_INVALID_ARG
+ *   decay_form    KDA_DECAY_CLAMPED: `decay` is log_alpha (fp32), A_log must be
+ *                 NULL and decay_bound is the lower bound; KDA_DECAY_GATED:
+ *                 `decay` is the logits z (in_dtype), A_log [H] and decay_bound
+ *                 = g_min as in kda_prefill_gated
+ *   out_gate      gate logits r [rows, H, d_v] in in_dtype, device, 16-byte
+ *                 aligned, not overlapping `out`; NULL = no output gate (out = o)
+ *   norm_weight   w [d_v] fp32, device; NULL = ones. Must be NULL without out_gate
+ *   norm_eps      finite, >= 0 (ignored without out_gate)
+ *   force_recurrent (prefill) nonzero runs the fp32 token-recurrent kernel
+ * The output gate is fused into every kernel (the chunked tensor-core kernel,
+ * the token-recurrent kernel and decode); it adds one read of the gate logits
+ * and no other memory traffic.
+ */
+typedef enum { KDA_DECAY_CLAMPED = 0, KDA_DECAY_GATED = 1 } kda_decay_form;
+
+typedef struct kda_prefill_params {
+  uint32_t struct_size;
+  kda_dtype in_dtype, out_dtype;
+  kda_decay_form decay_form;
+  int32_t num_seqs, H, d_k, d_v;
+  int64_t total_tokens;
+  const void *q, *k, *v;
+  const void *decay;          /* log_alpha (fp32) or z (in_dtype), [total_tokens, H, d_k] */
+  const float *A_log;         /* [H], gated form only                                     */
+  const float *beta;          /* [total_tokens, H]                                        */
+  const int32_t *cu_seqlens;  /* [num_seqs + 1]                                           */
+  const float *init_state;    /* [num_seqs, H, d_k, d_v] or NULL                          */
+  const void *out_gate;       /* [total_tokens, H, d_v] or NULL                           */
+  const float *norm_weight;   /* [d_v] or NULL                                            */
+  void *out;                  /* [total_tokens, H, d_v], out_dtype                        */
+  float *final_state;         /* [num_seqs, H, d_k, d_v] or NULL                          */
+  float decay_bound;          /* lower_bound (clamped) or g_min (gated)                   */
+  float scale;
+  float norm_eps;
+  int32_t force_recurrent;
+} kda_prefill_params;
+
+typedef struct kda_decode_params {
+  uint32_t struct_size;
+  kda_dtype in_dtype, out_dtype;
+  kda_decay_form decay_form;
+  int32_t B, H, d_k, d_v;
+  const void *q, *k, *v;
+  const void *decay;          /* log_alpha (fp32) or z (in_dtype), [B, H, d_k] */
+  const float *A_log;         /* [H], gated form only                          */
+  const float *beta;          /* [B, H]                                        */
+  float *state;               /* [B, H, d_k, d_v], updated in place            */
+  const void *out_gate;       /* [B, H, d_v] or NULL                           */
+  const float *norm_weight;   /* [d_v] or NULL                                 */
+  void *out;                  /* [B, H, d_v], out_dtype                        */
+  float decay_bound;
+  float scale;
+  float norm_eps;
+  int32_t reserved;           /* set to 0                                      */
+} kda_decode_params;
+
+kda_status kda_prefill_ex(const kda_prefill_params *params, void *stream);
+kda_status kda_decode_ex(const kda_decode_params *params, void *stream);
+
+/*
  * kda_check_device_error -- synchronises `stream`, then reads and clears the
  * library's device error word. Returns KDA_OK, KDA_ERR_TIMEOUT if a kernel's
  * bounded wait gave up since the last check, or KDA_ERR_CUDA if the

@@ -27,6 +27,32 @@ _lock = threading.Lock()
 _lib = None
 
 
+KDA_DECAY_CLAMPED, KDA_DECAY_GATED = 0, 1
+
+
+class PrefillParams(ctypes.Structure):
+    """``kda_prefill_params`` of include/kda.h, field for field."""
+    _fields_ = [("struct_size", ctypes.c_uint32), ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("decay_form", ctypes.c_int32), ("num_seqs", ctypes.c_int32), ("H", ctypes.c_int32),
+                ("d_k", ctypes.c_int32), ("d_v", ctypes.c_int32), ("total_tokens", ctypes.c_int64),
+                ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("decay", ctypes.c_void_p),
+                ("A_log", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
+                ("init_state", ctypes.c_void_p), ("out_gate", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("final_state", ctypes.c_void_p), ("decay_bound", ctypes.c_float),
+                ("scale", ctypes.c_float), ("norm_eps", ctypes.c_float), ("force_recurrent", ctypes.c_int32)]
+
+
+class DecodeParams(ctypes.Structure):
+    """``kda_decode_params`` of include/kda.h, field for field."""
+    _fields_ = [("struct_size", ctypes.c_uint32), ("in_dtype", ctypes.c_int32), ("out_dtype", ctypes.c_int32),
+                ("decay_form", ctypes.c_int32), ("B", ctypes.c_int32), ("H", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("decay", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("beta", ctypes.c_void_p),
+                ("state", ctypes.c_void_p), ("out_gate", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p),
+                ("out", ctypes.c_void_p), ("decay_bound", ctypes.c_float), ("scale", ctypes.c_float),
+                ("norm_eps", ctypes.c_float), ("reserved", ctypes.c_int32)]
+
+
 class KdaError(RuntimeError):
     def __init__(self, status: int, what: str):
         self.status = status
@@ -49,6 +75,10 @@ def _declare(lib):
     lib.kda_prefill_gated_recurrent.restype = i32
     lib.kda_decode_gated.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, vp]
     lib.kda_decode_gated.restype = i32
+    lib.kda_prefill_ex.argtypes = [ctypes.POINTER(PrefillParams), vp]
+    lib.kda_prefill_ex.restype = i32
+    lib.kda_decode_ex.argtypes = [ctypes.POINTER(DecodeParams), vp]
+    lib.kda_decode_ex.restype = i32
     lib.kda_check_device_error.argtypes = [vp]
     lib.kda_check_device_error.restype = i32
     lib.kda_status_string.argtypes = [i32]
@@ -166,6 +196,91 @@ def prefill_gated(q, k, v, z, A_log, beta, cu_seqlens, init_state=None, *, out=N
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_gated_recurrent" if recurrent else "kda_prefill_gated")
     return out, final_state
+
+
+def _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min):
+    """(decay_form, decay tensor, A_log, bound) for exactly one of log_alpha or (z, A_log)."""
+    if (log_alpha is None) == (z is None):
+        raise ValueError("pass exactly one of log_alpha (clamped form) or z with A_log (gated form)")
+    if log_alpha is not None:
+        if A_log is not None:
+            raise ValueError("A_log belongs to the gated form (z)")
+        if log_alpha.dtype != torch.float32:
+            raise TypeError("log_alpha must be float32")
+        return KDA_DECAY_CLAMPED, log_alpha, None, float(lower_bound)
+    if A_log is None or A_log.dtype != torch.float32:
+        raise TypeError("the gated form needs A_log [H] float32")
+    if z.dtype != q.dtype:
+        raise TypeError("z must have the dtype of q")
+    return KDA_DECAY_GATED, z, A_log, float(g_min)
+
+
+def prefill_ex(q, k, v, beta, cu_seqlens, *, log_alpha=None, lower_bound: float = -5.0, z=None, A_log=None,
+               g_min: float = -5.0, init_state=None, out_gate=None, norm_weight=None, norm_eps: float = 1e-6,
+               out=None, final_state=None, out_dtype=torch.float32, scale: float = 1.0, stream=None,
+               recurrent: bool = False, want_final: bool = True):
+    """Prefill through the parameter block (``kda_prefill_ex``): the clamped (``log_alpha``) or
+    gated (``z``, ``A_log``) log-decay, and optionally the output gate with head-wise RMSNorm,
+    ``out = Sigmoid(out_gate) * norm_weight * o / sqrt(mean(o^2) + norm_eps)`` per token and head.
+    out_gate [T, H, d_v] in the dtype of q; norm_weight [d_v] float32 or None (ones).
+    Returns (out, final_state or None)."""
+    T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    N = cu_seqlens.shape[0] - 1
+    form, decay, A, bound = _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min)
+    if k.dtype != q.dtype or v.dtype != q.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if out_gate is not None and out_gate.dtype != q.dtype:
+        raise TypeError("out_gate must have the dtype of q")
+    if norm_weight is not None and norm_weight.dtype != torch.float32:
+        raise TypeError("norm_weight must be float32")
+    if beta.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
+        raise TypeError("beta must be float32 and cu_seqlens int32")
+    if out is None:
+        out = torch.empty((T, H, d_v), dtype=out_dtype, device=q.device)
+    if final_state is None and want_final:
+        final_state = torch.empty((N, H, d_k, d_v), dtype=torch.float32, device=q.device)
+    _check_cuda(q, k, v, decay, A, beta, cu_seqlens, init_state, out_gate, norm_weight, out, final_state)
+    p = PrefillParams(struct_size=ctypes.sizeof(PrefillParams), in_dtype=_io_dtype(q.dtype),
+                      out_dtype=_io_dtype(out.dtype), decay_form=form, num_seqs=N, H=H, d_k=d_k, d_v=d_v,
+                      total_tokens=T, q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(), decay=decay.data_ptr(),
+                      A_log=None if A is None else A.data_ptr(), beta=beta.data_ptr(),
+                      cu_seqlens=cu_seqlens.data_ptr(),
+                      init_state=None if init_state is None else init_state.data_ptr(),
+                      out_gate=None if out_gate is None else out_gate.data_ptr(),
+                      norm_weight=None if norm_weight is None else norm_weight.data_ptr(), out=out.data_ptr(),
+                      final_state=None if final_state is None else final_state.data_ptr(), decay_bound=bound,
+                      scale=float(scale), norm_eps=float(norm_eps), force_recurrent=int(bool(recurrent)))
+    st = lib().kda_prefill_ex(ctypes.byref(p), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_ex")
+    return out, final_state
+
+
+def decode_ex(q, k, v, beta, state, *, log_alpha=None, lower_bound: float = -5.0, z=None, A_log=None,
+              g_min: float = -5.0, out_gate=None, norm_weight=None, norm_eps: float = 1e-6, out=None,
+              out_dtype=torch.float32, scale: float = 1.0, stream=None):
+    """One decode step through the parameter block (``kda_decode_ex``); ``state`` is updated in
+    place. Decay and output-gate options as in ``prefill_ex``. Returns out [B, H, d_v]."""
+    B, H, d_k = q.shape
+    d_v = v.shape[-1]
+    form, decay, A, bound = _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min)
+    if out_gate is not None and out_gate.dtype != q.dtype:
+        raise TypeError("out_gate must have the dtype of q")
+    if out is None:
+        out = torch.empty((B, H, d_v), dtype=out_dtype, device=q.device)
+    _check_cuda(q, k, v, decay, A, beta, state, out_gate, norm_weight, out)
+    p = DecodeParams(struct_size=ctypes.sizeof(DecodeParams), in_dtype=_io_dtype(q.dtype),
+                     out_dtype=_io_dtype(out.dtype), decay_form=form, B=B, H=H, d_k=d_k, d_v=d_v, q=q.data_ptr(),
+                     k=k.data_ptr(), v=v.data_ptr(), decay=decay.data_ptr(),
+                     A_log=None if A is None else A.data_ptr(), beta=beta.data_ptr(), state=state.data_ptr(),
+                     out_gate=None if out_gate is None else out_gate.data_ptr(),
+                     norm_weight=None if norm_weight is None else norm_weight.data_ptr(), out=out.data_ptr(),
+                     decay_bound=bound, scale=float(scale), norm_eps=float(norm_eps), reserved=0)
+    st = lib().kda_decode_ex(ctypes.byref(p), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_ex")
+    return out
 
 
 def decode_gated(q, k, v, z, A_log, beta, state, *, out=None, out_dtype=torch.float32, g_min: float = -5.0,

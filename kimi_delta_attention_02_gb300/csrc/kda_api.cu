@@ -34,19 +34,23 @@ uint32_t *device_error_word() {
 }
 
 // Each launcher takes the decay input as `decay` + `A_log`: log_alpha (fp32) with A_log null
-// (the clamped form), or the gated form's logits z (input dtype) with A_log [H].
+// (the clamped form), or the gated form's logits z (input dtype) with A_log [H]; and the output
+// gate as `out_gate` (gate logits, input dtype; null = plain read-out) + `norm_weight` + `norm_eps`.
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
-                          const float *beta, float *state, void *out, int B, int H, int d_k, int d_v, bool in_bf16,
-                          bool out_bf16, float lb, float scale, cudaStream_t stream);
+                          const float *beta, float *state, const void *out_gate, const float *norm_weight,
+                          float norm_eps, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
+                          float lb, float scale, cudaStream_t stream);
 cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                              const float *beta, const int32_t *cu_seqlens, int num_seqs, int H, int d_k, int d_v,
                              bool in_bf16, bool out_bf16, float lb, float scale, const float *init_state,
-                             void *out, float *final_state, cudaStream_t stream);
+                             const void *out_gate, const float *norm_weight, float norm_eps, void *out,
+                             float *final_state, cudaStream_t stream);
 bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb);
 kda_status launch_chunked(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                           const float *beta, const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H,
-                          bool out_bf16, float lb, float scale, const float *init_state, void *out,
-                          float *final_state, cudaStream_t stream);
+                          bool out_bf16, float lb, float scale, const float *init_state, const void *out_gate,
+                          const float *norm_weight, float norm_eps, void *out, float *final_state,
+                          cudaStream_t stream);
 
 namespace {
 
@@ -57,7 +61,8 @@ bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0
 kda_status check_prefill_args(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                               const float *beta, const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                               int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype,
-                              const float *init_state, const void *out, const float *final_state) {
+                              const float *init_state, const void *out, const float *final_state,
+                              const void *out_gate = nullptr, const float *norm_weight = nullptr) {
   if (in_dtype != KDA_F32 && in_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (out_dtype != KDA_F32 && out_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
@@ -82,10 +87,13 @@ kda_status check_prefill_args(const void *q, const void *k, const void *v, const
   };
   const size_t nk = size_t(total_tokens) * H * d_k, nv = size_t(total_tokens) * H * d_v;
   const size_t ns = size_t(num_seqs) * H * d_k * d_v * 4;
-  const void *ins[6] = {q, k, v, decay, beta, A_log};
-  const size_t in_bytes[6] = {nk * es, nk * es, nv * es, nk * (A_log ? es : 4), size_t(total_tokens) * H * 4,
-                              A_log ? size_t(H) * 4 : 0};
-  for (int i = 0; i < 6; ++i) {
+  if (total_tokens > 0 && out_gate != nullptr && !aligned16(out_gate)) return KDA_ERR_INVALID_ARG;
+  if (norm_weight != nullptr && !aligned4(norm_weight)) return KDA_ERR_INVALID_ARG;
+  const void *ins[8] = {q, k, v, decay, beta, A_log, out_gate, norm_weight};
+  const size_t in_bytes[8] = {nk * es, nk * es, nv * es, nk * (A_log ? es : 4), size_t(total_tokens) * H * 4,
+                              A_log ? size_t(H) * 4 : 0, out_gate ? nv * es : 0,
+                              norm_weight ? size_t(d_v) * 4 : 0};
+  for (int i = 0; i < 8; ++i) {
     if (overlaps(out, nv * eo, ins[i], in_bytes[i])) return KDA_ERR_INVALID_ARG;
     if (overlaps(final_state, ns, ins[i], in_bytes[i])) return KDA_ERR_INVALID_ARG;
   }
@@ -102,28 +110,40 @@ kda_status check_gate_args(const float *A_log, float g_min) {
   return KDA_OK;
 }
 
+// the output gate's parameters: the weight only with gate logits, eps finite and >= 0
+kda_status check_out_gate_args(const void *out_gate, const float *norm_weight, float norm_eps) {
+  if (out_gate == nullptr) return norm_weight == nullptr ? KDA_OK : KDA_ERR_INVALID_ARG;
+  if (!(norm_eps >= 0.f) || !(norm_eps < INFINITY)) return KDA_ERR_INVALID_ARG;  // rejects NaN and inf
+  return KDA_OK;
+}
+
 kda_status prefill_impl(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                         const float *beta, const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
                         int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype, float lb,
                         float scale, const float *init_state, void *out, float *final_state, void *stream,
-                        bool force_recurrent) {
-  const kda_status st = check_prefill_args(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, d_k,
-                                           d_v, in_dtype, out_dtype, init_state, out, final_state);
+                        bool force_recurrent, const void *out_gate = nullptr, const float *norm_weight = nullptr,
+                        float norm_eps = 0.f) {
+  kda_status st = check_out_gate_args(out_gate, norm_weight, norm_eps);
+  if (st != KDA_OK) return st;
+  st = check_prefill_args(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype,
+                          out_dtype, init_state, out, final_state, out_gate, norm_weight);
   if (st != KDA_OK) return st;
   if (num_seqs == 0) return KDA_OK;
+  if (total_tokens == 0) out_gate = norm_weight = nullptr;  // nothing is read out
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (!force_recurrent && total_tokens > 0 && chunked_supported(d_k, d_v, in_dtype == KDA_BF16, lb))
     return launch_chunked(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, out_dtype == KDA_BF16,
-                          lb, scale, init_state, out, final_state, s);
+                          lb, scale, init_state, out_gate, norm_weight, norm_eps, out, final_state, s);
   const cudaError_t err = launch_recurrent(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, H, d_k, d_v,
-                                           in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale, init_state, out,
-                                           final_state, s);
+                                           in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale, init_state,
+                                           out_gate, norm_weight, norm_eps, out, final_state, s);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status decode_impl(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                        const float *beta, float *state, void *out, int32_t B, int32_t H, int32_t d_k, int32_t d_v,
-                       kda_dtype in_dtype, kda_dtype out_dtype, float lb, float scale, void *stream) {
+                       kda_dtype in_dtype, kda_dtype out_dtype, float lb, float scale, void *stream,
+                       const void *out_gate = nullptr, const float *norm_weight = nullptr, float norm_eps = 0.f) {
   if (in_dtype != KDA_F32 && in_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (out_dtype != KDA_F32 && out_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
@@ -133,10 +153,25 @@ kda_status decode_impl(const void *q, const void *k, const void *v, const void *
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(decay) || !aligned16(state) ||
       !aligned16(out) || !aligned4(beta))
     return KDA_ERR_INVALID_ARG;
-  const cudaError_t err = launch_decode(q, k, v, decay, A_log, beta, state, out, B, H, d_k, d_v,
-                                        in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale,
+  const kda_status st = check_out_gate_args(out_gate, norm_weight, norm_eps);
+  if (st != KDA_OK) return st;
+  if ((out_gate && !aligned16(out_gate)) || (norm_weight && !aligned4(norm_weight))) return KDA_ERR_INVALID_ARG;
+  if (out_gate) {  // the written read-out must not overlap the gate logits or the state
+    const size_t nv = size_t(B) * H * d_v, eo = out_dtype == KDA_BF16 ? 2 : 4, es = in_dtype == KDA_BF16 ? 2 : 4;
+    const char *po = static_cast<const char *>(out), *pg = static_cast<const char *>(out_gate);
+    if (po < pg + nv * es && pg < po + nv * eo) return KDA_ERR_INVALID_ARG;
+  }
+  const cudaError_t err = launch_decode(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps, out,
+                                        B, H, d_k, d_v, in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale,
                                         static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+// the decay form of a parameter block: the clamped form takes no A_log, the gated one needs it
+kda_status check_decay_form(kda_decay_form form, const float *A_log, float bound) {
+  if (form == KDA_DECAY_CLAMPED) return A_log == nullptr ? KDA_OK : KDA_ERR_INVALID_ARG;
+  if (form == KDA_DECAY_GATED) return check_gate_args(A_log, bound);
+  return KDA_ERR_INVALID_ARG;
 }
 
 }  // namespace
@@ -199,6 +234,25 @@ kda_status kda_decode_gated(const void *q, const void *k, const void *v, const v
   const kda_status st = check_gate_args(A_log, g_min);
   if (st != KDA_OK) return st;
   return decode_impl(q, k, v, z, A_log, beta, state, out, B, H, d_k, d_v, in_dtype, out_dtype, g_min, scale, stream);
+}
+
+kda_status kda_prefill_ex(const kda_prefill_params *p, void *stream) {
+  if (p == nullptr || p->struct_size != sizeof(kda_prefill_params)) return KDA_ERR_INVALID_ARG;
+  const kda_status st = check_decay_form(p->decay_form, p->A_log, p->decay_bound);
+  if (st != KDA_OK) return st;
+  return prefill_impl(p->q, p->k, p->v, p->decay, p->A_log, p->beta, p->cu_seqlens, p->num_seqs, p->total_tokens,
+                      p->H, p->d_k, p->d_v, p->in_dtype, p->out_dtype, p->decay_bound, p->scale, p->init_state,
+                      p->out, p->final_state, stream, p->force_recurrent != 0, p->out_gate, p->norm_weight,
+                      p->norm_eps);
+}
+
+kda_status kda_decode_ex(const kda_decode_params *p, void *stream) {
+  if (p == nullptr || p->struct_size != sizeof(kda_decode_params)) return KDA_ERR_INVALID_ARG;
+  const kda_status st = check_decay_form(p->decay_form, p->A_log, p->decay_bound);
+  if (st != KDA_OK) return st;
+  return decode_impl(p->q, p->k, p->v, p->decay, p->A_log, p->beta, p->state, p->out, p->B, p->H, p->d_k, p->d_v,
+                     p->in_dtype, p->out_dtype, p->decay_bound, p->scale, stream, p->out_gate, p->norm_weight,
+                     p->norm_eps);
 }
 
 kda_status kda_check_device_error(void *stream) {

@@ -1,0 +1,896 @@
+// kda_chunked_kernel.cuh -- tensor-core chunkwise KDA prefill (bf16 q/k/v, d_k = d_v = 128).
+//
+// Kimi K3 -- Architecture Notes, section 1.2: the kernel is recurrent across
+// chunks and parallel within each chunk; relative decay is kept in range with
+// 16-token tiles, and with log-decay >= -5 every rescaling factor inside a tile
+// stays below e^80, so all intra-chunk products are dense tensor-core matmuls.
+//
+// Math for one chunk of L <= 32 tokens entered with state S (d_k x d_v), from
+// the section 1.1 recurrence. G_t = cumulative clamped log-decay inside the
+// chunk, Gamma_t = exp(G_t):
+//   A[t,i] = b_t sum_c k_tc k_ic e^{G_tc - G_ic}   (i < t)      T = (I + A)^{-1}
+//   P[t,i] =     sum_c q_tc k_ic e^{G_tc - G_ic}   (i <= t)     T' = T Diag(b)
+//   W = T' (K * Gamma),  U~ = T' V,  U = U~ - W S
+//   O = (Q * Gamma) S + P U,   S <- Diag(Gamma_last) S + (K * e^{G_last - G})^T U
+// e^{G_t - G_i} is split at one reference per chunk, r = G at the end of its first
+// 16-token subtile: e^{G_t - G_i} = f_t g_i with f = e^{G - r}, g = 1 / f. Both
+// lie in [e^-80, e^80] (at most 16 clamped steps on either side of r), inside the
+// fp32 / tf32 range. The Gram products [Q * f ; K * f] (K * g)^T are exact on
+// and below the diagonal, where the two factors meet as e^{G_t - G_i} <= 1; the
+// entries above it may overflow and are never read. Every other operand is the
+// same rescaled by a per-channel constant: Q * Gamma = (Q * f) e^r,
+// K * Gamma = (K * f) e^r, K * e^{G_last - G} = (K * g) e^{G_last - r}.
+//
+// Precision. Outputs and states are heavy-tailed (their largest entries are
+// about ten times their rms), so a per-element relative error e shows up as
+// about 10e in max|error| / rms. bf16 operands (e = 2^-9) therefore cannot meet
+// a 2e-2 bound. The Gram operands carry factors up to e^80 and go through the
+// tensor cores as tf32 (fp32 range, rounded to nearest, e = 2^-11); every other
+// operand is bounded (|factor| <= 1, T' and U of order one) and goes as fp16
+// (e = 2^-11), which needs no more shared memory than bf16. Accumulation is
+// fp32 throughout and the state is kept in fp32 (tensor memory).
+//
+// Layout of the work. One CTA per (sequence, head) chain: 16 compute warps and one
+// issuing warp (one thread of it issues every TMA load and tensor-core MMA, so the
+// ~90 cycles each MMA issue takes never holds up the compute warps). The fp32
+// state S^T (rows v = value channels, columns c = key channels) stays in tensor
+// memory for the whole sequence, in two copies used alternately. Each iteration
+// j runs the state chain of chunk j interleaved with the state-independent work
+// of chunks j+1 and j+2, so that each tensor-core group runs while the threads
+// work on the other streams:
+//   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy
+//   P6  chain j : -W^T of chunk j into the [-W^T | Q~^T] tile (its MMA ran during
+//                 P1); MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]           (N = 64)
+//   P2  next j+2: decay prefix sums and the operand tiles (a thread owns one key
+//                 channel and 8 tokens)
+//   P3  chain j : U^T to fp16; MMA2: [O^T | S^T] += U^T [P ; K^^T]^T   (N = 160),
+//                 then the Gram of chunk j+2 (kind::tf32, M = 64 rows [Q f ; K f] x
+//                 N = 32 keys K g), queued behind MMA2, which the chain needs first
+//   P4  next j+1: warps 2, 3, 6, 7 (whose TMEM lanes hold the key rows of the Gram) take
+//                 A out of TMEM, invert I + A (8 x 8 and 16 x 16 blocks) and form T',
+//                 while the other 12 warps convert v to fp16, take P out of TMEM and
+//                 write O^T of chunk j (P5) to global memory, optionally through the
+//                 output gate of section 1.3 (RMSNorm over the 128 value channels and
+//                 the Sigmoid of the gate logits, whose tile TMA brings into the S^T
+//                 tile once MMA1 has read it);
+//                 W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
+// Per-chunk operand tiles are double-buffered by chunk parity ([P ; K^^T] three
+// times, since it lives from P2 of chunk j to MMA2 of chunk j + 2), and so are the
+// Gram accumulators. TMA brings q, k and log-decay one chunk ahead of P2 and v two
+// chunks ahead of P4 (128-byte swizzle).
+#pragma once
+
+#include <cuda.h>
+
+#include <type_traits>
+
+#include "kda_common.cuh"
+
+namespace kda {
+namespace chunked {
+
+constexpr int kC = 32;      // chunk length (two 16-token subtiles)
+constexpr int kD = 128;     // d_k = d_v
+constexpr int kWorkers = 512;               // 16 compute warps
+constexpr int kThreads = kWorkers + 32;     // + one warp that issues TMA loads and MMAs
+constexpr int kALd = 36;    // fp32 row stride of the A / T scratch
+constexpr float kLog2e = 1.4426950408889634f;
+
+// shared-memory map (bytes from a 1024-aligned base)
+constexpr uint32_t OFF_QKG = 0;              // q [32][128] bf16 | k | log-decay [32][128] fp32 (or bf16 logits)
+constexpr uint32_t SQ = 0, SK = 8 * 1024, SG = 16 * 1024;
+constexpr uint32_t OFF_V = 32 * 1024;        // two v stages [32][128] bf16, converted to fp16 in place
+constexpr uint32_t OFF_QK = 48 * 1024;       // Gram A side, tf32 [64 rows][128 c]: Q f (rows t), K f (rows 32 + t)
+constexpr uint32_t OFF_B = 80 * 1024;        // Gram B side, tf32 [32 rows i][128 c]: K g
+constexpr uint32_t OFF_ST = 96 * 1024;       // S^T fp16 [128][128]; the inverse's fp32 A, T, X alias it,
+constexpr uint32_t G_A = 0, G_T = 5 * 1024, G_X = 10 * 1024;  // and so does the output gate's logit tile
+constexpr uint32_t G_R = 16 * 1024;          // (bf16 [32 tokens][128], loaded once MMA1 has read S^T)
+constexpr uint32_t G_O = 16 * 1024;          // and the output rows of a full chunk on their way to the TMA store
+constexpr uint32_t OFF_UT = 128 * 1024;      // U^T fp16 [128][32], 64-byte swizzle
+constexpr uint32_t OFF_TP = 136 * 1024;      // T' fp16 [64][32], 64-byte swizzle; rows 32..63 stay zero
+constexpr uint32_t OFF_KG = 140 * 1024;      // 2 x Kg^T = (K * Gamma)^T fp16 [128 c][32 i], 64-byte swizzle
+constexpr uint32_t kKGBytes = 8 * 1024;
+constexpr uint32_t OFF_WQ = 156 * 1024;      // 2 x [-W^T | Q~^T] fp16 [128 c][64] (MN-major B of MMA1)
+constexpr uint32_t kWQBytes = 16 * 1024;
+constexpr uint32_t OFF_PK = 188 * 1024;      // 3 x [P ; K^^T] fp16 [160 rows][32], 64-byte swizzle
+constexpr uint32_t kPKBytes = 10 * 1024;
+constexpr uint32_t OFF_MISC = 218 * 1024;    // beta x2, Gamma_last x2, group decay totals, barriers
+constexpr uint32_t OFF_SS = OFF_MISC + 3456; // output gate: per-token partial sums of squares [32][4] fp32
+constexpr uint32_t kSmemBytes = 222 * 1024 + 1024;
+static_assert(OFF_SS + 32 * 16 + 1023 <= kSmemBytes, "shared memory map exceeds the allocation");
+
+// TMEM columns: two groups [U^T | O^T | S^T] (32 + 32 + 128) used by chunk parity, then
+// Gram (chunk parity 0), W^T, Gram (parity 1). Chunk j's MMA1 and MMA2 write group j % 2;
+// its MMA2 leaves the state for chunk j + 1 there, which P1 of chunk j + 1 reads and
+// rewrites, decayed, into the other.
+constexpr uint32_t TM_GROUP = 192, TM_O = 32, TM_SS = 64, TM_GRAM = 384, TM_W = 416, TM_COLS = 512;
+__device__ __forceinline__ uint32_t tm_grp(int b) { return TM_GROUP * uint32_t(b); }
+__device__ __forceinline__ uint32_t tm_gram(int c) { return TM_GRAM + 64u * uint32_t(c & 1); }
+
+constexpr uint32_t IDESC_GRAM = umma_idesc(UMMA_TF32, 64, 32, false, false, false);
+constexpr uint32_t IDESC_WT = umma_idesc(UMMA_F16, 128, 32, false, false, false);  // W^T = Kg^T T'^T
+constexpr uint32_t IDESC_UT = umma_idesc(UMMA_F16, 128, 64, true, false, false);   // [U~^T | 0] = V^T [T'; 0]^T
+constexpr uint32_t IDESC_UO = umma_idesc(UMMA_F16, 128, 64, false, true, false);   // += S^T [-W^T | Q~^T]
+constexpr uint32_t IDESC_OS = umma_idesc(UMMA_F16, 128, 160, false, false, false); // [O^T | S^T] += U^T [P ; K^^T]^T
+
+__device__ __forceinline__ uint64_t kdesc128(uint32_t addr) { return umma_desc(addr, 16, 1024, kSwizzle128B); }
+__device__ __forceinline__ uint64_t kdesc64(uint32_t addr) { return umma_desc(addr, 16, 512, kSwizzle64B); }
+__device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t lbo) {
+  return umma_desc(addr, lbo, 1024, kSwizzle128B);
+}
+// Advance a descriptor's start address by `bytes` (shared-memory addresses here stay below
+// 2^18, so the 14-bit address field never carries into the next field).
+__device__ __forceinline__ uint64_t dadv(uint64_t desc, uint32_t bytes) { return desc + uint64_t(bytes >> 4); }
+
+template <typename T>
+__device__ __forceinline__ void st_at(uint8_t *base, uint32_t off, T v) {
+  *reinterpret_cast<T *>(base + off) = v;
+}
+__device__ __forceinline__ uint4 pack8_f16(const float *x) {
+  return make_uint4(pack_f16x2(x[0], x[1]), pack_f16x2(x[2], x[3]), pack_f16x2(x[4], x[5]), pack_f16x2(x[6], x[7]));
+}
+// 2^x on the SFU (ex2.approx, subnormal results flushed to zero)
+__device__ __forceinline__ float exp2_sfu(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+struct Bars {
+  uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate;
+};
+static_assert(OFF_MISC + (2 * 32 + 2 * 128 + 4 * 128) * 4 + sizeof(Bars) + 8 <= OFF_SS, "misc overlaps");
+
+// The output gate of section 1.3: bf16 gate logits r [T, H, 128], the RMSNorm weight w [128]
+// (nullptr = ones) and eps.
+struct OutGate {
+  const uint16_t *r;
+  const float *w;
+  float eps;
+};
+
+// kGated: the log-decay is the gated form g = g_min Sigmoid(e^{A_h} z) of section 1.2 (tm_g
+// then maps the bf16 logits z; lb holds g_min); otherwise tm_g maps the fp32 log_alpha,
+// clamped below at lb. kNormGate: each output row is written as Sigmoid(r) * w * o / rms(o)
+// (section 1.3) instead of o; tm_r maps the gate logits, for L2 prefetches.
+template <bool kOutBF16, bool kGated, bool kNormGate>
+__global__ void __launch_bounds__(kThreads, 1)
+    kda_chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                       const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_o,
+                       const OutGate og,
+                       const float *__restrict__ A_log, const float *__restrict__ beta,
+                       const int32_t *__restrict__ cu_seqlens,
+                       const float *__restrict__ init_state, void *__restrict__ out,
+                       float *__restrict__ final_state, int H, float lb, float scale, uint32_t *err_word) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  float *s_beta = reinterpret_cast<float *>(sm + OFF_MISC);  // [2][32] beta by chunk parity
+  float *s_gamma = s_beta + 2 * 32;                           // [2][128] Gamma_last by chunk parity
+  float *s_tot = s_gamma + 2 * 128;                           // [4][128] log2 decay of each 8-token group
+  Bars *bars = reinterpret_cast<Bars *>(s_tot + 4 * 128);
+  uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + 1);
+  float4 *s_ss = reinterpret_cast<float4 *>(sm + OFF_SS);    // [32 tokens] x 4 lane quarters: sums of o^2
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3, grp = warp >> 2;  // TMEM lane quarter, column group (compute warps)
+  const bool worker = tid < kWorkers;              // warps 0..15; warp 16 issues TMA loads and MMAs
+  const int h = int(blockIdx.x % H);
+  const int64_t n = blockIdx.x / H;
+  const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
+  const int n_chunks = int((eos - bos + kC - 1) / kC);
+  const uint32_t sbase = smem_u32(sm);
+  const float a_h = kGated ? __expf(A_log[h]) : 0.f;  // e^{A_h} of the gated form
+
+  if (tid == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_g);
+    if (kNormGate) tma_prefetch_desc(&tm_r);
+    tma_prefetch_desc(&tm_o);
+    mbar_init(&bars->qkg, 1);
+    mbar_init(&bars->v[0], 1);
+    mbar_init(&bars->v[1], 1);
+    mbar_init(&bars->mma1, 1);
+    mbar_init(&bars->gram[0], 1);
+    mbar_init(&bars->gram[1], 1);
+    mbar_init(&bars->mma2, 1);
+    mbar_init(&bars->wu, 1);
+    mbar_init(&bars->gate, 1);
+    fence_mbarrier_init();
+    s_tmem[1] = 0u;  // abort flag
+  }
+  if (warp == 0) {
+    tmem_alloc(s_tmem, TM_COLS);
+    tmem_relinquish();
+  }
+  // rows 32..63 of the T' tile stay zero: the U~ product reads them to clear the O^T columns
+  for (int e = tid; e < 32 * 4; e += kThreads)
+    st_at(sm, OFF_TP + sw64_chunk(32 + (e >> 2), e & 3), make_uint4(0, 0, 0, 0));
+
+  const int v_own = 32 * quarter + lane;  // state row (TMEM lane) of this thread; key channel in P2
+  const int64_t st_base = (n * H + h) * int64_t(kD) * kD;
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  const uint32_t lane_base = uint32_t(32 * quarter) << 16;
+  // this thread's 32 state columns in group b
+  auto s_cols = [&](int b) { return tmem + lane_base + tm_grp(b) + TM_SS + 32 * grp; };
+  if (worker) {  // the state entering chunk 0 sits where chunk -1 would have left it: group 1
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      float x[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        x[j] = init_state != nullptr ? init_state[st_base + int64_t(32 * grp + 16 * u + j) * kD + v_own] : 0.f;
+      tmem_st16(s_cols(1) + 16 * u, x);
+    }
+    tmem_st_wait();
+  }
+
+  auto chunk_t0 = [&](int c) { return bos + int64_t(c) * kC; };
+  auto chunk_len = [&](int c) {
+    const int64_t r = eos - chunk_t0(c);
+    return int(r < kC ? r : kC);
+  };
+  auto issue_qkg = [&](int c) {  // issuer
+    const int32_t t0 = int32_t(chunk_t0(c));
+    mbar_arrive_expect_tx(&bars->qkg, 2 * 8192 + (kGated ? 8192 : 16384));
+    tma_load_3d(sm + OFF_QKG + SQ, &tm_q, &bars->qkg, 0, h, t0);
+    tma_load_3d(sm + OFF_QKG + SQ + 4096, &tm_q, &bars->qkg, 64, h, t0);
+    tma_load_3d(sm + OFF_QKG + SK, &tm_k, &bars->qkg, 0, h, t0);
+    tma_load_3d(sm + OFF_QKG + SK + 4096, &tm_k, &bars->qkg, 64, h, t0);
+    tma_load_3d(sm + OFF_QKG + SG, &tm_g, &bars->qkg, 0, h, t0);
+  };
+  auto issue_v = [&](int c) {  // issuer
+    const int32_t t0 = int32_t(chunk_t0(c));
+    uint8_t *dst = sm + OFF_V + (c & 1) * 8192;
+    mbar_arrive_expect_tx(&bars->v[c & 1], 8192);
+    tma_load_3d(dst, &tm_v, &bars->v[c & 1], 0, h, t0);
+    tma_load_3d(dst + 4096, &tm_v, &bars->v[c & 1], 64, h, t0);
+    if (kNormGate) tma_prefetch_l2_3d(&tm_r, 0, h, t0);  // chunk c's gate logits, read when it is written
+  };
+
+  bool bad = false;  // a bounded wait of this thread gave up
+  volatile uint32_t *s_abort = s_tmem + 1;
+  // chunks whose q/k/g and v loads were issued last (the issuer's abort path waits for them)
+  int qkg_last = -1, v_last[2] = {-1, -1}, gate_last = -1;
+  bool store_pending = false;  // thread 0: an output tile store whose shared-memory read may be running
+  float b_next = (tid < kC && tid < eos - bos) ? beta[(bos + tid) * H + h] : 0.f;  // beta of chunk 0
+
+  // Synchronisation. The 16 compute warps meet on barrier BAR_WORK where they share
+  // data. They hand each finished group of operands to the issuing warp through one
+  // barrier per event (compute warps arrive, the issuer syncs), so MMA issue never
+  // holds them up. An event of chunk j + 1 always comes after a wait on an MMA or a
+  // load the issuer starts only past the same event of chunk j, so the compute warps
+  // never arrive twice at a barrier the issuer has not yet passed. If a compute
+  // thread's wait gave up, the compute warps raise s_abort before the hand-off the
+  // issuer waits for next, and both sides leave for the teardown.
+  constexpr uint32_t BAR_WORK = 1, H_COPY = 2, H_PREP = 3, H_U = 4, H_INV = 5, BAR_INV = 6;
+  auto handoff = [&](uint32_t id) {  // compute warps: operands of this event written
+    fence_proxy_async_smem();
+    tc_fence_before();
+    named_bar_arrive(id, kThreads);
+  };
+  auto give_up = [&](uint32_t id) {
+    if (tid == 0) *s_abort = 1u;
+    handoff(id);
+  };
+
+  // ------------------------------------------------------------------ P2: operand tiles
+  // Thread (channel ch = v_own, tokens 8 grp .. 8 grp + 7): the decay prefix sums run
+  // along its own 8 tokens; the 4 group totals of a channel meet in shared memory.
+  // Everything is kept in log2 units (x log2 e), so each factor is one ex2.
+  // Runs two chunks ahead of the state chain. Returns false when the compute warps give up.
+  auto prep = [&](int c) -> bool {
+    const int b = c & 1, L = chunk_len(c);
+    const int64_t t0 = chunk_t0(c);
+    const float b_pref = b_next;
+    if (tid < kC) b_next = (tid < eos - t0 - kC) ? beta[(t0 + kC + tid) * H + h] : 0.f;  // next chunk's
+    bad |= !mbar_wait_sleep(&bars->qkg, uint32_t(c & 1), err_word, DEVERR_TMA_TIMEOUT);
+    if (c >= 1)  // the Gram of chunk c - 1 has read the Gram tiles
+      bad |= !mbar_wait_sleep(&bars->gram[(c - 1) & 1], uint32_t(((c - 1) >> 1) & 1), err_word,
+                              DEVERR_MMA_TIMEOUT);
+    const int ch = v_own, tb = 8 * grp;
+    // Every chunk but the last of a sequence is full: it takes code without the masks.
+    const bool full = L == kC;
+    float lg[8];  // log2 of Gamma within the group: sum of the group's decays up to each token
+    auto decay_sums = [&](auto full_tag) {
+      constexpr bool kFull = decltype(full_tag)::value;
+      const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG) + tb * kD + ch;
+      const uint16_t *zin = reinterpret_cast<const uint16_t *>(sm + OFF_QKG + SG) + tb * kD + ch;
+      float run = 0.f;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {  // alpha = 1 past the end of the sequence
+        const float g = !(kFull || tb + r < L) ? 0.f
+                        : kGated              ? gated_log_decay(bf16_to_f32(zin[r * kD]), a_h, lb)
+                                              : clamp_log_decay(gin[r * kD], lb);
+        run = fmaf(g, kLog2e, run);
+        lg[r] = run;
+      }
+      s_tot[grp * kD + ch] = run;
+    };
+    if (full) decay_sums(std::true_type{});
+    else decay_sums(std::false_type{});
+    if (tid < kC) s_beta[b * kC + tid] = b_pref;
+    if (kNormGate && store_pending) {  // the U^T tile is written after this barrier
+      bulk_wait_read();
+      store_pending = false;
+    }
+    if (named_bar_or(BAR_WORK, kWorkers, bad)) {
+      give_up(H_PREP);
+      return false;
+    }
+    const uint32_t row = uint32_t(ch) * 128u, sw = uint32_t(ch) & 7u;
+    uint32_t hq[4], hk[4], hg[4];  // fp16 pairs
+    auto operands = [&](auto full_tag) {
+      constexpr bool kFull = decltype(full_tag)::value;
+      const float T0 = s_tot[ch], T1 = s_tot[kD + ch], T2 = s_tot[2 * kD + ch], T3 = s_tot[3 * kD + ch];
+      const float r2 = T0 + T1;                                                // log2 e^r
+      const float last2 = r2 + (T2 + T3);                                      // log2 Gamma_last
+      const float start = grp == 0 ? -r2 : grp == 1 ? -T1 : grp == 2 ? 0.f : T2;  // log2 e^{G_start - r}
+      const float tau0 = exp2_sfu(r2), tau1 = exp2_sfu(last2 - r2);
+      if (grp == 0) s_gamma[b * kD + ch] = exp2_sfu(last2);
+      // q and k of the 8 tokens: bf16 element (t, ch) of the 128-byte-swizzled TMA tiles
+      const uint32_t cc = uint32_t(ch & 63);
+      const uint8_t *qk0 = sm + OFF_QKG + (ch >> 6) * 4096 + tb * 128 + (cc & 7u) * 2;
+      const uint32_t xj = (cc >> 3) << 4;
+      // Gram operands, K-major tf32 (blocks of 32 channels, one 128-byte row per token): the 32
+      // lanes of a warp hold one whole row, so each 4-byte store is conflict-free. fp16 operands,
+      // one 16-byte chunk each: Q~^T (columns 32 + t of [-W^T | Q~^T]), K^^T (row 32 + ch of
+      // [P ; K^^T]) and Kg^T (row ch). Two halves of 4 tokens keep few values live.
+      const uint32_t cb = uint32_t(ch >> 5), cq = uint32_t(ch & 31) >> 2;
+      float *gq = reinterpret_cast<float *>(sm + OFF_QK + cb * 64 * 128 + tb * 128 + (ch & 3) * 4);
+      float *gk = reinterpret_cast<float *>(sm + OFF_QK + cb * 64 * 128 + (32 + tb) * 128 + (ch & 3) * 4);
+      float *gb = reinterpret_cast<float *>(sm + OFF_B + cb * 32 * 128 + tb * 128 + (ch & 3) * 4);
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        float qf[4], kf[4], kg[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int r = 4 * half + e;
+          const uint32_t off = r * 128 + (xj ^ uint32_t(r << 4));
+          const bool ok = kFull || tb + r < L;
+          const float q = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SQ + off)) : 0.f;
+          const float k = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SK + off)) : 0.f;
+          const float d = start + lg[r];  // log2 e^{G_t - r}
+          const float f = exp2_sfu(d), g = exp2_sfu(-d);
+          qf[e] = q * f;
+          kf[e] = k * f;
+          kg[e] = k * g;
+          const uint32_t o4 = (r * 128 + ((cq ^ uint32_t(r)) << 4)) >> 2;  // row tb + r, whose t & 7 = r
+          gq[o4] = round_tf32_alu(qf[e]);
+          gk[o4] = round_tf32_alu(kf[e]);
+          gb[o4] = round_tf32_alu(kg[e]);
+        }
+        hq[2 * half] = pack_f16x2(qf[0] * tau0, qf[1] * tau0);
+        hq[2 * half + 1] = pack_f16x2(qf[2] * tau0, qf[3] * tau0);
+        hk[2 * half] = pack_f16x2(kf[0] * tau0, kf[1] * tau0);
+        hk[2 * half + 1] = pack_f16x2(kf[2] * tau0, kf[3] * tau0);
+        hg[2 * half] = pack_f16x2(kg[0] * tau1, kg[1] * tau1);
+        hg[2 * half + 1] = pack_f16x2(kg[2] * tau1, kg[3] * tau1);
+      }
+    };
+    if (full) operands(std::true_type{});
+    else operands(std::false_type{});
+    handoff(H_PREP);  // the Gram operands are complete; the fp16 tiles are needed later
+    st_at(sm, OFF_PK + (c % 3) * kPKBytes + sw64_chunk(32u + ch, grp), make_uint4(hg[0], hg[1], hg[2], hg[3]));
+    st_at(sm, OFF_KG + b * kKGBytes + sw64_chunk(ch, grp), make_uint4(hk[0], hk[1], hk[2], hk[3]));
+    if (c >= 2)  // MMA1 of chunk c - 2 has read its [-W^T | Q~^T] buffer, which chunk c reuses
+      bad |= !mbar_wait_sleep(&bars->mma1, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
+    st_at(sm, OFF_WQ + b * kWQBytes + row + (((4u + grp) ^ sw) << 4), make_uint4(hq[0], hq[1], hq[2], hq[3]));
+    return true;
+  };
+
+  auto issue_gram = [&](int c) {  // issuer: 16 steps of 8 channels (32 bytes; 4 per 32-channel block)
+    const uint64_t qk = kdesc128(sbase + OFF_QK), bb = kdesc128(sbase + OFF_B);
+#pragma unroll
+    for (int ks = 0; ks < 16; ++ks) {
+      const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
+      umma_tf32(tmem + tm_gram(c), dadv(qk, kb * 64 * 128 + ko), dadv(bb, kb * 32 * 128 + ko), IDESC_GRAM,
+                ks > 0);
+    }
+    umma_commit(&bars->gram[c & 1]);
+  };
+
+  // Warps 2, 3, 6, 7 (TMEM lane quarters 2 and 3, column groups 0 and 1) form the inverse
+  // group: the key rows of the Gram (A) live in their lanes. The other 12 warps write
+  // outputs, convert v and take the query rows (P).
+  const bool inv_group = quarter >= 2 && grp < 2;
+  const int iw = (quarter - 2) + 2 * grp;  // inverse group: warp 0..3 of the group
+  const int itid = 32 * iw + lane;         // inverse group: thread 0..127 of the group
+
+  // ------------------------------------------------------------------ P5: outputs
+  // O^T of chunk j out of TMEM to global memory, on the 12 warps outside the inverse group:
+  // lane quarters 0 and 1 have 4 of them (8 tokens each), quarters 2 and 3 have 2 (16 each).
+  //
+  // With the output gate, a token's 128 channels are spread over four warps (one per lane
+  // quarter): each warp sums o^2 of its 32 channels for each of its tokens, the 12 warps meet
+  // on BAR_OUT, lane l of each warp then adds token l's four partial sums in a fixed order and
+  // passes 1 / rms to the other lanes. The gate logits of chunk j come by TMA into the S^T
+  // tile once MMA1 of chunk j has read it (issue_gate); O^T is read from TMEM twice (before and
+  // after the barrier) to keep few values live, and every value is formed before the (masked)
+  // stores, so that the stores do not order the arithmetic.
+  // Output rows of chunk j held by this thread (channel v_own, tokens t0 .. t0 + N - 1). With
+  // the output gate, a full chunk's rows go through shared memory and out with one TMA store by
+  // thread 0: the 16 scattered row stores per thread otherwise lengthen the output warps' path
+  // past the inverse's. A bf16 tile is staged in the U^T tile (free from MMA2 of chunk j until
+  // P3 of the next step): thread 0 waits for the store to have read it only before the operand
+  // barrier of the next step (or at once when the next step has none). An fp32 tile is staged
+  // in the upper half of the S^T tile, which the next step rewrites at its start, so thread 0
+  // waits before it joins the barrier that ends this step. Without the gate the output path is
+  // short enough for row stores, and a partial chunk (the last of a sequence) is always stored
+  // row by row, so that nothing past the sequence is written. Both paths round bf16 alike.
+  constexpr uint32_t BAR_OUT = 7;
+  auto write_rows = [&](const auto &x, int t0, int j, int L) {
+    constexpr int N = int(sizeof(x) / sizeof(x[0]));
+    if (kNormGate && L == kC) {
+      uint8_t *stage = kOutBF16 ? sm + OFF_UT : sm + OFF_ST + G_O;
+#pragma unroll
+      for (int e = 0; e < N; ++e) {
+        if constexpr (kOutBF16) reinterpret_cast<uint16_t *>(stage)[(t0 + e) * kD + v_own] = f32_to_bf16(x[e]);
+        else reinterpret_cast<float *>(stage)[(t0 + e) * kD + v_own] = x[e];
+      }
+      fence_proxy_async_smem();
+      named_bar_sync(BAR_OUT, 384);
+      if (tid == 0) {
+        tma_store_3d(&tm_o, stage, 0, h, int32_t(chunk_t0(j)));
+        bulk_commit();
+        if (kOutBF16 && j + 3 < n_chunks) store_pending = true;  // read before prep(j + 3)'s barrier
+        else bulk_wait_read();
+      }
+    } else {
+      const int64_t step = int64_t(H) * kD;
+      const int64_t base = ((chunk_t0(j) + t0) * H + h) * int64_t(kD) + v_own;
+#pragma unroll
+      for (int e = 0; e < N; ++e)
+        if (t0 + e < L) store_elem<kOutBF16>(out, base + e * step, x[e]);
+    }
+  };
+  auto issue_gate = [&](int c) {  // issuer
+    if constexpr (kNormGate) {
+      mbar_wait_sleep(&bars->mma1, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);  // S^T read
+      mbar_arrive_expect_tx(&bars->gate, 8192);
+      tma_load_3d(sm + OFF_ST + G_R, &tm_r, &bars->gate, 0, h, int32_t(chunk_t0(c)));
+    }
+  };
+  auto out_gated_rows = [&](auto n_tag, int t0, int j, int L, uint32_t ocols) {
+    constexpr int N = decltype(n_tag)::value;  // tokens of this warp: 8 or 16
+    const float w = og.w != nullptr ? og.w[v_own] : 1.f;
+    // Sigmoid(r) w first: the gate tile is there well before MMA2 has finished
+    bad |= !mbar_wait_sleep(&bars->gate, uint32_t(j & 1), err_word, DEVERR_TMA_TIMEOUT);
+    const uint16_t *rt = reinterpret_cast<const uint16_t *>(sm + OFF_ST + G_R) + t0 * kD + v_own;
+    float gw[N];
+#pragma unroll
+    for (int e = 0; e < N; ++e) gw[e] = w * sigmoid_approx(bf16_to_f32(rt[e * kD]));
+    bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
+    tc_fence_after();
+    float x[N];
+    if constexpr (N == 8) tmem_ld8(ocols + t0, x);
+    else tmem_ld16(ocols + t0, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < N; ++e) x[e] = (scale * x[e]) * (scale * x[e]);
+    const float part = lane_sums<N>(x, lane);
+    constexpr int kShift = N == 8 ? 2 : 1;  // lane l holds the sum of token (l >> kShift) & (N - 1)
+    if ((lane & ((1 << kShift) - 1)) == 0)
+      reinterpret_cast<float *>(s_ss)[4 * (t0 + ((lane >> kShift) & (N - 1))) + quarter] = part;
+    named_bar_sync(BAR_OUT, 384);
+    const float4 p = s_ss[t0 + (lane & (N - 1))];
+    const float rstd_l = rsqrtf(((p.x + p.y) + (p.z + p.w)) * (1.f / kD) + og.eps);  // token t0 + (lane & (N-1))
+    if constexpr (N == 8) tmem_ld8(ocols + t0, x);
+    else tmem_ld16(ocols + t0, x);
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < N; ++e) x[e] = scale * x[e] * __shfl_sync(0xffffffffu, rstd_l, e) * gw[e];
+    write_rows(x, t0, j, L);
+  };
+  auto out_chunk = [&](int j) {
+    if (!kNormGate) {
+      bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
+      tc_fence_after();
+    }
+    const int L = chunk_len(j);
+    const uint32_t ocols = tmem + lane_base + tm_grp(j & 1) + TM_O;
+    if constexpr (kNormGate) {
+      if (quarter < 2) out_gated_rows(std::integral_constant<int, 8>{}, 8 * grp, j, L, ocols);
+      else out_gated_rows(std::integral_constant<int, 16>{}, 16 * (grp - 2), j, L, ocols);
+    } else if (quarter < 2) {
+      float x[8];
+      tmem_ld8(ocols + 8 * grp, x);  // O^T row v, tokens 8 grp ..
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 8; ++e) x[e] *= scale;
+      write_rows(x, 8 * grp, j, L);
+    } else {
+      const int t0 = 16 * (grp - 2);
+      float x[16];
+      tmem_ld16(ocols + t0, x);  // O^T row v, tokens t0 ..
+      tmem_ld_wait();
+#pragma unroll
+      for (int e = 0; e < 16; ++e) x[e] *= scale;
+      write_rows(x, t0, j, L);
+    }
+  };
+
+  // ------------------------------------------------------------------ P4: P, A, inverse, T', v
+  // Inverse-side work of chunk c; the 12 warps outside the inverse group also write the
+  // outputs of chunk j_out (if >= 0). Returns false when the compute warps give up.
+  auto extract_inverse = [&](int c, int j_out) -> bool {
+    const int b = c & 1, L = chunk_len(c);
+    float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
+    if (inv_group) {
+      bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+      tc_fence_after();
+      {  // A rows t = 16 (quarter - 2) + lane (lanes 0..15; M = 64 layout), columns 16 grp .. + 15
+        const int s = quarter - 2, t = 16 * s + (lane & 15);
+        if (grp <= s) {  // columns past the row block are all zero and never read
+          float vals[16];
+          tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * grp, vals);
+          tmem_ld_wait();
+          if (lane < 16) {
+            const float bt = s_beta[b * kC + t];
+            const int lim = t < L ? t - 16 * grp : 0;  // keep i < t
+#pragma unroll
+            for (int e = 0; e < 16; ++e) vals[e] = e < lim ? bt * vals[e] : 0.f;
+            float4 *arow = reinterpret_cast<float4 *>(As + t * kALd + 16 * grp);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+              arow[q4] = make_float4(vals[4 * q4], vals[4 * q4 + 1], vals[4 * q4 + 2], vals[4 * q4 + 3]);
+          }
+        }
+      }
+      named_bar_sync(BAR_INV, 128);
+      // T = (I + A)^{-1}, then T' = T Diag(beta)
+      float *Ts = reinterpret_cast<float *>(sm + OFF_ST + G_T);
+      float *Xs = reinterpret_cast<float *>(sm + OFF_ST + G_X);
+      if (iw < 2) {
+        // diagonal block iw (16 x 16) in 8 x 8 pieces, warp-synchronous
+        const int base = 16 * iw;
+        if (lane < 16) {  // the two 8 x 8 diagonal pieces: lane = column of its piece
+          const int o = base + 8 * (lane >> 3), cc = lane & 7;
+          float x[8];
+#pragma unroll
+          for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+          for (int m = 0; m < 8; ++m) {
+            Ts[(o + m) * kALd + o + cc] = x[m];
+#pragma unroll
+            for (int r = m + 1; r < 8; ++r) x[r] = fmaf(-As[(o + r) * kALd + o + m], x[m], x[r]);
+          }
+        } else {  // the zero 8 x 8 piece above the diagonal
+          const int l = lane - 16;
+          *reinterpret_cast<float4 *>(Ts + (base + (l >> 1)) * kALd + base + 8 + 4 * (l & 1)) =
+              make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        __syncwarp();
+        // piece below the diagonal: -T_11 (A_10 T_00); lane (row r8, columns 2 c8, 2 c8 + 1)
+        float *Xw = Xs + 64 * iw;
+        const int r8 = lane >> 2, c8 = lane & 3;
+        float a8[8];
+        auto load8 = [&](const float *src) {
+          const float4 p0 = reinterpret_cast<const float4 *>(src)[0], p1 = reinterpret_cast<const float4 *>(src)[1];
+          a8[0] = p0.x;
+          a8[1] = p0.y;
+          a8[2] = p0.z;
+          a8[3] = p0.w;
+          a8[4] = p1.x;
+          a8[5] = p1.y;
+          a8[6] = p1.z;
+          a8[7] = p1.w;
+        };
+        load8(As + (base + 8 + r8) * kALd + base);
+        float2 acc8 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float2 t2 = *reinterpret_cast<const float2 *>(Ts + (base + k) * kALd + base + 2 * c8);
+          acc8.x = fmaf(a8[k], t2.x, acc8.x);
+          acc8.y = fmaf(a8[k], t2.y, acc8.y);
+        }
+        *reinterpret_cast<float2 *>(Xw + r8 * 8 + 2 * c8) = acc8;
+        __syncwarp();
+        load8(Ts + (base + 8 + r8) * kALd + base + 8);
+        acc8 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const float2 x2 = *reinterpret_cast<const float2 *>(Xw + k * 8 + 2 * c8);
+          acc8.x = fmaf(-a8[k], x2.x, acc8.x);
+          acc8.y = fmaf(-a8[k], x2.y, acc8.y);
+        }
+        *reinterpret_cast<float2 *>(Ts + (base + 8 + r8) * kALd + base + 2 * c8) = acc8;
+      } else {  // the zero 16 x 16 block above the diagonal
+        const int l = itid - 64;
+        *reinterpret_cast<float4 *>(Ts + (l >> 2) * kALd + 16 + 4 * (l & 3)) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+      named_bar_sync(BAR_INV, 128);
+      // block below the diagonal, T_10 = -T_11 (A_10 T_00): thread (row r, columns 2 c2, 2 c2 + 1)
+      const int r = itid >> 3, c2 = itid & 7;
+      float rowv[16];
+      auto load_row = [&](const float *src) {
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4) {
+          const float4 v4 = reinterpret_cast<const float4 *>(src)[q4];
+          rowv[4 * q4] = v4.x;
+          rowv[4 * q4 + 1] = v4.y;
+          rowv[4 * q4 + 2] = v4.z;
+          rowv[4 * q4 + 3] = v4.w;
+        }
+      };
+      load_row(As + (16 + r) * kALd);  // A_10 row r
+      float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float2 t2 = *reinterpret_cast<const float2 *>(Ts + k * kALd + 2 * c2);  // T_00 row k
+        acc.x = fmaf(rowv[k], t2.x, acc.x);
+        acc.y = fmaf(rowv[k], t2.y, acc.y);
+      }
+      *reinterpret_cast<float2 *>(Xs + r * 16 + 2 * c2) = acc;
+      named_bar_sync(BAR_INV, 128);
+      load_row(Ts + (16 + r) * kALd + 16);  // T_11 row r (zero above its diagonal)
+      acc = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        const float2 x2 = *reinterpret_cast<const float2 *>(Xs + k * 16 + 2 * c2);
+        acc.x = fmaf(-rowv[k], x2.x, acc.x);
+        acc.y = fmaf(-rowv[k], x2.y, acc.y);
+      }
+      *reinterpret_cast<float2 *>(Ts + (16 + r) * kALd + 2 * c2) = acc;
+      named_bar_sync(BAR_INV, 128);
+      {  // T' = T Diag(beta) -> fp16 [t][i]
+        const int t = itid >> 2, cj = itid & 3;
+        const float4 *trow = reinterpret_cast<const float4 *>(Ts + t * kALd + 8 * cj);
+        const float4 *brow = reinterpret_cast<const float4 *>(s_beta + b * kC + 8 * cj);
+        const float4 t0v = trow[0], t1v = trow[1], b0v = brow[0], b1v = brow[1];
+        const float x[8] = {t0v.x * b0v.x, t0v.y * b0v.y, t0v.z * b0v.z, t0v.w * b0v.w,
+                            t1v.x * b1v.x, t1v.y * b1v.y, t1v.z * b1v.z, t1v.w * b1v.w};
+        st_at(sm, OFF_TP + sw64_chunk(t, cj), pack8_f16(x));
+      }
+    } else {
+      // the 12 other warps: v tile of this chunk bf16 -> fp16 in place (rows past the end
+      // zeroed), the query rows P of the Gram, then the outputs of chunk j_out
+      const int ot = (quarter < 2 ? 64 * grp + 32 * quarter : 256 + 64 * (grp - 2) + 32 * (quarter - 2)) + lane;
+      bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
+      for (int e = ot; e < kC * 16; e += 384) {
+        const int t = e >> 4, cj = e & 15;
+        uint4 *p = reinterpret_cast<uint4 *>(sm + OFF_V + b * 8192 + sw128_chunk(t, cj & 7, cj >> 3, kC));
+        uint4 w = make_uint4(0, 0, 0, 0);
+        if (t < L) {
+          const uint4 bv = *p;
+          const float2 a0 = unpack_bf16x2(bv.x), a1 = unpack_bf16x2(bv.y), a2 = unpack_bf16x2(bv.z),
+                       a3 = unpack_bf16x2(bv.w);
+          const float x[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
+          w = pack8_f16(x);
+        }
+        *p = w;
+      }
+      if (quarter < 2) {  // P rows t = 16 quarter + lane (lanes 0..15), columns 8 grp .. + 7
+        bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+        tc_fence_after();
+        const int t = 16 * quarter + (lane & 15);
+        const bool have = grp < 2 * (quarter + 1);  // columns up to the row block's end
+        float vals[8];
+        if (have) {
+          tmem_ld8(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
+          tmem_ld_wait();
+        }
+        if (lane < 16) {
+          const int lim = (have && t < L) ? t + 1 - 8 * grp : 0;  // keep i <= t
+#pragma unroll
+          for (int e = 0; e < 8; ++e) vals[e] = e < lim ? vals[e] : 0.f;
+          st_at(sm + OFF_PK + (c % 3) * kPKBytes, sw64_chunk(t, grp), pack8_f16(vals));
+        }
+      }
+      if (j_out >= 0) out_chunk(j_out);
+    }
+    // the inverse's scratch aliases the S^T tile that the next chain step rewrites: all
+    // compute threads are past it before any goes on
+    fence_proxy_async_smem();
+    tc_fence_before();
+    const bool ab = named_bar_or(BAR_WORK, kWorkers, bad);
+    if (ab) give_up(H_INV);
+    else handoff(H_INV);
+    return !ab;
+  };
+
+  auto issue_wu = [&](int c) {  // issuer: W^T and [U~^T | 0]
+    const int b = c & 1;
+    const uint64_t tp = kdesc64(sbase + OFF_TP), kg = kdesc64(sbase + OFF_KG + b * kKGBytes),
+                   vin = mndesc(sbase + OFF_V + b * 8192, kC * 128);
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+      umma_f16(tmem + TM_W, dadv(kg, ks * 32), dadv(tp, ks * 32), IDESC_WT, ks > 0);
+      umma_f16(tmem + tm_grp(b), dadv(vin, ks * 2048), dadv(tp, ks * 32), IDESC_UT, ks > 0);
+    }
+    umma_commit(&bars->wu);
+  };
+
+  // ------------------------------------------------------------------ P6: -W^T
+  auto wt_extract = [&](int c) {
+    const int b = c & 1;
+    bad |= !mbar_wait_sleep(&bars->wu, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
+    tc_fence_after();
+    float x[8];
+    tmem_ld8(tmem + lane_base + TM_W + 8 * grp, x);  // W^T row c = v_own, columns t = 8 grp ..
+    tmem_ld_wait();
+#pragma unroll
+    for (int e = 0; e < 8; ++e) x[e] = -x[e];
+    const uint32_t cr = uint32_t(v_own);
+    st_at(sm + OFF_WQ + b * kWQBytes, cr * 128 + (((uint32_t(grp) ^ cr) & 7u) << 4), pack8_f16(x));
+  };
+
+  if (worker) {
+    // ---------------------------------------------------------------- compute warps
+    if (n_chunks > 0) {  // operands of chunks 0 and 1
+      if (!prep(0)) goto teardown;
+      if (n_chunks > 1 && !prep(1)) goto teardown;
+      if (!extract_inverse(0, -1)) goto teardown;
+    }
+    for (int j = 0; j < n_chunks; ++j) {
+      const int b = j & 1;
+      const bool more = j + 1 < n_chunks;
+      // ---------------- P1: chain j, fp16 copy of S^T; decayed S^T into group j % 2
+      if (j > 0 && inv_group) {  // the state MMA2 of chunk j - 1 left (the other warps waited for it)
+        bad |= !mbar_wait_sleep(&bars->mma2, uint32_t((j - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+        tc_fence_after();
+      }
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float x[16];
+        tmem_ld16(s_cols(b ^ 1) + 16 * u, x);
+        tmem_ld_wait();
+        const uint32_t col = uint32_t(32 * grp + 16 * u);  // state column c of x[0]
+        st_at(sm + OFF_ST, sw128_chunk(v_own, (col & 63u) >> 3, col >> 6, 128), pack8_f16(x));
+        st_at(sm + OFF_ST, sw128_chunk(v_own, ((col & 63u) >> 3) + 1, col >> 6, 128), pack8_f16(x + 8));
+        const float4 *gam = reinterpret_cast<const float4 *>(s_gamma + b * kD + col);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float4 gv = gam[e];
+          x[4 * e] *= gv.x;
+          x[4 * e + 1] *= gv.y;
+          x[4 * e + 2] *= gv.z;
+          x[4 * e + 3] *= gv.w;
+        }
+        tmem_st16(s_cols(b) + 16 * u, x);
+      }
+      tmem_st_wait();
+      // ---------------- P6: -W^T of chunk j (its W^T / U~^T MMA ran during P1) -> MMA1
+      wt_extract(j);
+      handoff(H_COPY);
+      // ---------------- P2: operand tiles of chunk j + 2 -> Gram
+      if (j + 2 < n_chunks && !prep(j + 2)) goto teardown;
+      // ---------------- P3: chain j, U^T to fp16 -> MMA2
+      bad |= !mbar_wait_sleep(&bars->mma1, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
+      tc_fence_after();
+      {
+        float x[8];
+        tmem_ld8(tmem + lane_base + tm_grp(b) + 8 * grp, x);  // U^T row v, columns t = 8 grp ..
+        tmem_ld_wait();
+        st_at(sm + OFF_UT, sw64_chunk(uint32_t(v_own), uint32_t(grp)), pack8_f16(x));
+      }
+      handoff(H_U);
+      // ---------------- P4 / P5: inverse side of chunk j + 1 -> W^T and U~^T, and outputs of chunk j
+      if (more) {
+        if (!extract_inverse(j + 1, j)) goto teardown;
+      } else if (!inv_group) {
+        out_chunk(j);
+      }
+    }
+    if (n_chunks > 0) {  // the last chunk's MMA2 (the warps outside the inverse group waited already)
+      bad |= !mbar_wait_sleep(&bars->mma2, uint32_t((n_chunks - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+      tc_fence_after();
+    }
+    if (final_state != nullptr) {  // the last chunk's MMA2 left the state in its group
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        float x[16];
+        tmem_ld16(s_cols((n_chunks + 1) & 1) + 16 * u, x);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 16; ++e) final_state[st_base + int64_t(32 * grp + 16 * u + e) * kD + v_own] = x[e];
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- issuing warp
+    // The whole warp follows the hand-offs; lane 0 issues.
+    const bool leader = lane == 0;
+    auto sync_on = [&](uint32_t id) {
+      named_bar_sync(id, kThreads);
+      tc_fence_after();
+      return *s_abort == 0u;
+    };
+    if (n_chunks > 0) {
+      if (leader) {
+        issue_qkg(0);
+        issue_v(0);
+        if (n_chunks > 1) issue_v(1);
+      }
+      qkg_last = 0;
+      v_last[0] = 0;
+      if (n_chunks > 1) v_last[1] = 1;
+      for (int c = 0; c < 2 && c < n_chunks; ++c) {
+        if (!sync_on(H_PREP)) goto issuer_abort;
+        if (leader) {
+          if (c + 1 < n_chunks) issue_qkg(c + 1);
+          issue_gram(c);
+        }
+        if (c + 1 < n_chunks) qkg_last = c + 1;
+      }
+      if (!sync_on(H_INV)) goto issuer_abort;
+      if (leader) issue_wu(0);
+      if (n_chunks > 2) {  // v stage 0 is free once W^T / U~^T of chunk 0 are done
+        mbar_wait_sleep(&bars->wu, 0u, err_word, DEVERR_MMA_TIMEOUT);
+        if (leader) issue_v(2);
+        v_last[0] = 2;
+      }
+    }
+    for (int j = 0; j < n_chunks; ++j) {
+      const int b = j & 1;
+      const bool more = j + 1 < n_chunks;
+      if (!sync_on(H_COPY)) goto issuer_abort;
+      if (leader) {  // MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]
+        const uint64_t st = kdesc128(sbase + OFF_ST), wq = mndesc(sbase + OFF_WQ + b * kWQBytes, 128 * 128);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {
+          const uint32_t kb = ks >> 2, ko = (ks & 3) * 32;
+          umma_f16(tmem + tm_grp(b), dadv(st, kb * 16384 + ko), dadv(wq, ks * 2048), IDESC_UO, 1);
+        }
+        umma_commit(&bars->mma1);
+      }
+      if (j + 2 < n_chunks) {
+        if (!sync_on(H_PREP)) goto issuer_abort;
+        if (leader) {
+          if (j + 3 < n_chunks) issue_qkg(j + 3);
+          issue_gate(j);
+        }
+        if (j + 3 < n_chunks) qkg_last = j + 3;
+        if (kNormGate) gate_last = j;
+      }
+      if (!sync_on(H_U)) goto issuer_abort;
+      if (leader) {  // MMA2: [O^T | S^T] += U^T [P ; K^^T]^T
+        const uint64_t ut = kdesc64(sbase + OFF_UT), pk = kdesc64(sbase + OFF_PK + (j % 3) * kPKBytes);
+#pragma unroll
+        for (int ks = 0; ks < 2; ++ks)
+          umma_f16(tmem + tm_grp(b) + TM_O, dadv(ut, ks * 32), dadv(pk, ks * 32), IDESC_OS, 1);
+        umma_commit(&bars->mma2);
+        // the Gram of chunk j + 2 (its operands came at H_PREP) queues behind MMA2, which the
+        // chain waits for first; the Gram is needed only one iteration later
+        if (j + 2 < n_chunks) issue_gram(j + 2);
+      }
+      if (kNormGate && j + 2 >= n_chunks) {  // no operand hand-off left to piggyback on
+        if (leader) issue_gate(j);
+        gate_last = j;
+      }
+      if (more) {
+        if (!sync_on(H_INV)) goto issuer_abort;
+        if (leader) issue_wu(j + 1);
+        if (j + 3 < n_chunks) {  // v stage (j + 1) % 2 is free once W^T / U~^T of chunk j + 1 are done
+          mbar_wait_sleep(&bars->wu, uint32_t((j + 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+          if (leader) issue_v(j + 3);
+          v_last[(j + 3) & 1] = j + 3;
+        }
+      }
+    }
+  }
+  goto teardown;
+
+issuer_abort:
+  // the compute warps gave up: let this CTA's own loads in flight land (bounded) before exit
+  if (qkg_last >= 0) mbar_wait_sleep(&bars->qkg, uint32_t(qkg_last & 1), err_word, DEVERR_TMA_TIMEOUT);
+  for (int s = 0; s < 2; ++s)
+    if (v_last[s] >= 0) mbar_wait_sleep(&bars->v[s], uint32_t((v_last[s] >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
+  if (gate_last >= 0) mbar_wait_sleep(&bars->gate, uint32_t(gate_last & 1), err_word, DEVERR_TMA_TIMEOUT);
+
+teardown:
+  if (tid == 0) bulk_wait_all();  // the output tiles this thread stored
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, TM_COLS);
+}
+
+using KernelFn = decltype(&kda_chunked_kernel<false, false, false>);
+
+}  // namespace chunked
+}  // namespace kda

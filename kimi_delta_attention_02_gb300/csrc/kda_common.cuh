@@ -103,6 +103,46 @@ __device__ __forceinline__ float gated_log_decay(float z, float a_h, float g_min
   return __fdividef(g_min, 1.f + e);
 }
 
+// Sigmoid(x) = 1 / (1 + 2^{-x log2 e}) on the SFU: ex2.approx and rcp.approx (each about one
+// ulp). 2^{-x log2 e} = inf gives 0; a NaN stays NaN.
+__device__ __forceinline__ float sigmoid_approx(float x) {
+  float e, r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
+  return r;
+}
+
+// The output gate of Kimi K3 -- Architecture Notes, section 1.3 ("Full-rank output gate"):
+// out = Sigmoid(r) * w * o * rstd, with rstd = 1 / sqrt(mean of o^2 over the head's d_v
+// channels + eps) formed by the caller.
+__device__ __forceinline__ float output_gate(float o, float rstd, float w, float r) {
+  return o * rstd * w * sigmoid_approx(r);
+}
+
+// Sums v[e] over the 32 lanes of a warp for all N entries at once (N a power of two, 2..32):
+// each halving round sends one half of the remaining entries to the partner lane and adds the
+// other half, so N - 1 shuffles leave one entry per lane, which the remaining rounds sum as a
+// plain butterfly. Afterwards lane l holds the total of entry (l >> (5 - log2 N)) & (N - 1).
+// v is overwritten.
+template <int N>
+__device__ __forceinline__ float lane_sums(float (&v)[N], int lane) {
+  int off = 16;
+#pragma unroll
+  for (int n = N; n > 1; n >>= 1, off >>= 1) {
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < n / 2; ++i) {
+      const float send = upper ? v[i] : v[i + n / 2];
+      const float keep = upper ? v[i + n / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  float s = v[0];
+#pragma unroll
+  for (; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+  return s;
+}
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses and fences
 // ---------------------------------------------------------------------------
@@ -201,6 +241,25 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, ui
       "%5}], [%2];" ::"r"(smem_u32(smem_dst)),
       "l"(tmap), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
+}
+// Store a shared-memory tile to global memory through a tensor map (bulk-group completion):
+// the issuing thread commits the group and waits on it with bulk_wait_read (the tile may be
+// overwritten) or bulk_wait_all (the writes are done).
+__device__ __forceinline__ void tma_store_3d(const void *tmap, const void *smem_src, int32_t x, int32_t y,
+                                             int32_t z) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(tmap),
+               "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Bring a tile of a tensor map into L2 (no shared memory, no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void *tmap, int32_t x, int32_t y, int32_t z) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(tmap), "r"(x), "r"(y),
+               "r"(z)
+               : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");

@@ -13,6 +13,9 @@
 // streams through HBM fully coalesced. The 16 state loads of a thread are issued
 // before anything waits on them. The log-decay is either the clamped log_alpha
 // input or, in the gated form (section 1.2), g = g_min * Sigmoid(e^{A_h} z).
+// Optionally the read-out goes through the output gate of section 1.3,
+// Sigmoid(r) * w * o / rms(o), before it is written: warp 0 holds the whole d_v
+// row, so the RMS is one warp reduction.
 #include "kda_common.cuh"
 
 namespace kda {
@@ -20,11 +23,12 @@ namespace kda {
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeRowsPerThread = 16;  // 128 key rows / 8 row groups
 
-template <bool kInBF16, bool kOutBF16, bool kGated>
+template <bool kInBF16, bool kOutBF16, bool kGated, bool kNormGate>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
     kda_decode_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                       const void *__restrict__ decay, const float *__restrict__ A_log,
-                      const float *__restrict__ beta, float *__restrict__ state, void *__restrict__ out, int H,
+                      const float *__restrict__ beta, float *__restrict__ state, const void *__restrict__ out_gate,
+                      const float *__restrict__ norm_weight, float norm_eps, void *__restrict__ out, int H,
                       int d_k, int d_v, float lb, float scale) {
   __shared__ float s_k[128], s_q[128], s_a[128], s_v[128];
   __shared__ float s_red_y[8][128], s_red_z[8][128];
@@ -106,25 +110,49 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       __stcs(reinterpret_cast<float4 *>(S + int64_t(c) * d_v + col), w);
     }
   }
-  if (ty == 0 && col_ok) {
+  if (ty == 0) {
+    float o[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) store_elem<kOutBF16>(out, bh * d_v + col + e, scale * (zt[e] + u[e] * kq));
+    for (int e = 0; e < 4; ++e) o[e] = col_ok ? scale * (zt[e] + u[e] * kq) : 0.f;
+    if constexpr (kNormGate) {
+      float ss = (o[0] * o[0] + o[1] * o[1]) + (o[2] * o[2] + o[3] * o[3]);
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+      const float rstd = rsqrtf(ss / float(d_v) + norm_eps);
+      if (col_ok) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float w = norm_weight != nullptr ? norm_weight[col + e] : 1.f;
+          const float r = load_elem<kInBF16>(out_gate, bh * d_v + col + e);
+          store_elem<kOutBF16>(out, bh * d_v + col + e, output_gate(o[e], rstd, w, r));
+        }
+      }
+    } else if (col_ok) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) store_elem<kOutBF16>(out, bh * d_v + col + e, o[e]);
+    }
   }
 }
 
-// decay: log_alpha (fp32) when A_log is null, else the gated form's logits z (input dtype)
+// decay: log_alpha (fp32) when A_log is null, else the gated form's logits z (input dtype).
+// out_gate: gate logits [B, H, d_v] (input dtype) of the output gate, or null (out = o).
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
-                          const float *beta, float *state, void *out, int B, int H, int d_k, int d_v, bool in_bf16,
-                          bool out_bf16, float lb, float scale, cudaStream_t stream) {
+                          const float *beta, float *state, const void *out_gate, const float *norm_weight,
+                          float norm_eps, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
+                          float lb, float scale, cudaStream_t stream) {
   const dim3 grid(unsigned(int64_t(B) * H)), block(kDecodeThreads);
-  using Kern = decltype(&kda_decode_kernel<false, false, false>);
-  static const Kern table[8] = {
-      kda_decode_kernel<false, false, false>, kda_decode_kernel<false, false, true>,
-      kda_decode_kernel<false, true, false>,  kda_decode_kernel<false, true, true>,
-      kda_decode_kernel<true, false, false>,  kda_decode_kernel<true, false, true>,
-      kda_decode_kernel<true, true, false>,   kda_decode_kernel<true, true, true>};
-  const Kern kern = table[4 * int(in_bf16) + 2 * int(out_bf16) + int(A_log != nullptr)];
-  kern<<<grid, block, 0, stream>>>(q, k, v, decay, A_log, beta, state, out, H, d_k, d_v, lb, scale);
+  using Kern = decltype(&kda_decode_kernel<false, false, false, false>);
+#define KDA_DEC_ROW(ng)                                                                                        \
+  kda_decode_kernel<false, false, false, ng>, kda_decode_kernel<false, false, true, ng>,                       \
+      kda_decode_kernel<false, true, false, ng>, kda_decode_kernel<false, true, true, ng>,                     \
+      kda_decode_kernel<true, false, false, ng>, kda_decode_kernel<true, false, true, ng>,                     \
+      kda_decode_kernel<true, true, false, ng>, kda_decode_kernel<true, true, true, ng>
+  static const Kern table[16] = {KDA_DEC_ROW(false), KDA_DEC_ROW(true)};
+#undef KDA_DEC_ROW
+  const Kern kern =
+      table[8 * int(out_gate != nullptr) + 4 * int(in_bf16) + 2 * int(out_bf16) + int(A_log != nullptr)];
+  kern<<<grid, block, 0, stream>>>(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps, out, H, d_k,
+                                   d_v, lb, scale);
   return cudaGetLastError();
 }
 

@@ -21,6 +21,9 @@ Recipe (the pages publish no dataset; every workload is synthetic):
   channel, cast to the workload dtype, and one log-scale A_h = 0.5 N(0, 1) per
   head in fp32. Through g = -5 Sigmoid(e^{A_h} z) this spreads the retention
   over nearly the whole bounded range (alpha from about e^-5 to 1).
+* output gate: gate logits r ~ N(0, 1) per value channel, cast to the workload
+  dtype (standing in for W_g x), and one RMSNorm weight w = 1 + 0.1 N(0, 1) per
+  value channel in fp32 (a weight near its initial value of ones).
 
 Every (tensor, head[, step]) pair draws from its own ``torch.Generator``
 stream, so any single head can be regenerated without the others and large
@@ -35,7 +38,7 @@ import numpy as np
 import torch
 
 # tensor ids used to derive stream seeds
-_Q, _K, _V, _LA, _BETA, _INIT, _Z, _A = 1, 2, 3, 4, 5, 6, 7, 8
+_Q, _K, _V, _LA, _BETA, _INIT, _Z, _A, _R, _W = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
 
 
 def _stream(seed: int, tensor_id: int, head: int, step: int, device) -> torch.Generator:
@@ -58,7 +61,8 @@ class PrefillCase:
     """One packed varlen prefill problem. Token-major layouts:
     q, k [T_tot, H, d_k]; v [T_tot, H, d_v] (dtype); log_alpha [T_tot, H, d_k] fp32;
     beta [T_tot, H] fp32; cu_seqlens [N+1] int32; init_state [N, H, d_k, d_v] fp32 or None;
-    gated form only: z [T_tot, H, d_k] (dtype) and A_log [H] fp32."""
+    gated form only: z [T_tot, H, d_k] (dtype) and A_log [H] fp32; output gate only:
+    out_gate [T_tot, H, d_v] (dtype) and norm_weight [d_v] fp32."""
     name: str
     q: torch.Tensor
     k: torch.Tensor
@@ -70,6 +74,8 @@ class PrefillCase:
     lengths: list = field(default_factory=list)
     z: torch.Tensor | None = None
     A_log: torch.Tensor | None = None
+    out_gate: torch.Tensor | None = None
+    norm_weight: torch.Tensor | None = None
 
     @property
     def total_tokens(self) -> int:
@@ -86,9 +92,11 @@ class PrefillCase:
 
 def make_prefill(lengths, H: int, d_k: int = 128, d_v: int = 128, *, dtype=torch.bfloat16,
                  device="cpu", seed: int = 0, init_std: float | None = 0.02,
-                 log_alpha_mode: str = "softplus", name: str = "prefill", gated: bool = False) -> PrefillCase:
+                 log_alpha_mode: str = "softplus", name: str = "prefill", gated: bool = False,
+                 out_gate: bool = False) -> PrefillCase:
     """Generate a packed prefill problem. ``init_std=None`` means no initial state;
-    ``gated`` adds the gated form's decay logits z and log-scales A_log."""
+    ``gated`` adds the gated form's decay logits z and log-scales A_log; ``out_gate``
+    adds the output gate's logits and RMSNorm weight."""
     lengths = [int(x) for x in lengths]
     T = int(sum(lengths))
     N = len(lengths)
@@ -122,6 +130,11 @@ def make_prefill(lengths, H: int, d_k: int = 128, d_v: int = 128, *, dtype=torch
         for h in range(H):
             case.z[:, h] = (-1.0 + 2.0 * _randn((T, d_k), seed, _Z, h, 0, device)).to(dtype)
             case.A_log[h] = 0.5 * _randn((1,), seed, _A, h, 0, device)[0]
+    if out_gate:
+        case.out_gate = torch.empty((T, H, d_v), dtype=dtype, device=device)
+        for h in range(H):
+            case.out_gate[:, h] = _randn((T, d_v), seed, _R, h, 0, device).to(dtype)
+        case.norm_weight = 1.0 + 0.1 * _randn((d_v,), seed, _W, 0, 0, device)
     return case
 
 
@@ -144,6 +157,9 @@ PREFILL_WORKLOADS = {
     "prefill_long_T1M_H32": dict(lengths=[1 << 20], H=32, dtype=torch.bfloat16, init_std=None),
     # the gated decay form on the K3-shaped layer
     "prefill_k3_gated_T4096_H96": dict(lengths=[4096], H=96, dtype=torch.bfloat16, init_std=0.02, gated=True),
+    # the K3-shaped layer with the gated decay and the output gate (bf16 output)
+    "prefill_k3_outgate_T4096_H96": dict(lengths=[4096], H=96, dtype=torch.bfloat16, init_std=0.02, gated=True,
+                                         out_gate=True),
 }
 
 
@@ -167,6 +183,8 @@ class DecodeStep:
     beta: torch.Tensor
     z: torch.Tensor | None = None
     A_log: torch.Tensor | None = None
+    out_gate: torch.Tensor | None = None
+    norm_weight: torch.Tensor | None = None
 
 
 def make_decode_state(B: int, H: int, d_k: int = 128, d_v: int = 128, *, device="cpu", seed: int = 0,
@@ -178,7 +196,8 @@ def make_decode_state(B: int, H: int, d_k: int = 128, d_v: int = 128, *, device=
 
 
 def make_decode_step(step: int, B: int, H: int, d_k: int = 128, d_v: int = 128, *,
-                     dtype=torch.bfloat16, device="cpu", seed: int = 0, gated: bool = False) -> DecodeStep:
+                     dtype=torch.bfloat16, device="cpu", seed: int = 0, gated: bool = False,
+                     out_gate: bool = False) -> DecodeStep:
     """Fresh inputs for decode step ``step`` (streams differ per step)."""
     s = step + 1
     q = _unit_rows(_randn((B, H, d_k), seed, _Q, 0, s, device)).to(dtype)
@@ -190,6 +209,9 @@ def make_decode_step(step: int, B: int, H: int, d_k: int = 128, d_v: int = 128, 
     if gated:
         st.z = (-1.0 + 2.0 * _randn((B, H, d_k), seed, _Z, 0, s, device)).to(dtype)
         st.A_log = 0.5 * _randn((H,), seed, _A, 0, 0, device)
+    if out_gate:
+        st.out_gate = _randn((B, H, d_v), seed, _R, 0, s, device).to(dtype)
+        st.norm_weight = 1.0 + 0.1 * _randn((d_v,), seed, _W, 0, 0, device)
     return st
 
 

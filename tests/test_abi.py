@@ -34,7 +34,7 @@ def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert {"kda_prefill", "kda_decode", "kda_prefill_recurrent", "kda_check_device_error",
             "kda_status_string", "kda_version", "kda_selftest_umma", "kda_prefill_gated",
-            "kda_prefill_gated_recurrent", "kda_decode_gated"} <= set(names)
+            "kda_prefill_gated_recurrent", "kda_decode_gated", "kda_prefill_ex", "kda_decode_ex"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -156,3 +156,72 @@ def test_decode_gated_rejects(lib, over, expect):
     st = lib.kda_decode_gated(a["q"], a["k"], a["v"], a["z"], a["A"], a["beta"], a["state"], a["out"], a["B"],
                               a["H"], a["dk"], a["dv"], a["dtype"], a["odtype"], a["gmin"], 1.0, NULL)
     assert st == expect
+
+
+def _prefill_ex(lib, **over):
+    """A parameter block with fake device addresses: validation must reject before any CUDA call."""
+    f = dict(struct_size=ctypes.sizeof(B.PrefillParams), in_dtype=1, out_dtype=0, decay_form=0, num_seqs=1, H=2,
+             d_k=128, d_v=128, total_tokens=4, q=0x10000, k=0x20000, v=0x30000, decay=0x40000, A_log=None,
+             beta=0x50000, cu_seqlens=0x60000, init_state=None, out_gate=0xb0000, norm_weight=0xc0000,
+             out=0x70000, final_state=0x80000, decay_bound=-5.0, scale=1.0, norm_eps=1e-6, force_recurrent=0)
+    f.update(over)
+    return lib.kda_prefill_ex(ctypes.byref(B.PrefillParams(**f)), NULL)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(struct_size=148), B.KDA_ERR_INVALID_ARG),                 # not this library's struct
+    (dict(decay_form=2), B.KDA_ERR_INVALID_ARG),
+    (dict(A_log=0xa0000), B.KDA_ERR_INVALID_ARG),                   # A_log with the clamped form
+    (dict(decay_form=1), B.KDA_ERR_INVALID_ARG),                    # gated form without A_log
+    (dict(decay_form=1, A_log=0xa0000, decay_bound=1.0), B.KDA_ERR_INVALID_ARG),
+    (dict(out_gate=None), B.KDA_ERR_INVALID_ARG),                   # a weight without gate logits
+    (dict(norm_eps=float("nan")), B.KDA_ERR_INVALID_ARG),
+    (dict(norm_eps=-1.0), B.KDA_ERR_INVALID_ARG),
+    (dict(norm_eps=float("inf")), B.KDA_ERR_INVALID_ARG),
+    (dict(out_gate=0xb0008), B.KDA_ERR_INVALID_ARG),                # misaligned gate logits
+    (dict(norm_weight=0xc0002), B.KDA_ERR_INVALID_ARG),
+    (dict(out=0xb0000), B.KDA_ERR_INVALID_ARG),                     # output over the gate logits
+    (dict(final_state=0xc0000), B.KDA_ERR_INVALID_ARG),             # final state over the weight
+    (dict(in_dtype=5), B.KDA_ERR_INVALID_ARG),
+    (dict(d_v=129), B.KDA_ERR_UNSUPPORTED),
+    (dict(q=None), B.KDA_ERR_INVALID_ARG),
+])
+def test_prefill_ex_rejects(lib, over, expect):
+    assert _prefill_ex(lib, **over) == expect
+
+
+def test_prefill_ex_accepts_empty_work(lib):
+    assert _prefill_ex(lib, num_seqs=0, total_tokens=0, q=None, k=None, v=None, decay=None, beta=None, out=None,
+                       final_state=None, out_gate=None, norm_weight=None) == B.KDA_OK
+    assert _prefill_ex(lib, num_seqs=0, total_tokens=0, decay_form=1, A_log=0xa0000) == B.KDA_OK
+
+
+def _decode_ex(lib, **over):
+    f = dict(struct_size=ctypes.sizeof(B.DecodeParams), in_dtype=1, out_dtype=0, decay_form=0, B=2, H=2, d_k=128,
+             d_v=128, q=0x10000, k=0x20000, v=0x30000, decay=0x40000, A_log=None, beta=0x50000, state=0x90000,
+             out_gate=0xb0000, norm_weight=None, out=0x70000, decay_bound=-5.0, scale=1.0, norm_eps=1e-6,
+             reserved=0)
+    f.update(over)
+    return lib.kda_decode_ex(ctypes.byref(B.DecodeParams(**f)), NULL)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(struct_size=0), B.KDA_ERR_INVALID_ARG),
+    (dict(decay_form=7), B.KDA_ERR_INVALID_ARG),
+    (dict(A_log=0xa0000), B.KDA_ERR_INVALID_ARG),
+    (dict(decay_form=1, A_log=0xa0000, decay_bound=float("nan")), B.KDA_ERR_INVALID_ARG),
+    (dict(out_gate=None, norm_weight=0xc0000), B.KDA_ERR_INVALID_ARG),
+    (dict(norm_eps=-0.5), B.KDA_ERR_INVALID_ARG),
+    (dict(out_gate=0xb0004), B.KDA_ERR_INVALID_ARG),
+    (dict(out=0xb0000), B.KDA_ERR_INVALID_ARG),                     # output over the gate logits
+    (dict(d_v=6), B.KDA_ERR_UNSUPPORTED),
+    (dict(state=None), B.KDA_ERR_INVALID_ARG),
+])
+def test_decode_ex_rejects(lib, over, expect):
+    assert _decode_ex(lib, **over) == expect
+
+
+def test_parameter_blocks_have_the_header_layout():
+    """The ctypes mirrors add up to the sizes the header's field order gives on LP64 (no padding)."""
+    assert ctypes.sizeof(B.PrefillParams) == 16 + 16 + 8 + 12 * 8 + 16
+    assert ctypes.sizeof(B.DecodeParams) == 16 + 16 + 10 * 8 + 16
