@@ -20,6 +20,8 @@ Notes, section 1.1 "Kimi Delta Attention"):
   exact rational arithmetic (``fractions.Fraction``), for tiny inputs.
 * ``epilogue`` -- the output gate with head-wise RMSNorm of section 1.3
   ("Full-rank output gate"), applied to a read-out, in numpy fp64.
+* ``prologue`` -- the input prologue of section 1.1 (short convolution, Swish,
+  L2 norm of q and k), with per-sequence convolution states, in numpy fp64.
 
 Parity status: every function here is pinned by the ``-m "not gpu"`` tests
 (exact brute force, closed forms, invariants, recurrent/chunked agreement and
@@ -32,3 +34,4 @@ from .recurrent import (kda_recurrent, kda_recurrent_mutant, kda_recurrent_gated
 from .chunked import kda_chunked, chunk_quantities  # noqa: F401
 from .exact import kda_exact  # noqa: F401
 from .epilogue import output_gate_rmsnorm, EPILOGUE_MUTATIONS  # noqa: F401
+from .prologue import kda_prologue, short_conv, PROLOGUE_MUTATIONS  # noqa: F401
