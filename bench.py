@@ -56,6 +56,8 @@ PREFILL_FLOPS_PER_TOKEN_HEAD = 6 * 128 * 128 + 64 * (3 * 128 + 2 * 128)
 GATED_BYTES_PER_TOKEN_HEAD = 1540
 # gated decay + output gate (bf16 gate logits in, bf16 output): 768 + 256 + 4 + 256 + 256 = 1540
 OUTGATE_BYTES_PER_TOKEN_HEAD = 1540
+# input prologue: raw q, k, v read + processed q, k, v written, bf16: 2 x 3 x 256 = 1536
+PROLOGUE_BYTES_PER_TOKEN_HEAD = 1536
 # decode, per (sequence, head): state read + write (131,072) + q,k,v bf16 (768) + log_alpha (512)
 # + beta (4) + out fp32 (512) = 132,868 bytes
 DECODE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4 + 3 * 256 + 512 + 4 + 512
@@ -241,6 +243,34 @@ def time_decode(steps_per_rep, reps, warmup, world, seed=0):
     return [a.elapsed_time(b) for a, b in ev]
 
 
+def time_prologue(steps, warmup, world, seed=0):
+    """The input prologue (ShortConv, Swish, L2 norm) on the K3-shaped layer's raw projections,
+    T=4096, H=96, bf16, with initial and final convolution states. Returns per-launch ms."""
+    from kimi_delta_attention_02_gb300 import binding, workloads
+    case = workloads.make_prologue([PREFILL["T"]], H=PREFILL["H"], device="cuda", seed=seed)
+    q, k, v = torch.empty_like(case.q_raw), torch.empty_like(case.k_raw), torch.empty_like(case.v_raw)
+    fin = torch.empty_like(case.conv_init)
+    stream = torch.cuda.current_stream()
+
+    def run():
+        binding.prologue(case.q_raw, case.k_raw, case.v_raw, case.conv_weight, case.cu_seqlens, case.conv_init,
+                         q=q, k=k, v=v, conv_final=fin, stream=stream)
+    for _ in range(warmup):
+        run()
+    binding.check_device_error(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    binding.check_device_error(stream)
+    return [a.elapsed_time(b) for a, b in ev]
+
+
 def time_e2e(case_cpu, steps, warmup):
     """Prefill through pinned host buffers: every step copies its inputs host -> device, runs
     kda_prefill and copies out + final state back to pinned host memory. Steps are streamed
@@ -336,7 +366,7 @@ def main():
     with ClockSampler(local) as clocks:
         total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world)
         dec_ms = None if args.prefill_only else time_decode(DECODE["steps"], 1, 1, world, seed=rank)
-        gated_ms = outgate_ms = None
+        gated_ms = outgate_ms = prologue_ms = None
         if not args.prefill_only and args.heads == PREFILL["H"]:
             gcase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
             _, g_launch = time_prefill(gcase, args.steps, args.warmup, world, gated=True)
@@ -346,6 +376,8 @@ def main():
             _, o_launch = time_prefill(ocase, args.steps, args.warmup, world, out_gate=True)
             outgate_ms = sum(o_launch) / len(o_launch)
             del ocase
+            p_launch = time_prologue(args.steps, args.warmup, world, seed=rank)
+            prologue_ms = sum(p_launch) / len(p_launch)
     if args.prefill_only:
         if rank == 0:
             print(json.dumps({"prefill_only": True, "heads": H, "ms_per_step": total_ms / args.steps,
@@ -379,6 +411,13 @@ def main():
                    "tokens_per_s": world * T / (outgate_ms / 1e3), "GB/s": o_gbs, "peak": hbm_gbs,
                    "frac": o_gbs / hbm_gbs, "alg_bytes": o_bytes, "out_dtype": "bf16",
                    "tensor_frac": alg_flops / (outgate_ms / 1e3) / 1e12 / tf_burst}
+    prologue = None
+    if prologue_ms is not None:
+        # raw q, k, v read + q, k, v written (bf16) per token-head, weights, states read and written
+        p_bytes = T * H * PROLOGUE_BYTES_PER_TOKEN_HEAD + H * 384 * 16 + 2 * case.num_seqs * H * 3 * 384 * 2
+        p_gbs = p_bytes / (prologue_ms / 1e3) / 1e9
+        prologue = {"workload": "prologue_k3_T4096_H96", "launch_ms": prologue_ms, "GB/s": p_gbs, "peak": hbm_gbs,
+                    "frac": p_gbs / hbm_gbs, "alg_bytes": p_bytes, "tokens_per_s": world * T / (prologue_ms / 1e3)}
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     dec_bytes = DECODE["B"] * DECODE["H"] * DECODE_BYTES_PER_SEQ_HEAD
     dec_gbs = dec_bytes / (dec_avg_ms / 1e3) / 1e9
@@ -419,6 +458,7 @@ def main():
                        "launches": len(dec_ms)},
             "gated_decay": gated,
             "output_gate": outgate,
+            "prologue": prologue,
             "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk,
             "gpu_launches": args.steps,  # one prefill launch per timed step (decode: its own region)
         }

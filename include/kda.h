@@ -192,6 +192,9 @@ kda_status kda_decode_gated(const void *q, const void *k, const void *v, const v
  *   norm_weight   w [d_v] fp32, device; NULL = ones. Must be NULL without out_gate
  *   norm_eps      finite, >= 0 (ignored without out_gate)
  *   force_recurrent (prefill) nonzero runs the fp32 token-recurrent kernel
+ *   conv_weight, conv_state, l2_eps (decode) the input prologue of kda_prologue
+ *                 applied to the token's raw q, k, v, with the sequence's
+ *                 convolution state shifted in place (NULL state = no prologue)
  * The output gate is fused into every kernel (the chunked tensor-core kernel,
  * the token-recurrent kernel and decode); it adds one read of the gate logits
  * and no other memory traffic.
@@ -233,14 +236,51 @@ typedef struct kda_decode_params {
   const void *out_gate;       /* [B, H, d_v] or NULL                           */
   const float *norm_weight;   /* [d_v] or NULL                                 */
   void *out;                  /* [B, H, d_v], out_dtype                        */
+  const float *conv_weight;   /* prologue: [H, 2 d_k + d_v, 4] fp32, or NULL   */
+  void *conv_state;           /* prologue: [B, H, 3, 2 d_k + d_v] in_dtype,
+                                 read and shifted in place; NULL = q, k, v are
+                                 used as given (no prologue)                   */
   float decay_bound;
   float scale;
   float norm_eps;
-  int32_t reserved;           /* set to 0                                      */
+  float l2_eps;               /* prologue: eps of the L2 norm, finite, >= 0    */
 } kda_decode_params;
 
 kda_status kda_prefill_ex(const kda_prefill_params *params, void *stream);
 kda_status kda_decode_ex(const kda_decode_params *params, void *stream);
+
+/*
+ * kda_prologue -- the input prologue of a KDA layer over packed sequences (Kimi K3 --
+ * Architecture Notes, section 1.1: the q/k/v projections pass a short convolution,
+ * then Swish, and q and k are then L2-normalised; kernel size 4 from the visualiser
+ * page "Kimi K3"). Per token t, head h and channel c of each projection x:
+ *
+ *     conv_t = sum_{j=0..3} w[h, c, j] * x_{t-3+j}    (causal, depthwise, no bias)
+ *     u_t    = conv_t * Sigmoid(conv_t)                (Swish)
+ *     q_t, k_t = u_t / sqrt(sum_c u_tc^2 + l2_eps);    v_t = u_t
+ *
+ * Inputs before a sequence's first token come from its convolution state (its three
+ * previous raw inputs, oldest first), or are zero.
+ *
+ *   q_raw, k_raw [total_tokens, H, d_k], v_raw [total_tokens, H, d_v]   dtype
+ *   conv_weight  [H, 2 d_k + d_v, 4] fp32: the q channels, then k, then v
+ *   cu_seqlens   [num_seqs + 1] int32, as in kda_prefill (trusted)
+ *   conv_init    [num_seqs, H, 3, 2 d_k + d_v] dtype, or NULL for zeros
+ *   q, k, v      outputs, shaped as the raw inputs, dtype (bf16 rounds to nearest-even)
+ *   conv_final   [num_seqs, H, 3, 2 d_k + d_v] dtype, written, or NULL: each
+ *                sequence's last three raw inputs (shifted in from conv_init when
+ *                the sequence is shorter), ready for kda_decode_ex's conv_state
+ *
+ * Outputs must not overlap the inputs or each other (conv_final may not alias
+ * conv_init). Sizes: 1 <= d_k, d_v <= 128, 1 <= H <= 65535. The results are the inputs of
+ * kda_prefill / kda_prefill_ex. One HBM-bound pass: reads each raw input once and
+ * writes each result once. Enqueues on `stream`.
+ */
+kda_status kda_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
+                        const float *conv_weight, const int32_t *cu_seqlens, int32_t num_seqs,
+                        int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v, kda_dtype dtype,
+                        const void *conv_init, float l2_eps, void *q, void *k, void *v,
+                        void *conv_final, void *stream);
 
 /*
  * kda_check_device_error -- synchronises `stream`, then reads and clears the

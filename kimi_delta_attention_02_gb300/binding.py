@@ -49,8 +49,9 @@ class DecodeParams(ctypes.Structure):
                 ("d_v", ctypes.c_int32), ("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("decay", ctypes.c_void_p), ("A_log", ctypes.c_void_p), ("beta", ctypes.c_void_p),
                 ("state", ctypes.c_void_p), ("out_gate", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p),
-                ("out", ctypes.c_void_p), ("decay_bound", ctypes.c_float), ("scale", ctypes.c_float),
-                ("norm_eps", ctypes.c_float), ("reserved", ctypes.c_int32)]
+                ("out", ctypes.c_void_p), ("conv_weight", ctypes.c_void_p), ("conv_state", ctypes.c_void_p),
+                ("decay_bound", ctypes.c_float), ("scale", ctypes.c_float), ("norm_eps", ctypes.c_float),
+                ("l2_eps", ctypes.c_float)]
 
 
 class KdaError(RuntimeError):
@@ -79,6 +80,8 @@ def _declare(lib):
     lib.kda_prefill_ex.restype = i32
     lib.kda_decode_ex.argtypes = [ctypes.POINTER(DecodeParams), vp]
     lib.kda_decode_ex.restype = i32
+    lib.kda_prologue.argtypes = [vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, vp, f32, vp, vp, vp, vp, vp]
+    lib.kda_prologue.restype = i32
     lib.kda_check_device_error.argtypes = [vp]
     lib.kda_check_device_error.restype = i32
     lib.kda_status_string.argtypes = [i32]
@@ -258,10 +261,14 @@ def prefill_ex(q, k, v, beta, cu_seqlens, *, log_alpha=None, lower_bound: float 
 
 
 def decode_ex(q, k, v, beta, state, *, log_alpha=None, lower_bound: float = -5.0, z=None, A_log=None,
-              g_min: float = -5.0, out_gate=None, norm_weight=None, norm_eps: float = 1e-6, out=None,
-              out_dtype=torch.float32, scale: float = 1.0, stream=None):
+              g_min: float = -5.0, out_gate=None, norm_weight=None, norm_eps: float = 1e-6, conv_weight=None,
+              conv_state=None, l2_eps: float = 1e-6, out=None, out_dtype=torch.float32, scale: float = 1.0,
+              stream=None):
     """One decode step through the parameter block (``kda_decode_ex``); ``state`` is updated in
-    place. Decay and output-gate options as in ``prefill_ex``. Returns out [B, H, d_v]."""
+    place. Decay and output-gate options as in ``prefill_ex``. With ``conv_state`` [B, H, 3,
+    2 d_k + d_v] (dtype of q; shifted in place) and ``conv_weight`` [H, 2 d_k + d_v, 4] float32,
+    q, k, v are the raw projections and pass the prologue of ``prologue`` first.
+    Returns out [B, H, d_v]."""
     B, H, d_k = q.shape
     d_v = v.shape[-1]
     form, decay, A, bound = _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min)
@@ -269,18 +276,52 @@ def decode_ex(q, k, v, beta, state, *, log_alpha=None, lower_bound: float = -5.0
         raise TypeError("out_gate must have the dtype of q")
     if out is None:
         out = torch.empty((B, H, d_v), dtype=out_dtype, device=q.device)
-    _check_cuda(q, k, v, decay, A, beta, state, out_gate, norm_weight, out)
+    _check_cuda(q, k, v, decay, A, beta, state, out_gate, norm_weight, conv_weight, conv_state, out)
+    if conv_state is not None and conv_state.dtype != q.dtype:
+        raise TypeError("conv_state must have the dtype of q")
     p = DecodeParams(struct_size=ctypes.sizeof(DecodeParams), in_dtype=_io_dtype(q.dtype),
                      out_dtype=_io_dtype(out.dtype), decay_form=form, B=B, H=H, d_k=d_k, d_v=d_v, q=q.data_ptr(),
                      k=k.data_ptr(), v=v.data_ptr(), decay=decay.data_ptr(),
                      A_log=None if A is None else A.data_ptr(), beta=beta.data_ptr(), state=state.data_ptr(),
                      out_gate=None if out_gate is None else out_gate.data_ptr(),
                      norm_weight=None if norm_weight is None else norm_weight.data_ptr(), out=out.data_ptr(),
-                     decay_bound=bound, scale=float(scale), norm_eps=float(norm_eps), reserved=0)
+                     conv_weight=None if conv_weight is None else conv_weight.data_ptr(),
+                     conv_state=None if conv_state is None else conv_state.data_ptr(),
+                     decay_bound=bound, scale=float(scale), norm_eps=float(norm_eps), l2_eps=float(l2_eps))
     st = lib().kda_decode_ex(ctypes.byref(p), _stream_handle(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_ex")
     return out
+
+
+def prologue(q_raw, k_raw, v_raw, conv_weight, cu_seqlens, conv_init=None, *, l2_eps: float = 1e-6, q=None,
+             k=None, v=None, conv_final=None, want_final: bool = True, stream=None):
+    """The input prologue (``kda_prologue``): 4-tap causal ShortConv per sequence, Swish, and the
+    L2 norm of q and k. q_raw, k_raw [T, H, d_k], v_raw [T, H, d_v] (bf16 or fp32, one dtype);
+    conv_weight [H, 2 d_k + d_v, 4] float32; conv_init [N, H, 3, 2 d_k + d_v] or None.
+    Returns (q, k, v, conv_final or None), the inputs of ``prefill``."""
+    T, H, d_k = q_raw.shape
+    d_v = v_raw.shape[-1]
+    N = cu_seqlens.shape[0] - 1
+    dt = _io_dtype(q_raw.dtype)
+    if k_raw.dtype != q_raw.dtype or v_raw.dtype != q_raw.dtype:
+        raise TypeError("q, k and v must share one dtype")
+    if conv_weight.dtype != torch.float32 or cu_seqlens.dtype != torch.int32:
+        raise TypeError("conv_weight must be float32 and cu_seqlens int32")
+    if conv_init is not None and conv_init.dtype != q_raw.dtype:
+        raise TypeError("conv_init must have the dtype of q")
+    q = torch.empty_like(q_raw) if q is None else q
+    k = torch.empty_like(k_raw) if k is None else k
+    v = torch.empty_like(v_raw) if v is None else v
+    if conv_final is None and want_final:
+        conv_final = torch.empty((N, H, 3, 2 * d_k + d_v), dtype=q_raw.dtype, device=q_raw.device)
+    _check_cuda(q_raw, k_raw, v_raw, conv_weight, cu_seqlens, conv_init, q, k, v, conv_final)
+    st = lib().kda_prologue(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(conv_weight), _ptr(cu_seqlens), N, T, H,
+                            d_k, d_v, dt, _ptr(conv_init), float(l2_eps), _ptr(q), _ptr(k), _ptr(v),
+                            _ptr(conv_final), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prologue")
+    return q, k, v, conv_final
 
 
 def decode_gated(q, k, v, z, A_log, beta, state, *, out=None, out_dtype=torch.float32, g_min: float = -5.0,

@@ -38,8 +38,13 @@ uint32_t *device_error_word() {
 // gate as `out_gate` (gate logits, input dtype; null = plain read-out) + `norm_weight` + `norm_eps`.
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                           const float *beta, float *state, const void *out_gate, const float *norm_weight,
-                          float norm_eps, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
-                          float lb, float scale, cudaStream_t stream);
+                          float norm_eps, const float *conv_w, void *conv_state, float l2_eps, void *out, int B,
+                          int H, int d_k, int d_v, bool in_bf16, bool out_bf16, float lb, float scale,
+                          cudaStream_t stream);
+cudaError_t launch_prologue(const void *q_raw, const void *k_raw, const void *v_raw, const float *conv_w,
+                            const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H, int d_k, int d_v,
+                            bool bf16, const void *conv_init, float eps, void *q, void *k, void *v,
+                            void *conv_final, cudaStream_t stream);
 cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                              const float *beta, const int32_t *cu_seqlens, int num_seqs, int H, int d_k, int d_v,
                              bool in_bf16, bool out_bf16, float lb, float scale, const float *init_state,
@@ -140,10 +145,19 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const void 
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
+bool finite_nonneg(float x) { return x >= 0.f && x < INFINITY; }  // false for NaN
+
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || !na || !nb) return false;
+  const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+  return pa < pb + nb && pb < pa + na;
+}
+
 kda_status decode_impl(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                        const float *beta, float *state, void *out, int32_t B, int32_t H, int32_t d_k, int32_t d_v,
                        kda_dtype in_dtype, kda_dtype out_dtype, float lb, float scale, void *stream,
-                       const void *out_gate = nullptr, const float *norm_weight = nullptr, float norm_eps = 0.f) {
+                       const void *out_gate = nullptr, const float *norm_weight = nullptr, float norm_eps = 0.f,
+                       const float *conv_weight = nullptr, void *conv_state = nullptr, float l2_eps = 0.f) {
   if (in_dtype != KDA_F32 && in_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (out_dtype != KDA_F32 && out_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
@@ -161,9 +175,20 @@ kda_status decode_impl(const void *q, const void *k, const void *v, const void *
     const char *po = static_cast<const char *>(out), *pg = static_cast<const char *>(out_gate);
     if (po < pg + nv * es && pg < po + nv * eo) return KDA_ERR_INVALID_ARG;
   }
-  const cudaError_t err = launch_decode(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps, out,
-                                        B, H, d_k, d_v, in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale,
-                                        static_cast<cudaStream_t>(stream));
+  if (conv_state != nullptr) {  // the prologue: weights and state on the device, eps finite
+    if (conv_weight == nullptr || !aligned16(conv_weight) || !aligned16(conv_state) || !finite_nonneg(l2_eps))
+      return KDA_ERR_INVALID_ARG;
+    const size_t es = in_dtype == KDA_BF16 ? 2 : 4, eo = out_dtype == KDA_BF16 ? 2 : 4;
+    const size_t ncs = size_t(B) * H * 3 * (2 * d_k + d_v) * es;
+    if (overlaps(conv_state, ncs, state, size_t(B) * H * d_k * d_v * 4) ||
+        overlaps(conv_state, ncs, out, size_t(B) * H * d_v * eo))
+      return KDA_ERR_INVALID_ARG;
+  } else if (conv_weight != nullptr) {
+    return KDA_ERR_INVALID_ARG;  // weights without a state
+  }
+  const cudaError_t err = launch_decode(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps,
+                                        conv_weight, conv_state, l2_eps, out, B, H, d_k, d_v, in_dtype == KDA_BF16,
+                                        out_dtype == KDA_BF16, lb, scale, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -252,7 +277,46 @@ kda_status kda_decode_ex(const kda_decode_params *p, void *stream) {
   if (st != KDA_OK) return st;
   return decode_impl(p->q, p->k, p->v, p->decay, p->A_log, p->beta, p->state, p->out, p->B, p->H, p->d_k, p->d_v,
                      p->in_dtype, p->out_dtype, p->decay_bound, p->scale, stream, p->out_gate, p->norm_weight,
-                     p->norm_eps);
+                     p->norm_eps, p->conv_weight, p->conv_state, p->l2_eps);
+}
+
+kda_status kda_prologue(const void *q_raw, const void *k_raw, const void *v_raw, const float *conv_weight,
+                        const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
+                        int32_t d_v, kda_dtype dtype, const void *conv_init, float l2_eps, void *q, void *k, void *v,
+                        void *conv_final, void *stream) {
+  if (dtype != KDA_F32 && dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
+  if (num_seqs < 0 || total_tokens < 0 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
+  if (d_k > 128 || d_v > 128) return KDA_ERR_UNSUPPORTED;
+  if (total_tokens > INT32_MAX || H > 65535) return KDA_ERR_UNSUPPORTED;
+  if (num_seqs == 0 && total_tokens > 0) return KDA_ERR_INVALID_ARG;
+  if (!finite_nonneg(l2_eps)) return KDA_ERR_INVALID_ARG;
+  if (cu_seqlens == nullptr || !aligned4(cu_seqlens)) return KDA_ERR_INVALID_ARG;
+  if (conv_weight == nullptr || !aligned16(conv_weight)) return KDA_ERR_INVALID_ARG;
+  if (total_tokens > 0) {
+    if (!q_raw || !k_raw || !v_raw || !q || !k || !v) return KDA_ERR_INVALID_ARG;
+    if (!aligned16(q_raw) || !aligned16(k_raw) || !aligned16(v_raw) || !aligned16(q) || !aligned16(k) ||
+        !aligned16(v))
+      return KDA_ERR_INVALID_ARG;
+  }
+  if ((conv_init && !aligned16(conv_init)) || (conv_final && !aligned16(conv_final))) return KDA_ERR_INVALID_ARG;
+  const size_t es = dtype == KDA_BF16 ? 2 : 4;
+  const size_t nk = size_t(total_tokens) * H * d_k * es, nv = size_t(total_tokens) * H * d_v * es;
+  const size_t ns = size_t(num_seqs) * H * 3 * (2 * d_k + d_v) * es;
+  const void *ins[6] = {q_raw, k_raw, v_raw, conv_weight, cu_seqlens, conv_init};
+  const size_t in_bytes[6] = {nk, nk, nv, size_t(H) * (2 * d_k + d_v) * 16, size_t(num_seqs + 1) * 4, ns};
+  const void *outs[4] = {q, k, v, conv_final};
+  const size_t out_bytes[4] = {nk, nk, nv, conv_final ? ns : 0};
+  for (int o = 0; o < 4; ++o) {
+    for (int i = 0; i < 6; ++i)
+      if (overlaps(outs[o], out_bytes[o], ins[i], in_bytes[i])) return KDA_ERR_INVALID_ARG;
+    for (int o2 = o + 1; o2 < 4; ++o2)
+      if (overlaps(outs[o], out_bytes[o], outs[o2], out_bytes[o2])) return KDA_ERR_INVALID_ARG;
+  }
+  if (num_seqs == 0) return KDA_OK;
+  const cudaError_t err = launch_prologue(q_raw, k_raw, v_raw, conv_weight, cu_seqlens, num_seqs, total_tokens, H,
+                                          d_k, d_v, dtype == KDA_BF16, conv_init, l2_eps, q, k, v, conv_final,
+                                          static_cast<cudaStream_t>(stream));
+  return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
 kda_status kda_check_device_error(void *stream) {

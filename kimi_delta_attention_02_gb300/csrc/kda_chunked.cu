@@ -7,6 +7,7 @@
 #include <mutex>
 
 #include "kda_chunked_kernel.cuh"
+#include "kda_tma_host.h"
 
 namespace kda {
 namespace chunked {
@@ -37,26 +38,31 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 3-D map over a token-major [T, H, 128] tensor: dims (channel, head, token); boxes of
-// 32 tokens x 64 channels (bf16, 128-byte swizzle: the MMA operands q, k, v) or 32 tokens x
-// 128 channels without swizzle (the decay input: fp32 log_alpha or bf16 logits z; the
-// output gate's bf16 logits; the output, bf16 or fp32, written by TMA stores).
+// The chunked kernel's maps over [T, H, 128] tensors: boxes of 32 tokens x 64 channels (bf16,
+// 128-byte swizzle: the MMA operands q, k, v) or 32 tokens x 128 channels without swizzle (the
+// decay input: fp32 log_alpha or bf16 logits z; the output gate's bf16 logits; the output,
+// bf16 or fp32, written by TMA stores).
 bool make_map(CUtensorMap *map, const void *base, bool bf16, bool swizzled, int64_t T, int H) {
-  auto fn = encode_fn();
-  if (fn == nullptr) return false;
-  const uint64_t es = bf16 ? 2 : 4;
-  const cuuint64_t dims[3] = {cuuint64_t(chunked::kD), cuuint64_t(H), cuuint64_t(T)};
-  const cuuint64_t strides[2] = {cuuint64_t(chunked::kD * es), cuuint64_t(H) * chunked::kD * es};
-  const cuuint32_t box[3] = {swizzled ? 64u : 128u, 1u, cuuint32_t(chunked::kC)};
-  const cuuint32_t estr[3] = {1, 1, 1};
-  const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
-                        const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        swizzled ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return tensor_map_3d(map, base, bf16, T, H, chunked::kD, swizzled ? 64u : 128u, uint32_t(chunked::kC), swizzled);
 }
 
 }  // namespace
+
+bool tensor_map_3d(CUtensorMap *map, const void *base, bool bf16, int64_t T, int H, int d, uint32_t box_d,
+                   uint32_t box_t, bool swizzle128) {
+  auto fn = encode_fn();
+  if (fn == nullptr) return false;
+  const uint64_t es = bf16 ? 2 : 4;
+  const cuuint64_t dims[3] = {cuuint64_t(d), cuuint64_t(H), cuuint64_t(T)};
+  const cuuint64_t strides[2] = {cuuint64_t(d) * es, cuuint64_t(H) * d * es};
+  const cuuint32_t box[3] = {box_d, 1u, box_t};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = fn(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3,
+                        const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
 
 bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb) {
   return in_bf16 && d_k == chunked::kD && d_v == chunked::kD && lb >= -5.0f;

@@ -76,6 +76,9 @@ __device__ __forceinline__ float round_tf32_alu(float x) {
   return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
 }
 
+__device__ __forceinline__ float bf16_or_f32(uint16_t h) { return bf16_to_f32(h); }
+__device__ __forceinline__ float bf16_or_f32(float x) { return x; }
+
 // Element load/store for the two I/O dtypes (fp32 or bf16 bits).
 template <bool kBF16>
 __device__ __forceinline__ float load_elem(const void *base, int64_t idx) {
@@ -110,6 +113,34 @@ __device__ __forceinline__ float sigmoid_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * -1.4426950408889634f));
   asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + e));
   return r;
+}
+
+// Packed fp32 pairs (Blackwell's two-wide fp32 FMA / multiply / add: one instruction, two
+// results, each rounded as its scalar counterpart).
+__device__ __forceinline__ unsigned long long f2_pack(float2 a) {
+  unsigned long long r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a.x), "f"(a.y));
+  return r;
+}
+__device__ __forceinline__ float2 f2_unpack(unsigned long long r) {
+  float2 a;
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(r));
+  return a;
+}
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)), "l"(f2_pack(c)));
+  return f2_unpack(r);
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(r);
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  unsigned long long r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2_pack(a)), "l"(f2_pack(b)));
+  return f2_unpack(r);
 }
 
 // The output gate of Kimi K3 -- Architecture Notes, section 1.3 ("Full-rank output gate"):

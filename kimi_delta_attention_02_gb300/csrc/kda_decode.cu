@@ -15,7 +15,10 @@
 // input or, in the gated form (section 1.2), g = g_min * Sigmoid(e^{A_h} z).
 // Optionally the read-out goes through the output gate of section 1.3,
 // Sigmoid(r) * w * o / rms(o), before it is written: warp 0 holds the whole d_v
-// row, so the RMS is one warp reduction.
+// row, so the RMS is one warp reduction. Optionally the token's raw q, k, v first
+// pass the prologue of section 1.1 (4-tap short convolution over the sequence's
+// convolution state, which is shifted in place, then Swish, then the L2 norm of q
+// and k): the conv state adds 3 x (2 d_k + d_v) values per (sequence, head).
 #include "kda_common.cuh"
 
 namespace kda {
@@ -23,16 +26,24 @@ namespace kda {
 constexpr int kDecodeThreads = 256;
 constexpr int kDecodeRowsPerThread = 16;  // 128 key rows / 8 row groups
 
-template <bool kInBF16, bool kOutBF16, bool kGated, bool kNormGate>
+// The prologue's parameters: conv weights [H, 2 d_k + d_v, 4] fp32, the conv state
+// [B, H, 3, 2 d_k + d_v] (input dtype, read and shifted in place) and the L2 norm's eps.
+struct Prologue {
+  const float *w;
+  void *state;
+  float eps;
+};
+
+template <bool kInBF16, bool kOutBF16, bool kGated, bool kNormGate, bool kPrologue>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
     kda_decode_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                       const void *__restrict__ decay, const float *__restrict__ A_log,
                       const float *__restrict__ beta, float *__restrict__ state, const void *__restrict__ out_gate,
-                      const float *__restrict__ norm_weight, float norm_eps, void *__restrict__ out, int H,
-                      int d_k, int d_v, float lb, float scale) {
+                      const float *__restrict__ norm_weight, float norm_eps, const Prologue pro,
+                      void *__restrict__ out, int H, int d_k, int d_v, float lb, float scale) {
   __shared__ float s_k[128], s_q[128], s_a[128], s_v[128];
   __shared__ float s_red_y[8][128], s_red_z[8][128];
-  __shared__ float s_kq[8];
+  __shared__ float s_kq[8], s_nrm[2][4];
 
   const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
   const int64_t bh = blockIdx.x;  // (sequence, head) pair, head fastest
@@ -50,20 +61,64 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
-  // 2. token vectors: decay, key, query, value; k.q by warp reduction
-  float kq = 0.f;
+  // 2. token vectors: decay, key, query, value (through the prologue if asked); k.q by
+  // warp reduction
+  float kq = 0.f, kk = 0.f, qq = 0.f, vv = 0.f;
   if (tid < 128) {
-    float kk = 0.f, qq = 0.f, a = 0.f;
     if (tid < d_k) {
       kk = load_elem<kInBF16>(k, vec_base + tid);
       qq = load_elem<kInBF16>(q, vec_base + tid);
+    }
+    if (tid < d_v) vv = load_elem<kInBF16>(v, bh * d_v + tid);
+  }
+  if constexpr (kPrologue) {
+    if (tid < 128) {
+      const int C3 = 2 * d_k + d_v, h = int(bh % H);
+      const int64_t sb = bh * 3 * C3;
+      auto conv = [&](float xt, int cc) {  // 4 taps over (state, x_t); the state shifts by one
+        const float x0 = load_elem<kInBF16>(pro.state, sb + cc), x1 = load_elem<kInBF16>(pro.state, sb + C3 + cc),
+                    x2 = load_elem<kInBF16>(pro.state, sb + 2 * C3 + cc);
+        const float *w = pro.w + (int64_t(h) * C3 + cc) * 4;
+        float acc = w[0] * x0;
+        acc = fmaf(w[1], x1, acc);
+        acc = fmaf(w[2], x2, acc);
+        acc = fmaf(w[3], xt, acc);
+        store_elem<kInBF16>(pro.state, sb + cc, x1);
+        store_elem<kInBF16>(pro.state, sb + C3 + cc, x2);
+        store_elem<kInBF16>(pro.state, sb + 2 * C3 + cc, xt);
+        return acc * sigmoid_approx(acc);  // Swish
+      };
+      if (tid < d_k) {
+        qq = conv(qq, tid);
+        kk = conv(kk, d_k + tid);
+      }
+      if (tid < d_v) vv = conv(vv, 2 * d_k + tid);
+      float nq = qq * qq, nk = kk * kk;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        nq += __shfl_xor_sync(0xffffffffu, nq, o);
+        nk += __shfl_xor_sync(0xffffffffu, nk, o);
+      }
+      if (tx == 0) {
+        s_nrm[0][ty] = nq;
+        s_nrm[1][ty] = nk;
+      }
+    }
+    __syncthreads();
+    if (tid < 128) {
+      qq *= rsqrtf(((s_nrm[0][0] + s_nrm[0][1]) + (s_nrm[0][2] + s_nrm[0][3])) + pro.eps);
+      kk *= rsqrtf(((s_nrm[1][0] + s_nrm[1][1]) + (s_nrm[1][2] + s_nrm[1][3])) + pro.eps);
+    }
+  }
+  if (tid < 128) {
+    float a = 0.f;
+    if (tid < d_k)
       a = __expf(kGated ? gated_log_decay(load_elem<kInBF16>(decay, vec_base + tid), __expf(A_log[bh % H]), lb)
                         : clamp_log_decay(static_cast<const float *>(decay)[vec_base + tid], lb));
-    }
     s_k[tid] = kk;
     s_q[tid] = qq;
     s_a[tid] = a;
-    s_v[tid] = tid < d_v ? load_elem<kInBF16>(v, bh * d_v + tid) : 0.f;
+    s_v[tid] = vv;
     kq = kk * qq;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
@@ -136,23 +191,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
 
 // decay: log_alpha (fp32) when A_log is null, else the gated form's logits z (input dtype).
 // out_gate: gate logits [B, H, d_v] (input dtype) of the output gate, or null (out = o).
+// conv_w / conv_state: the prologue's weights and state, or null (q, k, v used as given).
 cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                           const float *beta, float *state, const void *out_gate, const float *norm_weight,
-                          float norm_eps, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
-                          float lb, float scale, cudaStream_t stream) {
+                          float norm_eps, const float *conv_w, void *conv_state, float l2_eps, void *out, int B,
+                          int H, int d_k, int d_v, bool in_bf16, bool out_bf16, float lb, float scale,
+                          cudaStream_t stream) {
   const dim3 grid(unsigned(int64_t(B) * H)), block(kDecodeThreads);
-  using Kern = decltype(&kda_decode_kernel<false, false, false, false>);
-#define KDA_DEC_ROW(ng)                                                                                        \
-  kda_decode_kernel<false, false, false, ng>, kda_decode_kernel<false, false, true, ng>,                       \
-      kda_decode_kernel<false, true, false, ng>, kda_decode_kernel<false, true, true, ng>,                     \
-      kda_decode_kernel<true, false, false, ng>, kda_decode_kernel<true, false, true, ng>,                     \
-      kda_decode_kernel<true, true, false, ng>, kda_decode_kernel<true, true, true, ng>
-  static const Kern table[16] = {KDA_DEC_ROW(false), KDA_DEC_ROW(true)};
+  using Kern = decltype(&kda_decode_kernel<false, false, false, false, false>);
+#define KDA_DEC_ROW(ng, pr)                                                                                    \
+  kda_decode_kernel<false, false, false, ng, pr>, kda_decode_kernel<false, false, true, ng, pr>,               \
+      kda_decode_kernel<false, true, false, ng, pr>, kda_decode_kernel<false, true, true, ng, pr>,             \
+      kda_decode_kernel<true, false, false, ng, pr>, kda_decode_kernel<true, false, true, ng, pr>,             \
+      kda_decode_kernel<true, true, false, ng, pr>, kda_decode_kernel<true, true, true, ng, pr>
+  static const Kern table[32] = {KDA_DEC_ROW(false, false), KDA_DEC_ROW(true, false), KDA_DEC_ROW(false, true),
+                                 KDA_DEC_ROW(true, true)};
 #undef KDA_DEC_ROW
-  const Kern kern =
-      table[8 * int(out_gate != nullptr) + 4 * int(in_bf16) + 2 * int(out_bf16) + int(A_log != nullptr)];
-  kern<<<grid, block, 0, stream>>>(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps, out, H, d_k,
-                                   d_v, lb, scale);
+  const bool pro = conv_state != nullptr;
+  const Kern kern = table[16 * int(pro) + 8 * int(out_gate != nullptr) + 4 * int(in_bf16) + 2 * int(out_bf16) +
+                          int(A_log != nullptr)];
+  const Prologue pr{conv_w, conv_state, l2_eps};
+  kern<<<grid, block, 0, stream>>>(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps, pr, out, H,
+                                   d_k, d_v, lb, scale);
   return cudaGetLastError();
 }
 

@@ -24,6 +24,10 @@ Recipe (the pages publish no dataset; every workload is synthetic):
 * output gate: gate logits r ~ N(0, 1) per value channel, cast to the workload
   dtype (standing in for W_g x), and one RMSNorm weight w = 1 + 0.1 N(0, 1) per
   value channel in fp32 (a weight near its initial value of ones).
+* input prologue: raw projections q, k, v ~ N(0, 1) in the workload dtype (not
+  normalised: the prologue normalises), convolution weights 0.5 N(0, 1) per
+  (head, channel, tap) in fp32, and convolution states (three earlier raw
+  inputs) ~ N(0, 1) in the workload dtype.
 
 Every (tensor, head[, step]) pair draws from its own ``torch.Generator``
 stream, so any single head can be regenerated without the others and large
@@ -38,7 +42,7 @@ import numpy as np
 import torch
 
 # tensor ids used to derive stream seeds
-_Q, _K, _V, _LA, _BETA, _INIT, _Z, _A, _R, _W = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10
+_Q, _K, _V, _LA, _BETA, _INIT, _Z, _A, _R, _W, _CW, _CS = 1, 2, 3, 4, 5, 6, 7, 8, 9, 10, 11, 12
 
 
 def _stream(seed: int, tensor_id: int, head: int, step: int, device) -> torch.Generator:
@@ -216,3 +220,49 @@ def make_decode_step(step: int, B: int, H: int, d_k: int = 128, d_v: int = 128, 
 
 
 DECODE_WORKLOAD = dict(B=256, H=96, d_k=128, d_v=128, steps=64, dtype=torch.bfloat16)
+
+
+@dataclass
+class PrologueCase:
+    """Raw projections for the input prologue over packed sequences: q_raw, k_raw [T_tot, H, d_k],
+    v_raw [T_tot, H, d_v] (dtype); conv_weight [H, 2 d_k + d_v, 4] fp32; cu_seqlens [N+1] int32;
+    conv_init [N, H, 3, 2 d_k + d_v] (dtype) or None."""
+    q_raw: torch.Tensor
+    k_raw: torch.Tensor
+    v_raw: torch.Tensor
+    conv_weight: torch.Tensor
+    cu_seqlens: torch.Tensor
+    conv_init: torch.Tensor | None
+    lengths: list = field(default_factory=list)
+
+
+def make_conv_weight(H: int, d_k: int = 128, d_v: int = 128, *, device="cpu", seed: int = 0) -> torch.Tensor:
+    C3 = 2 * d_k + d_v
+    w = torch.empty((H, C3, 4), dtype=torch.float32, device=device)
+    for h in range(H):
+        w[h] = 0.5 * _randn((C3, 4), seed, _CW, h, 0, device)
+    return w
+
+
+def make_conv_state(N: int, H: int, d_k: int = 128, d_v: int = 128, *, dtype=torch.bfloat16, device="cpu",
+                    seed: int = 0) -> torch.Tensor:
+    st = torch.empty((N, H, 3, 2 * d_k + d_v), dtype=dtype, device=device)
+    for h in range(H):
+        st[:, h] = _randn((N, 3, 2 * d_k + d_v), seed, _CS, h, 0, device).to(dtype)
+    return st
+
+
+def make_prologue(lengths, H: int, d_k: int = 128, d_v: int = 128, *, dtype=torch.bfloat16, device="cpu",
+                  seed: int = 0, with_state: bool = True) -> PrologueCase:
+    lengths = [int(x) for x in lengths]
+    T = int(sum(lengths))
+    q = torch.empty((T, H, d_k), dtype=dtype, device=device)
+    k = torch.empty((T, H, d_k), dtype=dtype, device=device)
+    v = torch.empty((T, H, d_v), dtype=dtype, device=device)
+    for h in range(H):
+        q[:, h] = _randn((T, d_k), seed, _Q, h, 0, device).to(dtype)
+        k[:, h] = _randn((T, d_k), seed, _K, h, 0, device).to(dtype)
+        v[:, h] = _randn((T, d_v), seed, _V, h, 0, device).to(dtype)
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(lengths)]).astype(np.int32), device=device)
+    st = make_conv_state(len(lengths), H, d_k, d_v, dtype=dtype, device=device, seed=seed) if with_state else None
+    return PrologueCase(q, k, v, make_conv_weight(H, d_k, d_v, device=device, seed=seed), cu, st, lengths)

@@ -34,7 +34,8 @@ def test_exports_every_declared_symbol(lib):
     names = declared_functions()
     assert {"kda_prefill", "kda_decode", "kda_prefill_recurrent", "kda_check_device_error",
             "kda_status_string", "kda_version", "kda_selftest_umma", "kda_prefill_gated",
-            "kda_prefill_gated_recurrent", "kda_decode_gated", "kda_prefill_ex", "kda_decode_ex"} <= set(names)
+            "kda_prefill_gated_recurrent", "kda_decode_gated", "kda_prefill_ex", "kda_decode_ex",
+            "kda_prologue"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -199,8 +200,8 @@ def test_prefill_ex_accepts_empty_work(lib):
 def _decode_ex(lib, **over):
     f = dict(struct_size=ctypes.sizeof(B.DecodeParams), in_dtype=1, out_dtype=0, decay_form=0, B=2, H=2, d_k=128,
              d_v=128, q=0x10000, k=0x20000, v=0x30000, decay=0x40000, A_log=None, beta=0x50000, state=0x90000,
-             out_gate=0xb0000, norm_weight=None, out=0x70000, decay_bound=-5.0, scale=1.0, norm_eps=1e-6,
-             reserved=0)
+             out_gate=0xb0000, norm_weight=None, out=0x70000, conv_weight=None, conv_state=None, decay_bound=-5.0,
+             scale=1.0, norm_eps=1e-6, l2_eps=1e-6)
     f.update(over)
     return lib.kda_decode_ex(ctypes.byref(B.DecodeParams(**f)), NULL)
 
@@ -216,6 +217,11 @@ def _decode_ex(lib, **over):
     (dict(out=0xb0000), B.KDA_ERR_INVALID_ARG),                     # output over the gate logits
     (dict(d_v=6), B.KDA_ERR_UNSUPPORTED),
     (dict(state=None), B.KDA_ERR_INVALID_ARG),
+    (dict(conv_weight=0xd0000), B.KDA_ERR_INVALID_ARG),             # conv weights without a state
+    (dict(conv_state=0xe0000), B.KDA_ERR_INVALID_ARG),              # a state without weights
+    (dict(conv_state=0xe0000, conv_weight=0xd0000, l2_eps=float("nan")), B.KDA_ERR_INVALID_ARG),
+    (dict(conv_state=0xe0008, conv_weight=0xd0000), B.KDA_ERR_INVALID_ARG),
+    (dict(conv_state=0x90000 + 4096, conv_weight=0xd0000), B.KDA_ERR_INVALID_ARG),  # inside the state
 ])
 def test_decode_ex_rejects(lib, over, expect):
     assert _decode_ex(lib, **over) == expect
@@ -224,4 +230,35 @@ def test_decode_ex_rejects(lib, over, expect):
 def test_parameter_blocks_have_the_header_layout():
     """The ctypes mirrors add up to the sizes the header's field order gives on LP64 (no padding)."""
     assert ctypes.sizeof(B.PrefillParams) == 16 + 16 + 8 + 12 * 8 + 16
-    assert ctypes.sizeof(B.DecodeParams) == 16 + 16 + 10 * 8 + 16
+    assert ctypes.sizeof(B.DecodeParams) == 16 + 16 + 12 * 8 + 16
+
+
+def _prologue(lib, **over):
+    a = dict(q_raw=0x10000, k_raw=0x20000, v_raw=0x30000, w=0x40000, cu=0x60000, N=1, T=4, H=2, dk=128, dv=128,
+             dtype=1, init=None, eps=1e-6, q=0x70000, k=0x80000, v=0x90000, fin=0xa0000)
+    a.update(over)
+    return lib.kda_prologue(a["q_raw"], a["k_raw"], a["v_raw"], a["w"], a["cu"], a["N"], a["T"], a["H"], a["dk"],
+                            a["dv"], a["dtype"], a["init"], a["eps"], a["q"], a["k"], a["v"], a["fin"], NULL)
+
+
+@pytest.mark.parametrize("over,expect", [
+    (dict(w=None), B.KDA_ERR_INVALID_ARG),
+    (dict(cu=None), B.KDA_ERR_INVALID_ARG),
+    (dict(q=None), B.KDA_ERR_INVALID_ARG),
+    (dict(v_raw=0x30008), B.KDA_ERR_INVALID_ARG),
+    (dict(dtype=3), B.KDA_ERR_INVALID_ARG),
+    (dict(eps=-1.0), B.KDA_ERR_INVALID_ARG),
+    (dict(eps=float("inf")), B.KDA_ERR_INVALID_ARG),
+    (dict(dk=200), B.KDA_ERR_UNSUPPORTED),
+    (dict(H=70000), B.KDA_ERR_UNSUPPORTED),
+    (dict(N=0), B.KDA_ERR_INVALID_ARG),                     # tokens without a sequence
+    (dict(q=0x10000), B.KDA_ERR_INVALID_ARG),               # output over an input
+    (dict(k=0x70000), B.KDA_ERR_INVALID_ARG),               # two outputs overlap
+    (dict(init=0xb0000, fin=0xb0000), B.KDA_ERR_INVALID_ARG),  # final state over the initial one
+])
+def test_prologue_rejects(lib, over, expect):
+    assert _prologue(lib, **over) == expect
+
+
+def test_prologue_accepts_empty_work(lib):
+    assert _prologue(lib, N=0, T=0, q_raw=None, k_raw=None, v_raw=None, q=None, k=None, v=None, fin=None) == B.KDA_OK
