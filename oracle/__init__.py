@@ -12,7 +12,8 @@ Notes, section 1.1 "Kimi Delta Attention"):
   (``kda_oracle.c``), threaded over (sequence, head) pairs. This is the oracle
   the GPU path is compared with. ``kda_recurrent_gated`` is the same recurrence
   with the log-decay of the gated form, ``g = g_min * Sigmoid(e^{A_h} z)``
-  (section 1.2, the K3 row of the mapping table).
+  (section 1.2, the K3 row of the mapping table); ``kda_recurrent_unbounded``
+  the unbounded map of the earlier models, ``g = -e^{A_h} Softplus(z)``.
 * ``chunked``  -- the chunkwise form (section 1.2: "recurrent across chunks and
   parallel within each chunk") in numpy fp64, with the chunk's triangular
   system solved by a library inverse. Pinned to ``recurrent`` by agreement.
@@ -30,7 +31,7 @@ pin is a printed value.
 """
 
 from .recurrent import (kda_recurrent, kda_recurrent_mutant, kda_recurrent_gated, MUTATIONS,  # noqa: F401
-                        GATE_MUTATIONS, oracle_library_path)
+                        GATE_MUTATIONS, oracle_library_path, kda_recurrent_unbounded, UNBOUNDED_MUTATIONS)
 from .chunked import kda_chunked, chunk_quantities  # noqa: F401
 from .exact import kda_exact  # noqa: F401
 from .epilogue import output_gate_rmsnorm, EPILOGUE_MUTATIONS  # noqa: F401

@@ -21,6 +21,9 @@
  * computed from decay logits z and a per-head log-scale A_h as
  *     g = g_min * Sigmoid(e^{A_h} z),   Sigmoid(x) = 1 / (1 + e^{-x}),
  * which lies in (g_min, 0) by construction, so no clamp is applied.
+ * Unbounded form (same table, the GDN / Mamba-2 / Kimi Linear row):
+ *     g = -e^{A_h} * Softplus(z),       Softplus(x) = log(1 + e^x),
+ * which lies in (-inf, 0).
  *
  * Expanding the product, (I - b k k^T) D S + b k v^T = D S + k (b (v - (D S)^T k))^T,
  * so each token is: decay the key rows of S, predict (D S)^T k, write the
@@ -54,7 +57,13 @@ enum {
   MUT_GATE_NO_EXP = 8,       /* gated form: A_h used where e^{A_h} belongs     */
   MUT_GATE_SOFTPLUS = 9,     /* gated form: the unbounded g = -e^{A_h} Softplus(z) */
   MUT_GATE_SIGN = 10,        /* gated form: Sigmoid(-e^{A_h} z)                */
+  MUT_UNB_NO_EXP = 11,       /* unbounded form: A_h where e^{A_h} belongs      */
+  MUT_UNB_SIGN = 12,         /* unbounded form: +e^{A_h} Softplus(z)           */
+  MUT_UNB_BOUNDED = 13,      /* unbounded form: the bounded map, g_min = -5    */
 };
+
+/* Softplus(x) = log(1 + e^x), without overflow for large x */
+static double softplus(double x) { return x > 0.0 ? x + log1p(exp(-x)) : log1p(exp(x)); }
 
 static double load(const void *base, int dtype, int64_t idx) {
   if (dtype == ORC_F64) return ((const double *)base)[idx];
@@ -69,7 +78,8 @@ static double load(const void *base, int dtype, int64_t idx) {
 typedef struct {
   const void *q, *k, *v, *log_alpha, *beta, *init;
   int dt_qk, dt_v, dt_la, dt_beta, dt_init;
-  const double *A_log; /* gated form: per-head log-scale (log_alpha then holds z); NULL: clamp */
+  const double *A_log; /* gated forms: per-head log-scale (log_alpha then holds z); NULL: clamp */
+  int unbounded;       /* with A_log: the unbounded map instead of the bounded one */
   const int64_t *cu;
   int64_t num_seqs, H, dk, dv;
   double lb, scale;
@@ -95,7 +105,12 @@ static void run_unit(job_t *J, int64_t unit, double *S, double *a, double *kk,
     const double b = load(J->beta, J->dt_beta, t * H + h);
     for (int64_t c = 0; c < dk; ++c) {
       double g = load(J->log_alpha, J->dt_la, row_k + c);
-      if (J->A_log) {
+      if (J->A_log && J->unbounded) {
+        /* g = -e^{A_h} Softplus(z) */
+        const double eA = (mut == MUT_UNB_NO_EXP) ? J->A_log[h] : exp(J->A_log[h]);
+        if (mut == MUT_UNB_BOUNDED) g = -5.0 / (1.0 + exp(-eA * g));
+        else g = (mut == MUT_UNB_SIGN ? 1.0 : -1.0) * eA * softplus(g);
+      } else if (J->A_log) {
         /* g = g_min Sigmoid(e^{A_h} z); lb holds g_min */
         const double x = (mut == MUT_GATE_NO_EXP) ? J->A_log[h] * g : exp(J->A_log[h]) * g;
         if (mut == MUT_GATE_SOFTPLUS) g = -exp(J->A_log[h]) * log1p(exp(g));
@@ -185,7 +200,7 @@ static void *worker(void *arg) {
  * With A_log non-NULL (one double per head) log_alpha holds the decay logits z
  * and lower_bound is g_min of the gated form. */
 static int oracle_run(const void *q, const void *k, int dt_qk, const void *v, int dt_v,
-                      const void *log_alpha, int dt_la, const double *A_log, const void *beta,
+                      const void *log_alpha, int dt_la, const double *A_log, int unbounded, const void *beta,
                       int dt_beta, const int64_t *cu_seqlens, int64_t num_seqs, int64_t H, int64_t dk,
                       int64_t dv, double lower_bound, double scale, const void *init_state,
                       int dt_init, double *out, double *final_state, int num_threads, int mutation) {
@@ -199,6 +214,7 @@ static int oracle_run(const void *q, const void *k, int dt_qk, const void *v, in
   memset(&J, 0, sizeof J);
   J.q = q; J.k = k; J.v = v; J.log_alpha = log_alpha; J.beta = beta; J.init = init_state;
   J.A_log = A_log;
+  J.unbounded = unbounded;
   J.dt_qk = dt_qk; J.dt_v = dt_v; J.dt_la = dt_la; J.dt_beta = dt_beta; J.dt_init = dt_init;
   J.cu = cu_seqlens; J.num_seqs = num_seqs; J.H = H; J.dk = dk; J.dv = dv;
   J.lb = lower_bound; J.scale = scale; J.out = out; J.final_state = final_state;
@@ -231,7 +247,7 @@ int kda_oracle_recurrent_mutant(const void *q, const void *k, int dt_qk, const v
                                 const void *init_state, int dt_init, double *out,
                                 double *final_state, int num_threads, int mutation) {
   if (mutation >= MUT_GATE_NO_EXP) return 1;
-  return oracle_run(q, k, dt_qk, v, dt_v, log_alpha, dt_la, NULL, beta, dt_beta, cu_seqlens,
+  return oracle_run(q, k, dt_qk, v, dt_v, log_alpha, dt_la, NULL, 0, beta, dt_beta, cu_seqlens,
                     num_seqs, H, dk, dv, lower_bound, scale, init_state, dt_init, out, final_state,
                     num_threads, mutation);
 }
@@ -254,8 +270,23 @@ int kda_oracle_recurrent_gated(const void *q, const void *k, int dt_qk, const vo
                                const void *init_state, int dt_init, double *out,
                                double *final_state, int num_threads, int mutation) {
   if (!A_log) return 1;
-  if (mutation != MUT_NONE && mutation < MUT_GATE_NO_EXP && mutation != MUT_NO_DECAY) return 1;
-  return oracle_run(q, k, dt_qk, v, dt_v, z, dt_z, A_log, beta, dt_beta, cu_seqlens, num_seqs, H,
+  if (mutation != MUT_NONE && (mutation < MUT_GATE_NO_EXP || mutation > MUT_GATE_SIGN) &&
+      mutation != MUT_NO_DECAY)
+    return 1;
+  return oracle_run(q, k, dt_qk, v, dt_v, z, dt_z, A_log, 0, beta, dt_beta, cu_seqlens, num_seqs, H,
                     dk, dv, g_min, scale, init_state, dt_init, out, final_state, num_threads,
                     mutation);
+}
+
+/* The unbounded form: z [T_tot, H, d_k] decay logits, A_log [H]; g = -e^{A_h} Softplus(z). */
+int kda_oracle_recurrent_unbounded(const void *q, const void *k, int dt_qk, const void *v, int dt_v,
+                                   const void *z, int dt_z, const double *A_log, const void *beta,
+                                   int dt_beta, const int64_t *cu_seqlens, int64_t num_seqs,
+                                   int64_t H, int64_t dk, int64_t dv, double scale,
+                                   const void *init_state, int dt_init, double *out,
+                                   double *final_state, int num_threads, int mutation) {
+  if (!A_log) return 1;
+  if (mutation != MUT_NONE && mutation < MUT_UNB_NO_EXP && mutation != MUT_NO_DECAY) return 1;
+  return oracle_run(q, k, dt_qk, v, dt_v, z, dt_z, A_log, 1, beta, dt_beta, cu_seqlens, num_seqs, H,
+                    dk, dv, 0.0, scale, init_state, dt_init, out, final_state, num_threads, mutation);
 }

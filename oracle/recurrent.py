@@ -7,7 +7,8 @@ section 1.1, ``S_t = (I - b_t k_t k_t^T) Diag(a_t) S_{t-1} + b_t k_t v_t^T``,
 ``o_t = S_t^T q_t``, with ``log a_t`` clamped below at ``lower_bound``
 (section 1.2), or, in the gated form of section 1.2 (the K3 row of its mapping
 table), computed from decay logits ``z`` and per-head log-scales ``A_h`` as
-``g = g_min * Sigmoid(e^{A_h} z)``.
+``g = g_min * Sigmoid(e^{A_h} z)``, or, in the unbounded form of the earlier
+models (the table's other row), as ``g = -e^{A_h} Softplus(z)``.
 """
 
 from __future__ import annotations
@@ -42,6 +43,13 @@ GATE_MUTATIONS = {
     "gate_no_exp": 8,
     "gate_softplus": 9,
     "gate_sign": 10,
+}
+
+# planted mistakes of the unbounded form, understood by kda_recurrent_unbounded(mutation=...)
+UNBOUNDED_MUTATIONS = {
+    "unbounded_no_exp": 11,
+    "unbounded_sign": 12,
+    "unbounded_bounded_map": 13,
 }
 
 _lock = threading.Lock()
@@ -80,6 +88,10 @@ def _load():
             fg.argtypes = [vp, vp, i32, vp, i32, vp, i32, vp, vp, i32, vp, i64, i64, i64, i64,
                            f64, f64, vp, i32, vp, vp, i32, i32]
             fg.restype = i32
+            fu = lib.kda_oracle_recurrent_unbounded
+            fu.argtypes = [vp, vp, i32, vp, i32, vp, i32, vp, vp, i32, vp, i64, i64, i64, i64,
+                           f64, vp, i32, vp, vp, i32, i32]
+            fu.restype = i32
             _lib = lib
     return _lib
 
@@ -162,6 +174,15 @@ def kda_recurrent(q, k, v, log_alpha, beta, cu_seqlens, *, lower_bound: float = 
                                 num_threads=num_threads)
 
 
+def kda_recurrent_unbounded(q, k, v, z, A_log, beta, cu_seqlens, *, scale: float = 1.0, init_state=None,
+                            num_threads: int | None = None, mutation: int = 0):
+    """fp64 KDA recurrence with the unbounded log-decay ``g = -e^{A_h} Softplus(z)`` of the earlier
+    models (Kimi K3 -- Architecture Notes, section 1.2, the GDN / Mamba-2 / Kimi Linear row of the
+    mapping table). Arguments as in ``kda_recurrent_gated`` (no g_min); ``mutation`` may be one of
+    ``UNBOUNDED_MUTATIONS``."""
+    return _run_gate(q, k, v, z, A_log, beta, cu_seqlens, None, scale, init_state, num_threads, mutation)
+
+
 def kda_recurrent_gated(q, k, v, z, A_log, beta, cu_seqlens, *, g_min: float = -5.0, scale: float = 1.0,
                         init_state=None, num_threads: int | None = None, mutation: int = 0):
     """fp64 KDA recurrence with the gated log-decay ``g = g_min * Sigmoid(e^{A_h} z)``.
@@ -170,6 +191,11 @@ def kda_recurrent_gated(q, k, v, z, A_log, beta, cu_seqlens, *, g_min: float = -
     ``kda_recurrent_mutant``. ``mutation`` may be one of ``GATE_MUTATIONS`` (or 1, no decay).
     Returns (out [T_tot, H, d_v], final_state [N, H, d_k, d_v]) as float64.
     """
+    return _run_gate(q, k, v, z, A_log, beta, cu_seqlens, g_min, scale, init_state, num_threads, mutation)
+
+
+def _run_gate(q, k, v, z, A_log, beta, cu_seqlens, g_min, scale, init_state, num_threads, mutation):
+    """Both gated forms: the bounded map with ``g_min``, the unbounded one when it is None."""
     lib = _load()
     qa, dt_qk = _as_array(q)
     ka, dt_k = _as_array(k)
@@ -207,9 +233,14 @@ def kda_recurrent_gated(q, k, v, z, A_log, beta, cu_seqlens, *, g_min: float = -
     def ptr(a):
         return None if a is None else a.ctypes.data
 
-    rc = lib.kda_oracle_recurrent_gated(
-        ptr(qa), ptr(ka), dt_qk, ptr(va), dt_v, ptr(za), dt_z, ptr(aa), ptr(ba), dt_b, ptr(cu), N, H, dk, dv,
-        float(g_min), float(scale), ptr(ia), dt_i, ptr(out), ptr(final), int(nt), int(mutation))
+    if g_min is None:
+        rc = lib.kda_oracle_recurrent_unbounded(
+            ptr(qa), ptr(ka), dt_qk, ptr(va), dt_v, ptr(za), dt_z, ptr(aa), ptr(ba), dt_b, ptr(cu), N, H, dk, dv,
+            float(scale), ptr(ia), dt_i, ptr(out), ptr(final), int(nt), int(mutation))
+    else:
+        rc = lib.kda_oracle_recurrent_gated(
+            ptr(qa), ptr(ka), dt_qk, ptr(va), dt_v, ptr(za), dt_z, ptr(aa), ptr(ba), dt_b, ptr(cu), N, H, dk, dv,
+            float(g_min), float(scale), ptr(ia), dt_i, ptr(out), ptr(final), int(nt), int(mutation))
     if rc != 0:
-        raise RuntimeError(f"kda_oracle_recurrent_gated failed with code {rc}")
+        raise RuntimeError(f"the gated oracle failed with code {rc}")
     return out, final

@@ -131,3 +131,63 @@ def test_gated_oracle_rejects_bad_arguments():
         kda_recurrent_gated(q, k, v, np.zeros_like(q), np.zeros(3), b, cu)  # A_log must be [H]
     with pytest.raises(RuntimeError):
         kda_recurrent_gated(q, k, v, np.zeros_like(q), np.zeros(2), b, cu, mutation=3)  # not a gate mutation
+
+
+# --- the unbounded form g = -e^{A_h} Softplus(z) (the mapping table's other row) ---------------
+
+from oracle import UNBOUNDED_MUTATIONS, kda_recurrent_unbounded  # noqa: E402
+
+NO_BOUND = -1.0e300  # a clamp no finite log-decay reaches
+
+
+def _unbounded(mutation):
+    def run(q, k, v, z, A, b, cu, S0):
+        return kda_recurrent_unbounded(q, k, v, z, A, b, cu, init_state=S0, num_threads=2, mutation=mutation)
+    return run
+
+
+def _plain(q, k, v, g, b, cu, S0):
+    return kda_recurrent(q, k, v, g, b, cu, lower_bound=NO_BOUND, init_state=S0, num_threads=2)
+
+
+def pin_unbounded_closed_forms(run):
+    """Softplus(0) = ln 2, Softplus(ln(e - 1)) = 1, Softplus(ln 3) = 2 ln 2: g = -e^{A_h} times these,
+    per head; with A_h = ln 3 and z = ln 3 the decay is 6 ln 2 (alpha = 1/64), far below -5."""
+    rng = np.random.default_rng(30)
+    q, k, v, b, cu, S0 = _problem(rng, 17, 3, 6, 5)
+    zs = np.array([0.0, np.log(np.e - 1.0), np.log(3.0)])
+    A = np.array([0.0, -1.0, np.log(3.0)])
+    z = np.broadcast_to(zs[rng.integers(0, 3, size=q.shape)], q.shape).copy()
+    sp = np.where(z == 0.0, np.log(2.0), np.where(z == np.log(3.0), 2.0 * np.log(2.0), 1.0))
+    g = -np.exp(A)[None, :, None] * sp
+    _close(run(q, k, v, z, A, b, cu, S0), _plain(q, k, v, g, b, cu, S0), 1e-14)
+
+
+def pin_unbounded_limits(run):
+    """z -> -inf gives g = 0 (alpha = 1); for large z, Softplus(z) = z to fp64 precision, so
+    g = -e^{A_h} z: at z = 40, A_h = 0 that is alpha = e^-40, a decay no bound of -5 allows."""
+    rng = np.random.default_rng(31)
+    q, k, v, b, cu, S0 = _problem(rng, 13, 2, 5, 4)
+    z = np.where(rng.standard_normal(q.shape) > 0, -800.0, 40.0)
+    A = np.array([0.0, 0.0])
+    g = np.where(z < 0, 0.0, -40.0)
+    _close(run(q, k, v, z, A, b, cu, S0), _plain(q, k, v, g, b, cu, S0), 1e-13)
+
+
+UNBOUNDED_PINS = [pin_unbounded_closed_forms, pin_unbounded_limits]
+
+
+@pytest.mark.parametrize("pin", UNBOUNDED_PINS, ids=lambda p: p.__name__)
+def test_unbounded_pins(pin):
+    pin(_unbounded(0))
+
+
+@pytest.mark.parametrize("name", sorted(UNBOUNDED_MUTATIONS))
+def test_planted_unbounded_mistake_is_caught(name):
+    failed = []
+    for pin in UNBOUNDED_PINS:
+        try:
+            pin(_unbounded(UNBOUNDED_MUTATIONS[name]))
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"no pin caught {name}"
