@@ -172,10 +172,17 @@ def prefill_traffic():
     return rec.get("bytes_per_launch") if h.hexdigest() == rec.get("sources_sha256") else None
 
 
-def time_prefill(case, steps, warmup, world, gated=False, out_gate=False):
+def time_prefill(case, steps, warmup, world, gated=False, out_gate=False, unbounded=False):
     from kimi_delta_attention_02_gb300 import binding
     out_dtype = torch.float32
-    if out_gate:  # gated decay, output gate, bf16 output: the parameter-block entry point
+    if unbounded:  # the earlier models' unbounded decay map: the token-recurrent kernel
+        args = ()
+
+        def fn(out, final_state, stream):
+            binding.prefill_ex(case.q, case.k, case.v, case.beta, case.cu_seqlens, z=case.z, A_log=case.A_log,
+                               init_state=case.init_state, unbounded=True, out=out, final_state=final_state,
+                               stream=stream)
+    elif out_gate:  # gated decay, output gate, bf16 output: the parameter-block entry point
         out_dtype = torch.bfloat16
         args = ()
 
@@ -366,7 +373,7 @@ def main():
     with ClockSampler(local) as clocks:
         total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world)
         dec_ms = None if args.prefill_only else time_decode(DECODE["steps"], 1, 1, world, seed=rank)
-        gated_ms = outgate_ms = prologue_ms = None
+        gated_ms = outgate_ms = prologue_ms = unbounded_ms = None
         if not args.prefill_only and args.heads == PREFILL["H"]:
             gcase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
             _, g_launch = time_prefill(gcase, args.steps, args.warmup, world, gated=True)
@@ -378,6 +385,10 @@ def main():
             del ocase
             p_launch = time_prologue(args.steps, args.warmup, world, seed=rank)
             prologue_ms = sum(p_launch) / len(p_launch)
+            ucase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
+            _, u_launch = time_prefill(ucase, 3, 1, world, unbounded=True)  # a few ms per launch
+            unbounded_ms = sum(u_launch) / len(u_launch)
+            del ucase
     if args.prefill_only:
         if rank == 0:
             print(json.dumps({"prefill_only": True, "heads": H, "ms_per_step": total_ms / args.steps,
@@ -418,6 +429,12 @@ def main():
         p_gbs = p_bytes / (prologue_ms / 1e3) / 1e9
         prologue = {"workload": "prologue_k3_T4096_H96", "launch_ms": prologue_ms, "GB/s": p_gbs, "peak": hbm_gbs,
                     "frac": p_gbs / hbm_gbs, "alg_bytes": p_bytes, "tokens_per_s": world * T / (prologue_ms / 1e3)}
+    unbounded = None
+    if unbounded_ms is not None:
+        unbounded = {"workload": "prefill_k3_gated_T4096_H96 through g = -e^A Softplus(z)",
+                     "kernel": "token-recurrent (the chunked kernels need a bounded decay)",
+                     "launch_ms": unbounded_ms, "tokens_per_s": world * T / (unbounded_ms / 1e3),
+                     "vs_bounded_chunked": (gated_ms / unbounded_ms) if gated_ms else None}
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     dec_bytes = DECODE["B"] * DECODE["H"] * DECODE_BYTES_PER_SEQ_HEAD
     dec_gbs = dec_bytes / (dec_avg_ms / 1e3) / 1e9
@@ -459,6 +476,7 @@ def main():
             "gated_decay": gated,
             "output_gate": outgate,
             "prologue": prologue,
+            "unbounded_decay": unbounded,
             "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk,
             "gpu_launches": args.steps,  # one prefill launch per timed step (decode: its own region)
         }

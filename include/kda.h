@@ -186,7 +186,13 @@ kda_status kda_decode_gated(const void *q, const void *k, const void *v, const v
  *   decay_form    KDA_DECAY_CLAMPED: `decay` is log_alpha (fp32), A_log must be
  *                 NULL and decay_bound is the lower bound; KDA_DECAY_GATED:
  *                 `decay` is the logits z (in_dtype), A_log [H] and decay_bound
- *                 = g_min as in kda_prefill_gated
+ *                 = g_min as in kda_prefill_gated; KDA_DECAY_UNBOUNDED: the map
+ *                 of the earlier models in the same section's table,
+ *                 g = -e^{A_h} * Softplus(z), Softplus(x) = log(1 + e^x), from the
+ *                 logits z (in_dtype) and A_log [H]; decay_bound is ignored. Its
+ *                 decay has no lower bound, so the chunked tensor-core kernel (which
+ *                 needs one) does not take it: a prefill runs the fp32
+ *                 token-recurrent kernel
  *   out_gate      gate logits r [rows, H, d_v] in in_dtype, device, 16-byte
  *                 aligned, not overlapping `out`; NULL = no output gate (out = o)
  *   norm_weight   w [d_v] fp32, device; NULL = ones. Must be NULL without out_gate
@@ -199,7 +205,7 @@ kda_status kda_decode_gated(const void *q, const void *k, const void *v, const v
  * the token-recurrent kernel and decode); it adds one read of the gate logits
  * and no other memory traffic.
  */
-typedef enum { KDA_DECAY_CLAMPED = 0, KDA_DECAY_GATED = 1 } kda_decay_form;
+typedef enum { KDA_DECAY_CLAMPED = 0, KDA_DECAY_GATED = 1, KDA_DECAY_UNBOUNDED = 2 } kda_decay_form;
 
 typedef struct kda_prefill_params {
   uint32_t struct_size;

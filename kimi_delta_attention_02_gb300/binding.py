@@ -27,7 +27,7 @@ _lock = threading.Lock()
 _lib = None
 
 
-KDA_DECAY_CLAMPED, KDA_DECAY_GATED = 0, 1
+KDA_DECAY_CLAMPED, KDA_DECAY_GATED, KDA_DECAY_UNBOUNDED = 0, 1, 2
 
 
 class PrefillParams(ctypes.Structure):
@@ -201,8 +201,9 @@ def prefill_gated(q, k, v, z, A_log, beta, cu_seqlens, init_state=None, *, out=N
     return out, final_state
 
 
-def _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min):
-    """(decay_form, decay tensor, A_log, bound) for exactly one of log_alpha or (z, A_log)."""
+def _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min, unbounded=False):
+    """(decay_form, decay tensor, A_log, bound) for exactly one of log_alpha or (z, A_log); with
+    ``unbounded`` the logits go through the unbounded map g = -e^{A_h} Softplus(z)."""
     if (log_alpha is None) == (z is None):
         raise ValueError("pass exactly one of log_alpha (clamped form) or z with A_log (gated form)")
     if log_alpha is not None:
@@ -215,22 +216,24 @@ def _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min):
         raise TypeError("the gated form needs A_log [H] float32")
     if z.dtype != q.dtype:
         raise TypeError("z must have the dtype of q")
-    return KDA_DECAY_GATED, z, A_log, float(g_min)
+    return (KDA_DECAY_UNBOUNDED if unbounded else KDA_DECAY_GATED), z, A_log, float(g_min)
 
 
 def prefill_ex(q, k, v, beta, cu_seqlens, *, log_alpha=None, lower_bound: float = -5.0, z=None, A_log=None,
                g_min: float = -5.0, init_state=None, out_gate=None, norm_weight=None, norm_eps: float = 1e-6,
                out=None, final_state=None, out_dtype=torch.float32, scale: float = 1.0, stream=None,
-               recurrent: bool = False, want_final: bool = True):
+               recurrent: bool = False, want_final: bool = True, unbounded: bool = False):
     """Prefill through the parameter block (``kda_prefill_ex``): the clamped (``log_alpha``) or
     gated (``z``, ``A_log``) log-decay, and optionally the output gate with head-wise RMSNorm,
     ``out = Sigmoid(out_gate) * norm_weight * o / sqrt(mean(o^2) + norm_eps)`` per token and head.
+    ``unbounded=True`` (with z, A_log) takes the earlier models' map g = -e^{A_h} Softplus(z),
+    which runs on the token-recurrent kernel.
     out_gate [T, H, d_v] in the dtype of q; norm_weight [d_v] float32 or None (ones).
     Returns (out, final_state or None)."""
     T, H, d_k = q.shape
     d_v = v.shape[-1]
     N = cu_seqlens.shape[0] - 1
-    form, decay, A, bound = _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min)
+    form, decay, A, bound = _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min, unbounded)
     if k.dtype != q.dtype or v.dtype != q.dtype:
         raise TypeError("q, k and v must share one dtype")
     if out_gate is not None and out_gate.dtype != q.dtype:
@@ -263,7 +266,7 @@ def prefill_ex(q, k, v, beta, cu_seqlens, *, log_alpha=None, lower_bound: float 
 def decode_ex(q, k, v, beta, state, *, log_alpha=None, lower_bound: float = -5.0, z=None, A_log=None,
               g_min: float = -5.0, out_gate=None, norm_weight=None, norm_eps: float = 1e-6, conv_weight=None,
               conv_state=None, l2_eps: float = 1e-6, out=None, out_dtype=torch.float32, scale: float = 1.0,
-              stream=None):
+              stream=None, unbounded: bool = False):
     """One decode step through the parameter block (``kda_decode_ex``); ``state`` is updated in
     place. Decay and output-gate options as in ``prefill_ex``. With ``conv_state`` [B, H, 3,
     2 d_k + d_v] (dtype of q; shifted in place) and ``conv_weight`` [H, 2 d_k + d_v, 4] float32,
@@ -271,7 +274,7 @@ def decode_ex(q, k, v, beta, state, *, log_alpha=None, lower_bound: float = -5.0
     Returns out [B, H, d_v]."""
     B, H, d_k = q.shape
     d_v = v.shape[-1]
-    form, decay, A, bound = _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min)
+    form, decay, A, bound = _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min, unbounded)
     if out_gate is not None and out_gate.dtype != q.dtype:
         raise TypeError("out_gate must have the dtype of q")
     if out is None:

@@ -36,20 +36,20 @@ uint32_t *device_error_word() {
 // Each launcher takes the decay input as `decay` + `A_log`: log_alpha (fp32) with A_log null
 // (the clamped form), or the gated form's logits z (input dtype) with A_log [H]; and the output
 // gate as `out_gate` (gate logits, input dtype; null = plain read-out) + `norm_weight` + `norm_eps`.
-cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
-                          const float *beta, float *state, const void *out_gate, const float *norm_weight,
-                          float norm_eps, const float *conv_w, void *conv_state, float l2_eps, void *out, int B,
-                          int H, int d_k, int d_v, bool in_bf16, bool out_bf16, float lb, float scale,
-                          cudaStream_t stream);
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, int decay_form,
+                          const float *A_log, const float *beta, float *state, const void *out_gate,
+                          const float *norm_weight, float norm_eps, const float *conv_w, void *conv_state,
+                          float l2_eps, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
+                          float lb, float scale, cudaStream_t stream);
 cudaError_t launch_prologue(const void *q_raw, const void *k_raw, const void *v_raw, const float *conv_w,
                             const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H, int d_k, int d_v,
                             bool bf16, const void *conv_init, float eps, void *q, void *k, void *v,
                             void *conv_final, cudaStream_t stream);
-cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
-                             const float *beta, const int32_t *cu_seqlens, int num_seqs, int H, int d_k, int d_v,
-                             bool in_bf16, bool out_bf16, float lb, float scale, const float *init_state,
-                             const void *out_gate, const float *norm_weight, float norm_eps, void *out,
-                             float *final_state, cudaStream_t stream);
+cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *decay, int decay_form,
+                             const float *A_log, const float *beta, const int32_t *cu_seqlens, int num_seqs, int H,
+                             int d_k, int d_v, bool in_bf16, bool out_bf16, float lb, float scale,
+                             const float *init_state, const void *out_gate, const float *norm_weight,
+                             float norm_eps, void *out, float *final_state, cudaStream_t stream);
 bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb);
 kda_status launch_chunked(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                           const float *beta, const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H,
@@ -127,7 +127,8 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const void 
                         int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype, float lb,
                         float scale, const float *init_state, void *out, float *final_state, void *stream,
                         bool force_recurrent, const void *out_gate = nullptr, const float *norm_weight = nullptr,
-                        float norm_eps = 0.f) {
+                        float norm_eps = 0.f, int decay_form = -1) {
+  if (decay_form < 0) decay_form = A_log != nullptr ? DECAY_GATED : DECAY_CLAMPED;
   kda_status st = check_out_gate_args(out_gate, norm_weight, norm_eps);
   if (st != KDA_OK) return st;
   st = check_prefill_args(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype,
@@ -136,10 +137,12 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const void 
   if (num_seqs == 0) return KDA_OK;
   if (total_tokens == 0) out_gate = norm_weight = nullptr;  // nothing is read out
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (!force_recurrent && total_tokens > 0 && chunked_supported(d_k, d_v, in_dtype == KDA_BF16, lb))
+  // the chunked kernels need the bounded decay (clamped, or the gated map with g_min >= -5)
+  if (!force_recurrent && total_tokens > 0 && decay_form != DECAY_UNBOUNDED &&
+      chunked_supported(d_k, d_v, in_dtype == KDA_BF16, lb))
     return launch_chunked(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, out_dtype == KDA_BF16,
                           lb, scale, init_state, out_gate, norm_weight, norm_eps, out, final_state, s);
-  const cudaError_t err = launch_recurrent(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, H, d_k, d_v,
+  const cudaError_t err = launch_recurrent(q, k, v, decay, decay_form, A_log, beta, cu_seqlens, num_seqs, H, d_k, d_v,
                                            in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale, init_state,
                                            out_gate, norm_weight, norm_eps, out, final_state, s);
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
@@ -157,7 +160,9 @@ kda_status decode_impl(const void *q, const void *k, const void *v, const void *
                        const float *beta, float *state, void *out, int32_t B, int32_t H, int32_t d_k, int32_t d_v,
                        kda_dtype in_dtype, kda_dtype out_dtype, float lb, float scale, void *stream,
                        const void *out_gate = nullptr, const float *norm_weight = nullptr, float norm_eps = 0.f,
-                       const float *conv_weight = nullptr, void *conv_state = nullptr, float l2_eps = 0.f) {
+                       const float *conv_weight = nullptr, void *conv_state = nullptr, float l2_eps = 0.f,
+                       int decay_form = -1) {
+  if (decay_form < 0) decay_form = A_log != nullptr ? DECAY_GATED : DECAY_CLAMPED;
   if (in_dtype != KDA_F32 && in_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (out_dtype != KDA_F32 && out_dtype != KDA_BF16) return KDA_ERR_INVALID_ARG;
   if (B < 1 || H < 1 || d_k < 1 || d_v < 1) return KDA_ERR_INVALID_ARG;
@@ -186,16 +191,18 @@ kda_status decode_impl(const void *q, const void *k, const void *v, const void *
   } else if (conv_weight != nullptr) {
     return KDA_ERR_INVALID_ARG;  // weights without a state
   }
-  const cudaError_t err = launch_decode(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps,
+  const cudaError_t err = launch_decode(q, k, v, decay, decay_form, A_log, beta, state, out_gate, norm_weight, norm_eps,
                                         conv_weight, conv_state, l2_eps, out, B, H, d_k, d_v, in_dtype == KDA_BF16,
                                         out_dtype == KDA_BF16, lb, scale, static_cast<cudaStream_t>(stream));
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-// the decay form of a parameter block: the clamped form takes no A_log, the gated one needs it
+// the decay form of a parameter block: the clamped form takes no A_log, the gated ones need it
+// (the unbounded one has no bound to check)
 kda_status check_decay_form(kda_decay_form form, const float *A_log, float bound) {
   if (form == KDA_DECAY_CLAMPED) return A_log == nullptr ? KDA_OK : KDA_ERR_INVALID_ARG;
   if (form == KDA_DECAY_GATED) return check_gate_args(A_log, bound);
+  if (form == KDA_DECAY_UNBOUNDED) return (A_log != nullptr && aligned4(A_log)) ? KDA_OK : KDA_ERR_INVALID_ARG;
   return KDA_ERR_INVALID_ARG;
 }
 
@@ -268,7 +275,7 @@ kda_status kda_prefill_ex(const kda_prefill_params *p, void *stream) {
   return prefill_impl(p->q, p->k, p->v, p->decay, p->A_log, p->beta, p->cu_seqlens, p->num_seqs, p->total_tokens,
                       p->H, p->d_k, p->d_v, p->in_dtype, p->out_dtype, p->decay_bound, p->scale, p->init_state,
                       p->out, p->final_state, stream, p->force_recurrent != 0, p->out_gate, p->norm_weight,
-                      p->norm_eps);
+                      p->norm_eps, int(p->decay_form));
 }
 
 kda_status kda_decode_ex(const kda_decode_params *p, void *stream) {
@@ -277,7 +284,7 @@ kda_status kda_decode_ex(const kda_decode_params *p, void *stream) {
   if (st != KDA_OK) return st;
   return decode_impl(p->q, p->k, p->v, p->decay, p->A_log, p->beta, p->state, p->out, p->B, p->H, p->d_k, p->d_v,
                      p->in_dtype, p->out_dtype, p->decay_bound, p->scale, stream, p->out_gate, p->norm_weight,
-                     p->norm_eps, p->conv_weight, p->conv_state, p->l2_eps);
+                     p->norm_eps, p->conv_weight, p->conv_state, p->l2_eps, int(p->decay_form));
 }
 
 kda_status kda_prologue(const void *q_raw, const void *k_raw, const void *v_raw, const float *conv_weight,

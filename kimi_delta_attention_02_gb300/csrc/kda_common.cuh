@@ -174,6 +174,16 @@ __device__ __forceinline__ float lane_sums(float (&v)[N], int lane) {
   return s;
 }
 
+// The unbounded log-decay of the earlier models (Kimi K3 -- Architecture Notes, section 1.2,
+// the GDN / Mamba-2 / Kimi Linear row of the mapping table): g = -e^{A_h} Softplus(z), with
+// Softplus(z) = max(z, 0) + log(1 + e^{-|z|}) (no overflow for large |z|); a NaN stays NaN.
+__device__ __forceinline__ float unbounded_log_decay(float z, float a_h) {
+  return -a_h * (fmaxf(z, 0.f) + __logf(1.f + __expf(-fabsf(z))));
+}
+
+// Decay forms of the token-recurrent and decode kernels.
+enum : int { DECAY_CLAMPED = 0, DECAY_GATED = 1, DECAY_UNBOUNDED = 2 };
+
 // ---------------------------------------------------------------------------
 // Shared-memory addresses and fences
 // ---------------------------------------------------------------------------

@@ -34,7 +34,7 @@ struct Prologue {
   float eps;
 };
 
-template <bool kInBF16, bool kOutBF16, bool kGated, bool kNormGate, bool kPrologue>
+template <bool kInBF16, bool kOutBF16, int kDecay, bool kNormGate, bool kPrologue>
 __global__ void __launch_bounds__(kDecodeThreads, 2)
     kda_decode_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                       const void *__restrict__ decay, const float *__restrict__ A_log,
@@ -112,9 +112,14 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   }
   if (tid < 128) {
     float a = 0.f;
-    if (tid < d_k)
-      a = __expf(kGated ? gated_log_decay(load_elem<kInBF16>(decay, vec_base + tid), __expf(A_log[bh % H]), lb)
-                        : clamp_log_decay(static_cast<const float *>(decay)[vec_base + tid], lb));
+    if (tid < d_k) {
+      if constexpr (kDecay == DECAY_CLAMPED)
+        a = __expf(clamp_log_decay(static_cast<const float *>(decay)[vec_base + tid], lb));
+      else if constexpr (kDecay == DECAY_GATED)
+        a = __expf(gated_log_decay(load_elem<kInBF16>(decay, vec_base + tid), __expf(A_log[bh % H]), lb));
+      else
+        a = __expf(unbounded_log_decay(load_elem<kInBF16>(decay, vec_base + tid), __expf(A_log[bh % H])));
+    }
     s_k[tid] = kk;
     s_q[tid] = qq;
     s_a[tid] = a;
@@ -189,27 +194,28 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   }
 }
 
-// decay: log_alpha (fp32) when A_log is null, else the gated form's logits z (input dtype).
+// decay: log_alpha (fp32) for DECAY_CLAMPED, else the gated forms' logits z (input dtype) with A_log.
 // out_gate: gate logits [B, H, d_v] (input dtype) of the output gate, or null (out = o).
 // conv_w / conv_state: the prologue's weights and state, or null (q, k, v used as given).
-cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
-                          const float *beta, float *state, const void *out_gate, const float *norm_weight,
-                          float norm_eps, const float *conv_w, void *conv_state, float l2_eps, void *out, int B,
-                          int H, int d_k, int d_v, bool in_bf16, bool out_bf16, float lb, float scale,
-                          cudaStream_t stream) {
+cudaError_t launch_decode(const void *q, const void *k, const void *v, const void *decay, int decay_form,
+                          const float *A_log, const float *beta, float *state, const void *out_gate,
+                          const float *norm_weight, float norm_eps, const float *conv_w, void *conv_state,
+                          float l2_eps, void *out, int B, int H, int d_k, int d_v, bool in_bf16, bool out_bf16,
+                          float lb, float scale, cudaStream_t stream) {
   const dim3 grid(unsigned(int64_t(B) * H)), block(kDecodeThreads);
-  using Kern = decltype(&kda_decode_kernel<false, false, false, false, false>);
-#define KDA_DEC_ROW(ng, pr)                                                                                    \
-  kda_decode_kernel<false, false, false, ng, pr>, kda_decode_kernel<false, false, true, ng, pr>,               \
-      kda_decode_kernel<false, true, false, ng, pr>, kda_decode_kernel<false, true, true, ng, pr>,             \
-      kda_decode_kernel<true, false, false, ng, pr>, kda_decode_kernel<true, false, true, ng, pr>,             \
-      kda_decode_kernel<true, true, false, ng, pr>, kda_decode_kernel<true, true, true, ng, pr>
-  static const Kern table[32] = {KDA_DEC_ROW(false, false), KDA_DEC_ROW(true, false), KDA_DEC_ROW(false, true),
-                                 KDA_DEC_ROW(true, true)};
+  using Kern = decltype(&kda_decode_kernel<false, false, 0, false, false>);
+#define KDA_DEC_ROW(ib, ob, ng, pr) \
+  kda_decode_kernel<ib, ob, 0, ng, pr>, kda_decode_kernel<ib, ob, 1, ng, pr>, kda_decode_kernel<ib, ob, 2, ng, pr>
+#define KDA_DEC_BLOCK(ng, pr)                                                                        \
+  KDA_DEC_ROW(false, false, ng, pr), KDA_DEC_ROW(false, true, ng, pr), KDA_DEC_ROW(true, false, ng, pr), \
+      KDA_DEC_ROW(true, true, ng, pr)
+  static const Kern table[48] = {KDA_DEC_BLOCK(false, false), KDA_DEC_BLOCK(true, false),
+                                 KDA_DEC_BLOCK(false, true), KDA_DEC_BLOCK(true, true)};
+#undef KDA_DEC_BLOCK
 #undef KDA_DEC_ROW
   const bool pro = conv_state != nullptr;
-  const Kern kern = table[16 * int(pro) + 8 * int(out_gate != nullptr) + 4 * int(in_bf16) + 2 * int(out_bf16) +
-                          int(A_log != nullptr)];
+  const Kern kern = table[24 * int(pro) + 12 * int(out_gate != nullptr) + 6 * int(in_bf16) + 3 * int(out_bf16) +
+                          decay_form];
   const Prologue pr{conv_w, conv_state, l2_eps};
   kern<<<grid, block, 0, stream>>>(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps, pr, out, H,
                                    d_k, d_v, lb, scale);

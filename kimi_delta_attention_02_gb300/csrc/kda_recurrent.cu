@@ -11,9 +11,10 @@
 // 32 (kCG slice + w / 4) + l; the reductions over key rows go through shared
 // memory. Token t+1's inputs are fetched while token t is computed. It handles
 // every supported shape and both dtypes; the tensor-core chunked kernels are the
-// fast path for bf16, d = 128. The log-decay is either the clamped log_alpha input
-// or, in the gated form (section 1.2), g = g_min * Sigmoid(e^{A_h} z) from decay
-// logits z in the input dtype.
+// fast path for bf16, d = 128. The log-decay is the clamped log_alpha input, or, in
+// the gated form (section 1.2), g = g_min * Sigmoid(e^{A_h} z) from decay logits z in
+// the input dtype, or the unbounded g = -e^{A_h} Softplus(z) of the earlier models,
+// which only this kernel and decode accept (the chunked kernels need the bound).
 //
 // With the output gate of section 1.3 a CTA holds all value columns of its chain
 // (kCG = 4, 16 warps), so that the RMS of a token's read-out over its d_v channels
@@ -24,7 +25,7 @@ namespace kda {
 
 constexpr int kRecCols = 32;  // value columns per column group
 
-template <bool kInBF16, bool kOutBF16, bool kGated, bool kNormGate>
+template <bool kInBF16, bool kOutBF16, int kDecay, bool kNormGate>
 __global__ void __launch_bounds__(kNormGate ? 512 : 128)
     kda_recurrent_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                          const void *__restrict__ decay, const float *__restrict__ A_log,
@@ -50,7 +51,8 @@ __global__ void __launch_bounds__(kNormGate ? 512 : 128)
   const int col = slice * kCols + lc;
   const bool col_ok = col < d_v;
   const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
-  const float a_h = kGated ? __expf(A_log[h]) : 0.f;  // e^{A_h} of the gated form
+  constexpr bool kGated = kDecay != DECAY_CLAMPED;   // log-decay from logits z
+  const float a_h = kGated ? __expf(A_log[h]) : 0.f;  // e^{A_h} of the gated forms
   const float w_norm = (kNormGate && norm_weight != nullptr && col_ok) ? norm_weight[col] : 1.f;
 
   // state rows 32 rg + r of column `col`
@@ -88,7 +90,10 @@ __global__ void __launch_bounds__(kNormGate ? 512 : 128)
       const bool ch = tid < d_k;
       s_k[buf][tid] = ch ? pk : 0.f;
       s_q[buf][tid] = ch ? pq : 0.f;
-      s_a[buf][tid] = ch ? __expf(kGated ? gated_log_decay(pla, a_h, lb) : clamp_log_decay(pla, lb)) : 0.f;
+      s_a[buf][tid] = ch ? __expf(kDecay == DECAY_UNBOUNDED ? unbounded_log_decay(pla, a_h)
+                                  : kDecay == DECAY_GATED   ? gated_log_decay(pla, a_h, lb)
+                                                            : clamp_log_decay(pla, lb))
+                         : 0.f;
       float kq = ch ? pk * pq : 0.f;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
@@ -159,26 +164,26 @@ __global__ void __launch_bounds__(kNormGate ? 512 : 128)
   }
 }
 
-// decay: log_alpha (fp32) when A_log is null, else the gated form's logits z (input dtype).
+// decay: log_alpha (fp32) for DECAY_CLAMPED, else the gated forms' logits z (input dtype) with A_log.
 // out_gate: gate logits [T, H, d_v] (input dtype) of the output gate, or null (out = o).
-cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
-                             const float *beta, const int32_t *cu_seqlens, int num_seqs, int H, int d_k, int d_v,
-                             bool in_bf16, bool out_bf16, float lb, float scale, const float *init_state,
-                             const void *out_gate, const float *norm_weight, float norm_eps, void *out,
-                             float *final_state, cudaStream_t stream) {
+cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const void *decay, int decay_form,
+                             const float *A_log, const float *beta, const int32_t *cu_seqlens, int num_seqs, int H,
+                             int d_k, int d_v, bool in_bf16, bool out_bf16, float lb, float scale,
+                             const float *init_state, const void *out_gate, const float *norm_weight,
+                             float norm_eps, void *out, float *final_state, cudaStream_t stream) {
   const bool norm_gate = out_gate != nullptr;
   const int cols = norm_gate ? 4 * kRecCols : kRecCols;
   const int n_slices = (d_v + cols - 1) / cols;
   const dim3 grid(unsigned(int64_t(num_seqs) * H * n_slices)), block(norm_gate ? 512 : 128);
-  using Kern = decltype(&kda_recurrent_kernel<false, false, false, false>);
-#define KDA_REC_ROW(ng)                                                                              \
-  kda_recurrent_kernel<false, false, false, ng>, kda_recurrent_kernel<false, false, true, ng>,       \
-      kda_recurrent_kernel<false, true, false, ng>, kda_recurrent_kernel<false, true, true, ng>,     \
-      kda_recurrent_kernel<true, false, false, ng>, kda_recurrent_kernel<true, false, true, ng>,     \
-      kda_recurrent_kernel<true, true, false, ng>, kda_recurrent_kernel<true, true, true, ng>
-  static const Kern table[16] = {KDA_REC_ROW(false), KDA_REC_ROW(true)};
+  using Kern = decltype(&kda_recurrent_kernel<false, false, 0, false>);
+#define KDA_REC_ROW(ib, ob, ng) \
+  kda_recurrent_kernel<ib, ob, 0, ng>, kda_recurrent_kernel<ib, ob, 1, ng>, kda_recurrent_kernel<ib, ob, 2, ng>
+#define KDA_REC_BLOCK(ng) \
+  KDA_REC_ROW(false, false, ng), KDA_REC_ROW(false, true, ng), KDA_REC_ROW(true, false, ng), KDA_REC_ROW(true, true, ng)
+  static const Kern table[24] = {KDA_REC_BLOCK(false), KDA_REC_BLOCK(true)};
+#undef KDA_REC_BLOCK
 #undef KDA_REC_ROW
-  const Kern kern = table[8 * int(norm_gate) + 4 * int(in_bf16) + 2 * int(out_bf16) + int(A_log != nullptr)];
+  const Kern kern = table[12 * int(norm_gate) + 6 * int(in_bf16) + 3 * int(out_bf16) + decay_form];
   kern<<<grid, block, 0, stream>>>(q, k, v, decay, A_log, beta, cu_seqlens, init_state, out_gate, norm_weight,
                                    norm_eps, out, final_state, H, d_k, d_v, n_slices, lb, scale);
   return cudaGetLastError();

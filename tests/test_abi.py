@@ -175,6 +175,9 @@ def _prefill_ex(lib, **over):
     (dict(A_log=0xa0000), B.KDA_ERR_INVALID_ARG),                   # A_log with the clamped form
     (dict(decay_form=1), B.KDA_ERR_INVALID_ARG),                    # gated form without A_log
     (dict(decay_form=1, A_log=0xa0000, decay_bound=1.0), B.KDA_ERR_INVALID_ARG),
+    (dict(decay_form=2), B.KDA_ERR_INVALID_ARG),                    # unbounded form without A_log
+    (dict(decay_form=2, A_log=0xa0002), B.KDA_ERR_INVALID_ARG),     # misaligned A_log
+    (dict(decay_form=3, A_log=0xa0000), B.KDA_ERR_INVALID_ARG),
     (dict(out_gate=None), B.KDA_ERR_INVALID_ARG),                   # a weight without gate logits
     (dict(norm_eps=float("nan")), B.KDA_ERR_INVALID_ARG),
     (dict(norm_eps=-1.0), B.KDA_ERR_INVALID_ARG),
@@ -195,6 +198,7 @@ def test_prefill_ex_accepts_empty_work(lib):
     assert _prefill_ex(lib, num_seqs=0, total_tokens=0, q=None, k=None, v=None, decay=None, beta=None, out=None,
                        final_state=None, out_gate=None, norm_weight=None) == B.KDA_OK
     assert _prefill_ex(lib, num_seqs=0, total_tokens=0, decay_form=1, A_log=0xa0000) == B.KDA_OK
+    assert _prefill_ex(lib, num_seqs=0, total_tokens=0, decay_form=2, A_log=0xa0000, decay_bound=7.0) == B.KDA_OK
 
 
 def _decode_ex(lib, **over):
