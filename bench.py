@@ -61,6 +61,9 @@ PROLOGUE_BYTES_PER_TOKEN_HEAD = 1536
 # decode, per (sequence, head): state read + write (131,072) + q,k,v bf16 (768) + log_alpha (512)
 # + beta (4) + out fp32 (512) = 132,868 bytes
 DECODE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4 + 3 * 256 + 512 + 4 + 512
+# fused decode step: state read + write (131,072) + raw q,k,v (768) + z (256) + beta (4) + gate logits
+# (256) + out bf16 (256) + conv state read + write (2 x 3 x 384 x 2 = 4,608) = 137,220 bytes
+FUSED_DECODE_BYTES_PER_SEQ_HEAD = 2 * 128 * 128 * 4 + 3 * 256 + 256 + 4 + 256 + 256 + 2 * 3 * 384 * 2
 
 
 class ClockSampler:
@@ -221,17 +224,31 @@ def time_prefill(case, steps, warmup, world, gated=False, out_gate=False, unboun
     return total_ms, launch_ms
 
 
-def time_decode(steps_per_rep, reps, warmup, world, seed=0):
+def time_decode(steps_per_rep, reps, warmup, world, seed=0, fused=False):
+    """Decode steps on B=256 sequences, H=96. ``fused``: the whole layer step between the
+    projections -- the prologue on raw q, k, v (conv state shifted in place), the gated decay,
+    the recurrence and the output gate (bf16 out) -- in one kernel per step."""
     from kimi_delta_attention_02_gb300 import binding, workloads
     B, H = DECODE["B"], DECODE["H"]
     state = workloads.make_decode_state(B, H, device="cuda", seed=seed)
-    inputs = [workloads.make_decode_step(s, B, H, dtype=torch.bfloat16, device="cuda", seed=seed)
-              for s in range(steps_per_rep)]
-    out = torch.empty((B, H, 128), dtype=torch.float32, device="cuda")
+    inputs = [workloads.make_decode_step(s, B, H, dtype=torch.bfloat16, device="cuda", seed=seed, gated=fused,
+                                         out_gate=fused) for s in range(steps_per_rep)]
+    out = torch.empty((B, H, 128), dtype=torch.bfloat16 if fused else torch.float32, device="cuda")
     stream = torch.cuda.current_stream()
+    if fused:
+        conv_w = workloads.make_conv_weight(H, device="cuda", seed=seed)
+        conv_state = workloads.make_conv_state(B, H, device="cuda", seed=seed)
+
+        def step_fn(st):
+            binding.decode_ex(st.q, st.k, st.v, st.beta, state, z=st.z, A_log=st.A_log, out_gate=st.out_gate,
+                              norm_weight=st.norm_weight, conv_weight=conv_w, conv_state=conv_state, out=out,
+                              stream=stream)
+    else:
+        def step_fn(st):
+            binding.decode(st.q, st.k, st.v, st.log_alpha, st.beta, state, out=out, stream=stream)
     for _ in range(warmup):
         for st in inputs:
-            binding.decode(st.q, st.k, st.v, st.log_alpha, st.beta, state, out=out, stream=stream)
+            step_fn(st)
     binding.check_device_error(stream)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(reps * steps_per_rep)]
@@ -241,7 +258,7 @@ def time_decode(steps_per_rep, reps, warmup, world, seed=0):
     for _ in range(reps):
         for st in inputs:
             ev[i][0].record(stream)
-            binding.decode(st.q, st.k, st.v, st.log_alpha, st.beta, state, out=out, stream=stream)
+            step_fn(st)
             ev[i][1].record(stream)
             i += 1
     torch.cuda.synchronize()
@@ -373,7 +390,7 @@ def main():
     with ClockSampler(local) as clocks:
         total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world)
         dec_ms = None if args.prefill_only else time_decode(DECODE["steps"], 1, 1, world, seed=rank)
-        gated_ms = outgate_ms = prologue_ms = unbounded_ms = None
+        gated_ms = outgate_ms = prologue_ms = unbounded_ms = fdec_ms = None
         if not args.prefill_only and args.heads == PREFILL["H"]:
             gcase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
             _, g_launch = time_prefill(gcase, args.steps, args.warmup, world, gated=True)
@@ -385,6 +402,7 @@ def main():
             del ocase
             p_launch = time_prologue(args.steps, args.warmup, world, seed=rank)
             prologue_ms = sum(p_launch) / len(p_launch)
+            fdec_ms = time_decode(DECODE["steps"], 1, 1, world, seed=rank, fused=True)
             ucase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
             _, u_launch = time_prefill(ucase, 3, 1, world, unbounded=True)  # a few ms per launch
             unbounded_ms = sum(u_launch) / len(u_launch)
@@ -435,6 +453,13 @@ def main():
                      "kernel": "token-recurrent (the chunked kernels need a bounded decay)",
                      "launch_ms": unbounded_ms, "tokens_per_s": world * T / (unbounded_ms / 1e3),
                      "vs_bounded_chunked": (gated_ms / unbounded_ms) if gated_ms else None}
+    fdec = None
+    if fdec_ms is not None:
+        f_avg = sum(fdec_ms) / len(fdec_ms)
+        f_bytes = DECODE["B"] * DECODE["H"] * FUSED_DECODE_BYTES_PER_SEQ_HEAD
+        fdec = {"workload": "decode_B256_H96, prologue + gated decay + output gate, bf16 out",
+                "ms_per_step": f_avg, "GB/s": f_bytes / (f_avg / 1e3) / 1e9, "peak": hbm_gbs,
+                "frac": f_bytes / (f_avg / 1e3) / 1e9 / hbm_gbs, "alg_bytes": f_bytes, "launches": len(fdec_ms)}
     dec_avg_ms = sum(dec_ms) / len(dec_ms)
     dec_bytes = DECODE["B"] * DECODE["H"] * DECODE_BYTES_PER_SEQ_HEAD
     dec_gbs = dec_bytes / (dec_avg_ms / 1e3) / 1e9
@@ -476,6 +501,7 @@ def main():
             "gated_decay": gated,
             "output_gate": outgate,
             "prologue": prologue,
+            "decode_fused": fdec,
             "unbounded_decay": unbounded,
             "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk,
             "gpu_launches": args.steps,  # one prefill launch per timed step (decode: its own region)

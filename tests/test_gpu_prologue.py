@@ -4,7 +4,8 @@ sequences (tiles that straddle sequences, sequences shorter than the window, emp
 with and without initial states) and the fused decode step with its convolution state.
 
 Tolerances: a result in the workload dtype is within one rounding of the oracle (2^-8 of
-|ref| for bf16, 1e-5 for fp32) plus 1e-6 of the tensor's rms for the fp32 arithmetic; the
+|ref| for bf16, at most half a unit in the last place) plus 1e-5 of |ref| and 1e-6 of the
+tensor's rms for the fp32 arithmetic (fp32 results: 1e-5 of |ref|); the
 convolution states are raw inputs moved around, so they must match bit for bit."""
 
 import numpy as np
@@ -22,7 +23,7 @@ EPS = 1e-6
 
 def _close(gpu, ref, dtype):
     g = gpu.detach().double().cpu().numpy()
-    rel = 2.0 ** -8 if dtype == torch.bfloat16 else 1e-5
+    rel = (2.0 ** -8 + 1e-5) if dtype == torch.bfloat16 else 1e-5
     rms = float(np.sqrt(np.mean(ref * ref))) if ref.size else 0.0
     bad = np.abs(g - ref) > rel * np.abs(ref) + 1e-6 * rms
     assert not bad.any(), (int(bad.sum()), float(np.abs(g - ref).max()))
