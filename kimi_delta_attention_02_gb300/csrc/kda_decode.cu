@@ -75,24 +75,44 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     if (tid < 128) {
       const int C3 = 2 * d_k + d_v, h = int(bh % H);
       const int64_t sb = bh * 3 * C3;
-      auto conv = [&](float xt, int cc) {  // 4 taps over (state, x_t); the state shifts by one
-        const float x0 = load_elem<kInBF16>(pro.state, sb + cc), x1 = load_elem<kInBF16>(pro.state, sb + C3 + cc),
-                    x2 = load_elem<kInBF16>(pro.state, sb + 2 * C3 + cc);
-        const float *w = pro.w + (int64_t(h) * C3 + cc) * 4;
-        float acc = w[0] * x0;
-        acc = fmaf(w[1], x1, acc);
-        acc = fmaf(w[2], x2, acc);
-        acc = fmaf(w[3], xt, acc);
-        store_elem<kInBF16>(pro.state, sb + cc, x1);
-        store_elem<kInBF16>(pro.state, sb + C3 + cc, x2);
-        store_elem<kInBF16>(pro.state, sb + 2 * C3 + cc, xt);
-        return acc * sigmoid_approx(acc);  // Swish
-      };
-      if (tid < d_k) {
-        qq = conv(qq, tid);
-        kk = conv(kk, d_k + tid);
+      // every load first (the state stores below would otherwise order them), then the 4-tap
+      // convolutions, then the state shifted by one token
+      const bool onk = tid < d_k, onv = tid < d_v;
+      const int cc[3] = {tid, d_k + tid, 2 * d_k + tid};
+      const bool on[3] = {onk, onk, onv};
+      float xs[3][3], wv[3][4];
+#pragma unroll
+      for (int p = 0; p < 3; ++p) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) xs[p][j] = on[p] ? load_elem<kInBF16>(pro.state, sb + j * C3 + cc[p]) : 0.f;
+        const float4 w4 = on[p] ? *reinterpret_cast<const float4 *>(pro.w + (int64_t(h) * C3 + cc[p]) * 4)
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        wv[p][0] = w4.x;
+        wv[p][1] = w4.y;
+        wv[p][2] = w4.z;
+        wv[p][3] = w4.w;
       }
-      if (tid < d_v) vv = conv(vv, 2 * d_k + tid);
+      const float xt[3] = {qq, kk, vv};
+      float u[3];
+#pragma unroll
+      for (int p = 0; p < 3; ++p) {
+        float acc = wv[p][0] * xs[p][0];
+        acc = fmaf(wv[p][1], xs[p][1], acc);
+        acc = fmaf(wv[p][2], xs[p][2], acc);
+        acc = fmaf(wv[p][3], xt[p], acc);
+        u[p] = acc * sigmoid_approx(acc);  // Swish
+      }
+#pragma unroll
+      for (int p = 0; p < 3; ++p) {
+        if (on[p]) {
+          store_elem<kInBF16>(pro.state, sb + cc[p], xs[p][1]);
+          store_elem<kInBF16>(pro.state, sb + C3 + cc[p], xs[p][2]);
+          store_elem<kInBF16>(pro.state, sb + 2 * C3 + cc[p], xt[p]);
+        }
+      }
+      qq = onk ? u[0] : 0.f;
+      kk = onk ? u[1] : 0.f;
+      vv = onv ? u[2] : 0.f;
       float nq = qq * qq, nk = kk * kk;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
