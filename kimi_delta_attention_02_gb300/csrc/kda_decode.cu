@@ -61,59 +61,68 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
                                 : make_float4(0.f, 0.f, 0.f, 0.f);
   }
 
-  // 2. token vectors: decay, key, query, value (through the prologue if asked); k.q by
-  // warp reduction
-  float kq = 0.f, kk = 0.f, qq = 0.f, vv = 0.f;
-  if (tid < 128) {
-    if (tid < d_k) {
-      kk = load_elem<kInBF16>(k, vec_base + tid);
-      qq = load_elem<kInBF16>(q, vec_base + tid);
+  // 2. token vectors, spread over all 8 warps: warps 0-3 take the query and key channels (and
+  // k.q by warp reduction), warps 4-7 the value channels and the decay; through the prologue
+  // if asked.
+  const int c2 = tid & 127;  // channel of this thread in step 2
+  const bool lo = tid < 128;
+  float kq = 0.f, x0 = 0.f, x1 = 0.f;  // lo: query, key; hi: value, decay input
+  if (lo) {
+    if (c2 < d_k) {
+      x0 = load_elem<kInBF16>(q, vec_base + c2);
+      x1 = load_elem<kInBF16>(k, vec_base + c2);
     }
-    if (tid < d_v) vv = load_elem<kInBF16>(v, bh * d_v + tid);
+  } else {
+    if (c2 < d_v) x0 = load_elem<kInBF16>(v, bh * d_v + c2);
+    if (c2 < d_k)
+      x1 = kDecay == DECAY_CLAMPED ? static_cast<const float *>(decay)[vec_base + c2]
+                                   : load_elem<kInBF16>(decay, vec_base + c2);
   }
   if constexpr (kPrologue) {
-    if (tid < 128) {
-      const int C3 = 2 * d_k + d_v, h = int(bh % H);
-      const int64_t sb = bh * 3 * C3;
-      // every load first (the state stores below would otherwise order them), then the 4-tap
-      // convolutions, then the state shifted by one token
-      const bool onk = tid < d_k, onv = tid < d_v;
-      const int cc[3] = {tid, d_k + tid, 2 * d_k + tid};
-      const bool on[3] = {onk, onk, onv};
-      float xs[3][3], wv[3][4];
+    const int C3 = 2 * d_k + d_v, h = int(bh % H);
+    const int64_t sb = bh * 3 * C3;
+    // all loads first (the state stores below would otherwise order them), then the 4-tap
+    // convolutions and Swish, then the state shifted by one token
+    const int np = lo ? 2 : 1;  // convolutions of this thread: q and k, or v
+    const bool on = c2 < (lo ? d_k : d_v);
+    const int cc0 = lo ? c2 : 2 * d_k + c2, cc1 = d_k + c2;
+    float xs[2][3], wv[2][4];
 #pragma unroll
-      for (int p = 0; p < 3; ++p) {
+    for (int p = 0; p < 2; ++p) {
+      const int cc = p == 0 ? cc0 : cc1;
+      const bool onp = on && p < np;
 #pragma unroll
-        for (int j = 0; j < 3; ++j) xs[p][j] = on[p] ? load_elem<kInBF16>(pro.state, sb + j * C3 + cc[p]) : 0.f;
-        const float4 w4 = on[p] ? *reinterpret_cast<const float4 *>(pro.w + (int64_t(h) * C3 + cc[p]) * 4)
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        wv[p][0] = w4.x;
-        wv[p][1] = w4.y;
-        wv[p][2] = w4.z;
-        wv[p][3] = w4.w;
+      for (int j = 0; j < 3; ++j) xs[p][j] = onp ? load_elem<kInBF16>(pro.state, sb + j * C3 + cc) : 0.f;
+      const float4 w4 = onp ? *reinterpret_cast<const float4 *>(pro.w + (int64_t(h) * C3 + cc) * 4)
+                            : make_float4(0.f, 0.f, 0.f, 0.f);
+      wv[p][0] = w4.x;
+      wv[p][1] = w4.y;
+      wv[p][2] = w4.z;
+      wv[p][3] = w4.w;
+    }
+    const float xt[2] = {x0, lo ? x1 : 0.f};
+    float u[2];
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      float acc = wv[p][0] * xs[p][0];
+      acc = fmaf(wv[p][1], xs[p][1], acc);
+      acc = fmaf(wv[p][2], xs[p][2], acc);
+      acc = fmaf(wv[p][3], xt[p], acc);
+      u[p] = acc * sigmoid_approx(acc);  // Swish
+    }
+#pragma unroll
+    for (int p = 0; p < 2; ++p) {
+      if (on && p < np) {
+        const int cc = p == 0 ? cc0 : cc1;
+        store_elem<kInBF16>(pro.state, sb + cc, xs[p][1]);
+        store_elem<kInBF16>(pro.state, sb + C3 + cc, xs[p][2]);
+        store_elem<kInBF16>(pro.state, sb + 2 * C3 + cc, xt[p]);
       }
-      const float xt[3] = {qq, kk, vv};
-      float u[3];
-#pragma unroll
-      for (int p = 0; p < 3; ++p) {
-        float acc = wv[p][0] * xs[p][0];
-        acc = fmaf(wv[p][1], xs[p][1], acc);
-        acc = fmaf(wv[p][2], xs[p][2], acc);
-        acc = fmaf(wv[p][3], xt[p], acc);
-        u[p] = acc * sigmoid_approx(acc);  // Swish
-      }
-#pragma unroll
-      for (int p = 0; p < 3; ++p) {
-        if (on[p]) {
-          store_elem<kInBF16>(pro.state, sb + cc[p], xs[p][1]);
-          store_elem<kInBF16>(pro.state, sb + C3 + cc[p], xs[p][2]);
-          store_elem<kInBF16>(pro.state, sb + 2 * C3 + cc[p], xt[p]);
-        }
-      }
-      qq = onk ? u[0] : 0.f;
-      kk = onk ? u[1] : 0.f;
-      vv = onv ? u[2] : 0.f;
-      float nq = qq * qq, nk = kk * kk;
+    }
+    x0 = on ? u[0] : 0.f;
+    if (lo) {
+      x1 = on ? u[1] : 0.f;
+      float nq = x0 * x0, nk = x1 * x1;
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
         nq += __shfl_xor_sync(0xffffffffu, nq, o);
@@ -125,29 +134,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       }
     }
     __syncthreads();
-    if (tid < 128) {
-      qq *= rsqrtf(((s_nrm[0][0] + s_nrm[0][1]) + (s_nrm[0][2] + s_nrm[0][3])) + pro.eps);
-      kk *= rsqrtf(((s_nrm[1][0] + s_nrm[1][1]) + (s_nrm[1][2] + s_nrm[1][3])) + pro.eps);
+    if (lo) {
+      x0 *= rsqrtf(((s_nrm[0][0] + s_nrm[0][1]) + (s_nrm[0][2] + s_nrm[0][3])) + pro.eps);
+      x1 *= rsqrtf(((s_nrm[1][0] + s_nrm[1][1]) + (s_nrm[1][2] + s_nrm[1][3])) + pro.eps);
     }
   }
-  if (tid < 128) {
-    float a = 0.f;
-    if (tid < d_k) {
-      if constexpr (kDecay == DECAY_CLAMPED)
-        a = __expf(clamp_log_decay(static_cast<const float *>(decay)[vec_base + tid], lb));
-      else if constexpr (kDecay == DECAY_GATED)
-        a = __expf(gated_log_decay(load_elem<kInBF16>(decay, vec_base + tid), __expf(A_log[bh % H]), lb));
-      else
-        a = __expf(unbounded_log_decay(load_elem<kInBF16>(decay, vec_base + tid), __expf(A_log[bh % H])));
-    }
-    s_k[tid] = kk;
-    s_q[tid] = qq;
-    s_a[tid] = a;
-    s_v[tid] = vv;
-    kq = kk * qq;
+  if (lo) {
+    s_q[c2] = x0;
+    s_k[c2] = x1;
+    kq = x0 * x1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
     if (tx == 0) s_kq[ty] = kq;
+  } else {
+    float a = 0.f;
+    if (c2 < d_k) {
+      if constexpr (kDecay == DECAY_CLAMPED) a = __expf(clamp_log_decay(x1, lb));
+      else if constexpr (kDecay == DECAY_GATED) a = __expf(gated_log_decay(x1, __expf(A_log[bh % H]), lb));
+      else a = __expf(unbounded_log_decay(x1, __expf(A_log[bh % H])));
+    }
+    s_a[c2] = a;
+    s_v[c2] = x0;
   }
   const float b = beta[bh];
   __syncthreads();
