@@ -152,7 +152,8 @@ def sampled_heads(H: int = 32, count: int = 4, seed: int = 0):
     return sorted(int(x) for x in np.random.default_rng(seed).permutation(H)[:count])
 
 
-# The five graded workloads, by name. Each entry: (description, builder kwargs).
+# The named prefill workloads: the configurations the tests and the benchmark use (the graded
+# shapes plus the gated-decay and output-gate variants of the K3 layer). Each entry: builder kwargs.
 PREFILL_WORKLOADS = {
     "prefill_f32_T256_H2": dict(lengths=[256], H=2, dtype=torch.float32, init_std=None),
     "prefill_k3_T4096_H96": dict(lengths=[4096], H=96, dtype=torch.bfloat16, init_std=0.02),

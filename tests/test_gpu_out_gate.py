@@ -108,3 +108,17 @@ def test_decode(gated, dtype):
     y = output_gate_rmsnorm(o, cpu(st.out_gate), cpu(st.norm_weight), EPS)
     tol = TOL_BF16 if dtype == torch.bfloat16 else TOL_F32
     assert gated_output_err(out, y, o) <= tol and rel_max_err(state, f) <= tol
+
+
+def test_long_context_sampled_heads():
+    """T = 2^20, H = 32 (the long-context shape) with the gated decay and the output gate: two
+    seeded heads compared in full (heads are independent chains)."""
+    case = workloads.make_prefill([1 << 20], H=32, device="cuda", seed=0, init_std=None, gated=True, out_gate=True)
+    out, fin = _run(case, out_dtype=torch.bfloat16)
+    heads = workloads.sampled_heads(32, 2, seed=1)
+    sel = lambda t: t[:, heads].contiguous().cpu()
+    o_ref, f_ref = kda_recurrent_gated(sel(case.q), sel(case.k), sel(case.v), sel(case.z), case.A_log[heads].cpu(),
+                                       sel(case.beta), cpu(case.cu_seqlens).long().numpy())
+    y_ref = output_gate_rmsnorm(o_ref, sel(case.out_gate), cpu(case.norm_weight), EPS)
+    e_y = gated_output_err(out[:, heads], y_ref, o_ref, bf16_out=True)
+    assert e_y <= TOL_BF16 and rel_max_err(fin[:, heads], f_ref) <= TOL_BF16, e_y

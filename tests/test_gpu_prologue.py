@@ -128,3 +128,30 @@ def test_prefill_state_continues_into_decode():
     binding.check_device_error()
     _close(out, qf[37:].double().cpu().numpy(), torch.bfloat16)  # qf went through one bf16 rounding
     assert torch.equal(cs[0, :, 2, :128], full.q_raw[37])
+
+
+def test_prefill_pass_many_short_sequences():
+    """1,500 sequences of 0 to 4 tokens: tiles spanning many sequence starts, and more sequence
+    offsets than the kernel keeps in shared memory."""
+    lengths = [int(x) for x in np.random.default_rng(12).integers(0, 5, size=1500)]
+    case = workloads.make_prologue(lengths, H=2, device="cuda", seed=12)
+    _check(case, torch.bfloat16)
+
+
+@pytest.mark.parametrize("d_k,d_v", [(64, 96), (128, 32)])
+def test_decode_step_with_conv_state_odd_sizes(d_k, d_v):
+    B, H = 3, 2
+    dtype = torch.float32
+    st0 = workloads.make_decode_state(B, H, d_k, d_v, device="cuda", seed=13)
+    cs0 = workloads.make_conv_state(B, H, d_k, d_v, dtype=dtype, device="cuda", seed=13)
+    w = workloads.make_conv_weight(H, d_k, d_v, device="cuda", seed=13)
+    step = workloads.make_decode_step(0, B, H, d_k, d_v, dtype=dtype, device="cuda", seed=14)
+    state, cs = st0.clone(), cs0.clone()
+    out = binding.decode_ex(step.q, step.k, step.v, step.beta, state, log_alpha=step.log_alpha, conv_weight=w,
+                            conv_state=cs, l2_eps=EPS)
+    binding.check_device_error()
+    cu = np.arange(B + 1)
+    q, k, v, fin = kda_prologue(cpu(step.q), cpu(step.k), cpu(step.v), cpu(w), cu, cpu(cs0), eps=EPS)
+    o_ref, f_ref = kda_recurrent(q, k, v, cpu(step.log_alpha), cpu(step.beta), cu, init_state=cpu(st0))
+    assert np.array_equal(cs.double().cpu().numpy(), fin)
+    assert rel_max_err(out, o_ref) <= TOL_F32 and rel_max_err(state, f_ref) <= TOL_F32
