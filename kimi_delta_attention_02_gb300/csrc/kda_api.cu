@@ -61,6 +61,14 @@ namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+bool finite_nonneg(float x) { return x >= 0.f && x < INFINITY; }  // false for NaN
+
+// whether the byte ranges [a, a + na) and [b, b + nb) intersect (null or empty never does)
+bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
+  if (!a || !b || !na || !nb) return false;
+  const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
+  return pa < pb + nb && pb < pa + na;
+}
 
 // decay: log_alpha (fp32) when A_log is null, else the gated form's logits z (in_dtype)
 kda_status check_prefill_args(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
@@ -85,11 +93,6 @@ kda_status check_prefill_args(const void *q, const void *k, const void *v, const
   if (final_state && !aligned16(final_state)) return KDA_ERR_INVALID_ARG;
   // outputs must not overlap the inputs (final_state == init_state is allowed)
   const size_t es = in_dtype == KDA_BF16 ? 2 : 4, eo = out_dtype == KDA_BF16 ? 2 : 4;
-  auto overlaps = [](const void *a, size_t na, const void *b, size_t nb) {
-    if (!a || !b || !na || !nb) return false;
-    const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
-    return pa < pb + nb && pb < pa + na;
-  };
   const size_t nk = size_t(total_tokens) * H * d_k, nv = size_t(total_tokens) * H * d_v;
   const size_t ns = size_t(num_seqs) * H * d_k * d_v * 4;
   if (total_tokens > 0 && out_gate != nullptr && !aligned16(out_gate)) return KDA_ERR_INVALID_ARG;
@@ -148,14 +151,6 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const void 
   return err == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-bool finite_nonneg(float x) { return x >= 0.f && x < INFINITY; }  // false for NaN
-
-bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
-  if (!a || !b || !na || !nb) return false;
-  const char *pa = static_cast<const char *>(a), *pb = static_cast<const char *>(b);
-  return pa < pb + nb && pb < pa + na;
-}
-
 kda_status decode_impl(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
                        const float *beta, float *state, void *out, int32_t B, int32_t H, int32_t d_k, int32_t d_v,
                        kda_dtype in_dtype, kda_dtype out_dtype, float lb, float scale, void *stream,
@@ -175,10 +170,9 @@ kda_status decode_impl(const void *q, const void *k, const void *v, const void *
   const kda_status st = check_out_gate_args(out_gate, norm_weight, norm_eps);
   if (st != KDA_OK) return st;
   if ((out_gate && !aligned16(out_gate)) || (norm_weight && !aligned4(norm_weight))) return KDA_ERR_INVALID_ARG;
-  if (out_gate) {  // the written read-out must not overlap the gate logits or the state
+  if (out_gate) {  // the written read-out must not overlap the gate logits
     const size_t nv = size_t(B) * H * d_v, eo = out_dtype == KDA_BF16 ? 2 : 4, es = in_dtype == KDA_BF16 ? 2 : 4;
-    const char *po = static_cast<const char *>(out), *pg = static_cast<const char *>(out_gate);
-    if (po < pg + nv * es && pg < po + nv * eo) return KDA_ERR_INVALID_ARG;
+    if (overlaps(out, nv * eo, out_gate, nv * es)) return KDA_ERR_INVALID_ARG;
   }
   if (conv_state != nullptr) {  // the prologue: weights and state on the device, eps finite
     if (conv_weight == nullptr || !aligned16(conv_weight) || !aligned16(conv_state) || !finite_nonneg(l2_eps))
