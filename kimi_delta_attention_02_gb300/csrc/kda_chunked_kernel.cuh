@@ -552,15 +552,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int base = 16 * iw;
         if (lane < 16) {  // the two 8 x 8 diagonal pieces: lane = column of its piece
           const int o = base + 8 * (lane >> 3), cc = lane & 7;
-          float x[8];
+          float x[8], a[28];  // column cc of the piece's inverse; the piece's strictly lower entries
 #pragma unroll
           for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
 #pragma unroll
-          for (int m = 0; m < 8; ++m) {
-            Ts[(o + m) * kALd + o + cc] = x[m];
+          for (int m = 0, n = 0; m < 8; ++m)  // all loads before the first store (which may alias)
 #pragma unroll
-            for (int r = m + 1; r < 8; ++r) x[r] = fmaf(-As[(o + r) * kALd + o + m], x[m], x[r]);
-          }
+            for (int r = m + 1; r < 8; ++r, ++n) a[n] = As[(o + r) * kALd + o + m];
+#pragma unroll
+          for (int m = 0, n = 0; m < 8; ++m)
+#pragma unroll
+            for (int r = m + 1; r < 8; ++r, ++n) x[r] = fmaf(-a[n], x[m], x[r]);
+#pragma unroll
+          for (int m = 0; m < 8; ++m) Ts[(o + m) * kALd + o + cc] = x[m];
         } else {  // the zero 8 x 8 piece above the diagonal
           const int l = lane - 16;
           *reinterpret_cast<float4 *>(Ts + (base + (l >> 1)) * kALd + base + 8 + 4 * (l & 1)) =
