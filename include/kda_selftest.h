@@ -1,5 +1,5 @@
 /*
- * kda_selftest.h -- test-only entry point of libkda.
+ * kda_selftest.h -- test-only entry points of libkda.
  *
  * The chunked prefill kernels feed tcgen05.mma from shared-memory tiles in a
  * 128-byte-swizzled layout through hand-built descriptors. The pages describe
@@ -42,6 +42,22 @@ kda_status kda_selftest_umma(const float *A, const float *B, float *D, int32_t M
                              int32_t fmt, int32_t sw64, int32_t a_mn_major, int32_t b_mn_major, int32_t negate_a,
                              uint32_t a_lbo,
                              uint32_t a_sbo, uint32_t b_lbo, uint32_t b_sbo, int32_t *status, void *stream);
+
+/*
+ * kda_selftest_wait_timeout -- runs the library's bounded mbarrier wait on a
+ * phase that nothing completes, so that a test can check the failure path
+ * without faulting the GPU: the wait gives up after its limit (about 2 s),
+ * records KDA_ERR_TIMEOUT in the device error word (which the next
+ * kda_check_device_error reports and clears) and the kernel returns normally,
+ * leaving the context usable. No counterpart on the pages: this is the
+ * library's own failure detection.
+ *
+ *   status  device uint32, set to 1 when the wait gave up (0 if it had not)
+ *
+ * One CTA of 32 threads. Enqueued on `stream`; returns KDA_ERR_INVALID_ARG for
+ * a null or misaligned status pointer.
+ */
+kda_status kda_selftest_wait_timeout(uint32_t *status, void *stream);
 
 #ifdef __cplusplus
 }

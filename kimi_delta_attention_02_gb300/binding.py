@@ -90,6 +90,8 @@ def _declare(lib):
     lib.kda_version.restype = i32
     lib.kda_selftest_umma.argtypes = [vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, u32, u32, u32, u32, vp, vp]
     lib.kda_selftest_umma.restype = i32
+    lib.kda_selftest_wait_timeout.argtypes = [vp, vp]
+    lib.kda_selftest_wait_timeout.restype = i32
 
 
 def lib():
@@ -391,6 +393,18 @@ def selftest_umma(A, B, M, N, K, *, fmt="bf16", sw64=False, a_mn_major=False, b_
     if int(status.item()) != 0:
         raise KdaError(KDA_ERR_TIMEOUT, "kda_selftest_umma")
     return D
+
+
+def selftest_wait_timeout(stream=None):
+    """Runs a bounded wait that is never satisfied (``kda_selftest_wait_timeout``); returns the
+    kernel's status word (1 when the wait gave up). The device error word is left set for
+    ``check_device_error`` to report."""
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    st = lib().kda_selftest_wait_timeout(_ptr(status), _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_selftest_wait_timeout")
+    torch.cuda.synchronize()
+    return int(status.item())
 
 
 class HostPrefill:

@@ -121,3 +121,27 @@ extern "C" kda_status kda_selftest_umma(const float *A, const float *B, float *D
       device_error_word());
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
+
+namespace kda {
+namespace {
+
+// A bounded wait on a phase that never completes: the failure path of every wait in the library.
+__global__ void selftest_wait_kernel(uint32_t *status, uint32_t *err_word) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);  // one arrival expected; none comes
+    fence_mbarrier_init();
+  }
+  __syncthreads();
+  const bool ok = mbar_wait_sleep(&bar, 0u, err_word, DEVERR_TMA_TIMEOUT);
+  if (threadIdx.x == 0) *status = ok ? 0u : 1u;
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" kda_status kda_selftest_wait_timeout(uint32_t *status, void *stream) {
+  if (status == nullptr || (reinterpret_cast<uintptr_t>(status) & 3u) != 0) return KDA_ERR_INVALID_ARG;
+  kda::selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, kda::device_error_word());
+  return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}

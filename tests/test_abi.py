@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     assert {"kda_prefill", "kda_decode", "kda_prefill_recurrent", "kda_check_device_error",
             "kda_status_string", "kda_version", "kda_selftest_umma", "kda_prefill_gated",
             "kda_prefill_gated_recurrent", "kda_decode_gated", "kda_prefill_ex", "kda_decode_ex",
-            "kda_prologue"} <= set(names)
+            "kda_prologue", "kda_selftest_wait_timeout"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -266,3 +266,8 @@ def test_prologue_rejects(lib, over, expect):
 
 def test_prologue_accepts_empty_work(lib):
     assert _prologue(lib, N=0, T=0, q_raw=None, k_raw=None, v_raw=None, q=None, k=None, v=None, fin=None) == B.KDA_OK
+
+
+def test_wait_selftest_rejects_bad_status_pointer(lib):
+    assert lib.kda_selftest_wait_timeout(NULL, NULL) == B.KDA_ERR_INVALID_ARG
+    assert lib.kda_selftest_wait_timeout(0x1002, NULL) == B.KDA_ERR_INVALID_ARG
