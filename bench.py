@@ -175,16 +175,16 @@ def prefill_traffic():
     return rec.get("bytes_per_launch") if h.hexdigest() == rec.get("sources_sha256") else None
 
 
-def time_prefill(case, steps, warmup, world, gated=False, out_gate=False, unbounded=False):
+def time_prefill(case, steps, warmup, world, gated=False, out_gate=False, unbounded=False, recurrent=False):
     from kimi_delta_attention_02_gb300 import binding
     out_dtype = torch.float32
-    if unbounded:  # the earlier models' unbounded decay map: the token-recurrent kernel
+    if unbounded:  # the earlier models' unbounded decay map (chunked kernel, or forced token-recurrent)
         args = ()
 
         def fn(out, final_state, stream):
             binding.prefill_ex(case.q, case.k, case.v, case.beta, case.cu_seqlens, z=case.z, A_log=case.A_log,
-                               init_state=case.init_state, unbounded=True, out=out, final_state=final_state,
-                               stream=stream)
+                               init_state=case.init_state, unbounded=True, recurrent=recurrent, out=out,
+                               final_state=final_state, stream=stream)
     elif out_gate:  # gated decay, output gate, bf16 output: the parameter-block entry point
         out_dtype = torch.bfloat16
         args = ()
@@ -390,7 +390,7 @@ def main():
     with ClockSampler(local) as clocks:
         total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world)
         dec_ms = None if args.prefill_only else time_decode(DECODE["steps"], 1, 1, world, seed=rank)
-        gated_ms = outgate_ms = prologue_ms = unbounded_ms = fdec_ms = None
+        gated_ms = outgate_ms = prologue_ms = unbounded_ms = unbounded_rec_ms = unbounded_steep_ms = fdec_ms = None
         if not args.prefill_only and args.heads == PREFILL["H"]:
             gcase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
             _, g_launch = time_prefill(gcase, args.steps, args.warmup, world, gated=True)
@@ -404,8 +404,13 @@ def main():
             prologue_ms = sum(p_launch) / len(p_launch)
             fdec_ms = time_decode(DECODE["steps"], 1, 1, world, seed=rank, fused=True)
             ucase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
-            _, u_launch = time_prefill(ucase, 3, 1, world, unbounded=True)  # a few ms per launch
+            _, u_launch = time_prefill(ucase, args.steps, args.warmup, world, unbounded=True)
             unbounded_ms = sum(u_launch) / len(u_launch)
+            _, u_launch = time_prefill(ucase, 3, 1, world, unbounded=True, recurrent=True)  # a few ms per launch
+            unbounded_rec_ms = sum(u_launch) / len(u_launch)
+            ucase.z[:, :, ::3] = 40.0  # -40 e^{A_h} per step on every third channel: every chunk has wide channels
+            _, u_launch = time_prefill(ucase, args.steps, args.warmup, world, unbounded=True)
+            unbounded_steep_ms = sum(u_launch) / len(u_launch)
             del ucase
     if args.prefill_only:
         if rank == 0:
@@ -450,9 +455,12 @@ def main():
     unbounded = None
     if unbounded_ms is not None:
         unbounded = {"workload": "prefill_k3_gated_T4096_H96 through g = -e^A Softplus(z)",
-                     "kernel": "token-recurrent (the chunked kernels need a bounded decay)",
+                     "kernel": "chunked, position pairs for channels wide in a diagonal block",
                      "launch_ms": unbounded_ms, "tokens_per_s": world * T / (unbounded_ms / 1e3),
-                     "vs_bounded_chunked": (gated_ms / unbounded_ms) if gated_ms else None}
+                     "vs_bounded_chunked": (gated_ms / unbounded_ms) if gated_ms else None,
+                     "steep_launch_ms": unbounded_steep_ms,
+                     "steep": "logits +40 on every third channel (every chunk takes the position-pair step)",
+                     "token_recurrent_launch_ms": unbounded_rec_ms}
     fdec = None
     if fdec_ms is not None:
         f_avg = sum(fdec_ms) / len(fdec_ms)

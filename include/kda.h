@@ -190,8 +190,11 @@ kda_status kda_decode_gated(const void *q, const void *k, const void *v, const v
  *                 of the earlier models in the same section's table,
  *                 g = -e^{A_h} * Softplus(z), Softplus(x) = log(1 + e^x), from the
  *                 logits z (in_dtype) and A_log [H]; decay_bound is ignored. Its
- *                 decay has no lower bound, so the chunked tensor-core kernel (which
- *                 needs one) does not take it: a prefill runs the fp32
+ *                 decay has no lower bound: a bf16 prefill with d = 128 runs the
+ *                 chunked kernel, which forms the diagonal-block entries of channels
+ *                 decaying by more than about e^79 over 16 tokens from position
+ *                 pairs (Kimi K3 -- Architecture Notes, section 1.2, the Kimi Linear
+ *                 treatment of the diagonal tiles); other prefills run the fp32
  *                 token-recurrent kernel
  *   out_gate      gate logits r [rows, H, d_v] in in_dtype, device, 16-byte
  *                 aligned, not overlapping `out`; NULL = no output gate (out = o)

@@ -228,8 +228,8 @@ def prefill_ex(q, k, v, beta, cu_seqlens, *, log_alpha=None, lower_bound: float 
     """Prefill through the parameter block (``kda_prefill_ex``): the clamped (``log_alpha``) or
     gated (``z``, ``A_log``) log-decay, and optionally the output gate with head-wise RMSNorm,
     ``out = Sigmoid(out_gate) * norm_weight * o / sqrt(mean(o^2) + norm_eps)`` per token and head.
-    ``unbounded=True`` (with z, A_log) takes the earlier models' map g = -e^{A_h} Softplus(z),
-    which runs on the token-recurrent kernel.
+    ``unbounded=True`` (with z, A_log) takes the earlier models' map g = -e^{A_h} Softplus(z)
+    (chunked kernel for bf16 with d = 128, else the token-recurrent one).
     out_gate [T, H, d_v] in the dtype of q; norm_weight [d_v] float32 or None (ones).
     Returns (out, final_state or None)."""
     T, H, d_k = q.shape

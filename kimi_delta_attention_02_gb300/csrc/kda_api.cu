@@ -50,12 +50,12 @@ cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const 
                              int d_k, int d_v, bool in_bf16, bool out_bf16, float lb, float scale,
                              const float *init_state, const void *out_gate, const float *norm_weight,
                              float norm_eps, void *out, float *final_state, cudaStream_t stream);
-bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb);
-kda_status launch_chunked(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
-                          const float *beta, const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H,
-                          bool out_bf16, float lb, float scale, const float *init_state, const void *out_gate,
-                          const float *norm_weight, float norm_eps, void *out, float *final_state,
-                          cudaStream_t stream);
+bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb, int decay_form);
+kda_status launch_chunked(const void *q, const void *k, const void *v, const void *decay, int decay_form,
+                          const float *A_log, const float *beta, const int32_t *cu_seqlens, int num_seqs,
+                          int64_t total_tokens, int H, bool out_bf16, float lb, float scale, const float *init_state,
+                          const void *out_gate, const float *norm_weight, float norm_eps, void *out,
+                          float *final_state, cudaStream_t stream);
 
 namespace {
 
@@ -140,11 +140,12 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const void 
   if (num_seqs == 0) return KDA_OK;
   if (total_tokens == 0) out_gate = norm_weight = nullptr;  // nothing is read out
   const cudaStream_t s = static_cast<cudaStream_t>(stream);
-  // the chunked kernels need the bounded decay (clamped, or the gated map with g_min >= -5)
-  if (!force_recurrent && total_tokens > 0 && decay_form != DECAY_UNBOUNDED &&
-      chunked_supported(d_k, d_v, in_dtype == KDA_BF16, lb))
-    return launch_chunked(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, out_dtype == KDA_BF16,
-                          lb, scale, init_state, out_gate, norm_weight, norm_eps, out, final_state, s);
+  // the chunked kernels: bf16 inputs, d = 128; a bounded map with a lower bound >= -5, or the
+  // unbounded map
+  if (!force_recurrent && total_tokens > 0 && chunked_supported(d_k, d_v, in_dtype == KDA_BF16, lb, decay_form))
+    return launch_chunked(q, k, v, decay, decay_form, A_log, beta, cu_seqlens, num_seqs, total_tokens, H,
+                          out_dtype == KDA_BF16, lb, scale, init_state, out_gate, norm_weight, norm_eps, out,
+                          final_state, s);
   const cudaError_t err = launch_recurrent(q, k, v, decay, decay_form, A_log, beta, cu_seqlens, num_seqs, H, d_k, d_v,
                                            in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale, init_state,
                                            out_gate, norm_weight, norm_eps, out, final_state, s);

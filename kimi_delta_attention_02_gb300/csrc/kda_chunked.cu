@@ -1,7 +1,8 @@
 // kda_chunked.cu -- host side of the tensor-core chunkwise prefill (the kernel is in
 // kda_chunked_kernel.cuh): tensor maps, kernel choice and launch. The instantiations
-// without the output gate live here; those with it in kda_chunked_gate.cu, so that the
-// two halves compile in parallel.
+// of the bounded maps without the output gate live here; those with it in
+// kda_chunked_gate.cu and those of the unbounded map in kda_chunked_unbounded.cu, so that
+// the three compile in parallel.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -14,10 +15,13 @@ namespace chunked {
 
 // kernel with the output gate (kda_chunked_gate.cu)
 KernelFn gate_kernel(bool out_bf16, bool gated);
+// kernel of the unbounded map (kda_chunked_unbounded.cu)
+KernelFn unbounded_kernel(bool out_bf16, bool norm_gate);
 
 KernelFn plain_kernel(bool out_bf16, bool gated) {
-  return out_bf16 ? (gated ? kda_chunked_kernel<true, true, false> : kda_chunked_kernel<true, false, false>)
-                  : (gated ? kda_chunked_kernel<false, true, false> : kda_chunked_kernel<false, false, false>);
+  constexpr int C = DECAY_CLAMPED, G = DECAY_GATED;
+  return out_bf16 ? (gated ? kda_chunked_kernel<true, G, false> : kda_chunked_kernel<true, C, false>)
+                  : (gated ? kda_chunked_kernel<false, G, false> : kda_chunked_kernel<false, C, false>);
 }
 
 }  // namespace chunked
@@ -64,18 +68,22 @@ bool tensor_map_3d(CUtensorMap *map, const void *base, bool bf16, int64_t T, int
   return r == CUDA_SUCCESS;
 }
 
-bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb) {
-  return in_bf16 && d_k == chunked::kD && d_v == chunked::kD && lb >= -5.0f;
+// The bounded maps need log-decay >= -5 (the clamp's or the gated map's lower bound); the
+// unbounded map takes any decay.
+bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb, int decay_form) {
+  return in_bf16 && d_k == chunked::kD && d_v == chunked::kD && (decay_form == DECAY_UNBOUNDED || lb >= -5.0f);
 }
 
-// decay: log_alpha (fp32) when A_log is null, else the gated form's bf16 logits z.
+// decay: log_alpha (fp32) for DECAY_CLAMPED, else the bf16 logits z of the gated or the
+// unbounded map, with A_log.
 // out_gate: bf16 gate logits [T, H, 128] of the output gate, or null (out = o).
-kda_status launch_chunked(const void *q, const void *k, const void *v, const void *decay, const float *A_log,
-                          const float *beta, const int32_t *cu_seqlens, int num_seqs, int64_t total_tokens, int H,
-                          bool out_bf16, float lb, float scale, const float *init_state, const void *out_gate,
-                          const float *norm_weight, float norm_eps, void *out, float *final_state,
-                          cudaStream_t stream) {
-  const bool gated = A_log != nullptr, norm_gate = out_gate != nullptr;
+kda_status launch_chunked(const void *q, const void *k, const void *v, const void *decay, int decay_form,
+                          const float *A_log, const float *beta, const int32_t *cu_seqlens, int num_seqs,
+                          int64_t total_tokens, int H, bool out_bf16, float lb, float scale, const float *init_state,
+                          const void *out_gate, const float *norm_weight, float norm_eps, void *out,
+                          float *final_state, cudaStream_t stream) {
+  const bool gated = decay_form != DECAY_CLAMPED, norm_gate = out_gate != nullptr;
+  const bool unbounded = decay_form == DECAY_UNBOUNDED;
   CUtensorMap mq, mk, mv, mg, mr, mo;
   if (!make_map(&mq, q, true, true, total_tokens, H) || !make_map(&mk, k, true, true, total_tokens, H) ||
       !make_map(&mv, v, true, true, total_tokens, H) || !make_map(&mg, decay, gated, false, total_tokens, H))
@@ -87,14 +95,15 @@ kda_status launch_chunked(const void *q, const void *k, const void *v, const voi
     mr = mg;  // not read
   }
   const chunked::OutGate og{static_cast<const uint16_t *>(out_gate), norm_weight, norm_eps};
-  const chunked::KernelFn kern = norm_gate ? chunked::gate_kernel(out_bf16, gated)
-                                           : chunked::plain_kernel(out_bf16, gated);
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(chunked::kSmemBytes)) !=
-      cudaSuccess)
+  const chunked::KernelFn kern = unbounded   ? chunked::unbounded_kernel(out_bf16, norm_gate)
+                                 : norm_gate ? chunked::gate_kernel(out_bf16, gated)
+                                             : chunked::plain_kernel(out_bf16, gated);
+  const uint32_t smem = unbounded ? chunked::smem_bytes<DECAY_UNBOUNDED>() : chunked::smem_bytes<DECAY_CLAMPED>();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
     return KDA_ERR_CUDA;
   const dim3 grid(unsigned(int64_t(num_seqs) * H)), block(chunked::kThreads);
-  kern<<<grid, block, chunked::kSmemBytes, stream>>>(mq, mk, mv, mg, mr, mo, og, A_log, beta, cu_seqlens, init_state,
-                                                     out, final_state, H, lb, scale, device_error_word());
+  kern<<<grid, block, smem, stream>>>(mq, mk, mv, mg, mr, mo, og, A_log, beta, cu_seqlens, init_state, out,
+                                      final_state, H, lb, scale, device_error_word());
   return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

@@ -7,8 +7,9 @@ namespace kda {
 namespace chunked {
 
 KernelFn gate_kernel(bool out_bf16, bool gated) {
-  return out_bf16 ? (gated ? kda_chunked_kernel<true, true, true> : kda_chunked_kernel<true, false, true>)
-                  : (gated ? kda_chunked_kernel<false, true, true> : kda_chunked_kernel<false, false, true>);
+  constexpr int C = DECAY_CLAMPED, G = DECAY_GATED;
+  return out_bf16 ? (gated ? kda_chunked_kernel<true, G, true> : kda_chunked_kernel<true, C, true>)
+                  : (gated ? kda_chunked_kernel<false, G, true> : kda_chunked_kernel<false, C, true>);
 }
 
 }  // namespace chunked

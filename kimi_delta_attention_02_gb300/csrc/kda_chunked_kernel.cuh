@@ -21,6 +21,19 @@
 // same rescaled by a per-channel constant: Q * Gamma = (Q * f) e^r,
 // K * Gamma = (K * f) e^r, K * e^{G_last - G} = (K * g) e^{G_last - r}.
 //
+// Unbounded decay (the earlier models' map g = -e^{A_h} Softplus(z), the same
+// section): one step may fall far below -5, so a 16-token subtile can span more than
+// e^80 in some channel. The reference r = G at the subtile boundary still bounds the
+// block below the diagonal (rows t >= 16 by f <= 1, columns i < 16 by g <= 1); only
+// the two diagonal 16 x 16 blocks depend on the span. A channel whose decay over a
+// diagonal block exceeds 2^114 (about e^79) is "wide" there: its Gram operands for that
+// block are zero (rows t < 16 of [Q f ; K f] for the first block, columns i >= 16 of
+// K g for the second) and its share of the block's entries is formed from position
+// pairs, sum over the wide channels of x_tc k_ic e^{G_tc - G_ic} with one exponential
+// per pair and channel (the Kimi Linear treatment of the diagonal tiles), on the CUDA
+// cores, and added where A and P leave tensor memory. A chunk without a wide channel
+// runs exactly the bounded path; its cost is the map itself.
+//
 // Precision. Outputs and states are heavy-tailed (their largest entries are
 // about ten times their rms), so a per-element relative error e shows up as
 // about 10e in max|error| / rms. bf16 operands (e = 2^-9) therefore cannot meet
@@ -98,6 +111,25 @@ constexpr uint32_t OFF_MISC = 218 * 1024;    // beta x2, Gamma_last x2, group de
 constexpr uint32_t OFF_SS = OFF_MISC + 3456; // output gate: per-token partial sums of squares [32][4] fp32
 constexpr uint32_t kSmemBytes = 222 * 1024 + 1024;
 static_assert(OFF_SS + 32 * 16 + 1023 <= kSmemBytes, "shared memory map exceeds the allocation");
+// Unbounded decay only: the position-pair shares of the diagonal blocks, by chunk parity,
+// [2][512] fp32 (A entries first, then P; see pair_row_a), which takes the allocation to the
+// 227 KB a CTA may have. The cumulative log2 decays [32 tokens][128 c] of a chunk that has
+// wide channels pass through the lower half of the S^T tile (free between MMA1 and P4).
+constexpr uint32_t OFF_CORR = 222 * 1024;
+constexpr uint32_t kSmemBytesUnbounded = 226 * 1024 + 1024;
+static_assert(OFF_SS + 32 * 16 <= OFF_CORR && kSmemBytesUnbounded <= 232448, "unbounded map exceeds 227 KB");
+template <int kDecay>
+constexpr uint32_t smem_bytes() { return kDecay == DECAY_UNBOUNDED ? kSmemBytesUnbounded : kSmemBytes; }
+// a channel is wide in a diagonal block when its log2 decay over the block's tokens is below
+// -kWideBlock (the bound gives every Gram factor of a narrow channel a magnitude <= 2^114)
+constexpr float kWideBlock = 114.f;
+
+// A chunk's 512 position-pair shares: entries A[t][i] (i < t) of the two diagonal blocks
+// (120 each, row-major inside a block), then P[t][i] (i <= t, 136 each). The first slot of
+// row tl (block-local) of diagonal block blk:
+__host__ __device__ constexpr uint32_t pair_row_a(uint32_t blk, uint32_t tl) { return blk * 120 + tl * (tl - 1) / 2; }
+__host__ __device__ constexpr uint32_t pair_row_p(uint32_t blk, uint32_t tl) { return 240 + blk * 136 + tl * (tl + 1) / 2; }
+static_assert(pair_row_a(1, 15) + 14 == 239 && pair_row_p(1, 15) + 15 == 511, "pair share layout");
 
 // TMEM columns: two groups [U^T | O^T | S^T] (32 + 32 + 128) used by chunk parity, then
 // Gram (chunk parity 0), W^T, Gram (parity 1). Chunk j's MMA1 and MMA2 write group j % 2;
@@ -139,7 +171,7 @@ __device__ __forceinline__ float exp2_sfu(float x) {
 struct Bars {
   uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate;
 };
-static_assert(OFF_MISC + (2 * 32 + 2 * 128 + 4 * 128) * 4 + sizeof(Bars) + 8 <= OFF_SS, "misc overlaps");
+static_assert(OFF_MISC + (2 * 32 + 2 * 128 + 4 * 128) * 4 + sizeof(Bars) + 48 <= OFF_SS, "misc overlaps");
 
 // The output gate of section 1.3: bf16 gate logits r [T, H, 128], the RMSNorm weight w [128]
 // (nullptr = ones) and eps.
@@ -149,11 +181,12 @@ struct OutGate {
   float eps;
 };
 
-// kGated: the log-decay is the gated form g = g_min Sigmoid(e^{A_h} z) of section 1.2 (tm_g
-// then maps the bf16 logits z; lb holds g_min); otherwise tm_g maps the fp32 log_alpha,
-// clamped below at lb. kNormGate: each output row is written as Sigmoid(r) * w * o / rms(o)
+// kDecay: DECAY_GATED, the log-decay is the gated form g = g_min Sigmoid(e^{A_h} z) of
+// section 1.2 (tm_g then maps the bf16 logits z; lb holds g_min); DECAY_UNBOUNDED, the
+// unbounded map g = -e^{A_h} Softplus(z) of the same logits (lb unused); DECAY_CLAMPED,
+// tm_g maps the fp32 log_alpha, clamped below at lb. kNormGate: each output row is written as Sigmoid(r) * w * o / rms(o)
 // (section 1.3) instead of o; tm_r maps the gate logits, for L2 prefetches.
-template <bool kOutBF16, bool kGated, bool kNormGate>
+template <bool kOutBF16, int kDecay, bool kNormGate>
 __global__ void __launch_bounds__(kThreads, 1)
     kda_chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -180,7 +213,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
   const int n_chunks = int((eos - bos + kC - 1) / kC);
   const uint32_t sbase = smem_u32(sm);
-  const float a_h = kGated ? __expf(A_log[h]) : 0.f;  // e^{A_h} of the gated form
+  constexpr bool kGated = kDecay != DECAY_CLAMPED;  // tm_g maps bf16 logits
+  constexpr bool kUnb = kDecay == DECAY_UNBOUNDED;
+  const float a_h = kGated ? __expf(A_log[h]) : 0.f;  // e^{A_h} of the logit maps
 
   if (tid == 0) {
     tma_prefetch_desc(&tm_q);
@@ -199,7 +234,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->wu, 1);
     mbar_init(&bars->gate, 1);
     fence_mbarrier_init();
-    s_tmem[1] = 0u;  // abort flag
+    s_tmem[1] = 0u;            // abort flag
+    s_tmem[2] = s_tmem[3] = ~0u;  // unbounded map: the last chunk of each parity with wide channels
+    // (s_tmem[4 .. 11]: the wide channels of a chunk's two diagonal blocks, 4 x 32 bits each)
   }
   if (warp == 0) {
     tmem_alloc(s_tmem, TM_COLS);
@@ -306,6 +343,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int r = 0; r < 8; ++r) {  // alpha = 1 past the end of the sequence
         const float g = !(kFull || tb + r < L) ? 0.f
+                        : kUnb                ? unbounded_log_decay(bf16_to_f32(zin[r * kD]), a_h)
                         : kGated              ? gated_log_decay(bf16_to_f32(zin[r * kD]), a_h, lb)
                                               : clamp_log_decay(gin[r * kD], lb);
         run = fmaf(g, kLog2e, run);
@@ -324,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       give_up(H_PREP);
       return false;
     }
+    bool wide_here = false;  // unbounded map: this channel wide in this thread's diagonal block
     const uint32_t row = uint32_t(ch) * 128u, sw = uint32_t(ch) & 7u;
     uint32_t hq[4], hk[4], hg[4];  // fp16 pairs
     auto operands = [&](auto full_tag) {
@@ -334,6 +373,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float start = grp == 0 ? -r2 : grp == 1 ? -T1 : grp == 2 ? 0.f : T2;  // log2 e^{G_start - r}
       const float tau0 = exp2_sfu(r2), tau1 = exp2_sfu(last2 - r2);
       if (grp == 0) s_gamma[b * kD + ch] = exp2_sfu(last2);
+      // unbounded map: this channel wide in this thread's diagonal block (the same test as
+      // the position-pair step's)
+      const bool wide = kUnb && (grp < 2 ? T0 + T1 : T2 + T3) < -kWideBlock;
+      if constexpr (kUnb) {  // the wide channels of each diagonal block, 32 per warp
+        const uint32_t wm = __ballot_sync(0xffffffffu, wide);
+        if (lane == 0 && (grp & 1) == 0) s_tmem[4 + 4 * (grp >> 1) + quarter] = wm;
+        wide_here = wide;
+      }
       // q and k of the 8 tokens: bf16 element (t, ch) of the 128-byte-swizzled TMA tiles
       const uint32_t cc = uint32_t(ch & 63);
       const uint8_t *qk0 = sm + OFF_QKG + (ch >> 6) * 4096 + tb * 128 + (cc & 7u) * 2;
@@ -358,24 +405,97 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float k = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SK + off)) : 0.f;
           const float d = start + lg[r];  // log2 e^{G_t - r}
           const float f = exp2_sfu(d), g = exp2_sfu(-d);
-          qf[e] = q * f;
-          kf[e] = k * f;
-          kg[e] = k * g;
+          float qv = q * f, kv = k * f, gv = k * g;                  // tf32 Gram operands
+          qf[e] = qv * tau0;                                          // fp16 operands: Q Gamma,
+          kf[e] = kv * tau0;                                          // K Gamma,
+          kg[e] = gv * tau1;                                          // K e^{G_last - G}
+          if constexpr (kUnb) {
+            if (wide) {  // f (first block) or g (second) may overflow: out of the Gram, and
+              if (grp < 2) {  // the fp16 operands from their own exponentials (<= 1)
+                const float gm = exp2_sfu(d + r2);
+                qf[e] = q * gm;
+                kf[e] = k * gm;
+                qv = kv = 0.f;
+              } else {
+                kg[e] = k * exp2_sfu(last2 - r2 - d);
+                gv = 0.f;
+              }
+            }
+          }
           const uint32_t o4 = (r * 128 + ((cq ^ uint32_t(r)) << 4)) >> 2;  // row tb + r, whose t & 7 = r
-          gq[o4] = round_tf32_alu(qf[e]);
-          gk[o4] = round_tf32_alu(kf[e]);
-          gb[o4] = round_tf32_alu(kg[e]);
+          gq[o4] = round_tf32_alu(qv);
+          gk[o4] = round_tf32_alu(kv);
+          gb[o4] = round_tf32_alu(gv);
         }
-        hq[2 * half] = pack_f16x2(qf[0] * tau0, qf[1] * tau0);
-        hq[2 * half + 1] = pack_f16x2(qf[2] * tau0, qf[3] * tau0);
-        hk[2 * half] = pack_f16x2(kf[0] * tau0, kf[1] * tau0);
-        hk[2 * half + 1] = pack_f16x2(kf[2] * tau0, kf[3] * tau0);
-        hg[2 * half] = pack_f16x2(kg[0] * tau1, kg[1] * tau1);
-        hg[2 * half + 1] = pack_f16x2(kg[2] * tau1, kg[3] * tau1);
+        hq[2 * half] = pack_f16x2(qf[0], qf[1]);
+        hq[2 * half + 1] = pack_f16x2(qf[2], qf[3]);
+        hk[2 * half] = pack_f16x2(kf[0], kf[1]);
+        hk[2 * half + 1] = pack_f16x2(kf[2], kf[3]);
+        hg[2 * half] = pack_f16x2(kg[0], kg[1]);
+        hg[2 * half + 1] = pack_f16x2(kg[2], kg[3]);
       }
+    };
+    // Unbounded map. A thread whose channel is wide in its diagonal block puts its tokens'
+    // cumulative log2 decays (from the chunk start) into the S^T tile, once MMA1 of chunk
+    // c - 2 has read it: [128 c][36] (a row stride of 36 words keeps both the row writes and
+    // the column reads free of bank conflicts); the rows of narrow channels are not read.
+    float *Gs = reinterpret_cast<float *>(sm + OFF_ST);
+    auto stage_decays = [&](int c) {
+      if (c >= 2) bad |= !mbar_wait_sleep(&bars->mma1, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
+      const float T0 = s_tot[ch], T1 = s_tot[kD + ch], T2 = s_tot[2 * kD + ch];
+      const float g0 = grp == 0 ? 0.f : grp == 1 ? T0 : grp == 2 ? T0 + T1 : (T0 + T1) + T2;
+      float4 *dst = reinterpret_cast<float4 *>(Gs + ch * 36 + tb);
+      dst[0] = make_float4(g0 + lg[0], g0 + lg[1], g0 + lg[2], g0 + lg[3]);
+      dst[1] = make_float4(g0 + lg[4], g0 + lg[5], g0 + lg[6], g0 + lg[7]);
+    };
+    // A chunk with wide channels: their shares of the entries of the two diagonal blocks,
+    // A: sum_c k_tc k_ic e^{G_tc - G_ic} (i < t) and P: sum_c q_tc k_ic e^{G_tc - G_ic}
+    // (i <= t), from position pairs, one exponential (<= 1) per pair and wide channel,
+    // shared by A and P. Thread (block b, row tl, column il) owns entry (16 b + tl, 16 b + il)
+    // and walks the block's list of wide channels. Tokens past the end of the
+    // sequence only reach entries that P4 masks.
+    auto pair_shares = [&](int c) -> bool {
+      if (tid == 0) s_tmem[2 + (c & 1)] = uint32_t(c);  // for P4 of chunk c
+      const int pb = tid >> 8, tl = (tid >> 4) & 15, il = tid & 15;
+      const int t = 16 * pb + tl, i = 16 * pb + il;
+      float a = 0.f, p = 0.f;
+      if (il <= tl) {
+        // bf16 element (token, channel w) of the 128-byte-swizzled q / k tiles
+        auto elem = [&](uint32_t tile, int tok, int w) {
+          const uint32_t cw = uint32_t(w & 63);
+          return bf16_to_f32(*reinterpret_cast<const uint16_t *>(
+              sm + OFF_QKG + tile + uint32_t(w >> 6) * 4096u + uint32_t(tok) * 128u +
+              (((cw >> 3) ^ uint32_t(tok & 7)) << 4) + (cw & 7u) * 2u));
+        };
+#pragma unroll 1
+        for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t m = s_tmem[4 + 4 * pb + q4];
+          while (m != 0u) {
+            const int w = 32 * q4 + __ffs(int(m)) - 1;
+            m &= m - 1u;
+            const float e = exp2_sfu(Gs[w * 36 + t] - Gs[w * 36 + i]);
+            const float ke = elem(SK, i, w) * e;
+            a = fmaf(elem(SK, t, w), ke, a);
+            p = fmaf(elem(SQ, t, w), ke, p);
+          }
+        }
+      }
+      float *corr = reinterpret_cast<float *>(sm + OFF_CORR) + (c & 1) * 512;
+      if (il < tl) corr[pair_row_a(uint32_t(pb), uint32_t(tl)) + il] = a;
+      if (il <= tl) corr[pair_row_p(uint32_t(pb), uint32_t(tl)) + il] = p;
+      // every thread is past the decays before P4 reuses the S^T tile
+      if (named_bar_or(BAR_WORK, kWorkers, bad)) {
+        give_up(H_PREP);
+        return false;
+      }
+      return true;
     };
     if (full) operands(std::true_type{});
     else operands(std::false_type{});
+    if constexpr (kUnb) {  // one barrier: does any channel of this chunk need position pairs?
+      if (wide_here) stage_decays(c);
+      if (named_bar_or(BAR_WORK, kWorkers, wide_here || bad) && !pair_shares(c)) return false;
+    }
     handoff(H_PREP);  // the Gram operands are complete; the fp16 tiles are needed later
     st_at(sm, OFF_PK + (c % 3) * kPKBytes + sw64_chunk(32u + ch, grp), make_uint4(hg[0], hg[1], hg[2], hg[3]));
     st_at(sm, OFF_KG + b * kKGBytes + sw64_chunk(ch, grp), make_uint4(hk[0], hk[1], hk[2], hk[3]));
@@ -522,6 +642,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto extract_inverse = [&](int c, int j_out) -> bool {
     const int b = c & 1, L = chunk_len(c);
     float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
+    // unbounded map: the position-pair shares of chunk c's diagonal blocks, if it has any
+    const bool slow = kUnb && *reinterpret_cast<volatile uint32_t *>(s_tmem + 2 + b) == uint32_t(c);
+    const float *corr = reinterpret_cast<const float *>(sm + OFF_CORR) + b * 512;
     if (inv_group) {
       bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
       tc_fence_after();
@@ -534,6 +657,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (lane < 16) {
             const float bt = s_beta[b * kC + t];
             const int lim = t < L ? t - 16 * grp : 0;  // keep i < t
+            if (slow && grp == s) {
+              const float *cr = corr + pair_row_a(uint32_t(s), uint32_t(t & 15));
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                if (e < lim) vals[e] += cr[e];
+            }
 #pragma unroll
             for (int e = 0; e < 16; ++e) vals[e] = e < lim ? bt * vals[e] : 0.f;
             float4 *arow = reinterpret_cast<float4 *>(As + t * kALd + 16 * grp);
@@ -682,6 +811,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (lane < 16) {
           const int lim = (have && t < L) ? t + 1 - 8 * grp : 0;  // keep i <= t
+          if (slow && have && grp >= 2 * quarter) {  // columns inside the diagonal block
+            const float *cr = corr + pair_row_p(uint32_t(quarter), uint32_t(t & 15)) + 8 * (grp - 2 * quarter);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+              if (e < lim) vals[e] += cr[e];
+          }
 #pragma unroll
           for (int e = 0; e < 8; ++e) vals[e] = e < lim ? vals[e] : 0.f;
           st_at(sm + OFF_PK + (c % 3) * kPKBytes, sw64_chunk(t, grp), pack8_f16(vals));
@@ -894,7 +1029,7 @@ teardown:
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
-using KernelFn = decltype(&kda_chunked_kernel<false, false, false>);
+using KernelFn = decltype(&kda_chunked_kernel<false, DECAY_CLAMPED, false>);
 
 }  // namespace chunked
 }  // namespace kda

@@ -1,8 +1,8 @@
 """The unbounded log-decay of the earlier models, g = -e^{A_h} Softplus(z) (Kimi K3 --
 Architecture Notes, section 1.2, the GDN / Mamba-2 / Kimi Linear row of the mapping table),
-on the token-recurrent prefill kernel and in decode, against the fp64 oracle. Its decay has
-no lower bound, so a prefill request that would otherwise take the chunked tensor-core
-kernel runs the token-recurrent one; decays far beyond -5 per step are part of the cases."""
+in prefill (bf16 requests with d = 128 take the chunked kernel, the others the
+token-recurrent one) and in decode, against the fp64 oracle; decays far beyond -5 per step
+are part of the cases. The chunked kernel's own cases are in test_gpu_unbounded_chunked.py."""
 
 import numpy as np
 import pytest
@@ -46,15 +46,6 @@ def test_steep_decay_beyond_the_bound():
     out, fin = _run(case)
     o_ref, f_ref = _oracle(case)
     assert rel_max_err(out, o_ref) <= TOL_F32 and rel_max_err(fin, f_ref) <= TOL_F32
-
-
-def test_chunked_request_runs_the_recurrent_kernel():
-    """bf16, d = 128 would take the chunked kernel in the bounded forms; unbounded gives exactly the
-    forced token-recurrent result."""
-    case = workloads.make_prefill([65], H=2, device="cuda", seed=52, gated=True)
-    a, fa = _run(case)
-    b, fb = _run(case, recurrent=True)
-    assert torch.equal(a, b) and torch.equal(fa, fb)
 
 
 def test_with_output_gate():
