@@ -292,6 +292,15 @@ __device__ __forceinline__ void tma_store_3d(const void *tmap, const void *smem_
                "r"(smem_u32(smem_src)), "r"(x), "r"(y), "r"(z)
                : "memory");
 }
+// A small asynchronous copy global -> shared of kBytes (4, 8 or 16; both addresses aligned to
+// it), through L1; cp_async_wait_all makes this thread's copies visible to it.
+template <int kBytes>
+__device__ __forceinline__ void cp_async_small(void *smem, const void *gmem) {
+  static_assert(kBytes == 4 || kBytes == 8 || kBytes == 16, "cp.async takes 4, 8 or 16 bytes");
+  asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(smem)), "l"(gmem), "n"(kBytes)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

@@ -52,18 +52,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   const int col = 4 * tx;
   const bool col_ok = col < d_v;
 
-  // 1. issue all state loads of this thread (rows ty + 8 j)
-  float4 s4[kDecodeRowsPerThread];
-#pragma unroll
-  for (int j = 0; j < kDecodeRowsPerThread; ++j) {
-    const int c = ty + 8 * j;
-    s4[j] = (col_ok && c < d_k) ? __ldcs(reinterpret_cast<const float4 *>(S + int64_t(c) * d_v + col))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
-
-  // 2. token vectors, spread over all 8 warps: warps 0-3 take the query and key channels (and
+  // 1. token vectors, spread over all 8 warps: warps 0-3 take the query and key channels (and
   // k.q by warp reduction), warps 4-7 the value channels and the decay; through the prologue
-  // if asked.
+  // if asked. Their loads (and the prologue's convolution state and weights) are issued
+  // before the state's, so that the work that depends on them runs while the state streams in.
   const int c2 = tid & 127;  // channel of this thread in step 2
   const bool lo = tid < 128;
   float kq = 0.f, x0 = 0.f, x1 = 0.f;  // lo: query, key; hi: value, decay input
@@ -78,15 +70,15 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       x1 = kDecay == DECAY_CLAMPED ? static_cast<const float *>(decay)[vec_base + c2]
                                    : load_elem<kInBF16>(decay, vec_base + c2);
   }
+  // the prologue's loads: convolution state and weights of this thread's channels
+  const int C3 = 2 * d_k + d_v;
+  const int64_t sb = bh * 3 * C3;
+  const int np = lo ? 2 : 1;  // convolutions of this thread: q and k, or v
+  const bool on = c2 < (lo ? d_k : d_v);
+  const int cc0 = lo ? c2 : 2 * d_k + c2, cc1 = d_k + c2;
+  float xs[2][3], wv[2][4];
   if constexpr (kPrologue) {
-    const int C3 = 2 * d_k + d_v, h = int(bh % H);
-    const int64_t sb = bh * 3 * C3;
-    // all loads first (the state stores below would otherwise order them), then the 4-tap
-    // convolutions and Swish, then the state shifted by one token
-    const int np = lo ? 2 : 1;  // convolutions of this thread: q and k, or v
-    const bool on = c2 < (lo ? d_k : d_v);
-    const int cc0 = lo ? c2 : 2 * d_k + c2, cc1 = d_k + c2;
-    float xs[2][3], wv[2][4];
+    const int h = int(bh % H);
 #pragma unroll
     for (int p = 0; p < 2; ++p) {
       const int cc = p == 0 ? cc0 : cc1;
@@ -100,6 +92,29 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       wv[p][2] = w4.z;
       wv[p][3] = w4.w;
     }
+  }
+
+  // the output gate's logits of warp 0's columns, read at the very end: copied into shared
+  // memory now (the API keeps out_gate 16-byte aligned and d_v a multiple of 4)
+  constexpr int kEs = kInBF16 ? 2 : 4;
+  __shared__ __align__(16) uint8_t s_gr[128 * kEs];
+  if constexpr (kNormGate) {
+    if (ty == 0 && col_ok)
+      cp_async_small<4 * kEs>(s_gr + col * kEs, static_cast<const uint8_t *>(out_gate) + (bh * d_v + col) * kEs);
+  }
+
+  // 2. issue all state loads of this thread (rows ty + 8 j)
+  float4 s4[kDecodeRowsPerThread];
+#pragma unroll
+  for (int j = 0; j < kDecodeRowsPerThread; ++j) {
+    const int c = ty + 8 * j;
+    s4[j] = (col_ok && c < d_k) ? __ldcs(reinterpret_cast<const float4 *>(S + int64_t(c) * d_v + col))
+                                : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+
+  if constexpr (kPrologue) {
+    // the 4-tap convolutions and Swish, then the state shifted by one token (its loads all
+    // came first: the stores would otherwise order them)
     const float xt[2] = {x0, lo ? x1 : 0.f};
     float u[2];
 #pragma unroll
@@ -133,11 +148,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
         s_nrm[1][ty] = nk;
       }
     }
-    __syncthreads();
-    if (lo) {
-      x0 *= rsqrtf(((s_nrm[0][0] + s_nrm[0][1]) + (s_nrm[0][2] + s_nrm[0][3])) + pro.eps);
-      x1 *= rsqrtf(((s_nrm[1][0] + s_nrm[1][1]) + (s_nrm[1][2] + s_nrm[1][3])) + pro.eps);
-    }
+    // q and k stay unnormalised here: their norms are applied after the barrier below, as
+    // factors on y, z, k.q and the state update
   }
   if (lo) {
     s_q[c2] = x0;
@@ -182,18 +194,32 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
     zt[0] += za.x; zt[1] += za.y; zt[2] += za.z; zt[3] += za.w;
   }
   kq = s_kq[0] + s_kq[1] + s_kq[2] + s_kq[3];
+  float rk = 1.f;  // the prologue's L2 norms of q and k: 1 / |q|, 1 / |k|
+  if constexpr (kPrologue) {
+    const float rq = rsqrtf(((s_nrm[0][0] + s_nrm[0][1]) + (s_nrm[0][2] + s_nrm[0][3])) + pro.eps);
+    rk = rsqrtf(((s_nrm[1][0] + s_nrm[1][1]) + (s_nrm[1][2] + s_nrm[1][3])) + pro.eps);
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      yt[e] *= rk;
+      zt[e] *= rq;
+    }
+    kq *= rq * rk;
+  }
 
   // 4. delta-rule write u = b (v - y), S_t = S' + k u^T, o = scale (z + u (k.q))
-  float u[4];
+  float u[4], uk[4];  // uk = u / |k| when k is normalised here, so that k_c uk = k^_c u
 #pragma unroll
-  for (int e = 0; e < 4; ++e) u[e] = b * (s_v[(col + e) & 127] - yt[e]);
+  for (int e = 0; e < 4; ++e) {
+    u[e] = b * (s_v[(col + e) & 127] - yt[e]);
+    uk[e] = kPrologue ? u[e] * rk : u[e];
+  }
 #pragma unroll
   for (int j = 0; j < kDecodeRowsPerThread; ++j) {
     const int c = ty + 8 * j;
     if (col_ok && c < d_k) {
       const float kc = s_k[c];
-      const float4 w = make_float4(s4[j].x + kc * u[0], s4[j].y + kc * u[1], s4[j].z + kc * u[2],
-                                   s4[j].w + kc * u[3]);
+      const float4 w = make_float4(s4[j].x + kc * uk[0], s4[j].y + kc * uk[1], s4[j].z + kc * uk[2],
+                                   s4[j].w + kc * uk[3]);
       __stcs(reinterpret_cast<float4 *>(S + int64_t(c) * d_v + col), w);
     }
   }
@@ -207,10 +233,11 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
       const float rstd = rsqrtf(ss / float(d_v) + norm_eps);
       if (col_ok) {
+        cp_async_wait_all();
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float w = norm_weight != nullptr ? norm_weight[col + e] : 1.f;
-          const float r = load_elem<kInBF16>(out_gate, bh * d_v + col + e);
+          const float r = load_elem<kInBF16>(s_gr, col + e);
           store_elem<kOutBF16>(out, bh * d_v + col + e, output_gate(o[e], rstd, w, r));
         }
       }
