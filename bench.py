@@ -369,7 +369,16 @@ def main():
                     help="prefill heads (a smaller value is for profiler captures; the headline uses 96)")
     ap.add_argument("--prefill-only", action="store_true",
                     help="time the prefill kernel only (no decode, e2e or CPU baseline): for profiler captures")
+    ap.add_argument("--form", choices=["clamped", "gated", "outgate", "unbounded", "unbounded-steep", "fused"],
+                    default="clamped",
+                    help="with --prefill-only: the decay form timed (unbounded-steep: logits +40 on every "
+                         "third channel, so that every chunk takes the position-pair step)")
+    ap.add_argument("--decode-only", type=int, default=0, metavar="STEPS",
+                    help="run STEPS decode steps on B=256, H=96 (plain, or with --form fused the whole layer "
+                         "step) after 3 warm-up ones and print their mean time: for profiler captures")
     args = ap.parse_args()
+    if args.form != "clamped" and not (args.prefill_only or args.decode_only):
+        ap.error("--form goes with --prefill-only or --decode-only")
     args.warmup = max(args.warmup, 3)
 
     if args.impl == "reference":
@@ -382,13 +391,31 @@ def main():
     binding.lib()
     hbm_gbs, tf_burst, tf_sust, peak_src = peaks()
 
+    if args.decode_only:
+        if (args.form == "fused") != (args.form != "clamped"):
+            raise SystemExit("--decode-only takes --form clamped (plain) or fused")
+        ms = time_decode(args.decode_only, 1, 3, world, seed=rank, fused=args.form == "fused")
+        if rank == 0:
+            print(json.dumps({"decode_only": True, "form": args.form, "steps": args.decode_only,
+                              "ms_per_step": sum(ms) / len(ms)}), flush=True)
+        return
+    if args.form == "fused":
+        raise SystemExit("--form fused goes with --decode-only")
+    logits = args.form != "clamped"
     if args.heads == PREFILL["H"]:
-        case = workloads.prefill_workload(PREFILL["workload"], device="cuda", seed=rank)
+        name = {"clamped": PREFILL["workload"], "outgate": "prefill_k3_outgate_T4096_H96"}.get(
+            args.form, "prefill_k3_gated_T4096_H96")
+        case = workloads.prefill_workload(name, device="cuda", seed=rank)
     else:
-        case = workloads.make_prefill([PREFILL["T"]], H=args.heads, device="cuda", seed=rank)
+        case = workloads.make_prefill([PREFILL["T"]], H=args.heads, device="cuda", seed=rank, gated=logits,
+                                      out_gate=args.form == "outgate")
+    if args.form == "unbounded-steep":
+        case.z[:, :, ::3] = 40.0
     T, H = case.total_tokens, case.num_heads
     with ClockSampler(local) as clocks:
-        total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world)
+        total_ms, launch_ms = time_prefill(case, args.steps, args.warmup, world, gated=args.form == "gated",
+                                           out_gate=args.form == "outgate",
+                                           unbounded=args.form.startswith("unbounded"))
         dec_ms = None if args.prefill_only else time_decode(DECODE["steps"], 1, 1, world, seed=rank)
         gated_ms = outgate_ms = prologue_ms = unbounded_ms = unbounded_rec_ms = unbounded_steep_ms = fdec_ms = None
         if not args.prefill_only and args.heads == PREFILL["H"]:
@@ -414,7 +441,7 @@ def main():
             del ucase
     if args.prefill_only:
         if rank == 0:
-            print(json.dumps({"prefill_only": True, "heads": H, "ms_per_step": total_ms / args.steps,
+            print(json.dumps({"prefill_only": True, "form": args.form, "heads": H, "ms_per_step": total_ms / args.steps,
                               "launch_ms": sum(launch_ms) / len(launch_ms)}), flush=True)
         return
     total_ms = max_over_ranks(total_ms, world)
