@@ -300,6 +300,12 @@ __device__ __forceinline__ void cp_async_small(void *smem, const void *gmem) {
   asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(smem_u32(smem)), "l"(gmem), "n"(kBytes)
                : "memory");
 }
+// 16 bytes global -> shared through L2 only; ok == false writes 16 zero bytes and reads nothing
+__device__ __forceinline__ void cp_async_16_zfill(void *smem, const void *gmem, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(smem)), "l"(gmem),
+               "r"(ok ? 16 : 0)
+               : "memory");
+}
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }

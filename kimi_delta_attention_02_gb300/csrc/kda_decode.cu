@@ -9,9 +9,11 @@
 //
 // One CTA of 256 threads per (sequence, head). Thread (ty, tx) owns value
 // columns 4tx..4tx+3 of key rows ty, ty+8, ..., ty+120: every state access is a
-// 128-bit load or store and each warp touches whole 512-byte rows, so the state
-// streams through HBM fully coalesced. The 16 state loads of a thread are issued
-// before anything waits on them. The log-decay is either the clamped log_alpha
+// 128-bit copy or store and each warp touches whole 512-byte rows, so the state
+// streams through HBM fully coalesced. The state comes into shared memory by
+// cp.async (16 copies per thread, issued before anything waits on them), so that
+// it takes no registers: 80 registers and 72 KB of shared memory per CTA let
+// three CTAs share an SM. The log-decay is either the clamped log_alpha
 // input or, in the gated form (section 1.2), g = g_min * Sigmoid(e^{A_h} z).
 // Optionally the read-out goes through the output gate of section 1.3,
 // Sigmoid(r) * w * o / rms(o), before it is written: warp 0 holds the whole d_v
@@ -35,7 +37,7 @@ struct Prologue {
 };
 
 template <bool kInBF16, bool kOutBF16, int kDecay, bool kNormGate, bool kPrologue>
-__global__ void __launch_bounds__(kDecodeThreads, 2)
+__global__ void __launch_bounds__(kDecodeThreads, 3)
     kda_decode_kernel(const void *__restrict__ q, const void *__restrict__ k, const void *__restrict__ v,
                       const void *__restrict__ decay, const float *__restrict__ A_log,
                       const float *__restrict__ beta, float *__restrict__ state, const void *__restrict__ out_gate,
@@ -52,10 +54,27 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   const int col = 4 * tx;
   const bool col_ok = col < d_v;
 
+  // The state goes into shared memory (cp.async, L2 only; rows or columns past d_k, d_v read
+  // as zeros), so that it holds no registers and three CTAs fit on an SM. Where the copies
+  // are issued was measured per form: after the token loads when the prologue feeds a
+  // logit-mapped decay (0.51 against 0.56 ms for B=256, H=96), before them otherwise (with
+  // the prologue and the clamped decay 0.54 against 0.71 ms; with the output gate 0.47
+  // against 0.49 ms).
+  constexpr bool kTokensFirst = kPrologue && kDecay != DECAY_CLAMPED;
+  extern __shared__ __align__(16) float s_st[];  // [128 key rows][128 value columns]
+  auto issue_state_copies = [&]() {
+#pragma unroll
+    for (int j = 0; j < kDecodeRowsPerThread; ++j) {
+      const int c = ty + 8 * j;
+      const bool ok = col_ok && c < d_k;
+      cp_async_16_zfill(s_st + c * 128 + col, ok ? S + int64_t(c) * d_v + col : S, ok);
+    }
+  };
+  if constexpr (!kTokensFirst) issue_state_copies();
+
   // 1. token vectors, spread over all 8 warps: warps 0-3 take the query and key channels (and
   // k.q by warp reduction), warps 4-7 the value channels and the decay; through the prologue
-  // if asked. Their loads (and the prologue's convolution state and weights) are issued
-  // before the state's, so that the work that depends on them runs while the state streams in.
+  // if asked (the prologue's convolution state and weights are loaded here too).
   const int c2 = tid & 127;  // channel of this thread in step 2
   const bool lo = tid < 128;
   float kq = 0.f, x0 = 0.f, x1 = 0.f;  // lo: query, key; hi: value, decay input
@@ -103,14 +122,8 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
       cp_async_small<4 * kEs>(s_gr + col * kEs, static_cast<const uint8_t *>(out_gate) + (bh * d_v + col) * kEs);
   }
 
-  // 2. issue all state loads of this thread (rows ty + 8 j)
-  float4 s4[kDecodeRowsPerThread];
-#pragma unroll
-  for (int j = 0; j < kDecodeRowsPerThread; ++j) {
-    const int c = ty + 8 * j;
-    s4[j] = (col_ok && c < d_k) ? __ldcs(reinterpret_cast<const float4 *>(S + int64_t(c) * d_v + col))
-                                : make_float4(0.f, 0.f, 0.f, 0.f);
-  }
+  // 2. the state copies of this thread (rows ty + 8 j), issued here or before step 1
+  if constexpr (kTokensFirst) issue_state_copies();
 
   if constexpr (kPrologue) {
     // the 4-tap convolutions and Swish, then the state shifted by one token (its loads all
@@ -171,15 +184,18 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   const float b = beta[bh];
   __syncthreads();
 
-  // 3. decay rows, partial predictions y = S'^T k and readouts z = S'^T q
+  // 3. decay rows, partial predictions y = S'^T k and readouts z = S'^T q (each thread reads
+  // back the rows it copied)
+  cp_async_wait_all();
   float y[4] = {0.f, 0.f, 0.f, 0.f}, z[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int j = 0; j < kDecodeRowsPerThread; ++j) {
     const int c = ty + 8 * j;
     const float a = s_a[c & 127], kc = s_k[c & 127], qc = s_q[c & 127];
-    s4[j].x *= a; s4[j].y *= a; s4[j].z *= a; s4[j].w *= a;
-    y[0] += kc * s4[j].x; y[1] += kc * s4[j].y; y[2] += kc * s4[j].z; y[3] += kc * s4[j].w;
-    z[0] += qc * s4[j].x; z[1] += qc * s4[j].y; z[2] += qc * s4[j].z; z[3] += qc * s4[j].w;
+    float4 sv = *reinterpret_cast<const float4 *>(s_st + c * 128 + col);
+    sv.x *= a; sv.y *= a; sv.z *= a; sv.w *= a;
+    y[0] += kc * sv.x; y[1] += kc * sv.y; y[2] += kc * sv.z; y[3] += kc * sv.w;
+    z[0] += qc * sv.x; z[1] += qc * sv.y; z[2] += qc * sv.z; z[3] += qc * sv.w;
   }
   *reinterpret_cast<float4 *>(&s_red_y[ty][col]) = make_float4(y[0], y[1], y[2], y[3]);
   *reinterpret_cast<float4 *>(&s_red_z[ty][col]) = make_float4(z[0], z[1], z[2], z[3]);
@@ -217,9 +233,10 @@ __global__ void __launch_bounds__(kDecodeThreads, 2)
   for (int j = 0; j < kDecodeRowsPerThread; ++j) {
     const int c = ty + 8 * j;
     if (col_ok && c < d_k) {
-      const float kc = s_k[c];
-      const float4 w = make_float4(s4[j].x + kc * uk[0], s4[j].y + kc * uk[1], s4[j].z + kc * uk[2],
-                                   s4[j].w + kc * uk[3]);
+      const float kc = s_k[c], a = s_a[c];
+      const float4 sv = *reinterpret_cast<const float4 *>(s_st + c * 128 + col);
+      const float4 w = make_float4(fmaf(sv.x, a, kc * uk[0]), fmaf(sv.y, a, kc * uk[1]),
+                                   fmaf(sv.z, a, kc * uk[2]), fmaf(sv.w, a, kc * uk[3]));
       __stcs(reinterpret_cast<float4 *>(S + int64_t(c) * d_v + col), w);
     }
   }
@@ -271,7 +288,18 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const voi
   const Kern kern = table[24 * int(pro) + 12 * int(out_gate != nullptr) + 6 * int(in_bf16) + 3 * int(out_bf16) +
                           decay_form];
   const Prologue pr{conv_w, conv_state, l2_eps};
-  kern<<<grid, block, 0, stream>>>(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps, pr, out, H,
+  constexpr int kStateBytes = 128 * 128 * 4;  // the state tile in dynamic shared memory
+  static bool attr_set[48] = {};
+  const int idx = 24 * int(pro) + 12 * int(out_gate != nullptr) + 6 * int(in_bf16) + 3 * int(out_bf16) + decay_form;
+  if (!attr_set[idx]) {
+    // and the whole of the SM's unified memory as shared memory, so that three CTAs fit
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateBytes);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+    if (e != cudaSuccess) return e;
+    attr_set[idx] = true;
+  }
+  kern<<<grid, block, kStateBytes, stream>>>(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps, pr, out, H,
                                    d_k, d_v, lb, scale);
   return cudaGetLastError();
 }
