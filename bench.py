@@ -267,11 +267,11 @@ def time_decode(steps_per_rep, reps, warmup, world, seed=0, fused=False):
     return [a.elapsed_time(b) for a, b in ev]
 
 
-def time_prologue(steps, warmup, world, seed=0):
+def time_prologue(steps, warmup, world, seed=0, H=None):
     """The input prologue (ShortConv, Swish, L2 norm) on the K3-shaped layer's raw projections,
-    T=4096, H=96, bf16, with initial and final convolution states. Returns per-launch ms."""
+    T=4096, H=96 (or H), bf16, with initial and final convolution states. Returns per-launch ms."""
     from kimi_delta_attention_02_gb300 import binding, workloads
-    case = workloads.make_prologue([PREFILL["T"]], H=PREFILL["H"], device="cuda", seed=seed)
+    case = workloads.make_prologue([PREFILL["T"]], H=H or PREFILL["H"], device="cuda", seed=seed)
     q, k, v = torch.empty_like(case.q_raw), torch.empty_like(case.k_raw), torch.empty_like(case.v_raw)
     fin = torch.empty_like(case.conv_init)
     stream = torch.cuda.current_stream()
@@ -376,6 +376,8 @@ def main():
     ap.add_argument("--decode-only", type=int, default=0, metavar="STEPS",
                     help="run STEPS decode steps on B=256, H=96 (plain, or with --form fused the whole layer "
                          "step) after 3 warm-up ones and print their mean time: for profiler captures")
+    ap.add_argument("--prologue-only", action="store_true",
+                    help="time the input prologue pass only (T=4096, --heads heads): for profiler captures")
     args = ap.parse_args()
     if args.form != "clamped" and not (args.prefill_only or args.decode_only):
         ap.error("--form goes with --prefill-only or --decode-only")
@@ -391,6 +393,12 @@ def main():
     binding.lib()
     hbm_gbs, tf_burst, tf_sust, peak_src = peaks()
 
+    if args.prologue_only:
+        p_ms = time_prologue(args.steps, args.warmup, world, seed=rank, H=args.heads)
+        if rank == 0:
+            print(json.dumps({"prologue_only": True, "heads": args.heads, "launch_ms": sum(p_ms) / len(p_ms)}),
+                  flush=True)
+        return
     if args.decode_only:
         if (args.form == "fused") != (args.form != "clamped"):
             raise SystemExit("--decode-only takes --form clamped (plain) or fused")
