@@ -116,3 +116,19 @@ def test_long_sequence_heads():
     """T = 4096 at H = 4 with the gated workload's logits, full-size chunks throughout."""
     case = workloads.make_prefill([4096], H=4, device="cuda", seed=370, gated=True)
     _check(case)
+
+
+def test_benchmark_workload_sampled_heads():
+    """The benchmark's T=4096, H=96 logits through the unbounded map, in the launch `bench.py`
+    times, checked on four heads: the one with the largest e^{A_h} (the most chunks with wide
+    channels), the smallest, and two others."""
+    case = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda")
+    out, fin = _run(case)
+    A = case.A_log.cpu()
+    heads = sorted({int(A.argmax()), int(A.argmin()), 17, 60})
+    sel = lambda t: cpu(t[:, heads]).contiguous()
+    o_ref, f_ref = kda_recurrent_unbounded(sel(case.q), sel(case.k), sel(case.v), sel(case.z), A[heads].contiguous(),
+                                           sel(case.beta), cpu(case.cu_seqlens).long().numpy(),
+                                           init_state=cpu(case.init_state[:, heads]).contiguous(), num_threads=4)
+    e_o, e_f = rel_max_err(out[:, heads], o_ref), rel_max_err(fin[:, heads], f_ref)
+    assert e_o <= TOL_BF16 and e_f <= TOL_BF16, (heads, e_o, e_f)
