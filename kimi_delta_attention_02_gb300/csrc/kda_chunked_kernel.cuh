@@ -335,6 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Every chunk but the last of a sequence is full: it takes code without the masks.
     const bool full = L == kC;
     float lg[8];  // log2 of Gamma within the group: sum of the group's decays up to each token
+    bool maybe_wide = false;  // unbounded map: this group's decay passes half the wide bound
     auto decay_sums = [&](auto full_tag) {
       constexpr bool kFull = decltype(full_tag)::value;
       const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG) + tb * kD + ch;
@@ -350,6 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         lg[r] = run;
       }
       s_tot[grp * kD + ch] = run;
+      maybe_wide = kUnb && run < -0.5f * kWideBlock;  // a wide channel has such a group in its block
     };
     if (full) decay_sums(std::true_type{});
     else decay_sums(std::false_type{});
@@ -358,7 +360,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       bulk_wait_read();
       store_pending = false;
     }
-    if (named_bar_or(BAR_WORK, kWorkers, bad)) {
+    // unbounded map: `flagged` also says that some group decays past half the wide bound, so
+    // that only such chunks pay for the exact test below (which also catches a wait that gave up)
+    const bool flagged = named_bar_or(BAR_WORK, kWorkers, bad || maybe_wide);
+    if (!kUnb && flagged) {
       give_up(H_PREP);
       return false;
     }
@@ -492,9 +497,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     if (full) operands(std::true_type{});
     else operands(std::false_type{});
-    if constexpr (kUnb) {  // one barrier: does any channel of this chunk need position pairs?
-      if (wide_here) stage_decays(c);
-      if (named_bar_or(BAR_WORK, kWorkers, wide_here || bad) && !pair_shares(c)) return false;
+    if constexpr (kUnb) {  // does any channel of this chunk need position pairs?
+      if (flagged) {
+        if (wide_here) stage_decays(c);
+        if (named_bar_or(BAR_WORK, kWorkers, wide_here || bad) && !pair_shares(c)) return false;
+      }
     }
     handoff(H_PREP);  // the Gram operands are complete; the fp16 tiles are needed later
     st_at(sm, OFF_PK + (c % 3) * kPKBytes + sw64_chunk(32u + ch, grp), make_uint4(hg[0], hg[1], hg[2], hg[3]));
