@@ -21,6 +21,8 @@
 // pass the prologue of section 1.1 (4-tap short convolution over the sequence's
 // convolution state, which is shifted in place, then Swish, then the L2 norm of q
 // and k): the conv state adds 3 x (2 d_k + d_v) values per (sequence, head).
+#include <atomic>
+
 #include "kda_common.cuh"
 
 namespace kda {
@@ -289,15 +291,20 @@ cudaError_t launch_decode(const void *q, const void *k, const void *v, const voi
                           decay_form];
   const Prologue pr{conv_w, conv_state, l2_eps};
   constexpr int kStateBytes = 128 * 128 * 4;  // the state tile in dynamic shared memory
-  static bool attr_set[48] = {};
+  // the kernel attributes, set once per kernel and device (bit d of attr_set[idx] for device d;
+  // a device past 63 sets them at every launch)
+  static std::atomic<uint64_t> attr_set[48];
   const int idx = 24 * int(pro) + 12 * int(out_gate != nullptr) + 6 * int(in_bf16) + 3 * int(out_bf16) + decay_form;
-  if (!attr_set[idx]) {
+  int dev = 0;
+  if (const cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+  const uint64_t bit = dev < 64 ? uint64_t(1) << dev : 0;
+  if (bit == 0 || (attr_set[idx].load(std::memory_order_acquire) & bit) == 0) {
     // and the whole of the SM's unified memory as shared memory, so that three CTAs fit
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kStateBytes);
     if (e == cudaSuccess)
       e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return e;
-    attr_set[idx] = true;
+    attr_set[idx].fetch_or(bit, std::memory_order_release);
   }
   kern<<<grid, block, kStateBytes, stream>>>(q, k, v, decay, A_log, beta, state, out_gate, norm_weight, norm_eps, pr, out, H,
                                    d_k, d_v, lb, scale);
