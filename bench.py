@@ -381,6 +381,12 @@ def main():
     args = ap.parse_args()
     if args.form != "clamped" and not (args.prefill_only or args.decode_only):
         ap.error("--form goes with --prefill-only or --decode-only")
+    if args.decode_only and args.form not in ("clamped", "fused"):
+        ap.error("--decode-only takes --form clamped (plain) or fused")
+    if args.form == "fused" and not args.decode_only:
+        ap.error("--form fused goes with --decode-only")
+    if sum(map(bool, (args.prefill_only, args.decode_only, args.prologue_only))) > 1:
+        ap.error("--prefill-only, --decode-only and --prologue-only exclude one another")
     args.warmup = max(args.warmup, 3)
 
     if args.impl == "reference":
@@ -400,15 +406,11 @@ def main():
                   flush=True)
         return
     if args.decode_only:
-        if (args.form == "fused") != (args.form != "clamped"):
-            raise SystemExit("--decode-only takes --form clamped (plain) or fused")
         ms = time_decode(args.decode_only, 1, 3, world, seed=rank, fused=args.form == "fused")
         if rank == 0:
             print(json.dumps({"decode_only": True, "form": args.form, "steps": args.decode_only,
                               "ms_per_step": sum(ms) / len(ms)}), flush=True)
         return
-    if args.form == "fused":
-        raise SystemExit("--form fused goes with --decode-only")
     logits = args.form != "clamped"
     if args.heads == PREFILL["H"]:
         name = {"clamped": PREFILL["workload"], "outgate": "prefill_k3_outgate_T4096_H96"}.get(
