@@ -380,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (grp == 0) s_gamma[b * kD + ch] = exp2_sfu(last2);
       // unbounded map: this channel wide in this thread's diagonal block (the same test as
       // the position-pair step's)
-      const bool wide = kUnb && (grp < 2 ? T0 + T1 : T2 + T3) < -kWideBlock;
+      [[maybe_unused]] const bool wide = kUnb && (grp < 2 ? T0 + T1 : T2 + T3) < -kWideBlock;
       if constexpr (kUnb) {  // the wide channels of each diagonal block, 32 per warp
         const uint32_t wm = __ballot_sync(0xffffffffu, wide);
         if (lane == 0 && (grp & 1) == 0) s_tmem[4 + 4 * (grp >> 1) + quarter] = wm;
@@ -1036,7 +1036,11 @@ teardown:
   if (warp == 0) tmem_dealloc(tmem, TM_COLS);
 }
 
-using KernelFn = decltype(&kda_chunked_kernel<false, DECAY_CLAMPED, false>);
+// the kernel's pointer type, spelled out (naming an instantiation here would instantiate it in
+// every translation unit that includes this header)
+using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, OutGate,
+                          const float *, const float *, const int32_t *, const float *, void *, float *, int, float,
+                          float, uint32_t *);
 
 }  // namespace chunked
 }  // namespace kda

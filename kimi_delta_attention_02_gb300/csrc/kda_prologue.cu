@@ -35,7 +35,7 @@ __global__ void __launch_bounds__(kProThreads, 2)
                         void *__restrict__ q_out, void *__restrict__ k_out, void *__restrict__ v_out,
                         void *__restrict__ conv_final, int64_t T, int H, int d_k, int d_v, int n_tiles, float eps) {
   using Elem = typename std::conditional<kBF16, uint16_t, float>::type;
-  extern __shared__ __align__(16) uint8_t pro_smem[];
+  extern __shared__ __align__(128) uint8_t pro_smem[];
   Elem *s_x = reinterpret_cast<Elem *>(pro_smem);  // [kProTile + 3][C3]: raw rows t0 - 3 .. t0 + 31
   __shared__ int32_t s_seq[kProTile];
   __shared__ int64_t s_bos[kProTile];
