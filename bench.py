@@ -299,21 +299,25 @@ def time_e2e(case_cpu, steps, warmup):
     """Prefill through pinned host buffers: every step copies its inputs host -> device, runs
     kda_prefill and copies out + final state back to pinned host memory. Steps are streamed
     (binding.HostPrefillStream): the next step's inputs travel while the current one computes.
-    Returns (ms per step streamed, ms per step one at a time, h2d bytes, d2h bytes)."""
+    Also timed: the same with one copy stream for both directions ("half duplex": the kernel
+    still overlaps the copies, the two directions never do), and one step at a time.
+    Returns ({mode: ms per step}, h2d bytes, d2h bytes)."""
     from kimi_delta_attention_02_gb300 import binding
     hp = binding.HostPrefillStream(case_cpu.q, case_cpu.k, case_cpu.v, case_cpu.log_alpha, case_cpu.beta,
                                    case_cpu.cu_seqlens, case_cpu.init_state)
-    hp.run(warmup)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    hp.run(steps)
-    torch.cuda.synchronize()
-    stream_ms = (time.perf_counter() - t0) * 1e3 / steps
+    ms = {}
+    for mode in ("streamed", "half duplex"):
+        hp.run(warmup, duplex=mode == "streamed")
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        hp.run(steps, duplex=mode == "streamed")
+        torch.cuda.synchronize()
+        ms[mode] = (time.perf_counter() - t0) * 1e3 / steps
     t0 = time.perf_counter()
     for _ in range(steps):
         hp.run(1)
-    one_ms = (time.perf_counter() - t0) * 1e3 / steps
-    return stream_ms, one_ms, hp.h2d_bytes, hp.d2h_bytes
+    ms["one step at a time"] = (time.perf_counter() - t0) * 1e3 / steps
+    return ms, hp.h2d_bytes, hp.d2h_bytes
 
 
 def cpu_oracle_sample(case_cpu, heads: int):
@@ -513,10 +517,13 @@ def main():
     cpu_base = None
     if rank == 0:
         case_cpu = workloads.prefill_workload(PREFILL["workload"], device="cpu", seed=0)
-        e2e_ms, one_ms, h2d, d2h = time_e2e(case_cpu, max(4, args.steps // 2), 2)
-        e2e = {"value": T / (e2e_ms / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e2e_ms, "streamed": True,
-               "one_step_at_a_time": {"value": T / (one_ms / 1e3), "ms_per_step": one_ms}}
+        modes, h2d, d2h = time_e2e(case_cpu, max(4, args.steps // 2), 2)
+        # three ways of driving the host-buffer path are timed; the fastest is the line's value (on
+        # some hosts the link carries both directions at once more slowly than one after another)
+        best = min(modes, key=modes.get)
+        e2e = {"value": T / (modes[best] / 1e3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": modes[best], "mode": best,
+               "modes_ms_per_step": modes}
         if not args.no_cpu_baseline:
             heads = H  # the whole workload: a few seconds on the host's cores
             dt, cores, th = cpu_oracle_sample(case_cpu, heads)

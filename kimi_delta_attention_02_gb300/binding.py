@@ -495,9 +495,7 @@ class HostPrefillStream:
     def d2h_bytes(self) -> int:
         return self.host_out[0].numel() * self.host_out[0].element_size() + self.host_final[0].numel() * 4
 
-    def enqueue(self):
-        """Enqueue one step (copies in, kernel, copies back) without waiting."""
-        i = self.steps_done
+    def _in(self, i):
         b = i & 1
         with torch.cuda.stream(self.s_in):
             if i >= 2:
@@ -507,6 +505,9 @@ class HostPrefillStream:
             if self.dev_init[b] is not None:
                 self.dev_init[b].copy_(self.host_init, non_blocking=True)
             self.ev_in[b].record(self.s_in)
+
+    def _run(self, i):
+        b = i & 1
         with torch.cuda.stream(self.s_run):
             self.s_run.wait_event(self.ev_in[b])
             if i >= 2:
@@ -515,17 +516,40 @@ class HostPrefillStream:
             prefill(q, k, v, la, bt, cu, self.dev_init[b], out=self.dev_out[b], final_state=self.dev_final[b],
                     stream=self.s_run)
             self.ev_run[b].record(self.s_run)
-        with torch.cuda.stream(self.s_back):
-            self.s_back.wait_event(self.ev_run[b])
+
+    def _back(self, i, stream):
+        b = i & 1
+        with torch.cuda.stream(stream):
+            stream.wait_event(self.ev_run[b])
             self.host_out[b].copy_(self.dev_out[b], non_blocking=True)
             self.host_final[b].copy_(self.dev_final[b], non_blocking=True)
-            self.ev_back[b].record(self.s_back)
+            self.ev_back[b].record(stream)
+
+    def enqueue(self):
+        """Enqueue one step (copies in, kernel, copies back) without waiting."""
+        i = self.steps_done
+        self._in(i)
+        self._run(i)
+        self._back(i, self.s_back)
         self.steps_done += 1
 
-    def run(self, steps: int):
-        """Run ``steps`` streamed steps and return the last step's (out, final_state) on the host."""
-        for _ in range(steps):
-            self.enqueue()
+    def run(self, steps: int, duplex: bool = True):
+        """Run ``steps`` streamed steps and return the last step's (out, final_state) on the host.
+        ``duplex``: copies in and copies back on their own streams, so that both directions may
+        run at once; otherwise one copy stream carries step i+1's inputs and then step i's
+        results, so that the kernel still overlaps the copies but the two directions never do."""
+        if duplex:
+            for _ in range(steps):
+                self.enqueue()
+        elif steps > 0:
+            i0 = self.steps_done
+            self._in(i0)
+            for n in range(steps):
+                self._run(i0 + n)
+                if n + 1 < steps:
+                    self._in(i0 + n + 1)
+                self._back(i0 + n, self.s_in)
+            self.steps_done = i0 + steps
         b = (self.steps_done - 1) & 1
         self.ev_back[b].synchronize()
         return self.host_out[b], self.host_final[b]

@@ -140,17 +140,19 @@ def test_long_context_sampled_heads():
     _check(case, heads=workloads.sampled_heads(32, 4, seed=0))
 
 
-@pytest.mark.parametrize("streamed", [False, True])
+@pytest.mark.parametrize("streamed", [False, True, "half duplex"])
 def test_host_buffer_prefill_matches_device_call(streamed):
-    """The host-buffer paths (one step at a time, and streamed over two staging sets) return
-    exactly the device call's out and final state, at every step of a run."""
+    """The host-buffer paths (one step at a time, and streamed over two staging sets, with both
+    copy directions on their own streams or on one) return exactly the device call's out and
+    final state, at every step of a run; the streamed runs alternate the two modes."""
     case = workloads.make_prefill([40, 0, 97], H=4, device="cpu", seed=23)
     o_ref, f_ref = binding.prefill(*(t.cuda() for t in (case.q, case.k, case.v, case.log_alpha, case.beta,
                                                         case.cu_seqlens, case.init_state)))
     cls = binding.HostPrefillStream if streamed else binding.HostPrefill
     hp = cls(case.q, case.k, case.v, case.log_alpha, case.beta, case.cu_seqlens, case.init_state)
-    for steps in (1, 1, 3, 2):
-        out, fin = hp.run(steps) if streamed else hp()
+    for n, steps in enumerate((1, 1, 3, 2)):
+        duplex = streamed is True if n % 2 == 0 else streamed is not True
+        out, fin = hp.run(steps, duplex=duplex) if streamed else hp()
         assert out.device.type == "cpu" and fin.device.type == "cpu"
         assert torch.equal(out, o_ref.cpu()) and torch.equal(fin, f_ref.cpu())
     binding.check_device_error()
