@@ -191,3 +191,32 @@ def test_planted_unbounded_mistake_is_caught(name):
         except AssertionError:
             failed.append(pin.__name__)
     assert failed, f"no pin caught {name}"
+
+
+@pytest.mark.parametrize("chunk", [16, 32, 64])
+def test_unbounded_chunked_form_agrees_with_recurrence(chunk):
+    """The chunkwise form (oracle/chunked.py, every e^{G_t - G_i} formed from the difference,
+    i.e. from position pairs) and the token recurrence agree for the unbounded map with steps
+    of -80 on every third channel (far past the e^80 that a single reference could carry)
+    and ordinary steps elsewhere, over packed sequences of lengths that are no multiple of the
+    chunk."""
+    from oracle.chunked import kda_chunked
+    rng = np.random.default_rng(77)
+    lens = [45, 1, 70]
+    cu = np.concatenate([[0], np.cumsum(lens)])
+    T, H, d = cu[-1], 2, 8
+    q = rng.standard_normal((T, H, d))
+    k = rng.standard_normal((T, H, d))
+    k /= np.linalg.norm(k, axis=-1, keepdims=True)
+    v = rng.standard_normal((T, H, d))
+    z = -1.0 + 2.0 * rng.standard_normal((T, H, d))
+    z[:, :, ::3] = 40.0
+    A_log = np.array([np.log(2.0), -0.3])
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal((T, H))))
+    init = 0.1 * rng.standard_normal((len(lens), H, d, d))
+    g = -np.exp(A_log)[None, :, None] * (np.maximum(z, 0.0) + np.log1p(np.exp(-np.abs(z))))
+    o_c, f_c = kda_chunked(q, k, v, g, beta, cu, chunk=chunk, lower_bound=-np.inf, init_state=init)
+    o_r, f_r = kda_recurrent_unbounded(q, k, v, z, A_log, beta, cu, init_state=init, num_threads=2)
+    scale_o, scale_f = np.sqrt(np.mean(o_r ** 2)), np.sqrt(np.mean(f_r ** 2))
+    assert np.max(np.abs(o_c - o_r)) <= 1e-12 * scale_o and np.max(np.abs(f_c - f_r)) <= 1e-12 * scale_f
+    assert g.min() < -70.0  # the steep steps are there
