@@ -31,6 +31,9 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 PREFILL = dict(workload="prefill_k3_T4096_H96", T=4096, H=96, d_k=128, d_v=128, chunk=32)
+# the recipe both CPU baselines (ours' cpu_baseline and the reference arm) time, one step each
+ORACLE_SAMPLE = ("{heads} of {H} heads x {T} tokens per step: the whole workload, fp64 token-recurrent C oracle "
+                 "on the host's cores (the reference arm and cpu_baseline time this same sample)")
 DECODE = dict(B=256, H=96, d_k=128, d_v=128, steps=64)
 METRIC = "KDA prefill tokens/s (H=96,d=128) & % tensor roofline; decode GB/s vs HBM"
 
@@ -224,6 +227,54 @@ def time_prefill(case, steps, warmup, world, gated=False, out_gate=False, unboun
     return total_ms, launch_ms
 
 
+def time_named_prefill(name, steps, warmup, world, seed=0, workspace="auto"):
+    """kda_prefill on one named workload (built on the device, freed afterwards): per-launch ms,
+    total tokens, heads and sequences."""
+    from kimi_delta_attention_02_gb300 import binding, workloads
+    case = workloads.prefill_workload(name, device="cuda", seed=seed)
+    out = torch.empty(case.v.shape, dtype=torch.float32, device="cuda")
+    fin = torch.empty((case.num_seqs,) + tuple(case.q.shape[1:]) + (case.v.shape[-1],), dtype=torch.float32,
+                      device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def run():
+        binding.prefill(case.q, case.k, case.v, case.log_alpha, case.beta, case.cu_seqlens, case.init_state,
+                        out=out, final_state=fin, stream=stream, workspace=workspace)
+    for _ in range(warmup):
+        run()
+    binding.check_device_error(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for a, b in ev:
+        a.record(stream)
+        run()
+        b.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    binding.check_device_error(stream)
+    T, H, N = case.total_tokens, case.num_heads, case.num_seqs
+    in_bytes = sum(t.numel() * t.element_size() for t in (case.q, case.k, case.v, case.log_alpha, case.beta))
+    del case, out, fin
+    torch.cuda.empty_cache()
+    return [a.elapsed_time(b) for a, b in ev], T, H, N, in_bytes
+
+
+def prefill_line(name, ms, T, H, N, world, hbm_gbs, tf_burst, in_bytes, note):
+    """One workload's numbers: launch time, tokens/s and the HBM and tensor fractions of the
+    algorithmic work (fp32 output; 1,796 B per token-head with fp32 log_alpha, plus the states)."""
+    launch = sum(ms) / len(ms)
+    alg = T * H * PREFILL_BYTES_PER_TOKEN_HEAD + N * H * PREFILL_STATE_BYTES_PER_SEQ_HEAD
+    if in_bytes != T * H * (PREFILL_BYTES_PER_TOKEN_HEAD - 512):  # fp32 q/k/v: count the bytes read
+        alg = in_bytes + T * H * 512 + N * H * PREFILL_STATE_BYTES_PER_SEQ_HEAD
+    gbs = alg / (launch / 1e3) / 1e9
+    tf = T * H * PREFILL_FLOPS_PER_TOKEN_HEAD / (launch / 1e3) / 1e12
+    return {"workload": name, "launch_ms": launch, "tokens_per_s": world * T / (launch / 1e3),
+            "token_heads_per_s": world * T * H / (launch / 1e3), "GB/s": gbs, "peak": hbm_gbs,
+            "frac": gbs / hbm_gbs, "tensor_frac": tf / tf_burst, "alg_bytes": alg, "launches": len(ms),
+            "hbm_bound_ms": alg / hbm_gbs / 1e6, "kernel": note}
+
+
 def time_decode(steps_per_rep, reps, warmup, world, seed=0, fused=False):
     """Decode steps on B=256 sequences, H=96. ``fused``: the whole layer step between the
     projections -- the prologue on raw q, k, v (conv state shifted in place), the gated decay,
@@ -340,7 +391,7 @@ def run_reference(args, world, rank):
         return None
     from kimi_delta_attention_02_gb300 import workloads
     case = workloads.prefill_workload(PREFILL["workload"], device="cpu", seed=0)
-    heads = 16  # bounded sample per step: 16 of the 96 heads
+    heads = PREFILL["H"]  # the same sample as ours' cpu_baseline: every head, about a second per step
     for _ in range(args.warmup):
         cpu_oracle_sample(case, heads)
     times = []
@@ -356,8 +407,7 @@ def run_reference(args, world, rank):
             "config": {"workload": PREFILL["workload"], "global_batch": 1, "seq_len": PREFILL["T"],
                        "heads": PREFILL["H"], "d_k": 128, "d_v": 128, "parallelism": "cpu threads"},
             "cpu_baseline": {"value": tok_s, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                             "sample": f"{heads} of {PREFILL['H']} heads x {PREFILL['T']} tokens per step, "
-                                       "fp64 token-recurrent C oracle, scaled to the full workload"},
+                             "sample": ORACLE_SAMPLE.format(heads=heads, H=PREFILL["H"], T=PREFILL["T"])},
             "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
@@ -432,6 +482,7 @@ def main():
                                            unbounded=args.form.startswith("unbounded"))
         dec_ms = None if args.prefill_only else time_decode(DECODE["steps"], 1, 1, world, seed=rank)
         gated_ms = outgate_ms = prologue_ms = unbounded_ms = unbounded_rec_ms = unbounded_steep_ms = fdec_ms = None
+        extra = {}
         if not args.prefill_only and args.heads == PREFILL["H"]:
             gcase = workloads.prefill_workload("prefill_k3_gated_T4096_H96", device="cuda", seed=rank)
             _, g_launch = time_prefill(gcase, args.steps, args.warmup, world, gated=True)
@@ -453,6 +504,16 @@ def main():
             _, u_launch = time_prefill(ucase, args.steps, args.warmup, world, unbounded=True)
             unbounded_steep_ms = sum(u_launch) / len(u_launch)
             del ucase
+            torch.cuda.empty_cache()
+            # the other graded prefill shapes: config 0 (fp32, token-recurrent kernel), the varlen
+            # pack and the 1M-token sequence
+            extra = {}
+            for key, name, st, wu, note in (
+                    ("config0", "prefill_f32_T256_H2", args.steps, args.warmup, "fp32 token-recurrent"),
+                    ("varlen", "prefill_varlen8_H96", 5, 2, "chunked, one CTA per (sequence, head)"),
+                    ("long_context", "prefill_long_T1M_H32", 3, 1, "chunked, one CTA per head")):
+                ms, T_, H_, N_, ib = time_named_prefill(name, st, wu, world, seed=rank, workspace=None)
+                extra[key] = prefill_line(name, ms, T_, H_, N_, world, hbm_gbs, tf_burst, ib, note)
     if args.prefill_only:
         if rank == 0:
             print(json.dumps({"prefill_only": True, "form": args.form, "heads": H, "ms_per_step": total_ms / args.steps,
@@ -525,11 +586,10 @@ def main():
                "d2h_bytes_per_step": d2h, "ms_per_step": modes[best], "mode": best,
                "modes_ms_per_step": modes}
         if not args.no_cpu_baseline:
-            heads = H  # the whole workload: a few seconds on the host's cores
+            heads = H  # the whole workload, as the reference arm times it: about a second on the host's cores
             dt, cores, th = cpu_oracle_sample(case_cpu, heads)
             cpu_base = {"value": T * heads / H / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                        "sample": f"{heads} of {H} heads x {T} tokens (fp64 token-recurrent C oracle, "
-                                  f"{dt:.1f} s), scaled to the full workload"}
+                        "sample": ORACLE_SAMPLE.format(heads=heads, H=H, T=T), "seconds": dt}
 
     if rank == 0:
         clk = clocks.summary()
@@ -555,6 +615,7 @@ def main():
             "prologue": prologue,
             "decode_fused": fdec,
             "unbounded_decay": unbounded,
+            **extra,
             "cpu_baseline": cpu_base, "e2e": e2e, "clocks": clk,
             "gpu_launches": args.steps,  # one prefill launch per timed step (decode: its own region)
         }

@@ -32,7 +32,8 @@
  *    rounded to nearest-even. A bf16 output carries a relative rounding error
  *    of up to 2^-9 per element on top of the computation's own error.
  *  - Outputs must not alias inputs, except that final_state may equal
- *    init_state (in-place continuation of a prefill).
+ *    init_state (in-place continuation of a prefill). Every entry point checks
+ *    the byte ranges it is given and returns KDA_ERR_INVALID_ARG on an overlap.
  */
 #ifndef KDA_H
 #define KDA_H
@@ -49,7 +50,9 @@ typedef enum {
   KDA_ERR_INVALID_ARG = 1, /* null/misaligned pointer, bad size, bad enum          */
   KDA_ERR_UNSUPPORTED = 2, /* valid but outside what the kernels implement        */
   KDA_ERR_CUDA = 3,        /* a CUDA runtime call or kernel launch failed          */
-  KDA_ERR_TIMEOUT = 4      /* a kernel's bounded wait gave up (device error word)  */
+  KDA_ERR_TIMEOUT = 4,     /* a kernel's bounded wait gave up (device error word)  */
+  KDA_ERR_RANGE = 5        /* an input was outside the range the kernel that ran
+                              computes exactly (device error word; see kda_prefill) */
 } kda_status;
 
 typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
@@ -72,22 +75,52 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
  *   init_state  [num_seqs, H, d_k, d_v]  fp32, or NULL for zeros
  *   out         [total_tokens, H, d_v]   out_dtype, written
  *   final_state [num_seqs, H, d_k, d_v]  fp32, written, or NULL to skip
+ *   workspace   device scratch of workspace_bytes bytes (16-byte aligned), or
+ *               NULL with workspace_bytes = 0. Its size comes from
+ *               kda_prefill_workspace_size(); with at least that much the
+ *               library may use its parallel schedules (one long sequence split
+ *               into segments over more SMs, see kda_prefill_workspace_size),
+ *               with less it runs one CTA per (sequence, head) chain. The
+ *               contents need no initialisation and are garbage afterwards; the
+ *               workspace must not overlap any tensor argument and may not be
+ *               shared by calls that run at the same time.
  *
  * Sizes: 1 <= d_k, d_v <= 128, H >= 1, num_seqs >= 0, total_tokens >= 0.
  * bf16 inputs with d_k = d_v = 128 and lower_bound >= -5 run the tensor-core
  * chunked kernel; every other supported case (fp32 inputs, other head sizes, a
- * lower bound below -5) runs the fp32 token-recurrent kernel. The chunked
- * kernel rescales keys within 16-token tiles, which is exact in range only when
- * 16 * |log-decay| stays below 80 (Kimi K3 -- Architecture Notes, section 1.2):
- * hence the lower-bound condition and the expectation that log_alpha <= 0
- * (alpha is a retention factor in (0, 1], section 1.1).
+ * lower bound below -5) runs the fp32 token-recurrent kernel.
+ *
+ * Range of the chunked kernel. It rescales keys and queries around one
+ * reference point per 32-token chunk; with every clamped log-decay in
+ * [lower_bound, 0] (alpha a retention factor in (0, 1], section 1.1) the
+ * factors stay within e^80 (section 1.2) and every operand is finite. It also
+ * computes exactly any clamped log-decay up to +1/3 (so that no operand of a
+ * 32-token chunk can exceed 2^15.5, inside fp16). A clamped log-decay above
+ * +1/3 may overflow an operand: the kernel then records KDA_ERR_RANGE in the
+ * device error word (kda_check_device_error reports it) and the results of
+ * that call are unspecified. A retention factor above one also makes the state
+ * grow: the chunked kernel multiplies the state by its chunk operands through an
+ * fp16 copy, so state entries must stay below 65504 in magnitude (with alpha <= 1
+ * and unit-norm keys the state's norm grows by at most beta_t |v_t| per token).
+ * The token-recurrent kernel (kda_prefill_recurrent) takes any finite log-decay
+ * and keeps the state in fp32 throughout.
  * Enqueues work on `stream` and returns without synchronising.
  */
 kda_status kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha,
                        const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
                        int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
                        kda_dtype in_dtype, kda_dtype out_dtype, float lower_bound, float scale,
-                       const float *init_state, void *out, float *final_state, void *stream);
+                       const float *init_state, void *out, float *final_state, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
+ * kda_prefill_workspace_size -- bytes of device scratch that let kda_prefill
+ * (and kda_prefill_ex) use their parallel schedules for these sizes; 0 when
+ * none applies (then no workspace is needed). Pure host function, no CUDA
+ * call; the same arguments always give the same answer.
+ */
+size_t kda_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k,
+                                  int32_t d_v);
 
 /*
  * kda_prefill_recurrent -- same contract and results as kda_prefill, always on
@@ -118,6 +151,9 @@ kda_status kda_prefill_recurrent(const void *q, const void *k, const void *v,
  *   out         [B, H, d_v]   out_dtype, written with scale * S_t^T q_t
  *
  * Sizes: 1 <= d_k, d_v <= 128 and d_v a multiple of 4; B, H >= 1.
+ * No aliasing: state and out must not overlap each other or any input (q, k, v,
+ * log_alpha, beta), since every CTA reads its inputs while others write;
+ * KDA_ERR_INVALID_ARG otherwise.
  */
 kda_status kda_decode(const void *q, const void *k, const void *v, const float *log_alpha,
                       const float *beta, float *state, void *out, int32_t B, int32_t H,
@@ -230,6 +266,8 @@ typedef struct kda_prefill_params {
   float scale;
   float norm_eps;
   int32_t force_recurrent;
+  void *workspace;            /* device scratch or NULL, as in kda_prefill            */
+  size_t workspace_bytes;
 } kda_prefill_params;
 
 typedef struct kda_decode_params {
@@ -292,10 +330,16 @@ kda_status kda_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
                         void *conv_final, void *stream);
 
 /*
- * kda_check_device_error -- synchronises `stream`, then reads and clears the
- * library's device error word. Returns KDA_OK, KDA_ERR_TIMEOUT if a kernel's
- * bounded wait gave up since the last check, or KDA_ERR_CUDA if the
- * synchronisation itself failed.
+ * kda_check_device_error -- reads and clears the library's device error word in
+ * one atomic exchange, enqueued on `stream` behind the work already there, then
+ * synchronises `stream` and returns what the word held: KDA_OK, KDA_ERR_TIMEOUT
+ * if a kernel's bounded wait gave up, KDA_ERR_RANGE if a kernel met an input
+ * outside its range (KDA_ERR_TIMEOUT wins when both are set), or KDA_ERR_CUDA
+ * if a CUDA call failed. There is one word per device, shared by every stream
+ * and every call in the process: the check covers the work finished on
+ * `stream` and anything that any other stream recorded before the exchange;
+ * a code recorded after it is kept for the next check. Concurrent checks from
+ * several host threads are serialised by the library.
  */
 kda_status kda_check_device_error(void *stream);
 

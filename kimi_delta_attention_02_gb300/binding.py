@@ -20,7 +20,7 @@ LIB_PATH = os.path.join(_HERE, "libkda.so")
 ROOT = os.path.dirname(_HERE)
 HEADERS = [os.path.join(ROOT, "include", "kda.h"), os.path.join(ROOT, "include", "kda_selftest.h")]
 
-KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT = 0, 1, 2, 3, 4
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, KDA_ERR_RANGE = 0, 1, 2, 3, 4, 5
 KDA_F32, KDA_BF16 = 0, 1
 
 _lock = threading.Lock()
@@ -39,7 +39,8 @@ class PrefillParams(ctypes.Structure):
                 ("A_log", ctypes.c_void_p), ("beta", ctypes.c_void_p), ("cu_seqlens", ctypes.c_void_p),
                 ("init_state", ctypes.c_void_p), ("out_gate", ctypes.c_void_p), ("norm_weight", ctypes.c_void_p),
                 ("out", ctypes.c_void_p), ("final_state", ctypes.c_void_p), ("decay_bound", ctypes.c_float),
-                ("scale", ctypes.c_float), ("norm_eps", ctypes.c_float), ("force_recurrent", ctypes.c_int32)]
+                ("scale", ctypes.c_float), ("norm_eps", ctypes.c_float), ("force_recurrent", ctypes.c_int32),
+                ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class DecodeParams(ctypes.Structure):
@@ -62,9 +63,12 @@ class KdaError(RuntimeError):
 
 def _declare(lib):
     vp, i32, i64, f32, u32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_uint32
+    sz = ctypes.c_size_t
     prefill_args = [vp, vp, vp, vp, vp, vp, i32, i64, i32, i32, i32, i32, i32, f32, f32, vp, vp, vp, vp]
-    lib.kda_prefill.argtypes = prefill_args
+    lib.kda_prefill.argtypes = prefill_args[:-1] + [vp, sz, vp]
     lib.kda_prefill.restype = i32
+    lib.kda_prefill_workspace_size.argtypes = [i64, i32, i32, i32, i32]
+    lib.kda_prefill_workspace_size.restype = sz
     lib.kda_prefill_recurrent.argtypes = prefill_args
     lib.kda_prefill_recurrent.restype = i32
     lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, vp]
@@ -136,15 +140,38 @@ def _check_cuda(*tensors):
             raise ValueError("KDA tensors must be contiguous CUDA tensors")
 
 
+def workspace_size(total_tokens: int, num_seqs: int, H: int, d_k: int = 128, d_v: int = 128) -> int:
+    """Bytes of device scratch ``kda_prefill`` can use for these sizes (``kda_prefill_workspace_size``)."""
+    return int(lib().kda_prefill_workspace_size(int(total_tokens), int(num_seqs), int(H), int(d_k), int(d_v)))
+
+
+def _workspace(workspace, T, N, H, d_k, d_v, device):
+    """(pointer, bytes) of the scratch handed to the library: ``"auto"`` allocates what
+    ``kda_prefill_workspace_size`` asks for (through torch's caching allocator), ``None`` passes
+    none (one CTA per chain), a uint8 CUDA tensor is passed as given."""
+    if workspace is None:
+        return None, 0
+    if isinstance(workspace, str):
+        if workspace != "auto":
+            raise ValueError("workspace must be 'auto', None or a uint8 CUDA tensor")
+        n = workspace_size(T, N, H, d_k, d_v)
+        if n == 0:
+            return None, 0
+        workspace = torch.empty(n, dtype=torch.uint8, device=device)
+    _check_cuda(workspace)
+    return ctypes.c_void_p(workspace.data_ptr()), workspace.numel() * workspace.element_size()
+
+
 def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, out=None, final_state=None,
             out_dtype=torch.float32, lower_bound: float = -5.0, scale: float = 1.0, stream=None,
-            recurrent: bool = False, want_final: bool = True):
+            recurrent: bool = False, want_final: bool = True, workspace="auto"):
     """KDA prefill over packed variable-length sequences (``kda_prefill``).
 
     q, k [T, H, d_k], v [T, H, d_v] (bf16 or fp32, one dtype); log_alpha [T, H, d_k] fp32;
     beta [T, H] fp32; cu_seqlens [N+1] int32 (device); init_state [N, H, d_k, d_v] fp32 or None.
     Returns (out [T, H, d_v] in ``out_dtype`` (or out's dtype), final_state [N, H, d_k, d_v] or
     None). ``recurrent=True`` forces the fp32 token-recurrent kernel (``kda_prefill_recurrent``).
+    ``workspace``: see ``_workspace`` (the default lets the library pick its parallel schedule).
     """
     T, H, d_k = q.shape
     d_v = v.shape[-1]
@@ -162,10 +189,13 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, out=None, 
     if final_state is None and want_final:
         final_state = torch.empty((N, H, d_k, d_v), dtype=torch.float32, device=q.device)
     _check_cuda(q, k, v, log_alpha, beta, cu_seqlens, init_state, out, final_state)
-    fn = lib().kda_prefill_recurrent if recurrent else lib().kda_prefill
-    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(cu_seqlens), N, T, H, d_k, d_v, dt,
-            odt, float(lower_bound), float(scale), _ptr(init_state), _ptr(out), _ptr(final_state),
-            _stream_handle(stream))
+    args = (_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(cu_seqlens), N, T, H, d_k, d_v, dt,
+            odt, float(lower_bound), float(scale), _ptr(init_state), _ptr(out), _ptr(final_state))
+    if recurrent:
+        st = lib().kda_prefill_recurrent(*args, _stream_handle(stream))
+    else:
+        ws, ws_bytes = _workspace(workspace, T, N, H, d_k, d_v, q.device)
+        st = lib().kda_prefill(*args, ws, ws_bytes, _stream_handle(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_recurrent" if recurrent else "kda_prefill")
     return out, final_state
@@ -224,7 +254,7 @@ def _decay_fields(q, log_alpha, lower_bound, z, A_log, g_min, unbounded=False):
 def prefill_ex(q, k, v, beta, cu_seqlens, *, log_alpha=None, lower_bound: float = -5.0, z=None, A_log=None,
                g_min: float = -5.0, init_state=None, out_gate=None, norm_weight=None, norm_eps: float = 1e-6,
                out=None, final_state=None, out_dtype=torch.float32, scale: float = 1.0, stream=None,
-               recurrent: bool = False, want_final: bool = True, unbounded: bool = False):
+               recurrent: bool = False, want_final: bool = True, unbounded: bool = False, workspace="auto"):
     """Prefill through the parameter block (``kda_prefill_ex``): the clamped (``log_alpha``) or
     gated (``z``, ``A_log``) log-decay, and optionally the output gate with head-wise RMSNorm,
     ``out = Sigmoid(out_gate) * norm_weight * o / sqrt(mean(o^2) + norm_eps)`` per token and head.
@@ -249,6 +279,7 @@ def prefill_ex(q, k, v, beta, cu_seqlens, *, log_alpha=None, lower_bound: float 
     if final_state is None and want_final:
         final_state = torch.empty((N, H, d_k, d_v), dtype=torch.float32, device=q.device)
     _check_cuda(q, k, v, decay, A, beta, cu_seqlens, init_state, out_gate, norm_weight, out, final_state)
+    ws, ws_bytes = _workspace(None if recurrent else workspace, T, N, H, d_k, d_v, q.device)
     p = PrefillParams(struct_size=ctypes.sizeof(PrefillParams), in_dtype=_io_dtype(q.dtype),
                       out_dtype=_io_dtype(out.dtype), decay_form=form, num_seqs=N, H=H, d_k=d_k, d_v=d_v,
                       total_tokens=T, q=q.data_ptr(), k=k.data_ptr(), v=v.data_ptr(), decay=decay.data_ptr(),
@@ -258,7 +289,8 @@ def prefill_ex(q, k, v, beta, cu_seqlens, *, log_alpha=None, lower_bound: float 
                       out_gate=None if out_gate is None else out_gate.data_ptr(),
                       norm_weight=None if norm_weight is None else norm_weight.data_ptr(), out=out.data_ptr(),
                       final_state=None if final_state is None else final_state.data_ptr(), decay_bound=bound,
-                      scale=float(scale), norm_eps=float(norm_eps), force_recurrent=int(bool(recurrent)))
+                      scale=float(scale), norm_eps=float(norm_eps), force_recurrent=int(bool(recurrent)),
+                      workspace=ws, workspace_bytes=ws_bytes)
     st = lib().kda_prefill_ex(ctypes.byref(p), _stream_handle(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_ex")
@@ -367,7 +399,8 @@ def decode(q, k, v, log_alpha, beta, state, *, out=None, out_dtype=torch.float32
 
 
 def check_device_error(stream=None):
-    """Synchronise and raise if a kernel recorded a bounded-wait timeout."""
+    """Synchronise and raise if a kernel recorded a bounded-wait timeout or an input outside
+    its range (``KdaError.status`` tells which)."""
     st = lib().kda_check_device_error(_stream_handle(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_check_device_error")

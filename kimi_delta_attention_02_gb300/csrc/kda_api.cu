@@ -12,9 +12,15 @@ namespace kda {
 
 namespace {
 __device__ uint32_t g_device_error = 0;
+// what the last kda_check_device_error took out of g_device_error (read back by the host)
+__device__ uint32_t g_device_error_taken = 0;
 constexpr int kMaxDevices = 64;
 std::atomic<uint32_t *> g_error_word[kMaxDevices];
 std::mutex g_error_word_mu;
+std::mutex g_check_mu;  // one kda_check_device_error at a time: they share g_device_error_taken
+
+// Read and clear the error word in one step, behind the work already on the stream.
+__global__ void take_device_error_kernel() { g_device_error_taken = atomicExch(&g_device_error, 0u); }
 }  // namespace
 
 uint32_t *device_error_word() {
@@ -51,6 +57,7 @@ cudaError_t launch_recurrent(const void *q, const void *k, const void *v, const 
                              const float *init_state, const void *out_gate, const float *norm_weight,
                              float norm_eps, void *out, float *final_state, cudaStream_t stream);
 bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb, int decay_form);
+size_t prefill_workspace_bytes(int64_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v);
 kda_status launch_chunked(const void *q, const void *k, const void *v, const void *decay, int decay_form,
                           const float *A_log, const float *beta, const int32_t *cu_seqlens, int num_seqs,
                           int64_t total_tokens, int H, bool out_bf16, float lb, float scale, const float *init_state,
@@ -111,6 +118,27 @@ kda_status check_prefill_args(const void *q, const void *k, const void *v, const
   return KDA_OK;
 }
 
+// The workspace: NULL with 0 bytes, or a 16-byte-aligned device range that overlaps no tensor argument.
+kda_status check_workspace(const void *ws, size_t ws_bytes, const void *q, const void *k, const void *v,
+                           const void *decay, const float *A_log, const float *beta, const int32_t *cu_seqlens,
+                           int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                           kda_dtype in_dtype, kda_dtype out_dtype, const float *init_state, const void *out,
+                           const float *final_state, const void *out_gate, const float *norm_weight) {
+  if (ws == nullptr) return ws_bytes == 0 ? KDA_OK : KDA_ERR_INVALID_ARG;
+  if (ws_bytes == 0 || !aligned16(ws)) return KDA_ERR_INVALID_ARG;
+  const size_t es = in_dtype == KDA_BF16 ? 2 : 4, eo = out_dtype == KDA_BF16 ? 2 : 4;
+  const size_t nk = size_t(total_tokens) * H * d_k, nv = size_t(total_tokens) * H * d_v;
+  const size_t ns = size_t(num_seqs) * H * d_k * d_v * 4;
+  const void *args[12] = {q, k, v, decay, beta, A_log, out_gate, norm_weight, cu_seqlens, init_state, out,
+                          final_state};
+  const size_t bytes[12] = {nk * es, nk * es, nv * es, nk * (A_log ? es : 4), size_t(total_tokens) * H * 4,
+                            A_log ? size_t(H) * 4 : 0, out_gate ? nv * es : 0, norm_weight ? size_t(d_v) * 4 : 0,
+                            size_t(num_seqs + 1) * 4, init_state ? ns : 0, nv * eo, final_state ? ns : 0};
+  for (int i = 0; i < 12; ++i)
+    if (overlaps(ws, ws_bytes, args[i], bytes[i])) return KDA_ERR_INVALID_ARG;
+  return KDA_OK;
+}
+
 // the gated form's parameters: A_log [H] fp32 on the device, g_min finite and <= 0
 kda_status check_gate_args(const float *A_log, float g_min) {
   if (A_log == nullptr || !aligned4(A_log)) return KDA_ERR_INVALID_ARG;
@@ -130,12 +158,16 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const void 
                         int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype, float lb,
                         float scale, const float *init_state, void *out, float *final_state, void *stream,
                         bool force_recurrent, const void *out_gate = nullptr, const float *norm_weight = nullptr,
-                        float norm_eps = 0.f, int decay_form = -1) {
+                        float norm_eps = 0.f, int decay_form = -1, void *workspace = nullptr,
+                        size_t workspace_bytes = 0) {
   if (decay_form < 0) decay_form = A_log != nullptr ? DECAY_GATED : DECAY_CLAMPED;
   kda_status st = check_out_gate_args(out_gate, norm_weight, norm_eps);
   if (st != KDA_OK) return st;
   st = check_prefill_args(q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype,
                           out_dtype, init_state, out, final_state, out_gate, norm_weight);
+  if (st != KDA_OK) return st;
+  st = check_workspace(workspace, workspace_bytes, q, k, v, decay, A_log, beta, cu_seqlens, num_seqs, total_tokens,
+                       H, d_k, d_v, in_dtype, out_dtype, init_state, out, final_state, out_gate, norm_weight);
   if (st != KDA_OK) return st;
   if (num_seqs == 0) return KDA_OK;
   if (total_tokens == 0) out_gate = norm_weight = nullptr;  // nothing is read out
@@ -171,17 +203,29 @@ kda_status decode_impl(const void *q, const void *k, const void *v, const void *
   const kda_status st = check_out_gate_args(out_gate, norm_weight, norm_eps);
   if (st != KDA_OK) return st;
   if ((out_gate && !aligned16(out_gate)) || (norm_weight && !aligned4(norm_weight))) return KDA_ERR_INVALID_ARG;
-  if (out_gate) {  // the written read-out must not overlap the gate logits
-    const size_t nv = size_t(B) * H * d_v, eo = out_dtype == KDA_BF16 ? 2 : 4, es = in_dtype == KDA_BF16 ? 2 : 4;
-    if (overlaps(out, nv * eo, out_gate, nv * es)) return KDA_ERR_INVALID_ARG;
+  {  // state (read and rewritten) and out (written) must not overlap each other or any input
+    const size_t es = in_dtype == KDA_BF16 ? 2 : 4, eo = out_dtype == KDA_BF16 ? 2 : 4;
+    const size_t nk = size_t(B) * H * d_k, nv = size_t(B) * H * d_v, ns = size_t(B) * H * d_k * d_v * 4;
+    const void *ins[8] = {q, k, v, decay, beta, A_log, out_gate, norm_weight};
+    const size_t in_bytes[8] = {nk * es, nk * es, nv * es, nk * (A_log ? es : 4), size_t(B) * H * 4,
+                                A_log ? size_t(H) * 4 : 0, out_gate ? nv * es : 0, norm_weight ? size_t(d_v) * 4 : 0};
+    for (int i = 0; i < 8; ++i)
+      if (overlaps(state, ns, ins[i], in_bytes[i]) || overlaps(out, nv * eo, ins[i], in_bytes[i]))
+        return KDA_ERR_INVALID_ARG;
+    if (overlaps(out, nv * eo, state, ns)) return KDA_ERR_INVALID_ARG;
   }
   if (conv_state != nullptr) {  // the prologue: weights and state on the device, eps finite
     if (conv_weight == nullptr || !aligned16(conv_weight) || !aligned16(conv_state) || !finite_nonneg(l2_eps))
       return KDA_ERR_INVALID_ARG;
     const size_t es = in_dtype == KDA_BF16 ? 2 : 4, eo = out_dtype == KDA_BF16 ? 2 : 4;
     const size_t ncs = size_t(B) * H * 3 * (2 * d_k + d_v) * es;
+    const size_t nk = size_t(B) * H * d_k, nv = size_t(B) * H * d_v;
     if (overlaps(conv_state, ncs, state, size_t(B) * H * d_k * d_v * 4) ||
-        overlaps(conv_state, ncs, out, size_t(B) * H * d_v * eo))
+        overlaps(conv_state, ncs, out, nv * eo) || overlaps(conv_state, ncs, q, nk * es) ||
+        overlaps(conv_state, ncs, k, nk * es) || overlaps(conv_state, ncs, v, nv * es) ||
+        overlaps(conv_state, ncs, conv_weight, size_t(H) * (2 * d_k + d_v) * 16) ||
+        overlaps(state, size_t(B) * H * d_k * d_v * 4, conv_weight, size_t(H) * (2 * d_k + d_v) * 16) ||
+        overlaps(out, nv * eo, conv_weight, size_t(H) * (2 * d_k + d_v) * 16))
       return KDA_ERR_INVALID_ARG;
   } else if (conv_weight != nullptr) {
     return KDA_ERR_INVALID_ARG;  // weights without a state
@@ -220,9 +264,15 @@ kda_status kda_prefill_recurrent(const void *q, const void *k, const void *v, co
 kda_status kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha, const float *beta,
                        const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens, int32_t H, int32_t d_k,
                        int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype, float lower_bound, float scale,
-                       const float *init_state, void *out, float *final_state, void *stream) {
+                       const float *init_state, void *out, float *final_state, void *workspace,
+                       size_t workspace_bytes, void *stream) {
   return prefill_impl(q, k, v, log_alpha, nullptr, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype,
-                      out_dtype, lower_bound, scale, init_state, out, final_state, stream, false);
+                      out_dtype, lower_bound, scale, init_state, out, final_state, stream, false, nullptr, nullptr,
+                      0.f, -1, workspace, workspace_bytes);
+}
+
+size_t kda_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v) {
+  return prefill_workspace_bytes(total_tokens, num_seqs, H, d_k, d_v);
 }
 
 kda_status kda_prefill_gated(const void *q, const void *k, const void *v, const void *z, const float *A_log,
@@ -270,7 +320,7 @@ kda_status kda_prefill_ex(const kda_prefill_params *p, void *stream) {
   return prefill_impl(p->q, p->k, p->v, p->decay, p->A_log, p->beta, p->cu_seqlens, p->num_seqs, p->total_tokens,
                       p->H, p->d_k, p->d_v, p->in_dtype, p->out_dtype, p->decay_bound, p->scale, p->init_state,
                       p->out, p->final_state, stream, p->force_recurrent != 0, p->out_gate, p->norm_weight,
-                      p->norm_eps, int(p->decay_form));
+                      p->norm_eps, int(p->decay_form), p->workspace, p->workspace_bytes);
 }
 
 kda_status kda_decode_ex(const kda_decode_params *p, void *stream) {
@@ -322,13 +372,18 @@ kda_status kda_prologue(const void *q_raw, const void *k_raw, const void *v_raw,
 }
 
 kda_status kda_check_device_error(void *stream) {
-  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return KDA_ERR_CUDA;
+  const cudaStream_t s = static_cast<cudaStream_t>(stream);
+  std::lock_guard<std::mutex> lock(g_check_mu);
+  take_device_error_kernel<<<1, 1, 0, s>>>();
+  if (cudaGetLastError() != cudaSuccess) return KDA_ERR_CUDA;
   uint32_t word = 0;
-  if (cudaMemcpyFromSymbol(&word, g_device_error, sizeof word) != cudaSuccess) return KDA_ERR_CUDA;
-  if (word == 0) return KDA_OK;
-  const uint32_t zero = 0;
-  if (cudaMemcpyToSymbol(g_device_error, &zero, sizeof zero) != cudaSuccess) return KDA_ERR_CUDA;
-  return KDA_ERR_TIMEOUT;
+  if (cudaMemcpyFromSymbolAsync(&word, g_device_error_taken, sizeof word, 0, cudaMemcpyDeviceToHost, s) !=
+          cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return KDA_ERR_CUDA;
+  if (word & (DEVERR_TMA_TIMEOUT | DEVERR_MMA_TIMEOUT)) return KDA_ERR_TIMEOUT;
+  if (word & DEVERR_RANGE) return KDA_ERR_RANGE;
+  return KDA_OK;
 }
 
 const char *kda_status_string(kda_status status) {
@@ -338,6 +393,7 @@ const char *kda_status_string(kda_status status) {
     case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED";
     case KDA_ERR_CUDA: return "KDA_ERR_CUDA";
     case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT";
+    case KDA_ERR_RANGE: return "KDA_ERR_RANGE";
   }
   return "KDA_ERR_UNKNOWN";
 }

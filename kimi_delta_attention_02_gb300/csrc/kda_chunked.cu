@@ -68,6 +68,12 @@ bool tensor_map_3d(CUtensorMap *map, const void *base, bool bf16, int64_t T, int
   return r == CUDA_SUCCESS;
 }
 
+// Scratch of the parallel schedules (none yet: every chain runs in one CTA).
+size_t prefill_workspace_bytes(int64_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v) {
+  (void)total_tokens, (void)num_seqs, (void)H, (void)d_k, (void)d_v;
+  return 0;
+}
+
 // The bounded maps need log-decay >= -5 (the clamp's or the gated map's lower bound); the
 // unbounded map takes any decay.
 bool chunked_supported(int d_k, int d_v, bool in_bf16, float lb, int decay_form) {

@@ -123,6 +123,10 @@ constexpr uint32_t smem_bytes() { return kDecay == DECAY_UNBOUNDED ? kSmemBytesU
 // a channel is wide in a diagonal block when its log2 decay over the block's tokens is below
 // -kWideBlock (the bound gives every Gram factor of a narrow channel a magnitude <= 2^114)
 constexpr float kWideBlock = 114.f;
+// The largest clamped log-decay the clamped form computes exactly: with every log-decay of a
+// 32-token chunk in [-5, 1/3] no fp16 operand exceeds 2^(32/3 log2 e) = 2^15.4 (inside fp16's
+// 65504) and no tf32 Gram factor exceeds 2^115.4. A larger one is reported (DEVERR_RANGE).
+constexpr float kMaxGrowth = 1.f / 3.f;
 
 // A chunk's 512 position-pair shares: entries A[t][i] (i < t) of the two diagonal blocks
 // (120 each, row-major inside a block), then P[t][i] (i <= t, 136 each). The first slot of
@@ -169,7 +173,7 @@ __device__ __forceinline__ float exp2_sfu(float x) {
 }
 
 struct Bars {
-  uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate;
+  uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate, drain;
 };
 static_assert(OFF_MISC + (2 * 32 + 2 * 128 + 4 * 128) * 4 + sizeof(Bars) + 48 <= OFF_SS, "misc overlaps");
 
@@ -233,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->mma2, 1);
     mbar_init(&bars->wu, 1);
     mbar_init(&bars->gate, 1);
+    mbar_init(&bars->drain, 1);
     fence_mbarrier_init();
     s_tmem[1] = 0u;            // abort flag
     s_tmem[2] = s_tmem[3] = ~0u;  // unbounded map: the last chunk of each parity with wide channels
@@ -341,15 +346,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG) + tb * kD + ch;
       const uint16_t *zin = reinterpret_cast<const uint16_t *>(sm + OFF_QKG + SG) + tb * kD + ch;
       float run = 0.f;
+      bool grows = false;  // clamped form: a log-decay above kMaxGrowth
 #pragma unroll
       for (int r = 0; r < 8; ++r) {  // alpha = 1 past the end of the sequence
         const float g = !(kFull || tb + r < L) ? 0.f
                         : kUnb                ? unbounded_log_decay(bf16_to_f32(zin[r * kD]), a_h)
                         : kGated              ? gated_log_decay(bf16_to_f32(zin[r * kD]), a_h, lb)
                                               : clamp_log_decay(gin[r * kD], lb);
+        if (!kGated) grows |= g > kMaxGrowth;
         run = fmaf(g, kLog2e, run);
         lg[r] = run;
       }
+      if (!kGated && grows) raise_device_error(err_word, DEVERR_RANGE);  // the call's results are unspecified
       s_tot[grp * kD + ch] = run;
       maybe_wide = kUnb && run < -0.5f * kWideBlock;  // a wide channel has such a group in its block
     };
@@ -1023,7 +1031,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   goto teardown;
 
 issuer_abort:
-  // the compute warps gave up: let this CTA's own loads in flight land (bounded) before exit
+  // the compute warps gave up: let this CTA's own MMAs and loads in flight finish (bounded) before
+  // teardown frees the tensor memory and the CTA's shared memory. A commit tracks every tcgen05.mma
+  // this thread issued before it, so one more commit on a barrier of its own covers them all.
+  if (lane == 0) umma_commit(&bars->drain);
+  __syncwarp();
+  mbar_wait_sleep(&bars->drain, 0u, err_word, DEVERR_MMA_TIMEOUT);
   if (qkg_last >= 0) mbar_wait_sleep(&bars->qkg, uint32_t(qkg_last & 1), err_word, DEVERR_TMA_TIMEOUT);
   for (int s = 0; s < 2; ++s)
     if (v_last[s] >= 0) mbar_wait_sleep(&bars->v[s], uint32_t((v_last[s] >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);

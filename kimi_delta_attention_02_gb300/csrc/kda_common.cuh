@@ -14,14 +14,15 @@
 namespace kda {
 
 // ---------------------------------------------------------------------------
-// Device error word. Kernels OR a code into it when a bounded wait gives up;
-// kda_check_device_error() reads and clears it. It lives in kda_api.cu; kernels
+// Device error word. Kernels OR a code into it when a bounded wait gives up or
+// an input is out of their range; kda_check_device_error() reads and clears it. It lives in kda_api.cu; kernels
 // receive its device address (device_error_word()) as an argument.
 // ---------------------------------------------------------------------------
 enum : uint32_t {
   DEVERR_NONE = 0,
   DEVERR_TMA_TIMEOUT = 1u << 0,
   DEVERR_MMA_TIMEOUT = 1u << 1,
+  DEVERR_RANGE = 1u << 2,  // an input outside the range the kernel computes exactly
 };
 
 // Device address of the error word on the current device (nullptr if the

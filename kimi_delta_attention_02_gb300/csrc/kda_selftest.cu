@@ -98,6 +98,29 @@ __global__ void __launch_bounds__(128, 1)
 
 }  // namespace kda
 
+namespace kda {
+namespace {
+// Whether every shared-memory byte the MMAs of kda_selftest_umma read for one operand stays inside
+// its kSelftestTileBytes tile, given the descriptor offsets the caller chose. K-major: the last
+// instruction starts in 128-byte (or 64-byte) K block (steps - 1) / per_block, and its `rows` rows
+// span (rows / 8 - 1) SBO strides plus one 8-row atom. MN-major: the last instruction starts
+// (steps - 1) * 2048 bytes in, its rows of 64 elements span ceil(rows / 64) - 1 LBO strides, and
+// its 16 K rows one SBO stride plus one 8-row atom of 128 bytes.
+bool selftest_footprint_ok(uint32_t rows, uint32_t K, int fmt, bool sw64, bool mn_major, uint32_t lbo,
+                           uint32_t sbo) {
+  const uint64_t kstep = fmt == UMMA_TF32 ? 8 : 16, steps = K / kstep;
+  uint64_t end;
+  if (mn_major) {
+    end = (steps - 1) * 2048 + ((rows + 63) / 64 - 1) * uint64_t(lbo) + uint64_t(sbo) + 1024;
+  } else {
+    const uint64_t per_blk = sw64 ? 2 : 4, row_bytes = sw64 ? 64 : 128;
+    end = ((steps - 1) / per_blk) * rows * row_bytes + (rows / 8 - 1) * uint64_t(sbo) + 8 * row_bytes;
+  }
+  return end <= uint64_t(kSelftestTileBytes);
+}
+}  // namespace
+}  // namespace kda
+
 extern "C" kda_status kda_selftest_umma(const float *A, const float *B, float *D, int32_t M, int32_t N, int32_t K,
                                         int32_t fmt, int32_t sw64, int32_t a_mn_major, int32_t b_mn_major,
                                         int32_t negate_a,
@@ -113,6 +136,10 @@ extern "C" kda_status kda_selftest_umma(const float *A, const float *B, float *D
   if (fmt == UMMA_TF32 && negate_a) return KDA_ERR_UNSUPPORTED;
   if (sw64 && fmt == UMMA_TF32) return KDA_ERR_UNSUPPORTED;
   if (a_lbo > 32768 || a_sbo > 32768 || b_lbo > 32768 || b_sbo > 32768) return KDA_ERR_UNSUPPORTED;
+  // descriptors whose reads would leave the operand's staged tile
+  if (!selftest_footprint_ok(uint32_t(M), uint32_t(K), fmt, sw64 != 0, a_mn_major != 0, a_lbo, a_sbo) ||
+      !selftest_footprint_ok(uint32_t(N), uint32_t(K), fmt, sw64 != 0, b_mn_major != 0, b_lbo, b_sbo))
+    return KDA_ERR_UNSUPPORTED;
   const int smem = 2 * kSelftestTileBytes + 1024;
   if (cudaFuncSetAttribute(selftest_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return KDA_ERR_CUDA;

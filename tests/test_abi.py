@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     assert {"kda_prefill", "kda_decode", "kda_prefill_recurrent", "kda_check_device_error",
             "kda_status_string", "kda_version", "kda_selftest_umma", "kda_prefill_gated",
             "kda_prefill_gated_recurrent", "kda_decode_gated", "kda_prefill_ex", "kda_decode_ex",
-            "kda_prologue", "kda_selftest_wait_timeout"} <= set(names)
+            "kda_prologue", "kda_selftest_wait_timeout", "kda_prefill_workspace_size"} <= set(names)
     for name in names:
         assert hasattr(lib, name), name
 
@@ -43,6 +43,7 @@ def test_exports_every_declared_symbol(lib):
 def test_status_strings_and_version(lib):
     assert B.status_string(0) == "KDA_OK"
     assert B.status_string(4) == "KDA_ERR_TIMEOUT"
+    assert B.status_string(5) == "KDA_ERR_RANGE"
     assert B.status_string(99) == "KDA_ERR_UNKNOWN"
     assert lib.kda_version() >= 100
 
@@ -50,11 +51,14 @@ def test_status_strings_and_version(lib):
 def _prefill(lib, fn="kda_prefill", **over):
     """Call with host-side fake addresses: validation must reject before any CUDA call."""
     a = dict(q=0x10000, k=0x20000, v=0x30000, la=0x40000, beta=0x50000, cu=0x60000, N=1, T=4, H=2, dk=128,
-             dv=128, dtype=1, odtype=0, lb=-5.0, scale=1.0, init=NULL, out=0x70000, fin=0x80000, stream=NULL)
+             dv=128, dtype=1, odtype=0, lb=-5.0, scale=1.0, init=NULL, out=0x70000, fin=0x80000, ws=NULL,
+             ws_bytes=0, stream=NULL)
     a.update(over)
-    return getattr(lib, fn)(a["q"], a["k"], a["v"], a["la"], a["beta"], a["cu"], a["N"], a["T"], a["H"], a["dk"],
-                            a["dv"], a["dtype"], a["odtype"], a["lb"], a["scale"], a["init"], a["out"], a["fin"],
-                            a["stream"])
+    args = [a["q"], a["k"], a["v"], a["la"], a["beta"], a["cu"], a["N"], a["T"], a["H"], a["dk"], a["dv"], a["dtype"],
+            a["odtype"], a["lb"], a["scale"], a["init"], a["out"], a["fin"]]
+    if fn == "kda_prefill":
+        args += [a["ws"], a["ws_bytes"]]
+    return getattr(lib, fn)(*args, a["stream"])
 
 
 @pytest.mark.parametrize("fn", ["kda_prefill", "kda_prefill_recurrent"])
@@ -80,6 +84,26 @@ def test_prefill_rejects(lib, fn, over, expect):
     assert _prefill(lib, fn, **over) == expect
 
 
+@pytest.mark.parametrize("over", [
+    dict(ws=0x1000000, ws_bytes=0),                 # a workspace pointer without bytes
+    dict(ws=NULL, ws_bytes=4096),                   # bytes without a pointer
+    dict(ws=0x1000008, ws_bytes=4096),              # misaligned
+    dict(ws=0x70000, ws_bytes=4096),                # over the output
+    dict(ws=0x60000 - 16, ws_bytes=32),             # over cu_seqlens
+    dict(ws=0x80000 + 65536, ws_bytes=16),          # inside the final state
+])
+def test_prefill_rejects_bad_workspace(lib, over):
+    assert _prefill(lib, **over) == B.KDA_ERR_INVALID_ARG
+
+
+def test_workspace_size_is_a_pure_host_query(lib):
+    # no CUDA call: it answers on a machine without a GPU, the same way every time
+    for args in [(4096, 1, 96, 128, 128), (1 << 20, 1, 32, 128, 128), (135000, 8, 96, 128, 128), (0, 0, 1, 1, 1)]:
+        a = lib.kda_prefill_workspace_size(*args)
+        assert a == lib.kda_prefill_workspace_size(*args)
+        assert a % 16 == 0
+
+
 def test_prefill_accepts_empty_work(lib):
     # zero sequences and zero tokens: nothing to enqueue, no CUDA call is made
     assert _prefill(lib, N=0, T=0, q=NULL, k=NULL, v=NULL, la=NULL, beta=NULL, out=NULL, fin=NULL) == B.KDA_OK
@@ -90,12 +114,17 @@ def test_prefill_accepts_empty_work(lib):
     (dict(B=0), B.KDA_ERR_INVALID_ARG),
     (dict(dv=6), B.KDA_ERR_UNSUPPORTED),
     (dict(dk=256), B.KDA_ERR_UNSUPPORTED),
-    (dict(state=0x90004), B.KDA_ERR_INVALID_ARG),
+    (dict(state=0x1000004), B.KDA_ERR_INVALID_ARG),
     (dict(dtype=2), B.KDA_ERR_INVALID_ARG),
     (dict(odtype=-1), B.KDA_ERR_INVALID_ARG),
+    (dict(state=0x10000), B.KDA_ERR_INVALID_ARG),        # the state over q
+    (dict(state=0x40000 - 4096), B.KDA_ERR_INVALID_ARG), # the state running into log_alpha
+    (dict(out=0x20000), B.KDA_ERR_INVALID_ARG),          # out over k
+    (dict(out=0x50000), B.KDA_ERR_INVALID_ARG),          # out over beta
+    (dict(out=0x1000000 + 8192), B.KDA_ERR_INVALID_ARG), # out inside the state
 ])
 def test_decode_rejects(lib, over, expect):
-    a = dict(q=0x10000, k=0x20000, v=0x30000, la=0x40000, beta=0x50000, state=0x90000, out=0x70000, B=2, H=2,
+    a = dict(q=0x10000, k=0x20000, v=0x30000, la=0x40000, beta=0x50000, state=0x1000000, out=0x70000, B=2, H=2,
              dk=128, dv=128, dtype=1, odtype=0)
     a.update(over)
     st = lib.kda_decode(a["q"], a["k"], a["v"], a["la"], a["beta"], a["state"], a["out"], a["B"], a["H"], a["dk"],
@@ -110,6 +139,19 @@ def test_selftest_rejects_bad_shapes(lib):
     assert st == B.KDA_ERR_UNSUPPORTED  # tf32 operands are K-major only
     st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, 128, 64, 64, 5, 0, 0, 0, 0, 16, 1024, 16, 1024, 0x4000, NULL)
     assert st == B.KDA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("args", [
+    (128, 64, 64, 1, 0, 0, 0, 0, 16, 32768, 16, 1024),     # K-major A, 16 atoms 32 KB apart: far past its tile
+    (128, 64, 128, 1, 0, 0, 0, 0, 16, 1024, 16, 8192),     # K-major B rows 8 KB apart
+    (128, 128, 128, 0, 0, 1, 0, 0, 32768, 32768, 16, 1024),  # MN-major A: blocks and K groups 32 KB apart
+    (128, 256, 128, 1, 0, 0, 1, 0, 16, 1024, 32768, 1024), # MN-major B, 4 blocks of 64 columns 32 KB apart
+])
+def test_selftest_rejects_descriptors_outside_the_tile(lib, args):
+    M, N, K, fmt, sw64, amn, bmn, neg, albo, asbo, blbo, bsbo = args
+    st = lib.kda_selftest_umma(0x1000, 0x2000, 0x3000, M, N, K, fmt, sw64, amn, bmn, neg, albo, asbo, blbo, bsbo,
+                               0x4000, NULL)
+    assert st == B.KDA_ERR_UNSUPPORTED
 
 
 def _prefill_gated(lib, fn="kda_prefill_gated", **over):
@@ -164,7 +206,8 @@ def _prefill_ex(lib, **over):
     f = dict(struct_size=ctypes.sizeof(B.PrefillParams), in_dtype=1, out_dtype=0, decay_form=0, num_seqs=1, H=2,
              d_k=128, d_v=128, total_tokens=4, q=0x10000, k=0x20000, v=0x30000, decay=0x40000, A_log=None,
              beta=0x50000, cu_seqlens=0x60000, init_state=None, out_gate=0xb0000, norm_weight=0xc0000,
-             out=0x70000, final_state=0x80000, decay_bound=-5.0, scale=1.0, norm_eps=1e-6, force_recurrent=0)
+             out=0x70000, final_state=0x80000, decay_bound=-5.0, scale=1.0, norm_eps=1e-6, force_recurrent=0,
+             workspace=None, workspace_bytes=0)
     f.update(over)
     return lib.kda_prefill_ex(ctypes.byref(B.PrefillParams(**f)), NULL)
 
@@ -189,6 +232,8 @@ def _prefill_ex(lib, **over):
     (dict(in_dtype=5), B.KDA_ERR_INVALID_ARG),
     (dict(d_v=129), B.KDA_ERR_UNSUPPORTED),
     (dict(q=None), B.KDA_ERR_INVALID_ARG),
+    (dict(workspace=0x1000000), B.KDA_ERR_INVALID_ARG),               # workspace without bytes
+    (dict(workspace=0xb0000, workspace_bytes=64), B.KDA_ERR_INVALID_ARG),  # workspace over the gate logits
 ])
 def test_prefill_ex_rejects(lib, over, expect):
     assert _prefill_ex(lib, **over) == expect
@@ -203,7 +248,7 @@ def test_prefill_ex_accepts_empty_work(lib):
 
 def _decode_ex(lib, **over):
     f = dict(struct_size=ctypes.sizeof(B.DecodeParams), in_dtype=1, out_dtype=0, decay_form=0, B=2, H=2, d_k=128,
-             d_v=128, q=0x10000, k=0x20000, v=0x30000, decay=0x40000, A_log=None, beta=0x50000, state=0x90000,
+             d_v=128, q=0x10000, k=0x20000, v=0x30000, decay=0x40000, A_log=None, beta=0x50000, state=0x1000000,
              out_gate=0xb0000, norm_weight=None, out=0x70000, conv_weight=None, conv_state=None, decay_bound=-5.0,
              scale=1.0, norm_eps=1e-6, l2_eps=1e-6)
     f.update(over)
@@ -225,7 +270,10 @@ def _decode_ex(lib, **over):
     (dict(conv_state=0xe0000), B.KDA_ERR_INVALID_ARG),              # a state without weights
     (dict(conv_state=0xe0000, conv_weight=0xd0000, l2_eps=float("nan")), B.KDA_ERR_INVALID_ARG),
     (dict(conv_state=0xe0008, conv_weight=0xd0000), B.KDA_ERR_INVALID_ARG),
-    (dict(conv_state=0x90000 + 4096, conv_weight=0xd0000), B.KDA_ERR_INVALID_ARG),  # inside the state
+    (dict(conv_state=0x1000000 + 4096, conv_weight=0xd0000), B.KDA_ERR_INVALID_ARG),  # inside the state
+    (dict(conv_state=0x20000, conv_weight=0xd0000), B.KDA_ERR_INVALID_ARG),         # over k
+    (dict(state=0xb0000 - 4096), B.KDA_ERR_INVALID_ARG),                            # state into the gate logits
+    (dict(out=0x1000000 + 65536), B.KDA_ERR_INVALID_ARG),                           # out inside the state
 ])
 def test_decode_ex_rejects(lib, over, expect):
     assert _decode_ex(lib, **over) == expect
@@ -233,7 +281,7 @@ def test_decode_ex_rejects(lib, over, expect):
 
 def test_parameter_blocks_have_the_header_layout():
     """The ctypes mirrors add up to the sizes the header's field order gives on LP64 (no padding)."""
-    assert ctypes.sizeof(B.PrefillParams) == 16 + 16 + 8 + 12 * 8 + 16
+    assert ctypes.sizeof(B.PrefillParams) == 16 + 16 + 8 + 12 * 8 + 16 + 16
     assert ctypes.sizeof(B.DecodeParams) == 16 + 16 + 12 * 8 + 16
 
 

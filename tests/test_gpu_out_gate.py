@@ -62,6 +62,23 @@ def test_recurrent_fp32(d_v):
     _check(case, TOL_F32, recurrent=True)
 
 
+def test_recurrent_fp32_unscaled_metric_wide_row_norms():
+    """The output gate checked element by element with the plain metric max|dy| / rms(y), with no
+    per-row weighting: q rows scaled by 10^u, u uniform in [-3, 1], give read-out rows whose norms
+    span four decades, so an error confined to small-norm rows in the kernel's gate arithmetic
+    (the RMS, the reciprocal square root, eps) shows up unscaled here."""
+    case = workloads.make_prefill([9, 40], H=2, d_k=96, d_v=128, dtype=torch.float32, device="cuda", seed=47,
+                                  out_gate=True)
+    g = torch.Generator(device="cpu").manual_seed(47)
+    s = 10.0 ** (4.0 * torch.rand(case.q.shape[:2], generator=g) - 3.0)
+    case.q.mul_(s.to(case.q.device)[..., None])
+    out, fin = _run(case, recurrent=True)
+    y_ref, f_ref, o_ref = oracle_prefill_out_gate(case)
+    row = np.sqrt((o_ref ** 2).mean(-1))
+    assert row.max() / row.min() > 1e3
+    assert rel_max_err(out, y_ref) <= TOL_F32 and rel_max_err(fin, f_ref) <= TOL_F32
+
+
 def test_recurrent_matches_chunked():
     case = workloads.make_prefill([70, 3], H=2, device="cuda", seed=44, gated=True, out_gate=True)
     a, fa = _run(case)

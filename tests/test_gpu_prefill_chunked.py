@@ -73,6 +73,32 @@ def test_lower_bound_at_minus_five_is_exact_clamp():
     _check(case)
 
 
+def test_small_growth_is_computed_exactly():
+    """Clamped log-decays up to +1/3 (retention factors above one) stay inside the chunked
+    kernel's range: no status, and the oracle's results."""
+    case = workloads.make_prefill([200], H=2, device="cuda", seed=18)
+    case.log_alpha[20:51, 0, 5] = 0.25  # one key channel grows e^0.25 per token over 31 tokens (e^7.75)
+    case.log_alpha[40:60, 1, :8] = 0.33  # eight channels at the edge of the range for 20 tokens
+    _check(case)
+
+
+def test_range_guard_reports_growth_beyond_the_envelope():
+    """A clamped log-decay of +6 (alpha = e^6, far outside the method's (0, 1]) would overflow
+    the chunked kernel's rescaled operands: the kernel reports KDA_ERR_RANGE through the device
+    error word instead of returning silent Inf/NaN, and the token-recurrent kernel, which takes
+    any finite log-decay, still matches the oracle on the same input."""
+    case = workloads.make_prefill([96], H=2, device="cuda", seed=19)
+    case.log_alpha[10:13, 1, 7] = 6.0
+    binding.prefill(case.q, case.k, case.v, case.log_alpha, case.beta, case.cu_seqlens, case.init_state)
+    with pytest.raises(binding.KdaError) as err:
+        binding.check_device_error()
+    assert err.value.status == binding.KDA_ERR_RANGE
+    binding.check_device_error()  # the word was cleared by the check that reported it
+    o_r, f_r = _run(case, recurrent=True)
+    o_ref, f_ref = oracle_prefill(case)
+    assert rel_max_err(o_r, o_ref) <= TOL_BF16 and rel_max_err(f_r, f_ref) <= TOL_BF16
+
+
 def test_no_decay_and_zero_beta():
     case = workloads.make_prefill([190], H=2, device="cuda", seed=14)
     case.log_alpha.zero_()
