@@ -508,12 +508,20 @@ def main():
             # the other graded prefill shapes: config 0 (fp32, token-recurrent kernel), the varlen
             # pack and the 1M-token sequence
             extra = {}
+            # each with the schedule kda_prefill takes given the workspace it asks for, and without
+            # one (one CTA per (sequence, head) chain, in sequence order) for comparison
             for key, name, st, wu, note in (
                     ("config0", "prefill_f32_T256_H2", args.steps, args.warmup, "fp32 token-recurrent"),
-                    ("varlen", "prefill_varlen8_H96", 5, 2, "chunked, one CTA per (sequence, head)"),
-                    ("long_context", "prefill_long_T1M_H32", 3, 1, "chunked, one CTA per head")):
-                ms, T_, H_, N_, ib = time_named_prefill(name, st, wu, world, seed=rank, workspace=None)
+                    ("varlen", "prefill_varlen8_H96", 5, 2, "chunked, chains longest sequence first"),
+                    ("long_context", "prefill_long_T1M_H32", 3, 1, "chunked, segmented: 3 segments per head")):
+                ms, T_, H_, N_, ib = time_named_prefill(name, st, wu, world, seed=rank, workspace="auto")
                 extra[key] = prefill_line(name, ms, T_, H_, N_, world, hbm_gbs, tf_burst, ib, note)
+                if key != "config0":
+                    ms1, *_ = time_named_prefill(name, st, wu, world, seed=rank, workspace=None)
+                    one = sum(ms1) / len(ms1)
+                    extra[key]["without_workspace"] = {
+                        "launch_ms": one, "kernel": "chunked, one CTA per (sequence, head), sequence order",
+                        "speedup_of_schedule": one / extra[key]["launch_ms"]}
     if args.prefill_only:
         if rank == 0:
             print(json.dumps({"prefill_only": True, "form": args.form, "heads": H, "ms_per_step": total_ms / args.steps,

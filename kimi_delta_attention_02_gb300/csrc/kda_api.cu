@@ -62,7 +62,7 @@ kda_status launch_chunked(const void *q, const void *k, const void *v, const voi
                           const float *A_log, const float *beta, const int32_t *cu_seqlens, int num_seqs,
                           int64_t total_tokens, int H, bool out_bf16, float lb, float scale, const float *init_state,
                           const void *out_gate, const float *norm_weight, float norm_eps, void *out,
-                          float *final_state, cudaStream_t stream);
+                          float *final_state, void *workspace, size_t workspace_bytes, cudaStream_t stream);
 
 namespace {
 
@@ -177,7 +177,7 @@ kda_status prefill_impl(const void *q, const void *k, const void *v, const void 
   if (!force_recurrent && total_tokens > 0 && chunked_supported(d_k, d_v, in_dtype == KDA_BF16, lb, decay_form))
     return launch_chunked(q, k, v, decay, decay_form, A_log, beta, cu_seqlens, num_seqs, total_tokens, H,
                           out_dtype == KDA_BF16, lb, scale, init_state, out_gate, norm_weight, norm_eps, out,
-                          final_state, s);
+                          final_state, workspace, workspace_bytes, s);
   const cudaError_t err = launch_recurrent(q, k, v, decay, decay_form, A_log, beta, cu_seqlens, num_seqs, H, d_k, d_v,
                                            in_dtype == KDA_BF16, out_dtype == KDA_BF16, lb, scale, init_state,
                                            out_gate, norm_weight, norm_eps, out, final_state, s);

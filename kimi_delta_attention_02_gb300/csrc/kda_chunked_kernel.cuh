@@ -177,6 +177,22 @@ struct Bars {
 };
 static_assert(OFF_MISC + (2 * 32 + 2 * 128 + 4 * 128) * 4 + sizeof(Bars) + 48 <= OFF_SS, "misc overlaps");
 
+// Which token ranges the CTAs walk. count == 0: CTA b takes sequence n = b / H of cu_seqlens, or
+// n = order[b / H] when an order is given (the longest sequences first). count > 0: CTA b takes
+// run n = b / H, tokens [bos[n], eos[n]) of the packed tensors, with init_state / final_state
+// indexed by n and the run's flags: RUN_ZERO_V reads v as zeros (its TMA boxes start before the
+// tensor, where the copy fills zeros), RUN_INIT_IDENTITY / RUN_INIT_ZERO start from I or 0
+// instead of init_state, RUN_NO_OUT writes no output. The segmented schedule of one long
+// sequence runs its passes through this table.
+constexpr int kMaxRuns = 64;
+enum : uint32_t { RUN_ZERO_V = 1u, RUN_INIT_IDENTITY = 2u, RUN_INIT_ZERO = 4u, RUN_NO_OUT = 8u };
+struct Runs {
+  int32_t count;
+  const int32_t *order;
+  int32_t bos[kMaxRuns], eos[kMaxRuns];
+  uint32_t flags[kMaxRuns];
+};
+
 // The output gate of section 1.3: bf16 gate logits r [T, H, 128], the RMSNorm weight w [128]
 // (nullptr = ones) and eps.
 struct OutGate {
@@ -195,7 +211,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     kda_chunked_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                        const __grid_constant__ CUtensorMap tm_r, const __grid_constant__ CUtensorMap tm_o,
-                       const OutGate og,
+                       const OutGate og, const __grid_constant__ Runs runs,
                        const float *__restrict__ A_log, const float *__restrict__ beta,
                        const int32_t *__restrict__ cu_seqlens,
                        const float *__restrict__ init_state, void *__restrict__ out,
@@ -213,8 +229,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int quarter = warp & 3, grp = warp >> 2;  // TMEM lane quarter, column group (compute warps)
   const bool worker = tid < kWorkers;              // warps 0..15; warp 16 issues TMA loads and MMAs
   const int h = int(blockIdx.x % H);
-  const int64_t n = blockIdx.x / H;
-  const int64_t bos = cu_seqlens[n], eos = cu_seqlens[n + 1];
+  const int64_t blk = blockIdx.x / H;
+  const int64_t n = runs.count > 0 ? blk : runs.order != nullptr ? int64_t(runs.order[blk]) : blk;
+  const int64_t bos = runs.count > 0 ? runs.bos[blk] : cu_seqlens[n];
+  const int64_t eos = runs.count > 0 ? runs.eos[blk] : cu_seqlens[n + 1];
+  const uint32_t rflags = runs.count > 0 ? runs.flags[blk] : 0u;
+  const bool no_out = (rflags & RUN_NO_OUT) != 0;
   const int n_chunks = int((eos - bos + kC - 1) / kC);
   const uint32_t sbase = smem_u32(sm);
   constexpr bool kGated = kDecay != DECAY_CLAMPED;  // tm_g maps bf16 logits
@@ -266,8 +286,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int u = 0; u < 2; ++u) {
       float x[16];
 #pragma unroll
-      for (int j = 0; j < 16; ++j)
-        x[j] = init_state != nullptr ? init_state[st_base + int64_t(32 * grp + 16 * u + j) * kD + v_own] : 0.f;
+      for (int j = 0; j < 16; ++j) {
+        const int c = 32 * grp + 16 * u + j;  // key row of S
+        x[j] = (rflags & RUN_INIT_IDENTITY)                                 ? (c == v_own ? 1.f : 0.f)
+               : ((rflags & RUN_INIT_ZERO) || init_state == nullptr) ? 0.f
+                                                                      : init_state[st_base + int64_t(c) * kD + v_own];
+      }
       tmem_st16(s_cols(1) + 16 * u, x);
     }
     tmem_st_wait();
@@ -288,12 +312,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_3d(sm + OFF_QKG + SG, &tm_g, &bars->qkg, 0, h, t0);
   };
   auto issue_v = [&](int c) {  // issuer
-    const int32_t t0 = int32_t(chunk_t0(c));
+    // a run that reads v as zeros takes boxes 64 tokens before the tensor, which TMA fills with zeros
+    const int32_t t0 = (rflags & RUN_ZERO_V) ? -64 : int32_t(chunk_t0(c));
     uint8_t *dst = sm + OFF_V + (c & 1) * 8192;
     mbar_arrive_expect_tx(&bars->v[c & 1], 8192);
     tma_load_3d(dst, &tm_v, &bars->v[c & 1], 0, h, t0);
     tma_load_3d(dst + 4096, &tm_v, &bars->v[c & 1], 64, h, t0);
-    if (kNormGate) tma_prefetch_l2_3d(&tm_r, 0, h, t0);  // chunk c's gate logits, read when it is written
+    if (kNormGate && !no_out) tma_prefetch_l2_3d(&tm_r, 0, h, t0);  // chunk c's gate logits, read when written
   };
 
   bool bad = false;  // a bounded wait of this thread gave up
@@ -571,13 +596,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       fence_proxy_async_smem();
       named_bar_sync(BAR_OUT, 384);
-      if (tid == 0) {
+      if (tid == 0 && !no_out) {
         tma_store_3d(&tm_o, stage, 0, h, int32_t(chunk_t0(j)));
         bulk_commit();
         if (kOutBF16 && j + 3 < n_chunks) store_pending = true;  // read before prep(j + 3)'s barrier
         else bulk_wait_read();
       }
-    } else {
+    } else if (!no_out) {
       const int64_t step = int64_t(H) * kD;
       const int64_t base = ((chunk_t0(j) + t0) * H + h) * int64_t(kD) + v_own;
 #pragma unroll
@@ -1052,8 +1077,8 @@ teardown:
 // the kernel's pointer type, spelled out (naming an instantiation here would instantiate it in
 // every translation unit that includes this header)
 using KernelFn = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, OutGate,
-                          const float *, const float *, const int32_t *, const float *, void *, float *, int, float,
-                          float, uint32_t *);
+                          Runs, const float *, const float *, const int32_t *, const float *, void *, float *, int,
+                          float, float, uint32_t *);
 
 }  // namespace chunked
 }  // namespace kda
