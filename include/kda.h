@@ -123,6 +123,43 @@ size_t kda_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_
                                   int32_t d_v);
 
 /*
+ * kda_prefill_noalloc -- kda_prefill for callers that cannot allocate device memory.
+ *
+ * Some callers cannot produce the workspace kda_prefill asks for: a serving engine that
+ * reserves the whole GPU up front in its own pool and refuses any further cudaMalloc, a
+ * plugin inside a host framework that owns every device allocation, or code in a
+ * latency-critical region where cudaMalloc/cudaFree would stall or synchronise the device.
+ * This entry point takes the same arguments as kda_prefill without the workspace, runs the
+ * same validation, schedule and kernels, and allocates nothing (no cudaMalloc, cudaFree or
+ * allocating library routine): its scratch is a 16 MiB array inside the library's device
+ * code, which every GPU that loads the library holds until the process exits.
+ *
+ * Limit: the schedule's scratch, kda_prefill_workspace_size() of the same sizes, must fit
+ * in 16 MiB (16777216 bytes); larger sizes are refused with KDA_ERR_UNSUPPORTED before
+ * anything is enqueued. One long sequence with H heads needs (max(R, m) + m) * H * 64 KiB
+ * for its m segments and R segment runs (T = 2^20 with H = 32: 12 MiB); up to 8192 packed
+ * sequences need 4 bytes each.
+ *
+ * Set-up: the first call on a device, with that device current, looks up the array's
+ * device address once (it may load the library's device code); make that first call
+ * before any stream capture on the device. Later calls only enqueue work.
+ *
+ * Sharing: every call on a device uses the same array, which keeps the last call's
+ * contents; each call writes all the scratch it reads, so nothing needs clearing, but calls
+ * that overlap on the GPU (on different streams, or from different threads) race on it:
+ * order them on one stream or with events. On an argument error nothing is enqueued.
+ *
+ * No counterpart in the paper: the method needs no scratch memory at all; this is a
+ * deployment variant of the library's own parallel schedule.
+ */
+kda_status kda_prefill_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
+                               const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, int32_t H, int32_t d_k, int32_t d_v,
+                               kda_dtype in_dtype, kda_dtype out_dtype, float lower_bound,
+                               float scale, const float *init_state, void *out,
+                               float *final_state, void *stream);
+
+/*
  * kda_prefill_recurrent -- same contract and results as kda_prefill, always on
  * the fp32 token-recurrent kernel (one token at a time, state kept on chip).
  * Exposed for cross-checking the chunked kernels and as the reference-accuracy

@@ -70,6 +70,8 @@ def _declare(lib):
     lib.kda_prefill_workspace_size.argtypes = [i64, i32, i32, i32, i32]
     lib.kda_prefill_workspace_size.restype = sz
     lib.kda_prefill_recurrent.argtypes = prefill_args
+    lib.kda_prefill_noalloc.argtypes = prefill_args
+    lib.kda_prefill_noalloc.restype = i32
     lib.kda_prefill_recurrent.restype = i32
     lib.kda_decode.argtypes = [vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32, vp]
     lib.kda_decode.restype = i32
@@ -198,6 +200,24 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, out=None, 
         st = lib().kda_prefill(*args, ws, ws_bytes, _stream_handle(stream))
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_recurrent" if recurrent else "kda_prefill")
+    return out, final_state
+
+
+def prefill_noalloc(q, k, v, log_alpha, beta, cu_seqlens, init_state=None, *, out, final_state=None,
+                    lower_bound: float = -5.0, scale: float = 1.0, stream=None):
+    """``kda_prefill_noalloc``: kda_prefill with the library's own scratch instead of a workspace,
+    for callers that cannot allocate device memory (the caller still provides ``out`` and, if
+    wanted, ``final_state``; nothing is allocated here either)."""
+    T, H, d_k = q.shape
+    d_v = v.shape[-1]
+    N = cu_seqlens.shape[0] - 1
+    _check_cuda(q, k, v, log_alpha, beta, cu_seqlens, init_state, out, final_state)
+    st = lib().kda_prefill_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(cu_seqlens), N, T,
+                                   H, d_k, d_v, _io_dtype(q.dtype), _io_dtype(out.dtype), float(lower_bound),
+                                   float(scale), _ptr(init_state), _ptr(out), _ptr(final_state),
+                                   _stream_handle(stream))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_noalloc")
     return out, final_state
 
 

@@ -39,6 +39,39 @@ uint32_t *device_error_word() {
   return p;
 }
 
+// ---------------------------------------------------------------------------------------------
+// Scratch of kda_prefill_noalloc, for callers that cannot hand the library a workspace. It is a
+// file-scope device array, so every GPU that loads this library holds these 16 MiB until the
+// process exits. Host code may not use its name as a device address (on the host it names a
+// stand-in): noalloc_scratch() looks the address up once per device, with that device current.
+// ---------------------------------------------------------------------------------------------
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+std::atomic<void *> g_noalloc_ptr[kMaxDevices];
+std::mutex g_noalloc_mu;
+
+// Device address of g_noalloc_scratch on the current device (nullptr if the lookup failed). The
+// first call on a device does the lookup, which may load the library's device code: it must not
+// happen inside a stream capture.
+void *noalloc_scratch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  void *p = g_noalloc_ptr[dev].load(std::memory_order_acquire);
+  if (p != nullptr) return p;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  p = g_noalloc_ptr[dev].load(std::memory_order_relaxed);
+  if (p == nullptr) {
+    void *addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) return nullptr;
+    p = addr;
+    g_noalloc_ptr[dev].store(p, std::memory_order_release);
+  }
+  return p;
+}
+}  // namespace
+
 // Each launcher takes the decay input as `decay` + `A_log`: log_alpha (fp32) with A_log null
 // (the clamped form), or the gated form's logits z (input dtype) with A_log [H]; and the output
 // gate as `out_gate` (gate logits, input dtype; null = plain read-out) + `norm_weight` + `norm_eps`.
@@ -273,6 +306,25 @@ kda_status kda_prefill(const void *q, const void *k, const void *v, const float 
 
 size_t kda_prefill_workspace_size(int64_t total_tokens, int32_t num_seqs, int32_t H, int32_t d_k, int32_t d_v) {
   return prefill_workspace_bytes(total_tokens, num_seqs, H, d_k, d_v);
+}
+
+// kda_prefill with its scratch in g_noalloc_scratch instead of a caller's workspace: the same
+// validation, schedule and kernels, and no allocation of any kind. Sizes whose schedule needs more
+// scratch than the array holds are refused before anything is enqueued.
+kda_status kda_prefill_noalloc(const void *q, const void *k, const void *v, const float *log_alpha,
+                               const float *beta, const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                               int32_t H, int32_t d_k, int32_t d_v, kda_dtype in_dtype, kda_dtype out_dtype,
+                               float lower_bound, float scale, const float *init_state, void *out,
+                               float *final_state, void *stream) {
+  const kda_status st = check_prefill_args(q, k, v, log_alpha, nullptr, beta, cu_seqlens, num_seqs, total_tokens, H,
+                                           d_k, d_v, in_dtype, out_dtype, init_state, out, final_state);
+  if (st != KDA_OK) return st;
+  if (prefill_workspace_bytes(total_tokens, num_seqs, H, d_k, d_v) > kNoAllocScratchBytes) return KDA_ERR_UNSUPPORTED;
+  void *scratch = noalloc_scratch();
+  if (scratch == nullptr) return KDA_ERR_CUDA;
+  return prefill_impl(q, k, v, log_alpha, nullptr, beta, cu_seqlens, num_seqs, total_tokens, H, d_k, d_v, in_dtype,
+                      out_dtype, lower_bound, scale, init_state, out, final_state, stream, false, nullptr, nullptr,
+                      0.f, -1, scratch, kNoAllocScratchBytes);
 }
 
 kda_status kda_prefill_gated(const void *q, const void *k, const void *v, const void *z, const float *A_log,
