@@ -432,6 +432,9 @@ def main():
                          "step) after 3 warm-up ones and print their mean time: for profiler captures")
     ap.add_argument("--prologue-only", action="store_true",
                     help="time the input prologue pass only (T=4096, --heads heads): for profiler captures")
+    ap.add_argument("--workload", default=None,
+                    help="with --prefill-only: time kda_prefill on this named workload instead (e.g. "
+                         "prefill_f32_T256_H2, prefill_varlen8_H96), with the workspace it asks for")
     args = ap.parse_args()
     if args.form != "clamped" and not (args.prefill_only or args.decode_only):
         ap.error("--form goes with --prefill-only or --decode-only")
@@ -457,6 +460,14 @@ def main():
         p_ms = time_prologue(args.steps, args.warmup, world, seed=rank, H=args.heads)
         if rank == 0:
             print(json.dumps({"prologue_only": True, "heads": args.heads, "launch_ms": sum(p_ms) / len(p_ms)}),
+                  flush=True)
+        return
+    if args.workload is not None:
+        if not args.prefill_only:
+            ap.error("--workload goes with --prefill-only")
+        ms, *_ = time_named_prefill(args.workload, args.steps, args.warmup, world, seed=rank)
+        if rank == 0:
+            print(json.dumps({"prefill_only": True, "workload": args.workload, "launch_ms": sum(ms) / len(ms)}),
                   flush=True)
         return
     if args.decode_only:

@@ -84,8 +84,13 @@ namespace chunked {
 
 constexpr int kC = 32;      // chunk length (two 16-token subtiles)
 constexpr int kD = 128;     // d_k = d_v
-constexpr int kWorkers = 512;               // 16 compute warps
-constexpr int kThreads = kWorkers + 32;     // + one warp that issues TMA loads and MMAs
+constexpr int kWorkers = 512;               // 16 compute warps (warps 0..15)
+constexpr int kHandoff = kWorkers + 32;     // + warp 16, which issues TMA loads and MMAs
+// Warps 18 and 19 (TMEM lane quarters 2 and 3, where the key rows of the Gram land) are the
+// inverse pair of the bounded maps; warp 17 has no work. 20 warps at 96 registers each fit the
+// register file exactly as 17 would (registers are granted to warps in groups of four).
+constexpr int kInvWarp0 = 18;
+constexpr int kThreads = 640;
 constexpr int kALd = 36;    // fp32 row stride of the A / T scratch
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -108,7 +113,7 @@ constexpr uint32_t kWQBytes = 16 * 1024;
 constexpr uint32_t OFF_PK = 188 * 1024;      // 3 x [P ; K^^T] fp16 [160 rows][32], 64-byte swizzle
 constexpr uint32_t kPKBytes = 10 * 1024;
 constexpr uint32_t OFF_MISC = 218 * 1024;    // beta x2, Gamma_last x2, group decay totals, barriers
-constexpr uint32_t OFF_SS = OFF_MISC + 3456; // output gate: per-token partial sums of squares [32][4] fp32
+constexpr uint32_t OFF_SS = OFF_MISC + 3472; // output gate: per-token partial sums of squares [32][4] fp32
 constexpr uint32_t kSmemBytes = 222 * 1024 + 1024;
 static_assert(OFF_SS + 32 * 16 + 1023 <= kSmemBytes, "shared memory map exceeds the allocation");
 // Unbounded decay only: the position-pair shares of the diagonal blocks, by chunk parity,
@@ -173,7 +178,7 @@ __device__ __forceinline__ float exp2_sfu(float x) {
 }
 
 struct Bars {
-  uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate, drain;
+  uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate, drain, invd;
 };
 static_assert(OFF_MISC + (2 * 32 + 2 * 128 + 4 * 128) * 4 + sizeof(Bars) + 48 <= OFF_SS, "misc overlaps");
 
@@ -228,6 +233,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, grp = warp >> 2;  // TMEM lane quarter, column group (compute warps)
   const bool worker = tid < kWorkers;              // warps 0..15; warp 16 issues TMA loads and MMAs
+  // The bounded maps invert I + A on a pair of warps of their own (warps 18, 19), one chunk ahead
+  // of the state chain; the unbounded map keeps the inverse on four of the compute warps, whose
+  // scratch its position-pair step shares.
+  constexpr bool kDedInv = kDecay != DECAY_UNBOUNDED;
+  const bool inv_pair = kDedInv && warp >= kInvWarp0;
   const int h = int(blockIdx.x % H);
   const int64_t blk = blockIdx.x / H;
   const int64_t n = runs.count > 0 ? blk : runs.order != nullptr ? int64_t(runs.order[blk]) : blk;
@@ -258,6 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->wu, 1);
     mbar_init(&bars->gate, 1);
     mbar_init(&bars->drain, 1);
+    mbar_init(&bars->invd, 1);
     fence_mbarrier_init();
     s_tmem[1] = 0u;            // abort flag
     s_tmem[2] = s_tmem[3] = ~0u;  // unbounded map: the last chunk of each parity with wide channels
@@ -340,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto handoff = [&](uint32_t id) {  // compute warps: operands of this event written
     fence_proxy_async_smem();
     tc_fence_before();
-    named_bar_arrive(id, kThreads);
+    named_bar_arrive(id, kHandoff);
   };
   auto give_up = [&](uint32_t id) {
     if (tid == 0) *s_abort = 1u;
@@ -559,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Warps 2, 3, 6, 7 (TMEM lane quarters 2 and 3, column groups 0 and 1) form the inverse
   // group: the key rows of the Gram (A) live in their lanes. The other 12 warps write
   // outputs, convert v and take the query rows (P).
-  const bool inv_group = quarter >= 2 && grp < 2;
+  const bool inv_group = !kDedInv && quarter >= 2 && grp < 2;
   const int iw = (quarter - 2) + 2 * grp;  // inverse group: warp 0..3 of the group
   const int itid = 32 * iw + lane;         // inverse group: thread 0..127 of the group
 
@@ -585,6 +596,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // short enough for row stores, and a partial chunk (the last of a sequence) is always stored
   // row by row, so that nothing past the sequence is written. Both paths round bf16 alike.
   constexpr uint32_t BAR_OUT = 7;
+  constexpr uint32_t kOutThreads = kDedInv ? kWorkers : 384;  // the warps that write outputs
   auto write_rows = [&](const auto &x, int t0, int j, int L) {
     constexpr int N = int(sizeof(x) / sizeof(x[0]));
     if (kNormGate && L == kC) {
@@ -595,7 +607,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         else reinterpret_cast<float *>(stage)[(t0 + e) * kD + v_own] = x[e];
       }
       fence_proxy_async_smem();
-      named_bar_sync(BAR_OUT, 384);
+      named_bar_sync(BAR_OUT, kOutThreads);
       if (tid == 0 && !no_out) {
         tma_store_3d(&tm_o, stage, 0, h, int32_t(chunk_t0(j)));
         bulk_commit();
@@ -638,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kShift = N == 8 ? 2 : 1;  // lane l holds the sum of token (l >> kShift) & (N - 1)
     if ((lane & ((1 << kShift) - 1)) == 0)
       reinterpret_cast<float *>(s_ss)[4 * (t0 + ((lane >> kShift) & (N - 1))) + quarter] = part;
-    named_bar_sync(BAR_OUT, 384);
+    named_bar_sync(BAR_OUT, kOutThreads);
     const float4 p = s_ss[t0 + (lane & (N - 1))];
     const float rstd_l = rsqrtf(((p.x + p.y) + (p.z + p.w)) * (1.f / kD) + og.eps);  // token t0 + (lane & (N-1))
     if constexpr (N == 8) tmem_ld8(ocols + t0, x);
@@ -656,9 +668,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int L = chunk_len(j);
     const uint32_t ocols = tmem + lane_base + tm_grp(j & 1) + TM_O;
     if constexpr (kNormGate) {
-      if (quarter < 2) out_gated_rows(std::integral_constant<int, 8>{}, 8 * grp, j, L, ocols);
+      if (kDedInv || quarter < 2) out_gated_rows(std::integral_constant<int, 8>{}, 8 * grp, j, L, ocols);
       else out_gated_rows(std::integral_constant<int, 16>{}, 16 * (grp - 2), j, L, ocols);
-    } else if (quarter < 2) {
+    } else if (kDedInv || quarter < 2) {
       float x[8];
       tmem_ld8(ocols + 8 * grp, x);  // O^T row v, tokens 8 grp ..
       tmem_ld_wait();
@@ -674,6 +686,70 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int e = 0; e < 16; ++e) x[e] *= scale;
       write_rows(x, t0, j, L);
     }
+  };
+
+  // Diagonal 16 x 16 block iw of T = (I + A)^{-1} (rows and columns 16 iw ..) from A, in 8 x 8
+  // pieces, on one warp: the two diagonal pieces by forward substitution (16 lanes, a lane per
+  // column), the zero piece above them, then the piece below, -T_11 (A_10 T_00). Xs: 64 floats
+  // of scratch per block.
+  auto diag_block_inverse = [&](int iw, const float *As, float *Ts, float *Xs) {
+    // diagonal block iw (16 x 16) in 8 x 8 pieces, warp-synchronous
+    const int base = 16 * iw;
+    if (lane < 16) {  // the two 8 x 8 diagonal pieces: lane = column of its piece
+      const int o = base + 8 * (lane >> 3), cc = lane & 7;
+      float x[8], a[28];  // column cc of the piece's inverse; the piece's strictly lower entries
+#pragma unroll
+      for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
+#pragma unroll
+      for (int m = 0, n = 0; m < 8; ++m)  // all loads before the first store (which may alias)
+#pragma unroll
+        for (int r = m + 1; r < 8; ++r, ++n) a[n] = As[(o + r) * kALd + o + m];
+#pragma unroll
+      for (int m = 0, n = 0; m < 8; ++m)
+#pragma unroll
+        for (int r = m + 1; r < 8; ++r, ++n) x[r] = fmaf(-a[n], x[m], x[r]);
+#pragma unroll
+      for (int m = 0; m < 8; ++m) Ts[(o + m) * kALd + o + cc] = x[m];
+    } else {  // the zero 8 x 8 piece above the diagonal
+      const int l = lane - 16;
+      *reinterpret_cast<float4 *>(Ts + (base + (l >> 1)) * kALd + base + 8 + 4 * (l & 1)) =
+          make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    __syncwarp();
+    // piece below the diagonal: -T_11 (A_10 T_00); lane (row r8, columns 2 c8, 2 c8 + 1)
+    float *Xw = Xs + 64 * iw;
+    const int r8 = lane >> 2, c8 = lane & 3;
+    float a8[8];
+    auto load8 = [&](const float *src) {
+      const float4 p0 = reinterpret_cast<const float4 *>(src)[0], p1 = reinterpret_cast<const float4 *>(src)[1];
+      a8[0] = p0.x;
+      a8[1] = p0.y;
+      a8[2] = p0.z;
+      a8[3] = p0.w;
+      a8[4] = p1.x;
+      a8[5] = p1.y;
+      a8[6] = p1.z;
+      a8[7] = p1.w;
+      };
+      load8(As + (base + 8 + r8) * kALd + base);
+      float2 acc8 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 t2 = *reinterpret_cast<const float2 *>(Ts + (base + k) * kALd + base + 2 * c8);
+        acc8.x = fmaf(a8[k], t2.x, acc8.x);
+        acc8.y = fmaf(a8[k], t2.y, acc8.y);
+      }
+      *reinterpret_cast<float2 *>(Xw + r8 * 8 + 2 * c8) = acc8;
+      __syncwarp();
+      load8(Ts + (base + 8 + r8) * kALd + base + 8);
+      acc8 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const float2 x2 = *reinterpret_cast<const float2 *>(Xw + k * 8 + 2 * c8);
+        acc8.x = fmaf(-a8[k], x2.x, acc8.x);
+        acc8.y = fmaf(-a8[k], x2.y, acc8.y);
+      }
+      *reinterpret_cast<float2 *>(Ts + (base + 8 + r8) * kALd + base + 2 * c8) = acc8;
   };
 
   // ------------------------------------------------------------------ P4: P, A, inverse, T', v
@@ -717,63 +793,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       float *Ts = reinterpret_cast<float *>(sm + OFF_ST + G_T);
       float *Xs = reinterpret_cast<float *>(sm + OFF_ST + G_X);
       if (iw < 2) {
-        // diagonal block iw (16 x 16) in 8 x 8 pieces, warp-synchronous
-        const int base = 16 * iw;
-        if (lane < 16) {  // the two 8 x 8 diagonal pieces: lane = column of its piece
-          const int o = base + 8 * (lane >> 3), cc = lane & 7;
-          float x[8], a[28];  // column cc of the piece's inverse; the piece's strictly lower entries
-#pragma unroll
-          for (int r = 0; r < 8; ++r) x[r] = (r == cc) ? 1.f : 0.f;
-#pragma unroll
-          for (int m = 0, n = 0; m < 8; ++m)  // all loads before the first store (which may alias)
-#pragma unroll
-            for (int r = m + 1; r < 8; ++r, ++n) a[n] = As[(o + r) * kALd + o + m];
-#pragma unroll
-          for (int m = 0, n = 0; m < 8; ++m)
-#pragma unroll
-            for (int r = m + 1; r < 8; ++r, ++n) x[r] = fmaf(-a[n], x[m], x[r]);
-#pragma unroll
-          for (int m = 0; m < 8; ++m) Ts[(o + m) * kALd + o + cc] = x[m];
-        } else {  // the zero 8 x 8 piece above the diagonal
-          const int l = lane - 16;
-          *reinterpret_cast<float4 *>(Ts + (base + (l >> 1)) * kALd + base + 8 + 4 * (l & 1)) =
-              make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        __syncwarp();
-        // piece below the diagonal: -T_11 (A_10 T_00); lane (row r8, columns 2 c8, 2 c8 + 1)
-        float *Xw = Xs + 64 * iw;
-        const int r8 = lane >> 2, c8 = lane & 3;
-        float a8[8];
-        auto load8 = [&](const float *src) {
-          const float4 p0 = reinterpret_cast<const float4 *>(src)[0], p1 = reinterpret_cast<const float4 *>(src)[1];
-          a8[0] = p0.x;
-          a8[1] = p0.y;
-          a8[2] = p0.z;
-          a8[3] = p0.w;
-          a8[4] = p1.x;
-          a8[5] = p1.y;
-          a8[6] = p1.z;
-          a8[7] = p1.w;
-        };
-        load8(As + (base + 8 + r8) * kALd + base);
-        float2 acc8 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float2 t2 = *reinterpret_cast<const float2 *>(Ts + (base + k) * kALd + base + 2 * c8);
-          acc8.x = fmaf(a8[k], t2.x, acc8.x);
-          acc8.y = fmaf(a8[k], t2.y, acc8.y);
-        }
-        *reinterpret_cast<float2 *>(Xw + r8 * 8 + 2 * c8) = acc8;
-        __syncwarp();
-        load8(Ts + (base + 8 + r8) * kALd + base + 8);
-        acc8 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const float2 x2 = *reinterpret_cast<const float2 *>(Xw + k * 8 + 2 * c8);
-          acc8.x = fmaf(-a8[k], x2.x, acc8.x);
-          acc8.y = fmaf(-a8[k], x2.y, acc8.y);
-        }
-        *reinterpret_cast<float2 *>(Ts + (base + 8 + r8) * kALd + base + 2 * c8) = acc8;
+        diag_block_inverse(iw, As, Ts, Xs);
       } else {  // the zero 16 x 16 block above the diagonal
         const int l = itid - 64;
         *reinterpret_cast<float4 *>(Ts + (l >> 2) * kALd + 16 + 4 * (l & 3)) = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -824,9 +844,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // the 12 other warps: v tile of this chunk bf16 -> fp16 in place (rows past the end
       // zeroed), the query rows P of the Gram, then the outputs of chunk j_out
-      const int ot = (quarter < 2 ? 64 * grp + 32 * quarter : 256 + 64 * (grp - 2) + 32 * (quarter - 2)) + lane;
+      const int ot = kDedInv ? tid
+                             : (quarter < 2 ? 64 * grp + 32 * quarter : 256 + 64 * (grp - 2) + 32 * (quarter - 2)) + lane;
       bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
-      for (int e = ot; e < kC * 16; e += 384) {
+      for (int e = ot; e < kC * 16; e += int(kOutThreads)) {
         const int t = e >> 4, cj = e & 15;
         uint4 *p = reinterpret_cast<uint4 *>(sm + OFF_V + b * 8192 + sw128_chunk(t, cj & 7, cj >> 3, kC));
         uint4 w = make_uint4(0, 0, 0, 0);
@@ -865,13 +886,120 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (j_out >= 0) out_chunk(j_out);
     }
     // the inverse's scratch aliases the S^T tile that the next chain step rewrites: all
-    // compute threads are past it before any goes on
+    // compute threads are past it before any goes on (and, with the inverse pair, the pair
+    // has finished chunk c: its T' is written and its scratch released)
     fence_proxy_async_smem();
     tc_fence_before();
     const bool ab = named_bar_or(BAR_WORK, kWorkers, bad);
     if (ab) give_up(H_INV);
     else handoff(H_INV);
+    if (kDedInv && !ab) bad |= !mbar_wait_sleep(&bars->invd, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
     return !ab;
+  };
+
+  // ------------------------------------------------------------------ the inverse pair
+  // Warps 18 and 19 (bounded maps): T = (I + A)^{-1} and T' = T Diag(beta) of chunk c, while the
+  // compute warps run the chain of chunk c - 1 and build the operands of chunk c + 1. A lives in
+  // the lanes of TMEM quarters 2 (rows 0..15) and 3 (rows 16..31). The scratch (A, T, X) is the
+  // S^T tile, free once MMA1 of chunk c - 1 has read it; the T' tile is free once the W^T / U~^T
+  // MMA of chunk c - 1 has read it. The pair reports chunk c done on the invd barrier (after which
+  // the compute warps rewrite the S^T tile and the issuer reads T'). Returns false when a wait
+  // gave up.
+  constexpr uint32_t BAR_PAIR = 8;
+  auto inverse_pair = [&](int c) -> bool {
+    const int b = c & 1, L = chunk_len(c);
+    const int s = quarter - 2;          // diagonal block (rows 16 s ..) and TMEM quarter 2 + s
+    const int ptid = 32 * s + lane;     // 0 .. 63
+    float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
+    float *Ts = reinterpret_cast<float *>(sm + OFF_ST + G_T);
+    float *Xs = reinterpret_cast<float *>(sm + OFF_ST + G_X);
+    bool ok = mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+    if (c >= 1) ok &= mbar_wait_sleep(&bars->mma1, uint32_t((c - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+    tc_fence_after();
+    // A rows t = 16 s + lane (lanes 0..15; M = 64 layout), columns 16 h2 .. 16 h2 + 15 up to the
+    // row block's end (the entries past it are zero and never read); A[t][i] = beta_t G[t][i], i < t
+    for (int h2 = 0; h2 <= s; ++h2) {
+      float vals[16];
+      tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * h2, vals);
+      tmem_ld_wait();
+      if (lane < 16) {
+        const int t = 16 * s + lane;
+        const float bt = s_beta[b * kC + t];
+        const int lim = t < L ? t - 16 * h2 : 0;  // keep i < t
+#pragma unroll
+        for (int e = 0; e < 16; ++e) vals[e] = e < lim ? bt * vals[e] : 0.f;
+        float4 *arow = reinterpret_cast<float4 *>(As + t * kALd + 16 * h2);
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+          arow[q4] = make_float4(vals[4 * q4], vals[4 * q4 + 1], vals[4 * q4 + 2], vals[4 * q4 + 3]);
+      }
+    }
+    named_bar_sync(BAR_PAIR, 64);
+    diag_block_inverse(s, As, Ts, Xs);
+    // the zero 16 x 16 block above the diagonal: rows 0..15, columns 16..31
+    *reinterpret_cast<float4 *>(Ts + (ptid >> 2) * kALd + 16 + 4 * (ptid & 3)) = make_float4(0.f, 0.f, 0.f, 0.f);
+    named_bar_sync(BAR_PAIR, 64);
+    // block below the diagonal, T_10 = -T_11 (A_10 T_00): thread (row r, columns 4 c4 .. 4 c4 + 3)
+    const int r = ptid >> 2, c4 = ptid & 3;
+    float rowv[16];
+    auto load_row = [&](const float *src) {
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const float4 v4 = reinterpret_cast<const float4 *>(src)[q4];
+        rowv[4 * q4] = v4.x;
+        rowv[4 * q4 + 1] = v4.y;
+        rowv[4 * q4 + 2] = v4.z;
+        rowv[4 * q4 + 3] = v4.w;
+      }
+    };
+    load_row(As + (16 + r) * kALd);  // A_10 row r
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float4 t4 = *reinterpret_cast<const float4 *>(Ts + k * kALd + 4 * c4);  // T_00 row k
+      acc.x = fmaf(rowv[k], t4.x, acc.x);
+      acc.y = fmaf(rowv[k], t4.y, acc.y);
+      acc.z = fmaf(rowv[k], t4.z, acc.z);
+      acc.w = fmaf(rowv[k], t4.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(Xs + r * 16 + 4 * c4) = acc;
+    named_bar_sync(BAR_PAIR, 64);
+    load_row(Ts + (16 + r) * kALd + 16);  // T_11 row r (zero above its diagonal)
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      const float4 x4 = *reinterpret_cast<const float4 *>(Xs + k * 16 + 4 * c4);
+      acc.x = fmaf(-rowv[k], x4.x, acc.x);
+      acc.y = fmaf(-rowv[k], x4.y, acc.y);
+      acc.z = fmaf(-rowv[k], x4.z, acc.z);
+      acc.w = fmaf(-rowv[k], x4.w, acc.w);
+    }
+    *reinterpret_cast<float4 *>(Ts + (16 + r) * kALd + 4 * c4) = acc;
+    named_bar_sync(BAR_PAIR, 64);
+    // T' = T Diag(beta) -> fp16 [t][i]: thread (row t, columns 16 hc .. 16 hc + 15), once the
+    // W^T / U~^T product of chunk c - 1 has read the T' tile
+    if (c >= 1) ok &= mbar_wait_sleep(&bars->wu, uint32_t((c - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+    {
+      const int t = ptid >> 1, hc = ptid & 1;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int cj = 2 * hc + q;
+        const float4 *trow = reinterpret_cast<const float4 *>(Ts + t * kALd + 8 * cj);
+        const float4 *brow = reinterpret_cast<const float4 *>(s_beta + b * kC + 8 * cj);
+        const float4 t0v = trow[0], t1v = trow[1], b0v = brow[0], b1v = brow[1];
+        const float x[8] = {t0v.x * b0v.x, t0v.y * b0v.y, t0v.z * b0v.z, t0v.w * b0v.w,
+                            t1v.x * b1v.x, t1v.y * b1v.y, t1v.z * b1v.z, t1v.w * b1v.w};
+        st_at(sm, OFF_TP + sw64_chunk(t, cj), pack8_f16(x));
+      }
+    }
+    fence_proxy_async_smem();  // T' is read by the tensor cores
+    tc_fence_before();
+    // one verdict for the pair, then chunk c is reported done (also when a wait gave up, so that
+    // the waiters move on; the abort flag then tells the issuer and the compute warps)
+    const bool fail = named_bar_or(BAR_PAIR, 64, !ok);
+    if (fail && ptid == 0) *s_abort = 1u;
+    if (ptid == 0) mbar_arrive(&bars->invd);
+    return !fail;
   };
 
   auto issue_wu = [&](int c) {  // issuer: W^T and [U~^T | 0]
@@ -971,14 +1099,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int e = 0; e < 16; ++e) final_state[st_base + int64_t(32 * grp + 16 * u + e) * kD + v_own] = x[e];
       }
     }
-  } else {
+  } else if (inv_pair) {
+    // ---------------------------------------------------------------- inverse pair
+    for (int c = 0; c < n_chunks; ++c) {
+      if (!inverse_pair(c)) break;
+      // the compute warps gave up: leave (one verdict for the pair, so that both warps leave together)
+      if (named_bar_or(BAR_PAIR, 64, *s_abort != 0u)) break;
+    }
+  } else if (warp == kInvWarp0 - 2) {
     // ---------------------------------------------------------------- issuing warp
     // The whole warp follows the hand-offs; lane 0 issues.
     const bool leader = lane == 0;
     auto sync_on = [&](uint32_t id) {
-      named_bar_sync(id, kThreads);
+      named_bar_sync(id, kHandoff);
       tc_fence_after();
       return *s_abort == 0u;
+    };
+    // the inverse pair has written T' of chunk c (bounded; a pair that gave up raised the abort flag)
+    auto pair_done = [&](int c) {
+      if (!kDedInv) return true;
+      const bool ok = mbar_wait_sleep(&bars->invd, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
+      tc_fence_after();
+      return ok && *s_abort == 0u;
     };
     if (n_chunks > 0) {
       if (leader) {
@@ -997,7 +1139,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (c + 1 < n_chunks) qkg_last = c + 1;
       }
-      if (!sync_on(H_INV)) goto issuer_abort;
+      if (!sync_on(H_INV) || !pair_done(0)) goto issuer_abort;
       if (leader) issue_wu(0);
       if (n_chunks > 2) {  // v stage 0 is free once W^T / U~^T of chunk 0 are done
         mbar_wait_sleep(&bars->wu, 0u, err_word, DEVERR_MMA_TIMEOUT);
@@ -1043,7 +1185,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         gate_last = j;
       }
       if (more) {
-        if (!sync_on(H_INV)) goto issuer_abort;
+        if (!sync_on(H_INV) || !pair_done(j + 1)) goto issuer_abort;
         if (leader) issue_wu(j + 1);
         if (j + 3 < n_chunks) {  // v stage (j + 1) % 2 is free once W^T / U~^T of chunk j + 1 are done
           mbar_wait_sleep(&bars->wu, uint32_t((j + 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
