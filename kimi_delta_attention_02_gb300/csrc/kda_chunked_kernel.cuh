@@ -87,9 +87,10 @@ constexpr int kD = 128;     // d_k = d_v
 constexpr int kWorkers = 512;               // 16 compute warps (warps 0..15)
 constexpr int kHandoff = kWorkers + 32;     // + warp 16, which issues TMA loads and MMAs
 // Warps 18 and 19 (TMEM lane quarters 2 and 3, where the key rows of the Gram land) are the
-// inverse pair of the bounded maps; warp 17 has no work. 20 warps at 96 registers each fit the
-// register file exactly as 17 would (registers are granted to warps in groups of four).
-constexpr int kInvWarp0 = 18;
+// inverse pair of the bounded maps, and warp 17 issues their Gram MMAs (a second issuer, so that
+// the 16 Gram MMAs of a chunk do not queue in front of the chain's). 20 warps at 96 registers
+// each fit the register file exactly as 17 would (registers are granted to warps in groups of four).
+constexpr int kInvWarp0 = 18, kGramWarp = 17;
 constexpr int kThreads = 640;
 constexpr int kALd = 36;    // fp32 row stride of the A / T scratch
 constexpr float kLog2e = 1.4426950408889634f;
@@ -113,7 +114,7 @@ constexpr uint32_t kWQBytes = 16 * 1024;
 constexpr uint32_t OFF_PK = 188 * 1024;      // 3 x [P ; K^^T] fp16 [160 rows][32], 64-byte swizzle
 constexpr uint32_t kPKBytes = 10 * 1024;
 constexpr uint32_t OFF_MISC = 218 * 1024;    // beta x2, Gamma_last x2, group decay totals, barriers
-constexpr uint32_t OFF_SS = OFF_MISC + 3472; // output gate: per-token partial sums of squares [32][4] fp32
+constexpr uint32_t OFF_SS = OFF_MISC + 3504; // output gate: per-token partial sums of squares [32][4] fp32
 constexpr uint32_t kSmemBytes = 222 * 1024 + 1024;
 static_assert(OFF_SS + 32 * 16 + 1023 <= kSmemBytes, "shared memory map exceeds the allocation");
 // Unbounded decay only: the position-pair shares of the diagonal blocks, by chunk parity,
@@ -123,8 +124,10 @@ static_assert(OFF_SS + 32 * 16 + 1023 <= kSmemBytes, "shared memory map exceeds 
 constexpr uint32_t OFF_CORR = 222 * 1024;
 constexpr uint32_t kSmemBytesUnbounded = 226 * 1024 + 1024;
 static_assert(OFF_SS + 32 * 16 <= OFF_CORR && kSmemBytesUnbounded <= 232448, "unbounded map exceeds 227 KB");
+// Bounded maps: the same 4 KB hold the inverse pair's copy of A [32][32] fp32.
+constexpr uint32_t OFF_PAIR = OFF_CORR;
 template <int kDecay>
-constexpr uint32_t smem_bytes() { return kDecay == DECAY_UNBOUNDED ? kSmemBytesUnbounded : kSmemBytes; }
+constexpr uint32_t smem_bytes() { return kSmemBytesUnbounded; }
 // a channel is wide in a diagonal block when its log2 decay over the block's tokens is below
 // -kWideBlock (the bound gives every Gram factor of a narrow channel a magnitude <= 2^114)
 constexpr float kWideBlock = 114.f;
@@ -178,7 +181,7 @@ __device__ __forceinline__ float exp2_sfu(float x) {
 }
 
 struct Bars {
-  uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate, drain, invd;
+  uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate, drain, invd, aread[2], drain2, prep;
 };
 static_assert(OFF_MISC + (2 * 32 + 2 * 128 + 4 * 128) * 4 + sizeof(Bars) + 48 <= OFF_SS, "misc overlaps");
 
@@ -238,6 +241,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // scratch its position-pair step shares.
   constexpr bool kDedInv = kDecay != DECAY_UNBOUNDED;
   const bool inv_pair = kDedInv && warp >= kInvWarp0;
+  // Full chunks leave through a TMA store of a staged tile with the output gate.
+  constexpr bool kStaged = kNormGate;
+  // Plain read-out with the inverse pair: the outputs of chunk j - 1 leave with P1 of chunk j (both
+  // wait for MMA2 of chunk j - 1 and read tensor memory in the same round trip), and P of chunk
+  // j + 1 leaves tensor memory with U^T of chunk j in P3; no separate output phase.
+  constexpr bool kMerged = kDedInv && !kNormGate;
   const int h = int(blockIdx.x % H);
   const int64_t blk = blockIdx.x / H;
   const int64_t n = runs.count > 0 ? blk : runs.order != nullptr ? int64_t(runs.order[blk]) : blk;
@@ -269,6 +278,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->gate, 1);
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->invd, 1);
+    mbar_init(&bars->aread[0], 1);
+    mbar_init(&bars->aread[1], 1);
+    mbar_init(&bars->drain2, 1);
+    mbar_init(&bars->prep, kWorkers);  // every compute thread: the Gram operands of a chunk are written
     fence_mbarrier_init();
     s_tmem[1] = 0u;            // abort flag
     s_tmem[2] = s_tmem[3] = ~0u;  // unbounded map: the last chunk of each parity with wide channels
@@ -352,6 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     named_bar_arrive(id, kHandoff);
+    // with the inverse pair, the Gram warp learns of the Gram operands on an mbarrier (it issues
+    // the Gram; a bounded wait, so that it never waits on a hand-off that an abort skips)
+    if (kDedInv && id == H_PREP) mbar_arrive(&bars->prep);
   };
   auto give_up = [&](uint32_t id) {
     if (tid == 0) *s_abort = 1u;
@@ -400,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (full) decay_sums(std::true_type{});
     else decay_sums(std::false_type{});
     if (tid < kC) s_beta[b * kC + tid] = b_pref;
-    if (kNormGate && store_pending) {  // the U^T tile is written after this barrier
+    if (kStaged && store_pending) {  // the U^T tile is written after this barrier
       bulk_wait_read();
       store_pending = false;
     }
@@ -599,7 +615,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr uint32_t kOutThreads = kDedInv ? kWorkers : 384;  // the warps that write outputs
   auto write_rows = [&](const auto &x, int t0, int j, int L) {
     constexpr int N = int(sizeof(x) / sizeof(x[0]));
-    if (kNormGate && L == kC) {
+    if (kStaged && L == kC) {
       uint8_t *stage = kOutBF16 ? sm + OFF_UT : sm + OFF_ST + G_O;
 #pragma unroll
       for (int e = 0; e < N; ++e) {
@@ -752,6 +768,26 @@ __global__ void __launch_bounds__(kThreads, 1)
       *reinterpret_cast<float2 *>(Ts + (base + 8 + r8) * kALd + base + 2 * c8) = acc8;
   };
 
+  // P rows t = 16 quarter + lane (lanes 0..15) of chunk c, columns 8 grp .. + 7 (compute warps of
+  // TMEM quarters 0 and 1), into the [P ; K^^T] tile of chunk c. Waits for the tensor-memory loads
+  // issued before it as well.
+  auto extract_p = [&](int c) {
+    const int b = c & 1, L = chunk_len(c);
+    bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+    tc_fence_after();
+    const int t = 16 * quarter + (lane & 15);
+    const bool have = grp < 2 * (quarter + 1);  // columns up to the row block's end
+    float vals[8];
+    if (have) tmem_ld8(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
+    tmem_ld_wait();
+    if (lane < 16) {
+      const int lim = (have && t < L) ? t + 1 - 8 * grp : 0;  // keep i <= t
+#pragma unroll
+      for (int e = 0; e < 8; ++e) vals[e] = e < lim ? vals[e] : 0.f;
+      st_at(sm + OFF_PK + (c % 3) * kPKBytes, sw64_chunk(t, grp), pack8_f16(vals));
+    }
+  };
+
   // ------------------------------------------------------------------ P4: P, A, inverse, T', v
   // Inverse-side work of chunk c; the 12 warps outside the inverse group also write the
   // outputs of chunk j_out (if >= 0). Returns false when the compute warps give up.
@@ -844,9 +880,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // the 12 other warps: v tile of this chunk bf16 -> fp16 in place (rows past the end
       // zeroed), the query rows P of the Gram, then the outputs of chunk j_out
-      const int ot = kDedInv ? tid
+      // (with the inverse pair, the pair converts v)
+      const int ot = kDedInv ? kC * 16
                              : (quarter < 2 ? 64 * grp + 32 * quarter : 256 + 64 * (grp - 2) + 32 * (quarter - 2)) + lane;
-      bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
+      if (!kDedInv) bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
       for (int e = ot; e < kC * 16; e += int(kOutThreads)) {
         const int t = e >> 4, cj = e & 15;
         uint4 *p = reinterpret_cast<uint4 *>(sm + OFF_V + b * 8192 + sw128_chunk(t, cj & 7, cj >> 3, kC));
@@ -885,39 +922,43 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (j_out >= 0) out_chunk(j_out);
     }
-    // the inverse's scratch aliases the S^T tile that the next chain step rewrites: all
-    // compute threads are past it before any goes on (and, with the inverse pair, the pair
-    // has finished chunk c: its T' is written and its scratch released)
+    // the next chain step rewrites the S^T tile (the four-warp inverse's scratch, the output
+    // gate's tiles): all compute threads are past this phase before any goes on
     fence_proxy_async_smem();
     tc_fence_before();
     const bool ab = named_bar_or(BAR_WORK, kWorkers, bad);
-    if (ab) give_up(H_INV);
-    else handoff(H_INV);
-    if (kDedInv && !ab) bad |= !mbar_wait_sleep(&bars->invd, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
+    // with the inverse pair, the issuer needs nothing of this phase before W^T / U~^T (the pair
+    // hands over T' and v; P reaches MMA2 behind the next H_U): no hand-off
+    if (!kDedInv) {
+      if (ab) give_up(H_INV);
+      else handoff(H_INV);
+    } else if (ab && tid == 0) {
+      *s_abort = 1u;  // the issuer sees it at its next hand-off
+    }
     return !ab;
   };
 
   // ------------------------------------------------------------------ the inverse pair
-  // Warps 18 and 19 (bounded maps): T = (I + A)^{-1} and T' = T Diag(beta) of chunk c, while the
-  // compute warps run the chain of chunk c - 1 and build the operands of chunk c + 1. A lives in
-  // the lanes of TMEM quarters 2 (rows 0..15) and 3 (rows 16..31). The scratch (A, T, X) is the
-  // S^T tile, free once MMA1 of chunk c - 1 has read it; the T' tile is free once the W^T / U~^T
-  // MMA of chunk c - 1 has read it. The pair reports chunk c done on the invd barrier (after which
-  // the compute warps rewrite the S^T tile and the issuer reads T'). Returns false when a wait
-  // gave up.
+  // Warps 18 and 19 (bounded maps): T' = (I + A)^{-1} Diag(beta) of chunk c and the fp16 v tile of
+  // chunk c, while the compute warps run the chain of chunk c - 1 and build the operands of chunk
+  // c + 1. A lives in the lanes of TMEM quarters 2 (rows 0..15) and 3 (rows 16..31); both warps
+  // copy their rows into the pair's own 4 KB of shared memory, then warp 18 forms T' a row per
+  // lane: row j of T solves x^T (I + A) = e_j^T, i.e. x_m = [m == j] - sum_{i > m} x_i A[i][m]
+  // (A is strictly lower triangular), taken from m = 31 down with every finished x_i folded into
+  // the rows below it. The T' tile is free once the W^T / U~^T product of chunk c - 1 has read
+  // it. The pair reports chunk c done on the invd barrier, after which the issuer reads T' and v.
+  // Returns false when a wait gave up.
   constexpr uint32_t BAR_PAIR = 8;
   auto inverse_pair = [&](int c) -> bool {
     const int b = c & 1, L = chunk_len(c);
-    const int s = quarter - 2;          // diagonal block (rows 16 s ..) and TMEM quarter 2 + s
+    const int s = quarter - 2;          // TMEM quarter 2 + s holds A rows 16 s ..
     const int ptid = 32 * s + lane;     // 0 .. 63
-    float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
-    float *Ts = reinterpret_cast<float *>(sm + OFF_ST + G_T);
-    float *Xs = reinterpret_cast<float *>(sm + OFF_ST + G_X);
+    float *As = reinterpret_cast<float *>(sm + OFF_PAIR);  // [32][32]
     bool ok = mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
-    if (c >= 1) ok &= mbar_wait_sleep(&bars->mma1, uint32_t((c - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
     // A rows t = 16 s + lane (lanes 0..15; M = 64 layout), columns 16 h2 .. 16 h2 + 15 up to the
-    // row block's end (the entries past it are zero and never read); A[t][i] = beta_t G[t][i], i < t
+    // row block's end (the substitution reads no entry on or past a row's diagonal);
+    // A[t][i] = beta_t G[t][i] for i < t (and t inside the sequence), else 0
     for (int h2 = 0; h2 <= s; ++h2) {
       float vals[16];
       tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * h2, vals);
@@ -928,71 +969,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int lim = t < L ? t - 16 * h2 : 0;  // keep i < t
 #pragma unroll
         for (int e = 0; e < 16; ++e) vals[e] = e < lim ? bt * vals[e] : 0.f;
-        float4 *arow = reinterpret_cast<float4 *>(As + t * kALd + 16 * h2);
+        float4 *arow = reinterpret_cast<float4 *>(As + t * 32 + 16 * h2);
 #pragma unroll
         for (int q4 = 0; q4 < 4; ++q4)
           arow[q4] = make_float4(vals[4 * q4], vals[4 * q4 + 1], vals[4 * q4 + 2], vals[4 * q4 + 3]);
       }
     }
-    named_bar_sync(BAR_PAIR, 64);
-    diag_block_inverse(s, As, Ts, Xs);
-    // the zero 16 x 16 block above the diagonal: rows 0..15, columns 16..31
-    *reinterpret_cast<float4 *>(Ts + (ptid >> 2) * kALd + 16 + 4 * (ptid & 3)) = make_float4(0.f, 0.f, 0.f, 0.f);
-    named_bar_sync(BAR_PAIR, 64);
-    // block below the diagonal, T_10 = -T_11 (A_10 T_00): thread (row r, columns 4 c4 .. 4 c4 + 3)
-    const int r = ptid >> 2, c4 = ptid & 3;
-    float rowv[16];
-    auto load_row = [&](const float *src) {
+    // v of chunk c, bf16 -> fp16 in place (rows past the end zeroed): 8 of the 512 16-byte pieces each
+    ok &= mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        const float4 v4 = reinterpret_cast<const float4 *>(src)[q4];
-        rowv[4 * q4] = v4.x;
-        rowv[4 * q4 + 1] = v4.y;
-        rowv[4 * q4 + 2] = v4.z;
-        rowv[4 * q4 + 3] = v4.w;
+    for (int k = 0; k < 8; ++k) {
+      const int e = ptid + 64 * k, t = e >> 4, cj = e & 15;
+      uint4 *p = reinterpret_cast<uint4 *>(sm + OFF_V + b * 8192 + sw128_chunk(t, cj & 7, cj >> 3, kC));
+      uint4 w = make_uint4(0, 0, 0, 0);
+      if (t < L) {
+        const uint4 bv = *p;
+        const float2 a0 = unpack_bf16x2(bv.x), a1 = unpack_bf16x2(bv.y), a2 = unpack_bf16x2(bv.z),
+                     a3 = unpack_bf16x2(bv.w);
+        const float x[8] = {a0.x, a0.y, a1.x, a1.y, a2.x, a2.y, a3.x, a3.y};
+        w = pack8_f16(x);
       }
-    };
-    load_row(As + (16 + r) * kALd);  // A_10 row r
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float4 t4 = *reinterpret_cast<const float4 *>(Ts + k * kALd + 4 * c4);  // T_00 row k
-      acc.x = fmaf(rowv[k], t4.x, acc.x);
-      acc.y = fmaf(rowv[k], t4.y, acc.y);
-      acc.z = fmaf(rowv[k], t4.z, acc.z);
-      acc.w = fmaf(rowv[k], t4.w, acc.w);
+      *p = w;
     }
-    *reinterpret_cast<float4 *>(Xs + r * 16 + 4 * c4) = acc;
+    tc_fence_before();
     named_bar_sync(BAR_PAIR, 64);
-    load_row(Ts + (16 + r) * kALd + 16);  // T_11 row r (zero above its diagonal)
-    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (ptid == 0) mbar_arrive(&bars->aread[b]);  // A of chunk c is out of its Gram slot
+    if (s == 0) {
+      float2 x[16];  // row `lane` of T, as pairs of columns (packed fp32 FMAs)
 #pragma unroll
-    for (int k = 0; k < 16; ++k) {
-      const float4 x4 = *reinterpret_cast<const float4 *>(Xs + k * 16 + 4 * c4);
-      acc.x = fmaf(-rowv[k], x4.x, acc.x);
-      acc.y = fmaf(-rowv[k], x4.y, acc.y);
-      acc.z = fmaf(-rowv[k], x4.z, acc.z);
-      acc.w = fmaf(-rowv[k], x4.w, acc.w);
-    }
-    *reinterpret_cast<float4 *>(Ts + (16 + r) * kALd + 4 * c4) = acc;
-    named_bar_sync(BAR_PAIR, 64);
-    // T' = T Diag(beta) -> fp16 [t][i]: thread (row t, columns 16 hc .. 16 hc + 15), once the
-    // W^T / U~^T product of chunk c - 1 has read the T' tile
-    if (c >= 1) ok &= mbar_wait_sleep(&bars->wu, uint32_t((c - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
-    {
-      const int t = ptid >> 1, hc = ptid & 1;
+      for (int m = 0; m < 16; ++m) x[m] = make_float2(2 * m == lane ? 1.f : 0.f, 2 * m + 1 == lane ? 1.f : 0.f);
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int cj = 2 * hc + q;
-        const float4 *trow = reinterpret_cast<const float4 *>(Ts + t * kALd + 8 * cj);
-        const float4 *brow = reinterpret_cast<const float4 *>(s_beta + b * kC + 8 * cj);
-        const float4 t0v = trow[0], t1v = trow[1], b0v = brow[0], b1v = brow[1];
-        const float x[8] = {t0v.x * b0v.x, t0v.y * b0v.y, t0v.z * b0v.z, t0v.w * b0v.w,
-                            t1v.x * b1v.x, t1v.y * b1v.y, t1v.z * b1v.z, t1v.w * b1v.w};
-        st_at(sm, OFF_TP + sw64_chunk(t, cj), pack8_f16(x));
+      for (int i = 31; i >= 1; --i) {
+        const float xi = (i & 1) ? x[i >> 1].y : x[i >> 1].x;  // final: every row below i is folded in
+        const float2 nxi = make_float2(-xi, -xi);
+#pragma unroll
+        for (int m4 = 0; m4 < (i + 3) / 4; ++m4) {  // row i of A (the same for every lane)
+          const float4 a = *reinterpret_cast<const float4 *>(As + i * 32 + 4 * m4);
+          if (4 * m4 + 1 < i) x[2 * m4] = f2_fma(nxi, make_float2(a.x, a.y), x[2 * m4]);
+          else if (4 * m4 < i) x[2 * m4].x = fmaf(-xi, a.x, x[2 * m4].x);
+          if (4 * m4 + 3 < i) x[2 * m4 + 1] = f2_fma(nxi, make_float2(a.z, a.w), x[2 * m4 + 1]);
+          else if (4 * m4 + 2 < i) x[2 * m4 + 1].x = fmaf(-xi, a.z, x[2 * m4 + 1].x);
+        }
+      }
+      // T'[j][m] = T[j][m] beta_m -> fp16, row j = lane
+      if (c >= 1) ok &= mbar_wait_sleep(&bars->wu, uint32_t((c - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+      const float4 *bt = reinterpret_cast<const float4 *>(s_beta + b * kC);
+#pragma unroll
+      for (int cj = 0; cj < 4; ++cj) {
+        const float4 b0 = bt[2 * cj], b1 = bt[2 * cj + 1];
+        const float2 x0 = x[4 * cj], x1 = x[4 * cj + 1], x2 = x[4 * cj + 2], x3 = x[4 * cj + 3];
+        const float y[8] = {x0.x * b0.x, x0.y * b0.y, x1.x * b0.z, x1.y * b0.w,
+                            x2.x * b1.x, x2.y * b1.y, x3.x * b1.z, x3.y * b1.w};
+        st_at(sm, OFF_TP + sw64_chunk(uint32_t(lane), uint32_t(cj)), pack8_f16(y));
       }
     }
-    fence_proxy_async_smem();  // T' is read by the tensor cores
+    fence_proxy_async_smem();  // T' and v are read by the tensor cores
     tc_fence_before();
     // one verdict for the pair, then chunk c is reported done (also when a wait gave up, so that
     // the waiters move on; the abort flag then tells the issuer and the compute warps)
@@ -1033,16 +1064,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (n_chunks > 0) {  // operands of chunks 0 and 1
       if (!prep(0)) goto teardown;
       if (n_chunks > 1 && !prep(1)) goto teardown;
-      if (!extract_inverse(0, -1)) goto teardown;
+      if (kMerged) {
+        if (quarter < 2) extract_p(0);
+      } else if (!extract_inverse(0, -1)) {
+        goto teardown;
+      }
     }
     for (int j = 0; j < n_chunks; ++j) {
       const int b = j & 1;
       const bool more = j + 1 < n_chunks;
       // ---------------- P1: chain j, fp16 copy of S^T; decayed S^T into group j % 2
-      if (j > 0 && inv_group) {  // the state MMA2 of chunk j - 1 left (the other warps waited for it)
+      if (j > 0 && (inv_group || kMerged)) {  // the state MMA2 of chunk j - 1 left
         bad |= !mbar_wait_sleep(&bars->mma2, uint32_t((j - 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
         tc_fence_after();
       }
+      float ox[8];  // merged read-out: O^T row v of chunk j - 1, tokens 8 grp ..
+      if (kMerged && j > 0) tmem_ld8(tmem + lane_base + tm_grp(b ^ 1) + TM_O + 8 * grp, ox);
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         float x[16];
@@ -1063,6 +1100,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(s_cols(b) + 16 * u, x);
       }
       tmem_st_wait();
+      if (kMerged && j > 0) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ox[e] *= scale;
+        write_rows(ox, 8 * grp, j - 1, chunk_len(j - 1));
+      }
       // ---------------- P6: -W^T of chunk j (its W^T / U~^T MMA ran during P1) -> MMA1
       wt_extract(j);
       handoff(H_COPY);
@@ -1074,12 +1116,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         float x[8];
         tmem_ld8(tmem + lane_base + tm_grp(b) + 8 * grp, x);  // U^T row v, columns t = 8 grp ..
-        tmem_ld_wait();
+        if (kMerged && more && quarter < 2) extract_p(j + 1);  // waits for its loads with U^T's
+        else tmem_ld_wait();
         st_at(sm + OFF_UT, sw64_chunk(uint32_t(v_own), uint32_t(grp)), pack8_f16(x));
       }
       handoff(H_U);
       // ---------------- P4 / P5: inverse side of chunk j + 1 -> W^T and U~^T, and outputs of chunk j
-      if (more) {
+      if (kMerged) {
+        if (!more) out_chunk(j);
+      } else if (more) {
         if (!extract_inverse(j + 1, j)) goto teardown;
       } else if (!inv_group) {
         out_chunk(j);
@@ -1098,6 +1143,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) final_state[st_base + int64_t(32 * grp + 16 * u + e) * kD + v_own] = x[e];
       }
+    }
+  } else if (kDedInv && warp == kGramWarp) {
+    // ---------------------------------------------------------------- Gram warp
+    // The Gram of chunk c once its operand tiles are written (H_PREP) and the pair has taken A of
+    // chunk c - 2 out of the same tensor-memory slot. Lane 0 issues; on leaving early it waits for
+    // its own MMAs (bounded) before the teardown frees tensor memory.
+    bool issued = false;
+    for (int c = 0; c < n_chunks; ++c) {
+      const bool ok = mbar_wait_sleep(&bars->prep, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
+      tc_fence_after();
+      if (__any_sync(0xffffffffu, !ok || *s_abort != 0u)) break;  // one verdict for the warp
+      const bool read = c < 2 ||
+                        mbar_wait_sleep(&bars->aread[c & 1], uint32_t(((c - 2) >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+      if (__any_sync(0xffffffffu, !read)) {
+        if (lane == 0) *s_abort = 1u;
+        break;
+      }
+      tc_fence_after();
+      if (lane == 0) issue_gram(c);
+      issued = true;
+    }
+    if (issued && *s_abort != 0u) {
+      if (lane == 0) umma_commit(&bars->drain2);
+      __syncwarp();
+      mbar_wait_sleep(&bars->drain2, 0u, err_word, DEVERR_MMA_TIMEOUT);
     }
   } else if (inv_pair) {
     // ---------------------------------------------------------------- inverse pair
@@ -1135,11 +1205,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!sync_on(H_PREP)) goto issuer_abort;
         if (leader) {
           if (c + 1 < n_chunks) issue_qkg(c + 1);
-          issue_gram(c);
+          if (!kDedInv) issue_gram(c);
         }
         if (c + 1 < n_chunks) qkg_last = c + 1;
       }
-      if (!sync_on(H_INV) || !pair_done(0)) goto issuer_abort;
+      if ((!kDedInv && !sync_on(H_INV)) || !pair_done(0)) goto issuer_abort;
       if (leader) issue_wu(0);
       if (n_chunks > 2) {  // v stage 0 is free once W^T / U~^T of chunk 0 are done
         mbar_wait_sleep(&bars->wu, 0u, err_word, DEVERR_MMA_TIMEOUT);
@@ -1160,15 +1230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         umma_commit(&bars->mma1);
       }
-      if (j + 2 < n_chunks) {
-        if (!sync_on(H_PREP)) goto issuer_abort;
-        if (leader) {
-          if (j + 3 < n_chunks) issue_qkg(j + 3);
-          issue_gate(j);
-        }
-        if (j + 3 < n_chunks) qkg_last = j + 3;
-        if (kNormGate) gate_last = j;
-      }
+      // the operands of chunk j + 2 (H_PREP) come just before U^T of chunk j (H_U): MMA2 first,
+      // which the chain and the read-out wait for, then the next chunk's loads and the Gram of
+      // chunk j + 2, which queues behind MMA2 and is needed only one iteration later
+      if (j + 2 < n_chunks && !sync_on(H_PREP)) goto issuer_abort;
       if (!sync_on(H_U)) goto issuer_abort;
       if (leader) {  // MMA2: [O^T | S^T] += U^T [P ; K^^T]^T
         const uint64_t ut = kdesc64(sbase + OFF_UT), pk = kdesc64(sbase + OFF_PK + (j % 3) * kPKBytes);
@@ -1176,16 +1241,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int ks = 0; ks < 2; ++ks)
           umma_f16(tmem + tm_grp(b) + TM_O, dadv(ut, ks * 32), dadv(pk, ks * 32), IDESC_OS, 1);
         umma_commit(&bars->mma2);
-        // the Gram of chunk j + 2 (its operands came at H_PREP) queues behind MMA2, which the
-        // chain waits for first; the Gram is needed only one iteration later
-        if (j + 2 < n_chunks) issue_gram(j + 2);
+      }
+      if (j + 2 < n_chunks) {
+        if (leader) {
+          if (j + 3 < n_chunks) issue_qkg(j + 3);
+          issue_gate(j);
+          if (!kDedInv) issue_gram(j + 2);
+        }
+        if (j + 3 < n_chunks) qkg_last = j + 3;
+        if (kNormGate) gate_last = j;
       }
       if (kNormGate && j + 2 >= n_chunks) {  // no operand hand-off left to piggyback on
         if (leader) issue_gate(j);
         gate_last = j;
       }
       if (more) {
-        if (!sync_on(H_INV) || !pair_done(j + 1)) goto issuer_abort;
+        if ((!kDedInv && !sync_on(H_INV)) || !pair_done(j + 1)) goto issuer_abort;
         if (leader) issue_wu(j + 1);
         if (j + 3 < n_chunks) {  // v stage (j + 1) % 2 is free once W^T / U~^T of chunk j + 1 are done
           mbar_wait_sleep(&bars->wu, uint32_t((j + 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
