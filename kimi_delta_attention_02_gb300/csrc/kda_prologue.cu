@@ -7,8 +7,9 @@
 //                                                start x comes from its convolution state)
 //     u_t = conv_t Sigmoid(conv_t);   q_t, k_t = u_t / sqrt(sum_c u_tc^2 + eps);   v_t = u_t.
 //
-// The pass is bound by HBM bandwidth: it reads each raw input once and writes each result
-// once. One CTA of 12 warps takes a tile of 32 tokens of one head. The tile's raw rows (and
+// The pass reads each raw input once and writes each result once. In the general kernel one
+// CTA of 12 warps takes a tile of 32 tokens of one head (the persistent TMA kernel below walks
+// a head's tiles instead). The tile's raw rows (and
 // the 3 rows before it) are first copied to shared memory with coalesced loads. Then each
 // warp takes one projection and 8 tokens; a lane owns 4 adjacent channels of a token row, so
 // the 4 taps are 4 short shared-memory reads, the L2 norm of a token is one warp reduction,
@@ -249,20 +250,24 @@ __global__ void __launch_bounds__(kProThreads, 2)
 }
 
 // Persistent variant for d_k, d_v multiples of 8 (whole 16-byte rows): a CTA keeps one head
-// (its weights stay in registers) and walks that head's 32-token tiles with a TMA pipeline of
-// kProStages tiles (the next tiles' 35 rows of q, k and v land while the current one is
-// computed; rows before token 0 and past the end read as zero). Warp w takes projection w / 4
-// and tokens 8 (w % 4) .. + 7, a lane 4 adjacent channels of a row, so a token's L2 norm is one
-// warp reduction, the 4 taps come from a sliding window of shared-memory rows, and each lane
-// stores 8 or 16 bytes; the arithmetic runs on fp32 pairs.
+// (its weights stay in registers) and walks that head's 32-token tiles through a TMA pipeline of
+// kProStages tiles. Warp 12 only loads: it issues tile k + S into a stage once the 12 compute
+// warps have released it (an mbarrier per stage, one arrival per warp), so that no compute warp
+// waits on another: warp w (< 12) waits for the stage to land, finds its own tokens' sequences,
+// computes and releases the stage. Warp w takes projection w / 4 and tokens 8 (w % 4) .. + 7, a
+// lane 4 adjacent channels of a row, so a token's L2 norm is one warp reduction, the 4 taps come
+// from a sliding window of shared-memory rows, and each lane stores 8 or 16 bytes; the arithmetic
+// runs on fp32 pairs. Rows before token 0 and past the end read as zero.
 constexpr int kProRows = kProTile + 3;
+constexpr int kProWarps = kProThreads / 32;         // compute warps
+constexpr int kProTmaThreads = kProThreads + 32;    // + the loading warp
 template <bool kBF16>
-constexpr int kProStages = 2;  // 2 x 26,880 (bf16) or 2 x 53,760 (fp32) bytes of tiles per CTA
+constexpr int kProStages = kBF16 ? 3 : 2;  // 3 x 26,880 (bf16) or 2 x 53,760 (fp32) bytes of tiles per CTA
 
 __host__ __device__ constexpr uint32_t round128(uint32_t x) { return (x + 127u) & ~127u; }
 
 template <bool kBF16>
-__global__ void __launch_bounds__(kProThreads, 2)
+__global__ void __launch_bounds__(kProTmaThreads, 2)
     kda_prologue_tma_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                             const __grid_constant__ CUtensorMap tm_v, const float *__restrict__ conv_w,
                             const int32_t *__restrict__ cu_seqlens, int num_seqs,
@@ -272,10 +277,8 @@ __global__ void __launch_bounds__(kProThreads, 2)
   using Elem = typename std::conditional<kBF16, uint16_t, float>::type;
   constexpr uint32_t es = sizeof(Elem);
   extern __shared__ __align__(128) uint8_t pro_smem[];
-  __shared__ int32_t s_seq[kProTile];
-  __shared__ int64_t s_bos[kProTile];
   constexpr int S = kProStages<kBF16>;
-  __shared__ __align__(8) uint64_t s_bar[S];
+  __shared__ __align__(8) uint64_t s_full[S], s_empty[S];
   __shared__ uint32_t s_bad;
   constexpr int kCuSmem = 1024;  // sequence offsets kept in shared memory when they fit
   __shared__ int32_t s_cu[kCuSmem];
@@ -285,38 +288,50 @@ __global__ void __launch_bounds__(kProThreads, 2)
   const uint32_t off_k = round128(kProRows * d_k * es), off_v = 2 * off_k;
   const uint32_t stage_bytes = off_v + round128(kProRows * d_v * es);
   const uint32_t tx_bytes = kProRows * uint32_t(C3) * es;
-  // this CTA: head h_cta, tiles tile0, tile0 + m, ... (gridDim.x = m H)
+  // this CTA: head h, tiles tile0, tile0 + m, ... (gridDim.x = m H)
   const int m = int(gridDim.x) / H, h = int(blockIdx.x) % H, tile0 = int(blockIdx.x) / H;
   const bool cu_in_smem = num_seqs + 1 <= kCuSmem;
   if (cu_in_smem)
-    for (int i = tid; i <= num_seqs; i += kProThreads) s_cu[i] = cu_seqlens[i];
+    for (int i = tid; i <= num_seqs; i += kProTmaThreads) s_cu[i] = cu_seqlens[i];
   const int32_t *cu = cu_in_smem ? s_cu : cu_seqlens;
 
   if (tid == 0) {
-    for (int i = 0; i < S; ++i) mbar_init(&s_bar[i], 1);
+    for (int i = 0; i < S; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], kProWarps);
+    }
     fence_mbarrier_init();
     s_bad = 0u;
   }
-  __syncthreads();
-  auto issue = [&](int tile, int s) {  // one thread
-    const int32_t y0 = tile * kProTile - 3;
-    uint8_t *st = pro_smem + s * stage_bytes;
-    mbar_arrive_expect_tx(&s_bar[s], tx_bytes);
-    tma_load_3d(st, &tm_q, &s_bar[s], 0, h, y0);
-    tma_load_3d(st + off_k, &tm_k, &s_bar[s], 0, h, y0);
-    tma_load_3d(st + off_v, &tm_v, &s_bar[s], 0, h, y0);
-  };
-  int pending[S];  // thread 0: iteration whose load into a stage is not yet awaited
-  for (int i = 0; i < S; ++i) pending[i] = -1;
-  if (tid == 0) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    for (int i = 0; i < S; ++i)
-      if (tile0 + i * m < n_tiles) {
-        issue(tile0 + i * m, i);
-        pending[i] = i;
+  __syncthreads();  // barriers and sequence offsets ready; from here no CTA-wide barrier
+
+  if (warp == kProWarps) {
+    // ------------------------------------------------------------ loading warp (lane 0)
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      int k = 0;
+      for (int tile = tile0; tile < n_tiles; tile += m, ++k) {
+        const int s = k % S;
+        // the compute warps have released this stage (its previous tile, k - S)
+        if (k >= S && !mbar_wait_sleep(&s_empty[s], uint32_t(((k - S) / S) & 1), err_word, DEVERR_TMA_TIMEOUT)) {
+          s_bad = 1u;
+          break;
+        }
+        const int32_t y0 = tile * kProTile - 3;
+        uint8_t *st = pro_smem + s * stage_bytes;
+        mbar_arrive_expect_tx(&s_full[s], tx_bytes);
+        tma_load_3d(st, &tm_q, &s_full[s], 0, h, y0);
+        tma_load_3d(st + off_k, &tm_k, &s_full[s], 0, h, y0);
+        tma_load_3d(st + off_v, &tm_v, &s_full[s], 0, h, y0);
       }
+      // wait for the loads issued last (bounded) before this CTA's shared memory goes away
+      const int issued = k;
+      for (int kk = issued - S > 0 ? issued - S : 0; kk < issued; ++kk)
+        mbar_wait_sleep(&s_full[kk % S], uint32_t((kk / S) & 1), err_word, DEVERR_TMA_TIMEOUT);
+    }
+    return;
   }
 
   const int p = warp >> 2;
@@ -339,26 +354,33 @@ __global__ void __launch_bounds__(kProThreads, 2)
     wp[i][2] = make_float2(a.z, b.z);
     wp[i][3] = make_float2(a.w, b.w);
   }
-  __syncthreads();  // s_cu
+  // the last n with cu[n] <= t
+  auto seq_of = [&](int64_t t) {
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (cu[mid] <= t) lo = mid;
+      else hi = mid - 1;
+    }
+    return lo;
+  };
   int k = 0;
   for (int tile = tile0; tile < n_tiles; tile += m, ++k) {
     const int s = k % S;
     const int64_t t0 = int64_t(tile) * kProTile;
-    if (tid < kProTile) {  // sequence of each token: the last n with cu[n] <= t
-      const int64_t t = t0 + tid;
-      int lo = 0, hi = num_seqs - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (cu[mid] <= t) lo = mid;
-        else hi = mid - 1;
-      }
-      s_seq[tid] = lo;
-      s_bos[tid] = cu[lo];
+    // the sequences of this warp's tokens (lanes 0..7), and whether the whole tile with the 3 rows
+    // before it lies in one sequence (lanes 8 and 9 find the first and last token's)
+    int my_seq = 0;
+    int64_t my_bos = 0;
+    if (lane < 8 || lane == 8 || lane == 9) {
+      const int64_t t = lane < 8 ? t0 + tb + lane : lane == 8 ? t0 : t0 + kProTile - 1;
+      my_seq = seq_of(t < T ? t : T - 1);
+      my_bos = cu[my_seq];
     }
-    if (!mbar_wait_sleep(&s_bar[s], uint32_t((k / S) & 1), err_word, DEVERR_TMA_TIMEOUT)) s_bad = 1u;
-    __syncthreads();  // s_seq / s_bos written; stage s landed for everyone
-    if (s_bad != 0u) break;  // a load did not arrive: stop (thread 0 waits for the rest below)
-    if (tid == 0) pending[s] = -1;
+    const int seq_first = __shfl_sync(0xffffffffu, my_seq, 8), seq_last = __shfl_sync(0xffffffffu, my_seq, 9);
+    const int64_t bos_first = __shfl_sync(0xffffffffu, my_bos, 8);
+    const bool one_seq = t0 + kProTile <= T && seq_first == seq_last && t0 - 3 >= bos_first;
+    if (!mbar_wait_sleep(&s_full[s], uint32_t((k / S) & 1), err_word, DEVERR_TMA_TIMEOUT) || s_bad != 0u) break;
     const Elem *rows = reinterpret_cast<const Elem *>(pro_smem + s * stage_bytes + roff);  // [35][d]
     auto row4 = [&](int r, float2 (&x)[2]) {  // this lane's 4 channels of row r, as pairs
       if constexpr (kBF16) {
@@ -403,37 +425,91 @@ __global__ void __launch_bounds__(kProThreads, 2)
       }
     };
 
-    // every row of the tile and the 3 before it in one sequence: a sliding window
-    const bool one_seq = s_seq[0] == s_seq[kProTile - 1] && t0 - 3 >= s_bos[0];
-    if (one_seq) {
-      float2 win[4][2] = {};  // [row][channel pair]
-      if (on) {
-        row4(tb, win[1]);
-        row4(tb + 1, win[2]);
-        row4(tb + 2, win[3]);
-      }
+    // two consecutive tokens tok, tok + 1: Swish, the L2 norms of q / k in one halving reduction
+    // (lanes 0..15 end with token tok's sum of squares, lanes 16..31 with token tok + 1's), store
+    auto finish2 = [&](int64_t tok, float2 (&u)[2][2]) {
 #pragma unroll
-      for (int tt = 0; tt < 8; ++tt) {
+      for (int a = 0; a < 2; ++a)
 #pragma unroll
-        for (int j = 0; j < 3; ++j) {
-          win[j][0] = win[j + 1][0];
-          win[j][1] = win[j + 1][1];
+        for (int i = 0; i < 2; ++i) {  // Swish(x) = x / (1 + 2^{-x log2 e})
+          const float2 e = f2_mul(u[a][i], make_float2(-1.4426950408889634f, -1.4426950408889634f));
+          float2 den;
+          asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(den.x) : "f"(e.x));
+          asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(den.y) : "f"(e.y));
+          den = f2_add(den, make_float2(1.f, 1.f));
+          float2 r;
+          asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.x) : "f"(den.x));
+          asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r.y) : "f"(den.y));
+          u[a][i] = f2_mul(u[a][i], r);
         }
-        if (on) row4(tb + tt + 3, win[3]);
-        float2 u[2];
+      if (p < 2) {
+        float ss[2];
+#pragma unroll
+        for (int a = 0; a < 2; ++a) {
+          const float2 s2 = f2_fma(u[a][1], u[a][1], f2_mul(u[a][0], u[a][0]));
+          ss[a] = s2.x + s2.y;
+        }
+        const float tot = lane_sums<2>(ss, lane);  // token tok + (lane >> 4)
+        const float rn_l = rsqrtf(tot + eps);
+        const float rn0 = __shfl_sync(0xffffffffu, rn_l, 0), rn1 = __shfl_sync(0xffffffffu, rn_l, 16);
 #pragma unroll
         for (int i = 0; i < 2; ++i) {
-          u[i] = f2_mul(wp[i][0], win[0][i]);
-          u[i] = f2_fma(wp[i][1], win[1][i], u[i]);
-          u[i] = f2_fma(wp[i][2], win[2][i], u[i]);
-          u[i] = f2_fma(wp[i][3], win[3][i], u[i]);
+          u[0][i] = f2_mul(u[0][i], make_float2(rn0, rn0));
+          u[1][i] = f2_mul(u[1][i], make_float2(rn1, rn1));
         }
-        finish(t0 + tb + tt, u);
+      }
+#pragma unroll
+      for (int a = 0; a < 2; ++a) {
+        if (on && tok + a < T) {
+          const int64_t o = ((tok + a) * H + h) * d + c0;
+          if constexpr (kBF16)
+            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(x_out) + o) =
+                make_uint2(pack_bf16x2(u[a][0].x, u[a][0].y), pack_bf16x2(u[a][1].x, u[a][1].y));
+          else
+            *reinterpret_cast<float4 *>(static_cast<float *>(x_out) + o) =
+                make_float4(u[a][0].x, u[a][0].y, u[a][1].x, u[a][1].y);
+        }
+      }
+    };
+
+    if (one_seq) {  // every row of the tile and the 3 before it in one sequence: a sliding window
+      // two tokens per step (rows tb + tt .. tb + tt + 4): two independent chains, and one
+      // reduction for both tokens' L2 norms
+      float2 win[5][2] = {};  // [row][channel pair]
+      if (on) {
+        row4(tb, win[2]);
+        row4(tb + 1, win[3]);
+        row4(tb + 2, win[4]);
+      }
+#pragma unroll
+      for (int tt = 0; tt < 8; tt += 2) {
+#pragma unroll
+        for (int j = 0; j < 3; ++j) {
+          win[j][0] = win[j + 2][0];
+          win[j][1] = win[j + 2][1];
+        }
+        if (on) {
+          row4(tb + tt + 3, win[3]);
+          row4(tb + tt + 4, win[4]);
+        }
+        float2 u[2][2];  // [token][channel pair]
+#pragma unroll
+        for (int a = 0; a < 2; ++a)
+#pragma unroll
+          for (int i = 0; i < 2; ++i) {
+            u[a][i] = f2_mul(wp[i][0], win[a][i]);
+            u[a][i] = f2_fma(wp[i][1], win[a + 1][i], u[a][i]);
+            u[a][i] = f2_fma(wp[i][2], win[a + 2][i], u[a][i]);
+            u[a][i] = f2_fma(wp[i][3], win[a + 3][i], u[a][i]);
+          }
+        finish2(t0 + tb + tt, u);
       }
     } else {  // per token and tap: before its sequence start a token reads the state (or zero)
       for (int tt = 0; tt < 8; ++tt) {
         const int t = tb + tt;
-        const int64_t tok = t0 + t, bos = s_bos[t];
+        const int64_t tok = t0 + t;
+        const int seq = __shfl_sync(0xffffffffu, my_seq, tt);
+        const int64_t bos = __shfl_sync(0xffffffffu, my_bos, tt);
         float2 up[2] = {};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -443,7 +519,7 @@ __global__ void __launch_bounds__(kProThreads, 2)
             if (pos >= bos) {
               row4(t + j, x);
             } else if (conv_init != nullptr) {
-              const int64_t sb = ((int64_t(s_seq[t]) * H + h) * 3 + (3 + pos - bos)) * C3 + pbase + c0;
+              const int64_t sb = ((int64_t(seq) * H + h) * 3 + (3 + pos - bos)) * C3 + pbase + c0;
               x[0] = make_float2(load_elem<kBF16>(conv_init, sb), load_elem<kBF16>(conv_init, sb + 1));
               x[1] = make_float2(load_elem<kBF16>(conv_init, sb + 2), load_elem<kBF16>(conv_init, sb + 3));
             }
@@ -454,15 +530,8 @@ __global__ void __launch_bounds__(kProThreads, 2)
         finish(tok, up);
       }
     }
-    __syncthreads();  // stage s read by everyone
-    if (tid == 0 && tile + S * m < n_tiles) {
-      issue(tile + S * m, s);
-      pending[s] = k + S;
-    }
-  }
-  if (tid == 0) {  // loads this CTA issued and did not consume (after a wait that gave up)
-    for (int s2 = 0; s2 < S; ++s2)
-      if (pending[s2] >= 0) mbar_wait_sleep(&s_bar[s2], uint32_t((pending[s2] / S) & 1), err_word, DEVERR_TMA_TIMEOUT);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&s_empty[s]);  // this warp is done with the stage
   }
 }
 
@@ -482,7 +551,7 @@ cudaError_t launch_prologue(const void *q_raw, const void *k_raw, const void *v_
       return cudaErrorInvalidValue;
     auto kern = bf16 ? kda_prologue_tma_kernel<true> : kda_prologue_tma_kernel<false>;
     const uint32_t stage = 2 * round128(kProRows * d_k * es) + round128(kProRows * d_v * es);
-    const size_t smem = size_t(bf16 ? kProStages<true> : kProStages<false>) * stage;  // <= 107,520 bytes
+    const size_t smem = size_t(bf16 ? kProStages<true> : kProStages<false>) * stage;  // <= 107,520 bytes (80,640 bf16)
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, int(smem)) != cudaSuccess)
       return cudaGetLastError();
     int dev = 0, sms = 0;
@@ -492,8 +561,8 @@ cudaError_t launch_prologue(const void *q_raw, const void *k_raw, const void *v_
     // m CTAs per head, m H about two per SM (at least one per head)
     const int m = (2 * sms) / H > 1 ? (2 * sms) / H : 1;
     const unsigned grid = unsigned(m * H);
-    kern<<<grid, kProThreads, smem, stream>>>(mq, mk, mv, conv_w, cu_seqlens, num_seqs, conv_init, q, k, v,
-                                              total_tokens, H, d_k, d_v, n_tiles, eps, device_error_word());
+    kern<<<grid, kProTmaThreads, smem, stream>>>(mq, mk, mv, conv_w, cu_seqlens, num_seqs, conv_init, q, k, v,
+                                                 total_tokens, H, d_k, d_v, n_tiles, eps, device_error_word());
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
   }
