@@ -659,7 +659,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float x[N];
     if constexpr (N == 8) tmem_ld8(ocols + t0, x);
     else tmem_ld16(ocols + t0, x);
-    tmem_ld_wait();
+    tmem_ld_wait(x);
 #pragma unroll
     for (int e = 0; e < N; ++e) x[e] = (scale * x[e]) * (scale * x[e]);
     const float part = lane_sums<N>(x, lane);
@@ -671,7 +671,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float rstd_l = rsqrtf(((p.x + p.y) + (p.z + p.w)) * (1.f / kD) + og.eps);  // token t0 + (lane & (N-1))
     if constexpr (N == 8) tmem_ld8(ocols + t0, x);
     else tmem_ld16(ocols + t0, x);
-    tmem_ld_wait();
+    tmem_ld_wait(x);
 #pragma unroll
     for (int e = 0; e < N; ++e) x[e] = scale * x[e] * __shfl_sync(0xffffffffu, rstd_l, e) * gw[e];
     write_rows(x, t0, j, L);
@@ -689,7 +689,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (kDedInv || quarter < 2) {
       float x[8];
       tmem_ld8(ocols + 8 * grp, x);  // O^T row v, tokens 8 grp ..
-      tmem_ld_wait();
+      tmem_ld_wait(x);
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] *= scale;
       write_rows(x, 8 * grp, j, L);
@@ -697,7 +697,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int t0 = 16 * (grp - 2);
       float x[16];
       tmem_ld16(ocols + t0, x);  // O^T row v, tokens t0 ..
-      tmem_ld_wait();
+      tmem_ld_wait(x);
 #pragma unroll
       for (int e = 0; e < 16; ++e) x[e] *= scale;
       write_rows(x, t0, j, L);
@@ -771,15 +771,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   // P rows t = 16 quarter + lane (lanes 0..15) of chunk c, columns 8 grp .. + 7 (compute warps of
   // TMEM quarters 0 and 1), into the [P ; K^^T] tile of chunk c. Waits for the tensor-memory loads
   // issued before it as well.
-  auto extract_p = [&](int c) {
+  auto extract_p = [&](int c, auto &...also) {  // also: arrays loaded before it, completed by its wait
     const int b = c & 1, L = chunk_len(c);
     bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
     const int t = 16 * quarter + (lane & 15);
     const bool have = grp < 2 * (quarter + 1);  // columns up to the row block's end
-    float vals[8];
+    float vals[8] = {};
     if (have) tmem_ld8(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
-    tmem_ld_wait();
+    tmem_ld_wait(vals, also...);
     if (lane < 16) {
       const int lim = (have && t < L) ? t + 1 - 8 * grp : 0;  // keep i <= t
 #pragma unroll
@@ -805,10 +805,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (grp <= s) {  // columns past the row block are all zero and never read
           float vals[16];
           tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * grp, vals);
-          tmem_ld_wait();
+          tmem_ld_wait(vals);
           if (lane < 16) {
             const float bt = s_beta[b * kC + t];
-            const int lim = t < L ? t - 16 * grp : 0;  // keep i < t
+            const int lim = t < L ? t - 16 * opaque_int(grp) : 0;  // keep i < t (opaque: as for P below)
             if (slow && grp == s) {
               const float *cr = corr + pair_row_a(uint32_t(s), uint32_t(t & 15));
 #pragma unroll
@@ -905,10 +905,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         float vals[8];
         if (have) {
           tmem_ld8(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
-          tmem_ld_wait();
+          tmem_ld_wait(vals);
         }
         if (lane < 16) {
-          const int lim = (have && t < L) ? t + 1 - 8 * grp : 0;  // keep i <= t
+          // keep i <= t. In the unbounded map the column group goes in opaque: with it visible,
+          // nvcc 13.0 took this limit to be at least 2 there and dropped the mask on the entries
+          // above the diagonal. (The bounded maps compile right, and would spill with it.)
+          const int lim = (have && t < L) ? t + 1 - 8 * (kUnb ? opaque_int(grp) : grp) : 0;
           if (slow && have && grp >= 2 * quarter) {  // columns inside the diagonal block
             const float *cr = corr + pair_row_p(uint32_t(quarter), uint32_t(t & 15)) + 8 * (grp - 2 * quarter);
 #pragma unroll
@@ -962,7 +965,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int h2 = 0; h2 <= s; ++h2) {
       float vals[16];
       tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * h2, vals);
-      tmem_ld_wait();
+      tmem_ld_wait(vals);
       if (lane < 16) {
         const int t = 16 * s + lane;
         const float bt = s_beta[b * kC + t];
@@ -1052,7 +1055,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     float x[8];
     tmem_ld8(tmem + lane_base + TM_W + 8 * grp, x);  // W^T row c = v_own, columns t = 8 grp ..
-    tmem_ld_wait();
+    tmem_ld_wait(x);
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = -x[e];
     const uint32_t cr = uint32_t(v_own);
@@ -1084,7 +1087,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 2; ++u) {
         float x[16];
         tmem_ld16(s_cols(b ^ 1) + 16 * u, x);
-        tmem_ld_wait();
+        if constexpr (kMerged) tmem_ld_wait(x, ox);  // and the merged read-out's row
+        else tmem_ld_wait(x);
         const uint32_t col = uint32_t(32 * grp + 16 * u);  // state column c of x[0]
         st_at(sm + OFF_ST, sw128_chunk(v_own, (col & 63u) >> 3, col >> 6, 128), pack8_f16(x));
         st_at(sm + OFF_ST, sw128_chunk(v_own, ((col & 63u) >> 3) + 1, col >> 6, 128), pack8_f16(x + 8));
@@ -1116,8 +1120,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       {
         float x[8];
         tmem_ld8(tmem + lane_base + tm_grp(b) + 8 * grp, x);  // U^T row v, columns t = 8 grp ..
-        if (kMerged && more && quarter < 2) extract_p(j + 1);  // waits for its loads with U^T's
-        else tmem_ld_wait();
+        if (kMerged && more && quarter < 2) extract_p(j + 1, x);  // waits for U^T's load with its own
+        else tmem_ld_wait(x);
         st_at(sm + OFF_UT, sw64_chunk(uint32_t(v_own), uint32_t(grp)), pack8_f16(x));
       }
       handoff(H_U);
@@ -1139,7 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int u = 0; u < 2; ++u) {
         float x[16];
         tmem_ld16(s_cols((n_chunks + 1) & 1) + 16 * u, x);
-        tmem_ld_wait();
+        tmem_ld_wait(x);
 #pragma unroll
         for (int e = 0; e < 16; ++e) final_state[st_base + int64_t(32 * grp + 16 * u + e) * kD + v_own] = x[e];
       }
