@@ -43,29 +43,35 @@
 // (e = 2^-11), which needs no more shared memory than bf16. Accumulation is
 // fp32 throughout and the state is kept in fp32 (tensor memory).
 //
-// Layout of the work. One CTA per (sequence, head) chain: 16 compute warps and one
-// issuing warp (one thread of it issues every TMA load and tensor-core MMA, so the
-// ~90 cycles each MMA issue takes never holds up the compute warps). The fp32
-// state S^T (rows v = value channels, columns c = key channels) stays in tensor
-// memory for the whole sequence, in two copies used alternately. Each iteration
-// j runs the state chain of chunk j interleaved with the state-independent work
-// of chunks j+1 and j+2, so that each tensor-core group runs while the threads
-// work on the other streams:
-//   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy
+// Layout of the work. One CTA per (sequence, head) chain of 20 warps: 16 compute warps, one
+// issuing warp (one thread of it issues every TMA load and the chain's tensor-core MMAs, so the
+// ~50-120 cycles each MMA issue takes never holds up the compute warps) and, for the bounded
+// maps, a Gram warp that issues the Gram MMAs and an inverse pair (warps 18, 19) that inverts
+// I + A one chunk ahead of the chain. The fp32 state S^T (rows v = value channels, columns c =
+// key channels) stays in tensor memory for the whole sequence, in two copies used alternately.
+// Each iteration j runs the state chain of chunk j interleaved with the state-independent work
+// of chunks j+1 and j+2, so that each tensor-core group runs while the threads work on the
+// other streams:
+//   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy (bounded maps
+//                 without the output gate: O^T of chunk j - 1 leaves for global memory here)
 //   P6  chain j : -W^T of chunk j into the [-W^T | Q~^T] tile (its MMA ran during
 //                 P1); MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]           (N = 64)
 //   P2  next j+2: decay prefix sums and the operand tiles (a thread owns one key
-//                 channel and 8 tokens)
-//   P3  chain j : U^T to fp16; MMA2: [O^T | S^T] += U^T [P ; K^^T]^T   (N = 160),
-//                 then the Gram of chunk j+2 (kind::tf32, M = 64 rows [Q f ; K f] x
-//                 N = 32 keys K g), queued behind MMA2, which the chain needs first
-//   P4  next j+1: warps 2, 3, 6, 7 (whose TMEM lanes hold the key rows of the Gram) take
-//                 A out of TMEM, invert I + A (8 x 8 and 16 x 16 blocks) and form T',
-//                 while the other 12 warps convert v to fp16, take P out of TMEM and
-//                 write O^T of chunk j (P5) to global memory, optionally through the
-//                 output gate of section 1.3 (RMSNorm over the 128 value channels and
-//                 the Sigmoid of the gate logits, whose tile TMA brings into the S^T
-//                 tile once MMA1 has read it);
+//                 channel and 8 tokens); the Gram of chunk j+2 (kind::tf32, M = 64 rows
+//                 [Q f ; K f] x N = 32 keys K g) follows, queued behind MMA2
+//   P3  chain j : U^T to fp16 (bounded maps without the output gate: P of chunk j + 1 leaves
+//                 tensor memory in the same round trip); MMA2: [O^T | S^T] += U^T [P ; K^^T]^T
+//                 (N = 160)
+//   P4  next j+1: the inverse side. Bounded maps: the inverse pair takes A of chunk j + 1 out of
+//                 its TMEM lanes, forms T' = (I + A)^{-1} Diag(b) by back substitution (one
+//                 row per lane) and converts v to fp16 while the compute warps run P1..P3; the
+//                 pair hands T' over on an mbarrier, which alone gates W^T / U~^T. Unbounded map:
+//                 warps 2, 3, 6, 7 (whose TMEM lanes hold the key rows of the Gram) invert
+//                 I + A in 8 x 8 and 16 x 16 blocks while the other 12 warps convert v, take P
+//                 out of TMEM and write O^T of chunk j. With the output gate of section 1.3
+//                 (RMSNorm over the 128 value channels and the Sigmoid of the gate logits,
+//                 whose tile TMA brings into the S^T tile once MMA1 has read it) O^T of chunk
+//                 j leaves here too;
 //                 W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
 // Per-chunk operand tiles are double-buffered by chunk parity ([P ; K^^T] three
 // times, since it lives from P2 of chunk j to MMA2 of chunk j + 2), and so are the
@@ -657,9 +663,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
     float x[N];
-    if constexpr (N == 8) tmem_ld8(ocols + t0, x);
-    else tmem_ld16(ocols + t0, x);
-    tmem_ld_wait(x);
+    if constexpr (N == 8) tmem_ld8_wait(ocols + t0, x);
+    else tmem_ld16_wait(ocols + t0, x);
 #pragma unroll
     for (int e = 0; e < N; ++e) x[e] = (scale * x[e]) * (scale * x[e]);
     const float part = lane_sums<N>(x, lane);
@@ -669,9 +674,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     named_bar_sync(BAR_OUT, kOutThreads);
     const float4 p = s_ss[t0 + (lane & (N - 1))];
     const float rstd_l = rsqrtf(((p.x + p.y) + (p.z + p.w)) * (1.f / kD) + og.eps);  // token t0 + (lane & (N-1))
-    if constexpr (N == 8) tmem_ld8(ocols + t0, x);
-    else tmem_ld16(ocols + t0, x);
-    tmem_ld_wait(x);
+    if constexpr (N == 8) tmem_ld8_wait(ocols + t0, x);
+    else tmem_ld16_wait(ocols + t0, x);
 #pragma unroll
     for (int e = 0; e < N; ++e) x[e] = scale * x[e] * __shfl_sync(0xffffffffu, rstd_l, e) * gw[e];
     write_rows(x, t0, j, L);
@@ -688,16 +692,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       else out_gated_rows(std::integral_constant<int, 16>{}, 16 * (grp - 2), j, L, ocols);
     } else if (kDedInv || quarter < 2) {
       float x[8];
-      tmem_ld8(ocols + 8 * grp, x);  // O^T row v, tokens 8 grp ..
-      tmem_ld_wait(x);
+      tmem_ld8_wait(ocols + 8 * grp, x);  // O^T row v, tokens 8 grp ..
 #pragma unroll
       for (int e = 0; e < 8; ++e) x[e] *= scale;
       write_rows(x, 8 * grp, j, L);
     } else {
       const int t0 = 16 * (grp - 2);
       float x[16];
-      tmem_ld16(ocols + t0, x);  // O^T row v, tokens t0 ..
-      tmem_ld_wait(x);
+      tmem_ld16_wait(ocols + t0, x);  // O^T row v, tokens t0 ..
 #pragma unroll
       for (int e = 0; e < 16; ++e) x[e] *= scale;
       write_rows(x, t0, j, L);
@@ -804,8 +806,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int s = quarter - 2, t = 16 * s + (lane & 15);
         if (grp <= s) {  // columns past the row block are all zero and never read
           float vals[16];
-          tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * grp, vals);
-          tmem_ld_wait(vals);
+          tmem_ld16_wait(tmem + lane_base + tm_gram(c) + 16 * grp, vals);
           if (lane < 16) {
             const float bt = s_beta[b * kC + t];
             const int lim = t < L ? t - 16 * opaque_int(grp) : 0;  // keep i < t (opaque: as for P below)
@@ -904,8 +905,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool have = grp < 2 * (quarter + 1);  // columns up to the row block's end
         float vals[8];
         if (have) {
-          tmem_ld8(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
-          tmem_ld_wait(vals);
+          tmem_ld8_wait(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
         }
         if (lane < 16) {
           // keep i <= t. In the unbounded map the column group goes in opaque: with it visible,
@@ -964,8 +964,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // A[t][i] = beta_t G[t][i] for i < t (and t inside the sequence), else 0
     for (int h2 = 0; h2 <= s; ++h2) {
       float vals[16];
-      tmem_ld16(tmem + lane_base + tm_gram(c) + 16 * h2, vals);
-      tmem_ld_wait(vals);
+      tmem_ld16_wait(tmem + lane_base + tm_gram(c) + 16 * h2, vals);
       if (lane < 16) {
         const int t = 16 * s + lane;
         const float bt = s_beta[b * kC + t];
@@ -1054,8 +1053,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bad |= !mbar_wait_sleep(&bars->wu, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
     float x[8];
-    tmem_ld8(tmem + lane_base + TM_W + 8 * grp, x);  // W^T row c = v_own, columns t = 8 grp ..
-    tmem_ld_wait(x);
+    tmem_ld8_wait(tmem + lane_base + TM_W + 8 * grp, x);  // W^T row c = v_own, columns t = 8 grp ..
 #pragma unroll
     for (int e = 0; e < 8; ++e) x[e] = -x[e];
     const uint32_t cr = uint32_t(v_own);
@@ -1086,9 +1084,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         float x[16];
-        tmem_ld16(s_cols(b ^ 1) + 16 * u, x);
-        if constexpr (kMerged) tmem_ld_wait(x, ox);  // and the merged read-out's row
-        else tmem_ld_wait(x);
+        if constexpr (kMerged) {
+          tmem_ld16(s_cols(b ^ 1) + 16 * u, x);
+          tmem_ld_wait(x, ox);  // and the merged read-out's row
+        } else {
+          tmem_ld16_wait(s_cols(b ^ 1) + 16 * u, x);
+        }
         const uint32_t col = uint32_t(32 * grp + 16 * u);  // state column c of x[0]
         st_at(sm + OFF_ST, sw128_chunk(v_own, (col & 63u) >> 3, col >> 6, 128), pack8_f16(x));
         st_at(sm + OFF_ST, sw128_chunk(v_own, ((col & 63u) >> 3) + 1, col >> 6, 128), pack8_f16(x + 8));
@@ -1142,8 +1143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int u = 0; u < 2; ++u) {
         float x[16];
-        tmem_ld16(s_cols((n_chunks + 1) & 1) + 16 * u, x);
-        tmem_ld_wait(x);
+        tmem_ld16_wait(s_cols((n_chunks + 1) & 1) + 16 * u, x);
 #pragma unroll
         for (int e = 0; e < 16; ++e) final_state[st_base + int64_t(32 * grp + 16 * u + e) * kD + v_own] = x[e];
       }

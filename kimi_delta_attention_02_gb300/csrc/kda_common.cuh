@@ -265,23 +265,17 @@ __device__ __forceinline__ int opaque_int(int x) {
 // Named CTA barriers (ids 1..15; id 0 is the one __syncthreads uses). `n` counts
 // threads, a multiple of 32; each taking part warp executes the call as a whole.
 // An arrive does not wait; it releases the arriving threads' earlier writes to
-// the threads that sync on the same barrier. These are the aligned forms, which
-// the warp must execute together: a bounded mbarrier wait lets each lane leave its
-// polling loop on its own, so every helper below first brings the warp back
-// together with __syncwarp().
+// the threads that sync on the same barrier.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
-  __syncwarp();
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 __device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t n) {
-  __syncwarp();
   asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(n) : "memory");
 }
 // barrier among `n` threads that also returns the OR of `pred` over them
 __device__ __forceinline__ bool named_bar_or(uint32_t id, uint32_t n, bool pred) {
   uint32_t r;
-  __syncwarp();
   asm volatile(
       "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, %2, %3, p;\n selp.u32 %0, 1, 0, q;\n}\n"
       : "=r"(r)
@@ -342,22 +336,16 @@ __device__ __forceinline__ void tma_prefetch_desc(const void *tmap) {
 // ---------------------------------------------------------------------------
 // tcgen05: tensor memory allocation, MMA, commit, loads, fences
 // ---------------------------------------------------------------------------
-// The .sync.aligned forms below (alloc, relinquish, dealloc, ld, st and their waits) are executed
-// by the whole warp together; like the named barriers, each first reconverges the warp, which a
-// bounded mbarrier wait (each lane leaving its polling loop on its own) may have split.
 // Allocate `ncols` TMEM columns (power of two >= 32); whole warp; address -> *dst (smem).
 __device__ __forceinline__ void tmem_alloc(uint32_t *dst, uint32_t ncols) {
-  __syncwarp();
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst)),
                "r"(ncols)
                : "memory");
 }
 __device__ __forceinline__ void tmem_relinquish() {
-  __syncwarp();
   asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  __syncwarp();
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
@@ -394,7 +382,6 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
 // 32 lanes x 32-bit, 16 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {  // v: 16 registers
   uint32_t r[16];
-  __syncwarp();
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
@@ -406,10 +393,34 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {  // v: 16 
 // 32 lanes x 32-bit, 8 consecutive columns per thread.
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float *v) {
   uint32_t r[8];
-  __syncwarp();
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
                : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
                : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
+}
+// The same loads with their wait in one statement: the registers are complete when the
+// compiler first sees them (for a load whose wait follows at once).
+__device__ __forceinline__ void tmem_ld16_wait(uint32_t taddr, float *v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld8_wait(uint32_t taddr, float *v) {
+  uint32_t r[8];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+      : "r"(taddr)
+      : "memory");
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -425,14 +436,12 @@ __device__ __forceinline__ void tmem_regs_ready(float (&v)[N]) {
 }
 template <typename... Arrays>
 __device__ __forceinline__ void tmem_ld_wait(Arrays &...loaded) {
-  __syncwarp();
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
   (tmem_regs_ready(loaded), ...);
 }
 
 // 32 lanes x 32-bit, 16 consecutive columns per thread, registers -> tensor memory.
 __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
-  __syncwarp();
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
           taddr),
@@ -444,7 +453,6 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const float *v) {
       : "memory");
 }
 __device__ __forceinline__ void tmem_st_wait() {
-  __syncwarp();
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 

@@ -86,8 +86,7 @@ __global__ void __launch_bounds__(128, 1)
   if (ok) {
     for (int c0 = 0; c0 < N; c0 += 16) {
       float vals[16];
-      tmem_ld16(tmem + (uint32_t(32 * warp) << 16) + c0, vals);
-      tmem_ld_wait(vals);
+      tmem_ld16_wait(tmem + (uint32_t(32 * warp) << 16) + c0, vals);
       for (int j = 0; j < 16; ++j) D[(32 * warp + lane) * N + c0 + j] = vals[j];
     }
   }
