@@ -98,6 +98,9 @@ constexpr int kHandoff = kWorkers + 32;     // + warp 16, which issues TMA loads
 // each fit the register file exactly as 17 would (registers are granted to warps in groups of four).
 constexpr int kInvWarp0 = 18, kGramWarp = 17;
 constexpr int kThreads = 640;
+// Every warp from kInvWarp0 on runs the inverse pair's code, which indexes its lane quarter as 2 or 3:
+// the pair must be the launch's last two warps.
+static_assert(kThreads / 32 == kInvWarp0 + 2, "the inverse pair is the last two warps");
 constexpr int kALd = 36;    // fp32 row stride of the A / T scratch
 constexpr float kLog2e = 1.4426950408889634f;
 
@@ -246,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // of the state chain; the unbounded map keeps the inverse on four of the compute warps, whose
   // scratch its position-pair step shares.
   constexpr bool kDedInv = kDecay != DECAY_UNBOUNDED;
-  const bool inv_pair = kDedInv && warp >= kInvWarp0;
+  const bool inv_pair = kDedInv && warp >= kInvWarp0;  // warps 18, 19: the last two (see kThreads)
   // Full chunks leave through a TMA store of a staged tile with the output gate.
   constexpr bool kStaged = kNormGate;
   // Plain read-out with the inverse pair: the outputs of chunk j - 1 leave with P1 of chunk j (both
