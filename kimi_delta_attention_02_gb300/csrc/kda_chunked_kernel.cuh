@@ -407,18 +407,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float *gin = reinterpret_cast<const float *>(sm + OFF_QKG + SG) + tb * kD + ch;
       const uint16_t *zin = reinterpret_cast<const uint16_t *>(sm + OFF_QKG + SG) + tb * kD + ch;
       float run = 0.f;
-      bool grows = false;  // clamped form: a log-decay above kMaxGrowth
+      float gmax = -INFINITY;  // clamped form: the largest log-decay (NaN is not counted, as in g > bound)
 #pragma unroll
       for (int r = 0; r < 8; ++r) {  // alpha = 1 past the end of the sequence
         const float g = !(kFull || tb + r < L) ? 0.f
                         : kUnb                ? unbounded_log_decay(bf16_to_f32(zin[r * kD]), a_h)
                         : kGated              ? gated_log_decay(bf16_to_f32(zin[r * kD]), a_h, lb)
                                               : clamp_log_decay(gin[r * kD], lb);
-        if (!kGated) grows |= g > kMaxGrowth;
+        if (!kGated) gmax = fmaxf(gmax, g);
         run = fmaf(g, kLog2e, run);
         lg[r] = run;
       }
-      if (!kGated && grows) raise_device_error(err_word, DEVERR_RANGE);  // the call's results are unspecified
+      if (!kGated && gmax > kMaxGrowth) raise_device_error(err_word, DEVERR_RANGE);  // results unspecified
       s_tot[grp * kD + ch] = run;
       maybe_wide = kUnb && run < -0.5f * kWideBlock;  // a wide channel has such a group in its block
     };
@@ -479,9 +479,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           const float k = ok ? bf16_to_f32(*reinterpret_cast<const uint16_t *>(qk0 + SK + off)) : 0.f;
           const float d = start + lg[r];  // log2 e^{G_t - r}
           const float f = exp2_sfu(d), g = exp2_sfu(-d);
-          float qv = q * f, kv = k * f, gv = k * g;                  // tf32 Gram operands
-          qf[e] = qv * tau0;                                          // fp16 operands: Q Gamma,
-          kf[e] = kv * tau0;                                          // K Gamma,
+          const float2 qk_f = f2_mul(make_float2(q, k), make_float2(f, f));    // (packed pairs)
+          const float2 qk_t = f2_mul(qk_f, make_float2(tau0, tau0));
+          float qv = qk_f.x, kv = qk_f.y, gv = k * g;               // tf32 Gram operands
+          qf[e] = qk_t.x;                                             // fp16 operands: Q Gamma,
+          kf[e] = qk_t.y;                                             // K Gamma,
           kg[e] = gv * tau1;                                          // K e^{G_last - G}
           if constexpr (kUnb) {
             if (wide) {  // f (first block) or g (second) may overflow: out of the Gram, and
@@ -497,9 +499,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           const uint32_t o4 = (r * 128 + ((cq ^ uint32_t(r)) << 4)) >> 2;  // row tb + r, whose t & 7 = r
-          gq[o4] = round_tf32_alu(qv);
-          gk[o4] = round_tf32_alu(kv);
-          gb[o4] = round_tf32_alu(gv);
+          gq[o4] = round_tf32(qv);
+          gk[o4] = round_tf32(kv);
+          gb[o4] = round_tf32(gv);
         }
         hq[2 * half] = pack_f16x2(qf[0], qf[1]);
         hq[2 * half + 1] = pack_f16x2(qf[2], qf[3]);
@@ -642,9 +644,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (!no_out) {
       const int64_t step = int64_t(H) * kD;
       const int64_t base = ((chunk_t0(j) + t0) * H + h) * int64_t(kD) + v_own;
+      if (L == kC) {  // a full chunk: no masks
+        using E = typename std::conditional<kOutBF16, uint16_t, float>::type;
+        E *p = static_cast<E *>(out) + base;
 #pragma unroll
-      for (int e = 0; e < N; ++e)
-        if (t0 + e < L) store_elem<kOutBF16>(out, base + e * step, x[e]);
+        for (int e = 0; e < N; ++e, p += step) {
+          if constexpr (kOutBF16) *p = f32_to_bf16(x[e]);
+          else *p = x[e];
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < N; ++e)
+          if (t0 + e < L) store_elem<kOutBF16>(out, base + e * step, x[e]);
+      }
     }
   };
   auto issue_gate = [&](int c) {  // issuer
@@ -1098,19 +1110,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_at(sm + OFF_ST, sw128_chunk(v_own, ((col & 63u) >> 3) + 1, col >> 6, 128), pack8_f16(x + 8));
         const float4 *gam = reinterpret_cast<const float4 *>(s_gamma + b * kD + col);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
+        for (int e = 0; e < 4; ++e) {  // packed pairs: the same roundings as scalar multiplies
           const float4 gv = gam[e];
-          x[4 * e] *= gv.x;
-          x[4 * e + 1] *= gv.y;
-          x[4 * e + 2] *= gv.z;
-          x[4 * e + 3] *= gv.w;
+          const float2 lo = f2_mul(make_float2(x[4 * e], x[4 * e + 1]), make_float2(gv.x, gv.y));
+          const float2 hi = f2_mul(make_float2(x[4 * e + 2], x[4 * e + 3]), make_float2(gv.z, gv.w));
+          x[4 * e] = lo.x;
+          x[4 * e + 1] = lo.y;
+          x[4 * e + 2] = hi.x;
+          x[4 * e + 3] = hi.y;
         }
         tmem_st16(s_cols(b) + 16 * u, x);
       }
       tmem_st_wait();
       if (kMerged && j > 0) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e) ox[e] *= scale;
+        for (int e = 0; e < 8; e += 2) {  // packed pairs: the same roundings as scalar multiplies
+          const float2 y = f2_mul(make_float2(ox[e], ox[e + 1]), make_float2(scale, scale));
+          ox[e] = y.x;
+          ox[e + 1] = y.y;
+        }
         write_rows(ox, 8 * grp, j - 1, chunk_len(j - 1));
       }
       // ---------------- P6: -W^T of chunk j (its W^T / U~^T MMA ran during P1) -> MMA1

@@ -69,13 +69,6 @@ __device__ __forceinline__ float round_tf32(float x) {
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
   return __uint_as_float(r);
 }
-// The same rounding on the integer ALU: adding half a tf32 unit in the last place to
-// the magnitude bits and clearing the 13 dropped bits rounds half away from zero (a
-// carry into the exponent is the correct round-up). Finite inputs only: a NaN whose
-// payload sits in the dropped bits may come out as infinity.
-__device__ __forceinline__ float round_tf32_alu(float x) {
-  return __uint_as_float((__float_as_uint(x) + 0x1000u) & 0xffffe000u);
-}
 
 __device__ __forceinline__ float bf16_or_f32(uint16_t h) { return bf16_to_f32(h); }
 __device__ __forceinline__ float bf16_or_f32(float x) { return x; }
