@@ -72,7 +72,7 @@
 //                 (RMSNorm over the 128 value channels and the Sigmoid of the gate logits,
 //                 whose tile TMA brings into the S^T tile once MMA1 has read it) O^T of chunk
 //                 j leaves here too;
-//                 W^T = Kg^T T'^T and [U~^T | 0] = V^T [T'; 0]^T
+//                 -W^T = -Kg^T T'^T (negated by the MMA) and [U~^T | 0] = V^T [T'; 0]^T
 // Per-chunk operand tiles are double-buffered by chunk parity ([P ; K^^T] three
 // times, since it lives from P2 of chunk j to MMA2 of chunk j + 2), and so are the
 // Gram accumulators. TMA brings q, k and log-decay one chunk ahead of P2 and v two
@@ -153,7 +153,7 @@ __host__ __device__ constexpr uint32_t pair_row_p(uint32_t blk, uint32_t tl) { r
 static_assert(pair_row_a(1, 15) + 14 == 239 && pair_row_p(1, 15) + 15 == 511, "pair share layout");
 
 // TMEM columns: two groups [U^T | O^T | S^T] (32 + 32 + 128) used by chunk parity, then
-// Gram (chunk parity 0), W^T, Gram (parity 1). Chunk j's MMA1 and MMA2 write group j % 2;
+// Gram (chunk parity 0), -W^T, Gram (parity 1). Chunk j's MMA1 and MMA2 write group j % 2;
 // its MMA2 leaves the state for chunk j + 1 there, which P1 of chunk j + 1 reads and
 // rewrites, decayed, into the other.
 constexpr uint32_t TM_GROUP = 192, TM_O = 32, TM_SS = 64, TM_GRAM = 384, TM_W = 416, TM_COLS = 512;
@@ -161,7 +161,7 @@ __device__ __forceinline__ uint32_t tm_grp(int b) { return TM_GROUP * uint32_t(b
 __device__ __forceinline__ uint32_t tm_gram(int c) { return TM_GRAM + 64u * uint32_t(c & 1); }
 
 constexpr uint32_t IDESC_GRAM = umma_idesc(UMMA_TF32, 64, 32, false, false, false);
-constexpr uint32_t IDESC_WT = umma_idesc(UMMA_F16, 128, 32, false, false, false);  // W^T = Kg^T T'^T
+constexpr uint32_t IDESC_WT = umma_idesc(UMMA_F16, 128, 32, false, false, true);   // -W^T = -Kg^T T'^T (negate A)
 constexpr uint32_t IDESC_UT = umma_idesc(UMMA_F16, 128, 64, true, false, false);   // [U~^T | 0] = V^T [T'; 0]^T
 constexpr uint32_t IDESC_UO = umma_idesc(UMMA_F16, 128, 64, false, true, false);   // += S^T [-W^T | Q~^T]
 constexpr uint32_t IDESC_OS = umma_idesc(UMMA_F16, 128, 160, false, false, false); // [O^T | S^T] += U^T [P ; K^^T]^T
@@ -1068,9 +1068,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bad |= !mbar_wait_sleep(&bars->wu, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
     float x[8];
-    tmem_ld8_wait(tmem + lane_base + TM_W + 8 * grp, x);  // W^T row c = v_own, columns t = 8 grp ..
-#pragma unroll
-    for (int e = 0; e < 8; ++e) x[e] = -x[e];
+    tmem_ld8_wait(tmem + lane_base + TM_W + 8 * grp, x);  // -W^T row c = v_own, columns t = 8 grp ..
     const uint32_t cr = uint32_t(v_own);
     st_at(sm + OFF_WQ + b * kWQBytes, cr * 128 + (((uint32_t(grp) ^ cr) & 7u) << 4), pack8_f16(x));
   };
