@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kProTmaThreads, 2)
 
     // two consecutive tokens tok, tok + 1: Swish, the L2 norms of q / k in one halving reduction
     // (lanes 0..15 end with token tok's sum of squares, lanes 16..31 with token tok + 1's), store
-    auto finish2 = [&](int64_t tok, float2 (&u)[2][2]) {
+    auto finish2 = [&](Elem *op, float2 (&u)[2][2]) {  // op: this lane's channels of the first token
 #pragma unroll
       for (int a = 0; a < 2; ++a)
 #pragma unroll
@@ -458,21 +458,20 @@ __global__ void __launch_bounds__(kProTmaThreads, 2)
           u[1][i] = f2_mul(u[1][i], make_float2(rn1, rn1));
         }
       }
+      if (on) {  // both tokens lie inside the tile's one sequence, before T
 #pragma unroll
-      for (int a = 0; a < 2; ++a) {
-        if (on && tok + a < T) {
-          const int64_t o = ((tok + a) * H + h) * d + c0;
+        for (int a = 0; a < 2; ++a) {
+          Elem *o = op + int64_t(a) * H * d;
           if constexpr (kBF16)
-            *reinterpret_cast<uint2 *>(static_cast<uint16_t *>(x_out) + o) =
-                make_uint2(pack_bf16x2(u[a][0].x, u[a][0].y), pack_bf16x2(u[a][1].x, u[a][1].y));
+            *reinterpret_cast<uint2 *>(o) = make_uint2(pack_bf16x2(u[a][0].x, u[a][0].y), pack_bf16x2(u[a][1].x, u[a][1].y));
           else
-            *reinterpret_cast<float4 *>(static_cast<float *>(x_out) + o) =
-                make_float4(u[a][0].x, u[a][0].y, u[a][1].x, u[a][1].y);
+            *reinterpret_cast<float4 *>(o) = make_float4(u[a][0].x, u[a][0].y, u[a][1].x, u[a][1].y);
         }
       }
     };
 
     if (one_seq) {  // every row of the tile and the 3 before it in one sequence: a sliding window
+      Elem *out_tile = static_cast<Elem *>(x_out) + ((t0 + tb) * H + h) * d + c0;  // token t0 + tb
       // two tokens per step (rows tb + tt .. tb + tt + 4): two independent chains, and one
       // reduction for both tokens' L2 norms
       float2 win[5][2] = {};  // [row][channel pair]
@@ -502,7 +501,7 @@ __global__ void __launch_bounds__(kProTmaThreads, 2)
             u[a][i] = f2_fma(wp[i][2], win[a + 2][i], u[a][i]);
             u[a][i] = f2_fma(wp[i][3], win[a + 3][i], u[a][i]);
           }
-        finish2(t0 + tb + tt, u);
+        finish2(out_tile + int64_t(tt) * H * d, u);
       }
     } else {  // per token and tap: before its sequence start a token reads the state (or zero)
       for (int tt = 0; tt < 8; ++tt) {
