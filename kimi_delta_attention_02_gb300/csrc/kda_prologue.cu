@@ -471,15 +471,29 @@ __global__ void __launch_bounds__(kProTmaThreads, 2)
     };
 
     if (one_seq) {  // every row of the tile and the 3 before it in one sequence: a sliding window
-      Elem *out_tile = static_cast<Elem *>(x_out) + ((t0 + tb) * H + h) * d + c0;  // token t0 + tb
+      Elem *op = static_cast<Elem *>(x_out) + ((t0 + tb) * H + h) * d + c0;  // token t0 + tb
+      const int64_t ostep = int64_t(2) * H * d;                                  // two tokens
       // two tokens per step (rows tb + tt .. tb + tt + 4): two independent chains, and one
-      // reduction for both tokens' L2 norms
+      // reduction for both tokens' L2 norms; row and output pointers step instead of indexing
       float2 win[5][2] = {};  // [row][channel pair]
+      const Elem *rp = rows + tb * d + c0;  // row tb
+      auto rowp = [&](const Elem *r, float2 (&x)[2]) {
+        if constexpr (kBF16) {
+          const uint2 v2 = *reinterpret_cast<const uint2 *>(r);
+          x[0] = unpack_bf16x2(v2.x);
+          x[1] = unpack_bf16x2(v2.y);
+        } else {
+          const float4 a = *reinterpret_cast<const float4 *>(r);
+          x[0] = make_float2(a.x, a.y);
+          x[1] = make_float2(a.z, a.w);
+        }
+      };
       if (on) {
-        row4(tb, win[2]);
-        row4(tb + 1, win[3]);
-        row4(tb + 2, win[4]);
+        rowp(rp, win[2]);
+        rowp(rp + d, win[3]);
+        rowp(rp + 2 * d, win[4]);
       }
+      rp += 3 * d;  // row tb + 3
 #pragma unroll
       for (int tt = 0; tt < 8; tt += 2) {
 #pragma unroll
@@ -488,9 +502,10 @@ __global__ void __launch_bounds__(kProTmaThreads, 2)
           win[j][1] = win[j + 2][1];
         }
         if (on) {
-          row4(tb + tt + 3, win[3]);
-          row4(tb + tt + 4, win[4]);
+          rowp(rp, win[3]);
+          rowp(rp + d, win[4]);
         }
+        rp += 2 * d;
         float2 u[2][2];  // [token][channel pair]
 #pragma unroll
         for (int a = 0; a < 2; ++a)
@@ -501,7 +516,8 @@ __global__ void __launch_bounds__(kProTmaThreads, 2)
             u[a][i] = f2_fma(wp[i][2], win[a + 2][i], u[a][i]);
             u[a][i] = f2_fma(wp[i][3], win[a + 3][i], u[a][i]);
           }
-        finish2(out_tile + int64_t(tt) * H * d, u);
+        finish2(op, u);
+        op += ostep;
       }
     } else {  // per token and tap: before its sequence start a token reads the state (or zero)
       for (int tt = 0; tt < 8; ++tt) {
