@@ -371,10 +371,11 @@ def time_e2e(case_cpu, steps, warmup):
     return ms, hp.h2d_bytes, hp.d2h_bytes
 
 
-def cpu_oracle_sample(case_cpu, heads: int):
-    """fp64 oracle on the first `heads` heads of the workload; returns (seconds, threads, token-heads)."""
+def cpu_oracle_sample(case_cpu, heads: int, threads: int = 0):
+    """fp64 oracle on the first `heads` heads of the workload on `threads` host threads (0: every
+    core); returns (seconds, threads used, token-heads)."""
     from oracle import kda_recurrent
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     sl = lambda t: t[:, :heads].contiguous()
     init = case_cpu.init_state[:, :heads].contiguous()
     cu = case_cpu.cu_seqlens.long().numpy()
@@ -609,6 +610,10 @@ def main():
             dt, cores, th = cpu_oracle_sample(case_cpu, heads)
             cpu_base = {"value": T * heads / H / dt, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                         "sample": ORACLE_SAMPLE.format(heads=heads, H=H, T=T), "seconds": dt}
+            # and on one thread, for the per-core rate (2 heads: a fraction of a second)
+            dt1, _, _ = cpu_oracle_sample(case_cpu, 2, threads=1)
+            cpu_base["one_thread"] = {"value": T * 2 / H / dt1, "unit": "tokens/s", "cores": 1,
+                                      "sample": f"2 of {H} heads x {T} tokens, one host thread", "seconds": dt1}
 
     if rank == 0:
         clk = clocks.summary()
