@@ -609,9 +609,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // quarter): each warp sums o^2 of its 32 channels for each of its tokens, the 12 warps meet
   // on BAR_OUT, lane l of each warp then adds token l's four partial sums in a fixed order and
   // passes 1 / rms to the other lanes. The gate logits of chunk j come by TMA into the S^T
-  // tile once MMA1 of chunk j has read it (issue_gate); O^T is read from TMEM twice (before and
-  // after the barrier) to keep few values live, and every value is formed before the (masked)
-  // stores, so that the stores do not order the arithmetic.
+  // tile once MMA1 of chunk j has read it (issue_gate); O^T is read from TMEM once and kept in
+  // registers across the barrier, and every value is formed before the (masked) stores, so that
+  // the stores do not order the arithmetic.
   // Output rows of chunk j held by this thread (channel v_own, tokens t0 .. t0 + N - 1). With
   // the output gate, a full chunk's rows go through shared memory and out with one TMA store by
   // thread 0: the 16 scattered row stores per thread otherwise lengthen the output warps' path
@@ -677,22 +677,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int e = 0; e < N; ++e) gw[e] = w * sigmoid_approx(bf16_to_f32(rt[e * kD]));
     bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
     tc_fence_after();
-    float x[N];
+    float x[N], sq[N];  // x: the scaled read-out, kept across the barrier (no second TMEM read)
     if constexpr (N == 8) tmem_ld8_wait(ocols + t0, x);
     else tmem_ld16_wait(ocols + t0, x);
 #pragma unroll
-    for (int e = 0; e < N; ++e) x[e] = (scale * x[e]) * (scale * x[e]);
-    const float part = lane_sums<N>(x, lane);
+    for (int e = 0; e < N; ++e) {
+      x[e] = scale * x[e];
+      sq[e] = x[e] * x[e];
+    }
+    const float part = lane_sums<N>(sq, lane);
     constexpr int kShift = N == 8 ? 2 : 1;  // lane l holds the sum of token (l >> kShift) & (N - 1)
     if ((lane & ((1 << kShift) - 1)) == 0)
       reinterpret_cast<float *>(s_ss)[4 * (t0 + ((lane >> kShift) & (N - 1))) + quarter] = part;
     named_bar_sync(BAR_OUT, kOutThreads);
     const float4 p = s_ss[t0 + (lane & (N - 1))];
     const float rstd_l = rsqrtf(((p.x + p.y) + (p.z + p.w)) * (1.f / kD) + og.eps);  // token t0 + (lane & (N-1))
-    if constexpr (N == 8) tmem_ld8_wait(ocols + t0, x);
-    else tmem_ld16_wait(ocols + t0, x);
 #pragma unroll
-    for (int e = 0; e < N; ++e) x[e] = scale * x[e] * __shfl_sync(0xffffffffu, rstd_l, e) * gw[e];
+    for (int e = 0; e < N; ++e) x[e] = x[e] * __shfl_sync(0xffffffffu, rstd_l, e) * gw[e];
     write_rows(x, t0, j, L);
   };
   auto out_chunk = [&](int j) {
