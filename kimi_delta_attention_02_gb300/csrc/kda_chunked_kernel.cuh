@@ -52,15 +52,18 @@
 // Each iteration j runs the state chain of chunk j interleaved with the state-independent work
 // of chunks j+1 and j+2, so that each tensor-core group runs while the threads work on the
 // other streams:
-//   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy (bounded maps
-//                 without the output gate: O^T of chunk j - 1 leaves for global memory here)
+//   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy (bounded maps:
+//                 O^T of chunk j - 1 leaves for global memory here, read from tensor memory in
+//                 the same round trip; with the output gate of section 1.3, through the RMSNorm
+//                 over the 128 value channels and the Sigmoid of the gate logits, whose tile the
+//                 Gram warp loads into the Gram operand tiles that the Gram of chunk j + 1 freed)
 //   P6  chain j : -W^T of chunk j into the [-W^T | Q~^T] tile (its MMA ran during
 //                 P1); MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]           (N = 64)
 //   P2  next j+2: decay prefix sums and the operand tiles (a thread owns one key
 //                 channel and 8 tokens); the Gram of chunk j+2 (kind::tf32, M = 64 rows
 //                 [Q f ; K f] x N = 32 keys K g) follows, queued behind MMA2
-//   P3  chain j : U^T to fp16 (bounded maps without the output gate: P of chunk j + 1 leaves
-//                 tensor memory in the same round trip); MMA2: [O^T | S^T] += U^T [P ; K^^T]^T
+//   P3  chain j : U^T to fp16 (bounded maps: P of chunk j + 1 leaves tensor memory in the
+//                 same round trip); MMA2: [O^T | S^T] += U^T [P ; K^^T]^T
 //                 (N = 160)
 //   P4  next j+1: the inverse side. Bounded maps: the inverse pair takes A of chunk j + 1 out of
 //                 its TMEM lanes, forms T' = (I + A)^{-1} Diag(b) by back substitution (one
@@ -68,10 +71,9 @@
 //                 pair hands T' over on an mbarrier, which alone gates W^T / U~^T. Unbounded map:
 //                 warps 2, 3, 6, 7 (whose TMEM lanes hold the key rows of the Gram) invert
 //                 I + A in 8 x 8 and 16 x 16 blocks while the other 12 warps convert v, take P
-//                 out of TMEM and write O^T of chunk j. With the output gate of section 1.3
-//                 (RMSNorm over the 128 value channels and the Sigmoid of the gate logits,
-//                 whose tile TMA brings into the S^T tile once MMA1 has read it) O^T of chunk
-//                 j leaves here too;
+//                 out of TMEM and write O^T of chunk j (with the output gate, through the
+//                 RMSNorm and the gate, the logits tile brought by TMA into the S^T tile once
+//                 MMA1 has read it);
 //                 -W^T = -Kg^T T'^T (negated by the MMA) and [U~^T | 0] = V^T [T'; 0]^T
 // Per-chunk operand tiles are double-buffered by chunk parity ([P ; K^^T] three
 // times, since it lives from P2 of chunk j to MMA2 of chunk j + 2), and so are the
@@ -123,7 +125,7 @@ constexpr uint32_t kWQBytes = 16 * 1024;
 constexpr uint32_t OFF_PK = 188 * 1024;      // 3 x [P ; K^^T] fp16 [160 rows][32], 64-byte swizzle
 constexpr uint32_t kPKBytes = 10 * 1024;
 constexpr uint32_t OFF_MISC = 218 * 1024;    // beta x2, Gamma_last x2, group decay totals, barriers
-constexpr uint32_t OFF_SS = OFF_MISC + 3504; // output gate: per-token partial sums of squares [32][4] fp32
+constexpr uint32_t OFF_SS = OFF_MISC + 3520; // output gate: per-token partial sums of squares [32][4] fp32
 constexpr uint32_t kSmemBytes = 222 * 1024 + 1024;
 static_assert(OFF_SS + 32 * 16 + 1023 <= kSmemBytes, "shared memory map exceeds the allocation");
 // Unbounded decay only: the position-pair shares of the diagonal blocks, by chunk parity,
@@ -190,7 +192,7 @@ __device__ __forceinline__ float exp2_sfu(float x) {
 }
 
 struct Bars {
-  uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate, drain, invd, aread[2], drain2, prep;
+  uint64_t qkg, v[2], mma1, gram[2], mma2, wu, gate[4], drain, invd, aread[2], drain2, prep;
 };
 static_assert(OFF_MISC + (2 * 32 + 2 * 128 + 4 * 128) * 4 + sizeof(Bars) + 48 <= OFF_SS, "misc overlaps");
 
@@ -250,12 +252,13 @@ __global__ void __launch_bounds__(kThreads, 1)
   // scratch its position-pair step shares.
   constexpr bool kDedInv = kDecay != DECAY_UNBOUNDED;
   const bool inv_pair = kDedInv && warp >= kInvWarp0;  // warps 18, 19: the last two (see kThreads)
-  // Full chunks leave through a TMA store of a staged tile with the output gate.
-  constexpr bool kStaged = kNormGate;
-  // Plain read-out with the inverse pair: the outputs of chunk j - 1 leave with P1 of chunk j (both
-  // wait for MMA2 of chunk j - 1 and read tensor memory in the same round trip), and P of chunk
-  // j + 1 leaves tensor memory with U^T of chunk j in P3; no separate output phase.
-  constexpr bool kMerged = kDedInv && !kNormGate;
+  // With the four-warp inverse, full chunks leave the output gate through a TMA store of a staged tile.
+  constexpr bool kStaged = kNormGate && !kDedInv;
+  // Read-out with the inverse pair: the outputs of chunk j - 1 leave with P1 of chunk j (both wait
+  // for MMA2 of chunk j - 1 and read tensor memory in the same round trip; the output gate's
+  // logits of chunk j - 1 wait in the Gram operand tiles, see the Gram warp), and P of chunk j + 1
+  // leaves tensor memory with U^T of chunk j in P3; no separate output phase.
+  constexpr bool kMerged = kDedInv;
   const int h = int(blockIdx.x % H);
   const int64_t blk = blockIdx.x / H;
   const int64_t n = runs.count > 0 ? blk : runs.order != nullptr ? int64_t(runs.order[blk]) : blk;
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->gram[1], 1);
     mbar_init(&bars->mma2, 1);
     mbar_init(&bars->wu, 1);
-    mbar_init(&bars->gate, 1);
+    for (int i = 0; i < 4; ++i) mbar_init(&bars->gate[i], 1);
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->invd, 1);
     mbar_init(&bars->aread[0], 1);
@@ -305,6 +308,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     st_at(sm, OFF_TP + sw64_chunk(32 + (e >> 2), e & 3), make_uint4(0, 0, 0, 0));
 
   const int v_own = 32 * quarter + lane;  // state row (TMEM lane) of this thread; key channel in P2
+  const float w_own = (kNormGate && og.w != nullptr) ? og.w[v_own] : 1.f;  // RMSNorm weight of channel v_own
   const int64_t st_base = (n * H + h) * int64_t(kD) * kD;
 
   tc_fence_before();
@@ -602,26 +606,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int itid = 32 * iw + lane;         // inverse group: thread 0..127 of the group
 
   // ------------------------------------------------------------------ P5: outputs
-  // O^T of chunk j out of TMEM to global memory, on the 12 warps outside the inverse group:
-  // lane quarters 0 and 1 have 4 of them (8 tokens each), quarters 2 and 3 have 2 (16 each).
+  // O^T of chunk j out of TMEM to global memory. With the inverse pair every compute warp writes
+  // 8 tokens of its 32 channels, in P1 of chunk j + 1 (the last chunk after the loop); with the
+  // four-warp inverse, the 12 warps outside the inverse group do it in P4: lane quarters 0 and 1
+  // have 4 of them (8 tokens each), quarters 2 and 3 have 2 (16 each).
   //
   // With the output gate, a token's 128 channels are spread over four warps (one per lane
-  // quarter): each warp sums o^2 of its 32 channels for each of its tokens, the 12 warps meet
-  // on BAR_OUT, lane l of each warp then adds token l's four partial sums in a fixed order and
-  // passes 1 / rms to the other lanes. The gate logits of chunk j come by TMA into the S^T
-  // tile once MMA1 of chunk j has read it (issue_gate); O^T is read from TMEM once and kept in
-  // registers across the barrier, and every value is formed before the (masked) stores, so that
-  // the stores do not order the arithmetic.
-  // Output rows of chunk j held by this thread (channel v_own, tokens t0 .. t0 + N - 1). With
-  // the output gate, a full chunk's rows go through shared memory and out with one TMA store by
-  // thread 0: the 16 scattered row stores per thread otherwise lengthen the output warps' path
-  // past the inverse's. A bf16 tile is staged in the U^T tile (free from MMA2 of chunk j until
-  // P3 of the next step): thread 0 waits for the store to have read it only before the operand
-  // barrier of the next step (or at once when the next step has none). An fp32 tile is staged
-  // in the upper half of the S^T tile, which the next step rewrites at its start, so thread 0
-  // waits before it joins the barrier that ends this step. Without the gate the output path is
-  // short enough for row stores, and a partial chunk (the last of a sequence) is always stored
-  // row by row, so that nothing past the sequence is written. Both paths round bf16 alike.
+  // quarter): each warp sums o^2 of its 32 channels for each of its tokens, the output warps
+  // meet on BAR_OUT, lane l of each warp then adds token l's four partial sums in a fixed order
+  // and passes 1 / rms to the other lanes. The per-token partial sums have one buffer: the next
+  // read-out writes it only after MMA2 of a later chunk, which needs every output thread's
+  // hand-off after its reads of this one.
+  // Output rows of chunk j held by this thread (channel v_own, tokens t0 .. t0 + N - 1). They go
+  // out as row stores (a warp writes 32 consecutive channels of a token), except with the output
+  // gate and the four-warp inverse, where a full chunk's rows go through shared memory and out
+  // with one TMA store by thread 0: the 16 scattered row stores per thread there lengthen the
+  // output warps' path past the inverse's. A bf16 tile is staged in the U^T tile (free from MMA2
+  // of chunk j until P3 of the next step): thread 0 waits for the store to have read it only
+  // before the operand barrier of the next step (or at once when the next step has none). An
+  // fp32 tile is staged in the upper half of the S^T tile, which the next step rewrites at its
+  // start, so thread 0 waits before it joins the barrier that ends this step. A partial chunk
+  // (the last of a sequence) is always stored row by row, so that nothing past the sequence is
+  // written. Both paths round bf16 alike.
   constexpr uint32_t BAR_OUT = 7;
   constexpr uint32_t kOutThreads = kDedInv ? kWorkers : 384;  // the warps that write outputs
   auto write_rows = [&](const auto &x, int t0, int j, int L) {
@@ -659,27 +665,38 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
     }
   };
-  auto issue_gate = [&](int c) {  // issuer
-    if constexpr (kNormGate) {
+  // The output gate's logits of chunk c. With the four-warp inverse, one tile in the upper half of
+  // the S^T tile, loaded by the issuer once MMA1 of chunk c has read S^T (barrier gate[0], one
+  // phase per chunk). With the inverse pair, slot c % 4 of the Gram operand tiles, loaded by the
+  // Gram warp once the Gram of chunk c + 2 has read them (barrier gate[c % 4]); the read-out of
+  // chunk c, in P1 of chunk c + 1, reads it before the operand build of chunk c + 3 rewrites them.
+  auto gate_tile = [&](int c) {
+    return reinterpret_cast<const uint16_t *>(kDedInv ? sm + OFF_QK + uint32_t(c & 3) * 8192u : sm + OFF_ST + G_R);
+  };
+  auto wait_gate = [&](int c) {
+    if (kDedInv) bad |= !mbar_wait_sleep(&bars->gate[c & 3], uint32_t((c >> 2) & 1), err_word, DEVERR_TMA_TIMEOUT);
+    else bad |= !mbar_wait_sleep(&bars->gate[0], uint32_t(c & 1), err_word, DEVERR_TMA_TIMEOUT);
+  };
+  auto issue_gate = [&](int c) {  // issuer, four-warp inverse
+    if constexpr (kStaged) {
       mbar_wait_sleep(&bars->mma1, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);  // S^T read
-      mbar_arrive_expect_tx(&bars->gate, 8192);
-      tma_load_3d(sm + OFF_ST + G_R, &tm_r, &bars->gate, 0, h, int32_t(chunk_t0(c)));
+      mbar_arrive_expect_tx(&bars->gate[0], 8192);
+      tma_load_3d(sm + OFF_ST + G_R, &tm_r, &bars->gate[0], 0, h, int32_t(chunk_t0(c)));
     }
   };
-  auto out_gated_rows = [&](auto n_tag, int t0, int j, int L, uint32_t ocols) {
-    constexpr int N = decltype(n_tag)::value;  // tokens of this warp: 8 or 16
-    const float w = og.w != nullptr ? og.w[v_own] : 1.f;
-    // Sigmoid(r) w first: the gate tile is there well before MMA2 has finished
-    bad |= !mbar_wait_sleep(&bars->gate, uint32_t(j & 1), err_word, DEVERR_TMA_TIMEOUT);
-    const uint16_t *rt = reinterpret_cast<const uint16_t *>(sm + OFF_ST + G_R) + t0 * kD + v_own;
-    float gw[N];
+  // Sigmoid(r) w of this thread's rows (channel v_own, tokens t0 ..) of chunk c
+  auto gate_weights = [&](auto &gw, int t0, int c) {
+    constexpr int N = int(sizeof(gw) / sizeof(gw[0]));
+    const uint16_t *rt = gate_tile(c) + t0 * kD + v_own;
 #pragma unroll
-    for (int e = 0; e < N; ++e) gw[e] = w * sigmoid_approx(bf16_to_f32(rt[e * kD]));
-    bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
-    tc_fence_after();
-    float x[N], sq[N];  // x: the scaled read-out, kept across the barrier (no second TMEM read)
-    if constexpr (N == 8) tmem_ld8_wait(ocols + t0, x);
-    else tmem_ld16_wait(ocols + t0, x);
+    for (int e = 0; e < N; ++e) gw[e] = w_own * sigmoid_approx(bf16_to_f32(rt[e * kD]));
+  };
+  // x: this thread's rows of O^T of chunk j, as read from tensor memory. Scaled, divided by the
+  // rms over each token's 128 channels, gated and written; x is kept in registers across the
+  // barrier (no second tensor-memory read), and every value is formed before the (masked) stores.
+  auto norm_rows = [&](auto &x, const auto &gw, int t0, int j, int L) {
+    constexpr int N = int(sizeof(x) / sizeof(x[0]));  // tokens of this warp: 8 or 16
+    float sq[N];
 #pragma unroll
     for (int e = 0; e < N; ++e) {
       x[e] = scale * x[e];
@@ -695,6 +712,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int e = 0; e < N; ++e) x[e] = x[e] * __shfl_sync(0xffffffffu, rstd_l, e) * gw[e];
     write_rows(x, t0, j, L);
+  };
+  auto out_gated_rows = [&](auto n_tag, int t0, int j, int L, uint32_t ocols) {
+    constexpr int N = decltype(n_tag)::value;  // tokens of this warp: 8 or 16
+    if (kDedInv && no_out) return;  // (the Gram warp loads no logits then)
+    // Sigmoid(r) w first: the gate tile is there well before MMA2 has finished
+    wait_gate(j);
+    float gw[N];
+    gate_weights(gw, t0, j);
+    bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
+    tc_fence_after();
+    float x[N];
+    if constexpr (N == 8) tmem_ld8_wait(ocols + t0, x);
+    else tmem_ld16_wait(ocols + t0, x);
+    norm_rows(x, gw, t0, j, L);
   };
   auto out_chunk = [&](int j) {
     if (!kNormGate) {
@@ -1122,13 +1153,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tmem_st_wait();
       if (kMerged && j > 0) {
+        if constexpr (kNormGate) {
+          if (!no_out) {
+            wait_gate(j - 1);
+            float gw[8];
+            gate_weights(gw, 8 * grp, j - 1);
+            norm_rows(ox, gw, 8 * grp, j - 1, chunk_len(j - 1));
+          }
+        } else {
 #pragma unroll
-        for (int e = 0; e < 8; e += 2) {  // packed pairs: the same roundings as scalar multiplies
-          const float2 y = f2_mul(make_float2(ox[e], ox[e + 1]), make_float2(scale, scale));
-          ox[e] = y.x;
-          ox[e + 1] = y.y;
+          for (int e = 0; e < 8; e += 2) {  // packed pairs: the same roundings as scalar multiplies
+            const float2 y = f2_mul(make_float2(ox[e], ox[e + 1]), make_float2(scale, scale));
+            ox[e] = y.x;
+            ox[e + 1] = y.y;
+          }
+          write_rows(ox, 8 * grp, j - 1, chunk_len(j - 1));
         }
-        write_rows(ox, 8 * grp, j - 1, chunk_len(j - 1));
       }
       // ---------------- P6: -W^T of chunk j (its W^T / U~^T MMA ran during P1) -> MMA1
       wt_extract(j);
@@ -1174,6 +1214,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // chunk c - 2 out of the same tensor-memory slot. Lane 0 issues; on leaving early it waits for
     // its own MMAs (bounded) before the teardown frees tensor memory.
     bool issued = false;
+    int gate_hi = -1;  // output gate: the last chunk whose logits tile this warp has loaded
     for (int c = 0; c < n_chunks; ++c) {
       const bool ok = mbar_wait_sleep(&bars->prep, uint32_t(c & 1), err_word, DEVERR_MMA_TIMEOUT);
       tc_fence_after();
@@ -1187,7 +1228,28 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       if (lane == 0) issue_gram(c);
       issued = true;
+      // output gate: the logits of chunk c - 2 into the slot that this Gram frees, once it has read
+      // its operands; after the last Gram nothing rewrites the operand tiles, so the logits of the
+      // chunks left follow at once (at most three, in slots of their own)
+      const bool last = c == n_chunks - 1;
+      if (kNormGate && !no_out && (last || c >= 2)) {
+        const bool read_ops = mbar_wait_sleep(&bars->gram[c & 1], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+        if (__any_sync(0xffffffffu, !read_ops)) {
+          if (lane == 0) *s_abort = 1u;
+          break;
+        }
+        const int k1 = last ? c : c - 2;
+        if (lane == 0)
+          for (int k = c >= 2 ? c - 2 : 0; k <= k1; ++k) {
+            mbar_arrive_expect_tx(&bars->gate[k & 3], 8192);
+            tma_load_3d(sm + OFF_QK + uint32_t(k & 3) * 8192u, &tm_r, &bars->gate[k & 3], 0, h, int32_t(chunk_t0(k)));
+          }
+        gate_hi = k1;
+      }
     }
+    // the logits tiles in flight land before the teardown (the latest phase of each slot's barrier)
+    for (int k = gate_hi >= 3 ? gate_hi - 3 : 0; k <= gate_hi; ++k)
+      mbar_wait_sleep(&bars->gate[k & 3], uint32_t((k >> 2) & 1), err_word, DEVERR_TMA_TIMEOUT);
     if (issued && *s_abort != 0u) {
       if (lane == 0) umma_commit(&bars->drain2);
       __syncwarp();
@@ -1273,9 +1335,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!kDedInv) issue_gram(j + 2);
         }
         if (j + 3 < n_chunks) qkg_last = j + 3;
-        if (kNormGate) gate_last = j;
+        if (kStaged) gate_last = j;
       }
-      if (kNormGate && j + 2 >= n_chunks) {  // no operand hand-off left to piggyback on
+      if (kStaged && j + 2 >= n_chunks) {  // no operand hand-off left to piggyback on
         if (leader) issue_gate(j);
         gate_last = j;
       }
@@ -1302,7 +1364,7 @@ issuer_abort:
   if (qkg_last >= 0) mbar_wait_sleep(&bars->qkg, uint32_t(qkg_last & 1), err_word, DEVERR_TMA_TIMEOUT);
   for (int s = 0; s < 2; ++s)
     if (v_last[s] >= 0) mbar_wait_sleep(&bars->v[s], uint32_t((v_last[s] >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
-  if (gate_last >= 0) mbar_wait_sleep(&bars->gate, uint32_t(gate_last & 1), err_word, DEVERR_TMA_TIMEOUT);
+  if (gate_last >= 0) mbar_wait_sleep(&bars->gate[0], uint32_t(gate_last & 1), err_word, DEVERR_TMA_TIMEOUT);
 
 teardown:
   if (tid == 0) bulk_wait_all();  // the output tiles this thread stored

@@ -36,7 +36,7 @@ def _check(case, tol, **kw):
     return out
 
 
-@pytest.mark.parametrize("T", [1, 17, 32, 33, 100, 257])
+@pytest.mark.parametrize("T", [1, 17, 32, 33, 70, 96, 100, 257])
 @pytest.mark.parametrize("gated", [False, True])
 def test_chunked_lengths(T, gated):
     case = workloads.make_prefill([T], H=3, device="cuda", seed=40 + T, gated=gated, out_gate=True)
