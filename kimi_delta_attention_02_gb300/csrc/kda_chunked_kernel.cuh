@@ -287,7 +287,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->gram[1], 1);
     mbar_init(&bars->mma2, 1);
     mbar_init(&bars->wu, 1);
-    for (int i = 0; i < 4; ++i) mbar_init(&bars->gate[i], 1);
+    if constexpr (kNormGate) {  // (with the inverse pair, one per logits slot of the output gate)
+      for (int i = 0; i < 4; ++i) mbar_init(&bars->gate[i], 1);
+    } else {
+      mbar_init(&bars->gate[0], 1);
+    }
     mbar_init(&bars->drain, 1);
     mbar_init(&bars->invd, 1);
     mbar_init(&bars->aread[0], 1);
@@ -1152,27 +1156,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(s_cols(b) + 16 * u, x);
       }
       tmem_st_wait();
-      if (kMerged && j > 0) {
-        if constexpr (kNormGate) {
-          if (!no_out) {
-            wait_gate(j - 1);
-            float gw[8];
-            gate_weights(gw, 8 * grp, j - 1);
-            norm_rows(ox, gw, 8 * grp, j - 1, chunk_len(j - 1));
-          }
-        } else {
+      if (!kNormGate && kMerged && j > 0) {  // the read-out of chunk j - 1 (the gated one follows the hand-off)
 #pragma unroll
-          for (int e = 0; e < 8; e += 2) {  // packed pairs: the same roundings as scalar multiplies
-            const float2 y = f2_mul(make_float2(ox[e], ox[e + 1]), make_float2(scale, scale));
-            ox[e] = y.x;
-            ox[e + 1] = y.y;
-          }
-          write_rows(ox, 8 * grp, j - 1, chunk_len(j - 1));
+        for (int e = 0; e < 8; e += 2) {  // packed pairs: the same roundings as scalar multiplies
+          const float2 y = f2_mul(make_float2(ox[e], ox[e + 1]), make_float2(scale, scale));
+          ox[e] = y.x;
+          ox[e + 1] = y.y;
         }
+        write_rows(ox, 8 * grp, j - 1, chunk_len(j - 1));
       }
       // ---------------- P6: -W^T of chunk j (its W^T / U~^T MMA ran during P1) -> MMA1
       wt_extract(j);
       handoff(H_COPY);
+      if constexpr (kNormGate && kMerged) {  // the gated read-out of chunk j - 1 (its O^T came with
+        if (j > 0 && !no_out) {               // S^T in P1), beside MMA1
+          wait_gate(j - 1);
+          float gw[8];
+          gate_weights(gw, 8 * grp, j - 1);
+          norm_rows(ox, gw, 8 * grp, j - 1, chunk_len(j - 1));
+        }
+      }
       // ---------------- P2: operand tiles of chunk j + 2 -> Gram
       if (j + 2 < n_chunks && !prep(j + 2)) goto teardown;
       // ---------------- P3: chain j, U^T to fp16 -> MMA2
@@ -1231,25 +1234,30 @@ __global__ void __launch_bounds__(kThreads, 1)
       // output gate: the logits of chunk c - 2 into the slot that this Gram frees, once it has read
       // its operands; after the last Gram nothing rewrites the operand tiles, so the logits of the
       // chunks left follow at once (at most three, in slots of their own)
-      const bool last = c == n_chunks - 1;
-      if (kNormGate && !no_out && (last || c >= 2)) {
-        const bool read_ops = mbar_wait_sleep(&bars->gram[c & 1], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
-        if (__any_sync(0xffffffffu, !read_ops)) {
-          if (lane == 0) *s_abort = 1u;
-          break;
-        }
-        const int k1 = last ? c : c - 2;
-        if (lane == 0)
-          for (int k = c >= 2 ? c - 2 : 0; k <= k1; ++k) {
-            mbar_arrive_expect_tx(&bars->gate[k & 3], 8192);
-            tma_load_3d(sm + OFF_QK + uint32_t(k & 3) * 8192u, &tm_r, &bars->gate[k & 3], 0, h, int32_t(chunk_t0(k)));
+      if constexpr (kNormGate) {
+        const bool last = c == n_chunks - 1;
+        if (!no_out && (last || c >= 2)) {
+          const bool read_ops =
+              mbar_wait_sleep(&bars->gram[c & 1], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
+          if (__any_sync(0xffffffffu, !read_ops)) {
+            if (lane == 0) *s_abort = 1u;
+            break;
           }
-        gate_hi = k1;
+          const int k1 = last ? c : c - 2;
+          if (lane == 0)
+            for (int k = c >= 2 ? c - 2 : 0; k <= k1; ++k) {
+              mbar_arrive_expect_tx(&bars->gate[k & 3], 8192);
+              tma_load_3d(sm + OFF_QK + uint32_t(k & 3) * 8192u, &tm_r, &bars->gate[k & 3], 0, h,
+                          int32_t(chunk_t0(k)));
+            }
+          gate_hi = k1;
+        }
       }
     }
     // the logits tiles in flight land before the teardown (the latest phase of each slot's barrier)
-    for (int k = gate_hi >= 3 ? gate_hi - 3 : 0; k <= gate_hi; ++k)
-      mbar_wait_sleep(&bars->gate[k & 3], uint32_t((k >> 2) & 1), err_word, DEVERR_TMA_TIMEOUT);
+    if constexpr (kNormGate)
+      for (int k = gate_hi >= 3 ? gate_hi - 3 : 0; k <= gate_hi; ++k)
+        mbar_wait_sleep(&bars->gate[k & 3], uint32_t((k >> 2) & 1), err_word, DEVERR_TMA_TIMEOUT);
     if (issued && *s_abort != 0u) {
       if (lane == 0) umma_commit(&bars->drain2);
       __syncwarp();
