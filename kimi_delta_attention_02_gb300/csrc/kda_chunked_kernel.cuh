@@ -634,6 +634,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   // written. Both paths round bf16 alike.
   constexpr uint32_t BAR_OUT = 7;
   constexpr uint32_t kOutThreads = kDedInv ? kWorkers : 384;  // the warps that write outputs
+  // With the inverse pair, the four warps of column group grp (one per lane quarter) hold all 128
+  // channels of tokens 8 grp .. 8 grp + 7: the sums of squares meet on one barrier per group.
+  constexpr uint32_t BAR_NORM0 = 9;  // .. 12
   auto write_rows = [&](const auto &x, int t0, int j, int L) {
     constexpr int N = int(sizeof(x) / sizeof(x[0]));
     if (kStaged && L == kC) {
@@ -710,7 +713,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kShift = N == 8 ? 2 : 1;  // lane l holds the sum of token (l >> kShift) & (N - 1)
     if ((lane & ((1 << kShift) - 1)) == 0)
       reinterpret_cast<float *>(s_ss)[4 * (t0 + ((lane >> kShift) & (N - 1))) + quarter] = part;
-    named_bar_sync(BAR_OUT, kOutThreads);
+    if (kDedInv) named_bar_sync(BAR_NORM0 + uint32_t(grp), 128);
+    else named_bar_sync(BAR_OUT, kOutThreads);
     const float4 p = s_ss[t0 + (lane & (N - 1))];
     const float rstd_l = rsqrtf(((p.x + p.y) + (p.z + p.w)) * (1.f / kD) + og.eps);  // token t0 + (lane & (N-1))
 #pragma unroll
