@@ -53,12 +53,13 @@
 // of chunks j+1 and j+2, so that each tensor-core group runs while the threads work on the
 // other streams:
 //   P1  chain j : fp16 copy of S^T; Gamma_j-decayed S^T into the other copy (bounded maps:
-//                 O^T of chunk j - 1 leaves for global memory here, read from tensor memory in
-//                 the same round trip; with the output gate of section 1.3, through the RMSNorm
-//                 over the 128 value channels and the Sigmoid of the gate logits, whose tile the
-//                 Gram warp loads into the Gram operand tiles that the Gram of chunk j + 1 freed)
+//                 O^T of chunk j - 1 comes out of tensor memory in the same round trip)
 //   P6  chain j : -W^T of chunk j into the [-W^T | Q~^T] tile (its MMA ran during
-//                 P1); MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]           (N = 64)
+//                 P1); MMA1: [U^T | O^T] += S^T [-W^T | Q~^T]           (N = 64); bounded maps:
+//                 beside MMA1, O^T of chunk j - 1 leaves for global memory (with the output
+//                 gate of section 1.3, through the RMSNorm over the 128 value channels and the
+//                 Sigmoid of the gate logits, whose tile the Gram warp loads into the Gram
+//                 operand tiles that the Gram of chunk j + 1 freed)
 //   P2  next j+2: decay prefix sums and the operand tiles (a thread owns one key
 //                 channel and 8 tokens); the Gram of chunk j+2 (kind::tf32, M = 64 rows
 //                 [Q f ; K f] x N = 32 keys K g) follows, queued behind MMA2
@@ -611,7 +612,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   // ------------------------------------------------------------------ P5: outputs
   // O^T of chunk j out of TMEM to global memory. With the inverse pair every compute warp writes
-  // 8 tokens of its 32 channels, in P1 of chunk j + 1 (the last chunk after the loop); with the
+  // 8 tokens of its 32 channels, read in P1 of chunk j + 1 and written once MMA1 of chunk j + 1
+  // is issued (the last chunk after the loop); with the
   // four-warp inverse, the 12 warps outside the inverse group do it in P4: lane quarters 0 and 1
   // have 4 of them (8 tokens each), quarters 2 and 3 have 2 (16 each).
   //
@@ -1160,7 +1162,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(s_cols(b) + 16 * u, x);
       }
       tmem_st_wait();
-      if (!kNormGate && kMerged && j > 0) {  // the read-out of chunk j - 1 (the gated one follows the hand-off)
+      // ---------------- P6: -W^T of chunk j (its W^T / U~^T MMA ran during P1) -> MMA1
+      wt_extract(j);
+      handoff(H_COPY);
+      // ---------------- read-out of chunk j - 1 (its O^T came with S^T in P1), beside MMA1
+      if (!kNormGate && kMerged && j > 0) {
 #pragma unroll
         for (int e = 0; e < 8; e += 2) {  // packed pairs: the same roundings as scalar multiplies
           const float2 y = f2_mul(make_float2(ox[e], ox[e + 1]), make_float2(scale, scale));
@@ -1169,11 +1175,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         write_rows(ox, 8 * grp, j - 1, chunk_len(j - 1));
       }
-      // ---------------- P6: -W^T of chunk j (its W^T / U~^T MMA ran during P1) -> MMA1
-      wt_extract(j);
-      handoff(H_COPY);
-      if constexpr (kNormGate && kMerged) {  // the gated read-out of chunk j - 1 (its O^T came with
-        if (j > 0 && !no_out) {               // S^T in P1), beside MMA1
+      if constexpr (kNormGate && kMerged) {  // through the output gate
+        if (j > 0 && !no_out) {
           wait_gate(j - 1);
           float gw[8];
           gate_weights(gw, 8 * grp, j - 1);
