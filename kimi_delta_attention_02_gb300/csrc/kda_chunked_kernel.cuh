@@ -737,6 +737,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     else tmem_ld16_wait(ocols + t0, x);
     norm_rows(x, gw, t0, j, L);
   };
+  // the read-out without the output gate: this thread's rows of O^T of chunk j, scaled and written
+  auto plain_read_out = [&](float (&x)[8], int j) {
+#pragma unroll
+    for (int e = 0; e < 8; e += 2) {  // packed pairs: the same roundings as scalar multiplies
+      const float2 y = f2_mul(make_float2(x[e], x[e + 1]), make_float2(scale, scale));
+      x[e] = y.x;
+      x[e + 1] = y.y;
+    }
+    write_rows(x, 8 * grp, j, chunk_len(j));
+  };
   auto out_chunk = [&](int j) {
     if (!kNormGate) {
       bad |= !mbar_wait_sleep(&bars->mma2, uint32_t(j & 1), err_word, DEVERR_MMA_TIMEOUT);
@@ -1162,18 +1172,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(s_cols(b) + 16 * u, x);
       }
       tmem_st_wait();
+      if constexpr (kMerged && !kNormGate && kGated) {  // (the gated decay's read-out: here, which
+        if (j > 0) plain_read_out(ox, j - 1);           // measured faster than beside MMA1)
+      }
       // ---------------- P6: -W^T of chunk j (its W^T / U~^T MMA ran during P1) -> MMA1
       wt_extract(j);
       handoff(H_COPY);
       // ---------------- read-out of chunk j - 1 (its O^T came with S^T in P1), beside MMA1
-      if (!kNormGate && kMerged && j > 0) {
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {  // packed pairs: the same roundings as scalar multiplies
-          const float2 y = f2_mul(make_float2(ox[e], ox[e + 1]), make_float2(scale, scale));
-          ox[e] = y.x;
-          ox[e + 1] = y.y;
-        }
-        write_rows(ox, 8 * grp, j - 1, chunk_len(j - 1));
+      if constexpr (kMerged && !kNormGate && !kGated) {
+        if (j > 0) plain_read_out(ox, j - 1);
       }
       if constexpr (kNormGate && kMerged) {  // through the output gate
         if (j > 0 && !no_out) {
