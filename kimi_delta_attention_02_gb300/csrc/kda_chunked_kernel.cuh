@@ -858,8 +858,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // ------------------------------------------------------------------ P4: P, A, inverse, T', v
-  // Inverse-side work of chunk c; the 12 warps outside the inverse group also write the
-  // outputs of chunk j_out (if >= 0). Returns false when the compute warps give up.
+  // The four-warp inverse (unbounded map): inverse-side work of chunk c; the 12 warps outside the
+  // inverse group also write the outputs of chunk j_out (if >= 0). Returns false when the compute
+  // warps give up.
   auto extract_inverse = [&](int c, int j_out) -> bool {
     const int b = c & 1, L = chunk_len(c);
     float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
@@ -948,10 +949,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
       // the 12 other warps: v tile of this chunk bf16 -> fp16 in place (rows past the end
       // zeroed), the query rows P of the Gram, then the outputs of chunk j_out
-      // (with the inverse pair, the pair converts v)
-      const int ot = kDedInv ? kC * 16
-                             : (quarter < 2 ? 64 * grp + 32 * quarter : 256 + 64 * (grp - 2) + 32 * (quarter - 2)) + lane;
-      if (!kDedInv) bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
+      const int ot = (quarter < 2 ? 64 * grp + 32 * quarter : 256 + 64 * (grp - 2) + 32 * (quarter - 2)) + lane;
+      bad |= !mbar_wait_sleep(&bars->v[b], uint32_t((c >> 1) & 1), err_word, DEVERR_TMA_TIMEOUT);
       for (int e = ot; e < kC * 16; e += int(kOutThreads)) {
         const int t = e >> 4, cj = e & 15;
         uint4 *p = reinterpret_cast<uint4 *>(sm + OFF_V + b * 8192 + sw128_chunk(t, cj & 7, cj >> 3, kC));
@@ -992,19 +991,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (j_out >= 0) out_chunk(j_out);
     }
-    // the next chain step rewrites the S^T tile (the four-warp inverse's scratch, the output
-    // gate's tiles): all compute threads are past this phase before any goes on
+    // the next chain step rewrites the S^T tile (the inverse's scratch, the output gate's tiles):
+    // all compute threads are past this phase before any goes on
     fence_proxy_async_smem();
     tc_fence_before();
     const bool ab = named_bar_or(BAR_WORK, kWorkers, bad);
-    // with the inverse pair, the issuer needs nothing of this phase before W^T / U~^T (the pair
-    // hands over T' and v; P reaches MMA2 behind the next H_U): no hand-off
-    if (!kDedInv) {
-      if (ab) give_up(H_INV);
-      else handoff(H_INV);
-    } else if (ab && tid == 0) {
-      *s_abort = 1u;  // the issuer sees it at its next hand-off
-    }
+    if (ab) give_up(H_INV);
+    else handoff(H_INV);
     return !ab;
   };
 
