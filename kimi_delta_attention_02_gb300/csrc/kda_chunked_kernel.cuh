@@ -698,7 +698,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int N = int(sizeof(gw) / sizeof(gw[0]));
     const uint16_t *rt = gate_tile(c) + t0 * kD + v_own;
 #pragma unroll
-    for (int e = 0; e < N; ++e) gw[e] = w_own * sigmoid_approx(bf16_to_f32(rt[e * kD]));
+    for (int e = 0; e < N; e += 2) {  // packed pairs: the same roundings as scalar operations
+      const float2 g = f2_mul(make_float2(w_own, w_own),
+                              sigmoid2_approx(make_float2(bf16_to_f32(rt[e * kD]), bf16_to_f32(rt[(e + 1) * kD]))));
+      gw[e] = g.x;
+      gw[e + 1] = g.y;
+    }
   };
   // x: this thread's rows of O^T of chunk j, as read from tensor memory. Scaled, divided by the
   // rms over each token's 128 channels, gated and written; x is kept in registers across the
@@ -707,9 +712,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int N = int(sizeof(x) / sizeof(x[0]));  // tokens of this warp: 8 or 16
     float sq[N];
 #pragma unroll
-    for (int e = 0; e < N; ++e) {
-      x[e] = scale * x[e];
-      sq[e] = x[e] * x[e];
+    for (int e = 0; e < N; e += 2) {  // packed pairs: the same roundings as scalar multiplies
+      const float2 y = f2_mul(make_float2(scale, scale), make_float2(x[e], x[e + 1]));
+      const float2 y2 = f2_mul(y, y);
+      x[e] = y.x;
+      x[e + 1] = y.y;
+      sq[e] = y2.x;
+      sq[e + 1] = y2.y;
     }
     const float part = lane_sums<N>(sq, lane);
     constexpr int kShift = N == 8 ? 2 : 1;  // lane l holds the sum of token (l >> kShift) & (N - 1)
@@ -720,7 +729,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     const float4 p = s_ss[t0 + (lane & (N - 1))];
     const float rstd_l = rsqrtf(((p.x + p.y) + (p.z + p.w)) * (1.f / kD) + og.eps);  // token t0 + (lane & (N-1))
 #pragma unroll
-    for (int e = 0; e < N; ++e) x[e] = x[e] * __shfl_sync(0xffffffffu, rstd_l, e) * gw[e];
+    for (int e = 0; e < N; e += 2) {  // (x rstd) (Sigmoid(r) w), packed pairs
+      const float2 y = f2_mul(f2_mul(make_float2(x[e], x[e + 1]), make_float2(__shfl_sync(0xffffffffu, rstd_l, e),
+                                                                              __shfl_sync(0xffffffffu, rstd_l, e + 1))),
+                              make_float2(gw[e], gw[e + 1]));
+      x[e] = y.x;
+      x[e + 1] = y.y;
+    }
     write_rows(x, t0, j, L);
   };
   auto out_gated_rows = [&](auto n_tag, int t0, int j, int L, uint32_t ocols) {

@@ -137,6 +137,18 @@ __device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
   return f2_unpack(r);
 }
 
+// sigmoid_approx of two values, its multiply and add packed (the same roundings, so the same bits)
+__device__ __forceinline__ float2 sigmoid2_approx(float2 x) {
+  const float2 s = f2_mul(x, make_float2(-1.4426950408889634f, -1.4426950408889634f));
+  float e0, e1, r0, r1;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e0) : "f"(s.x));
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e1) : "f"(s.y));
+  const float2 d = f2_add(make_float2(e0, e1), make_float2(1.f, 1.f));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r0) : "f"(d.x));
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r1) : "f"(d.y));
+  return make_float2(r0, r1);
+}
+
 // The output gate of Kimi K3 -- Architecture Notes, section 1.3 ("Full-rank output gate"):
 // out = Sigmoid(r) * w * o * rstd, with rstd = 1 / sqrt(mean of o^2 over the head's d_v
 // channels + eps) formed by the caller.
