@@ -129,15 +129,17 @@ constexpr uint32_t OFF_MISC = 218 * 1024;    // beta x2, Gamma_last x2, group de
 constexpr uint32_t OFF_SS = OFF_MISC + 3520; // output gate: per-token partial sums of squares [32][4] fp32
 constexpr uint32_t kSmemBytes = 222 * 1024 + 1024;
 static_assert(OFF_SS + 32 * 16 + 1023 <= kSmemBytes, "shared memory map exceeds the allocation");
-// Unbounded decay only: the position-pair shares of the diagonal blocks, by chunk parity,
-// [2][512] fp32 (A entries first, then P; see pair_row_a), which takes the allocation to the
-// 227 KB a CTA may have. The cumulative log2 decays [32 tokens][128 c] of a chunk that has
-// wide channels pass through the lower half of the S^T tile (free between MMA1 and P4).
-constexpr uint32_t OFF_CORR = 222 * 1024;
+// The inverse pair's copy of A [32][32] fp32, which takes the allocation to the 227 KB a CTA may have.
+constexpr uint32_t OFF_PAIR = 222 * 1024;
 constexpr uint32_t kSmemBytesUnbounded = 226 * 1024 + 1024;
-static_assert(OFF_SS + 32 * 16 <= OFF_CORR && kSmemBytesUnbounded <= 232448, "unbounded map exceeds 227 KB");
-// Bounded maps: the same 4 KB hold the inverse pair's copy of A [32][32] fp32.
-constexpr uint32_t OFF_PAIR = OFF_CORR;
+static_assert(OFF_SS + 32 * 16 <= OFF_PAIR && kSmemBytesUnbounded <= 232448, "shared memory map exceeds 227 KB");
+// Unbounded decay only: the position-pair shares of the diagonal blocks, by chunk parity,
+// [2][512] fp32 (A entries first, then P; see pair_row_a), in the 8 KB that the bf16 decay logits
+// leave free in the q/k/decay staging area (no TMA load writes there). The cumulative log2 decays
+// [32 tokens][128 c] of a chunk that has wide channels pass through the lower half of the S^T
+// tile (free between MMA1 of chunk c - 2, which reads it, and P1 of chunk c - 1).
+constexpr uint32_t OFF_SHARES = OFF_QKG + SG + 8 * 1024;
+static_assert(OFF_SHARES + 2 * 512 * 4 <= OFF_V, "position-pair shares overlap the v stages");
 template <int kDecay>
 constexpr uint32_t smem_bytes() { return kSmemBytesUnbounded; }
 // a channel is wide in a diagonal block when its log2 decay over the block's tokens is below
@@ -248,10 +250,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quarter = warp & 3, grp = warp >> 2;  // TMEM lane quarter, column group (compute warps)
   const bool worker = tid < kWorkers;              // warps 0..15; warp 16 issues TMA loads and MMAs
-  // The bounded maps invert I + A on a pair of warps of their own (warps 18, 19), one chunk ahead
-  // of the state chain; the unbounded map keeps the inverse on four of the compute warps, whose
-  // scratch its position-pair step shares.
-  constexpr bool kDedInv = kDecay != DECAY_UNBOUNDED;
+  // Every map inverts I + A on a pair of warps of their own (warps 18, 19), one chunk ahead of the
+  // state chain. (The four-warp inverse on the compute warps below is the earlier form.)
+  constexpr bool kDedInv = true;
   const bool inv_pair = kDedInv && warp >= kInvWarp0;  // warps 18, 19: the last two (see kThreads)
   // With the four-warp inverse, full chunks leave the output gate through a TMA store of a staged tile.
   constexpr bool kStaged = kNormGate && !kDedInv;
@@ -565,7 +566,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      float *corr = reinterpret_cast<float *>(sm + OFF_CORR) + (c & 1) * 512;
+      float *corr = reinterpret_cast<float *>(sm + OFF_SHARES) + (c & 1) * 512;
       if (il < tl) corr[pair_row_a(uint32_t(pb), uint32_t(tl)) + il] = a;
       if (il <= tl) corr[pair_row_p(uint32_t(pb), uint32_t(tl)) + il] = p;
       // every thread is past the decays before P4 reuses the S^T tile
@@ -865,7 +866,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (have) tmem_ld8(tmem + lane_base + tm_gram(c) + 8 * grp, vals);
     tmem_ld_wait(vals, also...);
     if (lane < 16) {
-      const int lim = (have && t < L) ? t + 1 - 8 * grp : 0;  // keep i <= t
+      // keep i <= t. In the unbounded map the column group goes in opaque: with it visible,
+      // nvcc 13.0 took this limit to be at least 2 there and dropped the mask on the entries
+      // above the diagonal. (The bounded maps compile right, and would spill with it.)
+      const int lim = (have && t < L) ? t + 1 - 8 * (kUnb ? opaque_int(grp) : grp) : 0;
+      if constexpr (kUnb) {  // the position-pair shares of chunk c's diagonal blocks, if it has any
+        const bool slow = *reinterpret_cast<volatile uint32_t *>(s_tmem + 2 + b) == uint32_t(c);
+        if (slow && have && grp >= 2 * quarter) {  // columns inside the diagonal block
+          const float *cr = reinterpret_cast<const float *>(sm + OFF_SHARES) + b * 512 +
+                            pair_row_p(uint32_t(quarter), uint32_t(t & 15)) + 8 * (grp - 2 * quarter);
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (e < lim) vals[e] += cr[e];
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 8; ++e) vals[e] = e < lim ? vals[e] : 0.f;
       st_at(sm + OFF_PK + (c % 3) * kPKBytes, sw64_chunk(t, grp), pack8_f16(vals));
@@ -881,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
     // unbounded map: the position-pair shares of chunk c's diagonal blocks, if it has any
     const bool slow = kUnb && *reinterpret_cast<volatile uint32_t *>(s_tmem + 2 + b) == uint32_t(c);
-    const float *corr = reinterpret_cast<const float *>(sm + OFF_CORR) + b * 512;
+    const float *corr = reinterpret_cast<const float *>(sm + OFF_SHARES) + b * 512;
     if (inv_group) {
       bad |= !mbar_wait_sleep(&bars->gram[b], uint32_t((c >> 1) & 1), err_word, DEVERR_MMA_TIMEOUT);
       tc_fence_after();
@@ -1043,7 +1057,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane < 16) {
         const int t = 16 * s + lane;
         const float bt = s_beta[b * kC + t];
-        const int lim = t < L ? t - 16 * h2 : 0;  // keep i < t
+        const int lim = t < L ? t - 16 * (kUnb ? opaque_int(h2) : h2) : 0;  // keep i < t (opaque: as for P)
+        if constexpr (kUnb) {  // the diagonal block of a chunk with wide channels: their position-pair shares
+          const bool slow = *reinterpret_cast<volatile uint32_t *>(s_tmem + 2 + b) == uint32_t(c);
+          if (slow && h2 == s) {
+            const float *cr = reinterpret_cast<const float *>(sm + OFF_SHARES) + b * 512 + pair_row_a(uint32_t(s), uint32_t(lane));
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (e < lim) vals[e] += cr[e];
+          }
+        }
 #pragma unroll
         for (int e = 0; e < 16; ++e) vals[e] = e < lim ? bt * vals[e] : 0.f;
         float4 *arow = reinterpret_cast<float4 *>(As + t * 32 + 16 * h2);
