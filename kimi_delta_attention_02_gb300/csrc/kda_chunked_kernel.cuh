@@ -541,20 +541,41 @@ __global__ void __launch_bounds__(kThreads, 1)
     // and walks the block's list of wide channels. Tokens past the end of the
     // sequence only reach entries that P4 masks.
     auto pair_shares = [&](int c) -> bool {
-      if (tid == 0) s_tmem[2 + (c & 1)] = uint32_t(c);  // for P4 of chunk c
-      const int pb = tid >> 8, tl = (tid >> 4) & 15, il = tid & 15;
+      if (tid == 0) s_tmem[2 + (c & 1)] = uint32_t(c);  // for the A and P extraction of chunk c
+      // Work items: threads 0..479 take the 240 entries below the diagonals (120 per block), two
+      // adjacent lanes per entry, each over half of the channels (mask words 2 hh, 2 hh + 1);
+      // threads 480..511 take the 32 diagonal entries, which need P only and no exponential
+      // (e^{G_tc - G_tc} = 1).
+      const bool diag = tid >= 480;
+      const int hh = tid & 1, r = (tid >> 1) % 120;  // r: entry inside its block's lower triangle
+      const int pb = diag ? (tid - 480) >> 4 : (tid >> 1) / 120;
+      int tl = int((1.f + sqrtf(8.f * float(r) + 1.f)) * 0.5f);  // r = tl (tl - 1) / 2 + il, il < tl
+      if (tl * (tl - 1) / 2 > r) --tl;                             // (against rounding of the root)
+      else if ((tl + 1) * tl / 2 <= r) ++tl;
+      int il = r - tl * (tl - 1) / 2;
+      if (diag) tl = il = (tid - 480) & 15;
       const int t = 16 * pb + tl, i = 16 * pb + il;
+      // bf16 element (token, channel w) of the 128-byte-swizzled q / k tiles
+      auto elem = [&](uint32_t tile, int tok, int w) {
+        const uint32_t cw = uint32_t(w & 63);
+        return bf16_to_f32(*reinterpret_cast<const uint16_t *>(
+            sm + OFF_QKG + tile + uint32_t(w >> 6) * 4096u + uint32_t(tok) * 128u +
+            (((cw >> 3) ^ uint32_t(tok & 7)) << 4) + (cw & 7u) * 2u));
+      };
       float a = 0.f, p = 0.f;
-      if (il <= tl) {
-        // bf16 element (token, channel w) of the 128-byte-swizzled q / k tiles
-        auto elem = [&](uint32_t tile, int tok, int w) {
-          const uint32_t cw = uint32_t(w & 63);
-          return bf16_to_f32(*reinterpret_cast<const uint16_t *>(
-              sm + OFF_QKG + tile + uint32_t(w >> 6) * 4096u + uint32_t(tok) * 128u +
-              (((cw >> 3) ^ uint32_t(tok & 7)) << 4) + (cw & 7u) * 2u));
-        };
+      if (diag) {  // a whole warp: P[t][t] = sum over the wide channels of q_tc k_tc
 #pragma unroll 1
         for (int q4 = 0; q4 < 4; ++q4) {
+          uint32_t m = s_tmem[4 + 4 * pb + q4];
+          while (m != 0u) {
+            const int w = 32 * q4 + __ffs(int(m)) - 1;
+            m &= m - 1u;
+            p = fmaf(elem(SQ, t, w), elem(SK, t, w), p);
+          }
+        }
+      } else {  // whole warps too: the two halves of an entry meet by one shuffle
+#pragma unroll 1
+        for (int q4 = 2 * hh; q4 < 2 * hh + 2; ++q4) {
           uint32_t m = s_tmem[4 + 4 * pb + q4];
           while (m != 0u) {
             const int w = 32 * q4 + __ffs(int(m)) - 1;
@@ -565,10 +586,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             p = fmaf(elem(SQ, t, w), ke, p);
           }
         }
+        a += __shfl_xor_sync(0xffffffffu, a, 1);
+        p += __shfl_xor_sync(0xffffffffu, p, 1);
       }
       float *corr = reinterpret_cast<float *>(sm + OFF_SHARES) + (c & 1) * 512;
-      if (il < tl) corr[pair_row_a(uint32_t(pb), uint32_t(tl)) + il] = a;
-      if (il <= tl) corr[pair_row_p(uint32_t(pb), uint32_t(tl)) + il] = p;
+      if (diag) {
+        corr[pair_row_p(uint32_t(pb), uint32_t(tl)) + il] = p;
+      } else if (hh == 0) {
+        corr[pair_row_a(uint32_t(pb), uint32_t(tl)) + il] = a;
+        corr[pair_row_p(uint32_t(pb), uint32_t(tl)) + il] = p;
+      }
       // every thread is past the decays before P4 reuses the S^T tile
       if (named_bar_or(BAR_WORK, kWorkers, bad)) {
         give_up(H_PREP);
