@@ -63,19 +63,16 @@
 //   P2  next j+2: decay prefix sums and the operand tiles (a thread owns one key
 //                 channel and 8 tokens); the Gram of chunk j+2 (kind::tf32, M = 64 rows
 //                 [Q f ; K f] x N = 32 keys K g) follows, queued behind MMA2
-//   P3  chain j : U^T to fp16 (bounded maps: P of chunk j + 1 leaves tensor memory in the
-//                 same round trip); MMA2: [O^T | S^T] += U^T [P ; K^^T]^T
-//                 (N = 160)
-//   P4  next j+1: the inverse side. Bounded maps: the inverse pair takes A of chunk j + 1 out of
-//                 its TMEM lanes, forms T' = (I + A)^{-1} Diag(b) by back substitution (one
-//                 row per lane) and converts v to fp16 while the compute warps run P1..P3; the
-//                 pair hands T' over on an mbarrier, which alone gates W^T / U~^T. Unbounded map:
-//                 warps 2, 3, 6, 7 (whose TMEM lanes hold the key rows of the Gram) invert
-//                 I + A in 8 x 8 and 16 x 16 blocks while the other 12 warps convert v, take P
-//                 out of TMEM and write O^T of chunk j (with the output gate, through the
-//                 RMSNorm and the gate, the logits tile brought by TMA into the S^T tile once
-//                 MMA1 has read it);
-//                 -W^T = -Kg^T T'^T (negated by the MMA) and [U~^T | 0] = V^T [T'; 0]^T
+//   P3  chain j : U^T to fp16 (P of chunk j + 1 leaves tensor memory in the same round
+//                 trip); MMA2: [O^T | S^T] += U^T [P ; K^^T]^T  (N = 160)
+//   P4  next j+1: the inverse side. The inverse pair takes A of chunk j + 1 out of its TMEM
+//                 lanes, forms T' = (I + A)^{-1} Diag(b) by back substitution (one row per
+//                 lane) and converts v to fp16 while the compute warps run P1..P3; the pair
+//                 hands T' over on an mbarrier, which alone gates W^T / U~^T:
+//                 -W^T = -Kg^T T'^T (negated by the MMA) and [U~^T | 0] = V^T [T'; 0]^T.
+//                 (The earlier four-warp inverse, with warps 2, 3, 6, 7 inverting I + A in
+//                 8 x 8 and 16 x 16 blocks while 12 warps wrote the outputs, is still in this
+//                 file behind kDedInv; every instantiation now takes the pair.)
 // Per-chunk operand tiles are double-buffered by chunk parity ([P ; K^^T] three
 // times, since it lives from P2 of chunk j to MMA2 of chunk j + 2), and so are the
 // Gram accumulators. TMA brings q, k and log-decay one chunk ahead of P2 and v two
@@ -254,7 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // state chain. (The four-warp inverse on the compute warps below is the earlier form.)
   constexpr bool kDedInv = true;
   const bool inv_pair = kDedInv && warp >= kInvWarp0;  // warps 18, 19: the last two (see kThreads)
-  // With the four-warp inverse, full chunks leave the output gate through a TMA store of a staged tile.
+  // (Unused: with the four-warp inverse, full chunks left the output gate through a staged TMA store.)
   constexpr bool kStaged = kNormGate && !kDedInv;
   // Read-out with the inverse pair: the outputs of chunk j - 1 leave with P1 of chunk j (both wait
   // for MMA2 of chunk j - 1 and read tensor memory in the same round trip; the output gate's
@@ -539,7 +536,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (i <= t), from position pairs, one exponential (<= 1) per pair and wide channel,
     // shared by A and P. Thread (block b, row tl, column il) owns entry (16 b + tl, 16 b + il)
     // and walks the block's list of wide channels. Tokens past the end of the
-    // sequence only reach entries that P4 masks.
+    // sequence only reach entries that the A and P masks clear.
     auto pair_shares = [&](int c) -> bool {
       if (tid == 0) s_tmem[2 + (c & 1)] = uint32_t(c);  // for the A and P extraction of chunk c
       // Work items: threads 0..479 take the 240 entries below the diagonals (120 per block), two
@@ -596,7 +593,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         corr[pair_row_a(uint32_t(pb), uint32_t(tl)) + il] = a;
         corr[pair_row_p(uint32_t(pb), uint32_t(tl)) + il] = p;
       }
-      // every thread is past the decays before P4 reuses the S^T tile
+      // every thread is past the decays before P1 of the next chain step rewrites the S^T tile
       if (named_bar_or(BAR_WORK, kWorkers, bad)) {
         give_up(H_PREP);
         return false;
@@ -914,9 +911,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   };
 
   // ------------------------------------------------------------------ P4: P, A, inverse, T', v
-  // The four-warp inverse (unbounded map): inverse-side work of chunk c; the 12 warps outside the
-  // inverse group also write the outputs of chunk j_out (if >= 0). Returns false when the compute
-  // warps give up.
+  // The four-warp inverse (unused: every instantiation takes the inverse pair): inverse-side work of
+  // chunk c; the 12 warps outside the inverse group also write the outputs of chunk j_out (if >= 0).
+  // Returns false when the compute warps give up.
   auto extract_inverse = [&](int c, int j_out) -> bool {
     const int b = c & 1, L = chunk_len(c);
     float *As = reinterpret_cast<float *>(sm + OFF_ST + G_A);
@@ -1261,7 +1258,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         st_at(sm + OFF_UT, sw64_chunk(uint32_t(v_own), uint32_t(grp)), pack8_f16(x));
       }
       handoff(H_U);
-      // ---------------- P4 / P5: inverse side of chunk j + 1 -> W^T and U~^T, and outputs of chunk j
+      // ---------------- the last chunk's outputs (the inverse side of chunk j + 1 is the pair's)
       if (kMerged) {
         if (!more) out_chunk(j);
       } else if (more) {
