@@ -104,6 +104,48 @@ def test_workspace_size_is_a_pure_host_query(lib):
         assert a % 16 == 0
 
 
+def _planned_workspace(T, N, H, d_k=128, d_v=128):
+    """The schedules' workspace, restated from their plan: one sequence is cut into the largest
+    number m >= 2 of segments whose passes (pass 1: 2m - 3 runs, or 1 for m = 2; pass 3: m runs)
+    each fit one CTA per SM on 152 SMs, with segments (whole 32-token chunks) of at least 4096
+    tokens and at most 64 runs; its maps take max(runs, m) + m states of 128 x 128 fp32 per
+    head, each part rounded up to 256 bytes. Several sequences take the longest-first order
+    (4 bytes each, rounded up to 256) once their chains outnumber the SMs (at most 8192)."""
+    up256 = lambda n: (n + 255) // 256 * 256
+    state = 128 * 128 * 4
+    if d_k != 128 or d_v != 128 or H < 1 or T <= 0:
+        return 0
+    if N == 1:
+        best = None
+        for m in range(2, 65):
+            runs = 1 if m == 2 else 2 * m - 3
+            if runs > 64 or H * runs > 152 or H * m > 152:
+                break
+            L = ((T + m - 1) // m + 31) // 32 * 32
+            if L < 4096 or (m - 1) * L >= T:
+                break
+            best = (m, runs)
+        if best is None:
+            return 0
+        m, runs = best
+        return up256(max(runs, m) * H * state) + up256(m * H * state)
+    return up256(4 * N) if 1 < N <= 8192 and N * H > 152 else 0
+
+
+@pytest.mark.parametrize("T,N,H", [(1 << 20, 1, 32), (1 << 20, 1, 1), (1 << 20, 1, 96), (1 << 16, 1, 32),
+                                   (8192, 1, 8), (8191, 1, 8), (4096, 1, 96), (135000, 8, 96), (10000, 2, 76),
+                                   (10000, 2, 77), (10000, 200, 1), (10000, 9000, 1)])
+def test_workspace_sizes_follow_the_schedule_plan(lib, T, N, H):
+    assert lib.kda_prefill_workspace_size(T, N, H, 128, 128) == _planned_workspace(T, N, H)
+
+
+def test_workspace_of_the_long_context_shape(lib):
+    # T = 2^20, H = 32: three segments (pass 1 runs 3 chains per head; four segments would need
+    # 5 x 32 = 160 > 152 CTAs in pass 1), so 3 + 3 states per head: 6 x 32 x 64 KiB = 12 MiB
+    assert lib.kda_prefill_workspace_size(1 << 20, 1, 32, 128, 128) == 6 * 32 * 65536
+    assert lib.kda_prefill_workspace_size(1 << 20, 1, 32, 64, 128) == 0
+
+
 def test_prefill_accepts_empty_work(lib):
     # zero sequences and zero tokens: nothing to enqueue, no CUDA call is made
     assert _prefill(lib, N=0, T=0, q=NULL, k=NULL, v=NULL, la=NULL, beta=NULL, out=NULL, fin=NULL) == B.KDA_OK
