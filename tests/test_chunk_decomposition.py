@@ -121,3 +121,35 @@ def test_every_channel_narrow_needs_no_pairs():
     q, k, G = _chunk(rng, la)
     got, used = _split(q, k, G, False, drop_pairs=True)
     assert _close(got, _exact(q, k, G, False)) and used <= 16 * 0.5 / np.log(2.0) + 1e-9
+
+
+def _back_substitution_row(A, j):
+    """Row j of T = (I + A)^{-1} for strictly lower triangular A, as the inverse pair forms it:
+    x^T (I + A) = e_j^T, i.e. x_m = [m == j] - sum_{i > m} x_i A[i][m], from m = n - 1 down."""
+    n = A.shape[0]
+    x = np.zeros(n)
+    for m in range(n - 1, -1, -1):
+        x[m] = (1.0 if m == j else 0.0) - sum(x[i] * A[i, m] for i in range(m + 1, n))
+    return x
+
+
+@pytest.mark.parametrize("seed", [0, 1])
+def test_inverse_pair_back_substitution(seed):
+    rng = np.random.default_rng(20 + seed)
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal(C)))
+    k = rng.standard_normal((C, D)); k /= np.linalg.norm(k, axis=1, keepdims=True)
+    G = np.cumsum(-rng.uniform(0.0, 1.0, (C, D)), axis=0)
+    A = np.zeros((C, C))  # A[t, i] = beta_t sum_c k_tc k_ic e^{G_tc - G_ic}, i < t
+    for t in range(C):
+        for i in range(t):
+            A[t, i] = beta[t] * np.sum(k[t] * k[i] * np.exp(G[t] - G[i]))
+    T = np.stack([_back_substitution_row(A, j) for j in range(C)])
+    assert _close(T, np.linalg.inv(np.eye(C) + A))
+    assert np.allclose(np.triu(T, 1), 0.0) and np.allclose(np.diag(T), 1.0)  # unit lower triangular
+    # the same substitution with A transposed (A[m][i] where A[i][m] belongs) is not the inverse:
+    # checked on the last row, which is dense
+    j = C - 1
+    x = np.zeros(C)
+    for m in range(C - 1, -1, -1):
+        x[m] = (1.0 if m == j else 0.0) - sum(x[i] * A[m, i] for i in range(m + 1, C))
+    assert not _close(x, np.linalg.inv(np.eye(C) + A)[j])
